@@ -1,0 +1,18 @@
+"""CPU oracle for the low-bit weight GEMV/GEMM path -- TEST INFRASTRUCTURE ONLY.
+
+A plain, slow, obviously correct restatement of what the path computes, in fp64, written
+from the pages and independent of the CUDA path (no shared code, headers, tables or
+constants; neither side imports the other).  Only ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py`` may import it.  The product path never calls it.
+
+Modules
+  numerics  -- fp16/bf16 decoding and round-to-nearest-even into bf16.
+  int4      -- symmetric per-group INT4: dequantise, multiply, pack/unpack the layout.
+  binplane  -- ShiftAdd binary planes: dequantise, multiply, pack/unpack the layout.
+  verify    -- vocabulary argmax (lowest index on ties) and greedy prefix acceptance.
+
+Parity pins (tests/test_oracle_pins.py) tie every function to something other than
+itself: hand-worked 4x8 examples, brute force on tiny shapes, closed forms, invariants
+and library rounding routines.  No function here is "parity unpinned".
+"""
+from . import numerics, int4, binplane, verify  # noqa: F401

@@ -1,0 +1,322 @@
+"""Pins for the CPU oracle: each check ties an oracle function to something other than
+itself (hand-worked examples, brute force written another way, closed forms, invariants,
+library rounding routines), so a dropped term, a wrong sign or index or a transposed
+operand in the oracle fails here.  CPU only."""
+import hashlib
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import binplane, int4, numerics, verify
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_fixture(name):
+    rows = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            if ":" in line:
+                key, vals = line.split(":", 1)
+                rows[key.strip()] = vals.split()
+    return rows
+
+
+def _bf16(vals):
+    return numerics.bf16_bits(numerics.round_to_bf16(np.asarray(vals, dtype=np.float64)))
+
+
+def _f16(vals):
+    return np.asarray(vals, dtype=np.float64).astype(np.float16).view(np.uint16)
+
+
+# ------------------------------------------------------------------ numerics
+
+def test_round_to_bf16_matches_torch_on_fp32_values():
+    g = np.random.default_rng(11)
+    x32 = np.concatenate([
+        g.standard_normal(20000).astype(np.float32),
+        (g.standard_normal(5000) * 1e-30).astype(np.float32),
+        (g.standard_normal(5000) * 1e30).astype(np.float32),
+        # exact ties between two bf16 neighbours: 1 + 2^-8, 1 + 3*2^-8, -(2 + 2^-7)
+        np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(2 + 2 ** -7), 0.0, -0.0], dtype=np.float32),
+    ])
+    ref = torch.from_numpy(x32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = numerics.bf16_bits(numerics.round_to_bf16(x32.astype(np.float64)))
+    assert np.array_equal(got, ref)
+
+
+def test_round_to_bf16_ties_by_hand():
+    # 1 + 2^-8 lies halfway between 1 and 1 + 2^-7: ties go to the even neighbour, 1.
+    # 1 + 3*2^-8 lies halfway between 1 + 2^-7 and 1 + 2^-6: even neighbour is 1 + 2^-6.
+    # Just above a tie rounds up.
+    r = numerics.round_to_bf16(np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, 1 + 2 ** -8 + 2 ** -40,
+                                         255.5, 256.5 * 2, -3.0]))
+    assert list(r) == [1.0, 1 + 2 ** -6, 1 + 2 ** -7, 256.0, 512.0, -3.0]
+
+
+def test_decoders_are_exact():
+    v = np.array([0.5, -2.0, 1.0 / 3.0, 65504.0, 6.1e-5])
+    assert np.array_equal(numerics.f16_to_f64(_f16(v)), v.astype(np.float16).astype(np.float64))
+    x = np.array([1.0, -0.15625, 3.0e38, 1e-38])
+    bits = _bf16(x)
+    assert np.array_equal(numerics.bf16_to_f64(bits), numerics.round_to_bf16(x))
+
+
+def test_generator_roundings_are_representable_and_deterministic():
+    codes, scales, x = synth.int4_problem(0, 1, 256, 512)
+    assert codes.min() >= -8 and codes.max() <= 7
+    # drawn bf16 values are a fixed point of the oracle's rounding
+    xv = numerics.bf16_to_f64(x)
+    assert np.array_equal(numerics.round_to_bf16(xv), xv)
+    h = hashlib.sha256(codes.tobytes() + scales.tobytes() + x.tobytes()).hexdigest()
+    codes2, scales2, x2 = synth.int4_problem(0, 1, 256, 512)
+    assert h == hashlib.sha256(codes2.tobytes() + scales2.tobytes() + x2.tobytes()).hexdigest()
+    # the generator's own bf16 rounding agrees with the oracle's on fresh fp64 draws
+    d = np.random.default_rng(5).standard_normal(50000)
+    assert np.array_equal(synth.to_bf16_bits(d), _bf16(d))
+
+
+# ------------------------------------------------------------------ INT4
+
+@pytest.mark.parametrize("G", [4, 8])
+def test_int4_hand_example(G):
+    fx = _read_fixture("int4_hand_4x8.txt")
+    x = _bf16([float(v) for v in fx["x"]])[None, :]
+    q = np.array([[int(v) for v in fx[f"q{n}"]] for n in range(4)], dtype=np.int8)
+    s = _f16([[float(v) for v in fx[f"G{G}_s{n}"]] for n in range(4)])
+    y = int4.gemm(x, q, s, group=G)
+    assert np.array_equal(y[0], np.array([float(v) for v in fx[f"G{G}_y"]]))
+
+
+def _brute_int4(xv, q, s, G):
+    # group-sum-first, pure Python loops: sum_g s * (sum_{k in g} q * x)
+    M, K = xv.shape
+    N = q.shape[0]
+    out = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            tot = 0.0
+            for g in range(K // G):
+                part = 0.0
+                for k in range(g * G, (g + 1) * G):
+                    part += int(q[n, k]) * float(xv[m, k])
+                tot += float(s[n, g]) * part
+            out[m, n] = tot
+    return out
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 3, 128), (2, 5, 256), (3, 2, 384)])
+def test_int4_brute_force(M, N, K):
+    codes, scales, x = synth.int4_problem(123, M, N, K)
+    y = int4.gemm(x, codes, scales)
+    ref = _brute_int4(numerics.bf16_to_f64(x), codes, numerics.f16_to_f64(scales), 128)
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_int4_one_hot_and_group_closed_forms():
+    N, K = 7, 384
+    codes, scales, _ = synth.int4_problem(9, 1, N, K)
+    sv = numerics.f16_to_f64(scales)
+    # one-hot activation at k picks column k of W: y = RNE(s[n][k//128] * q[n][k])
+    for k in (0, 127, 128, 200, 383):
+        x = np.zeros((1, K)); x[0, k] = 1.0
+        y = int4.gemm(_bf16(x), codes, scales)
+        assert np.array_equal(y[0], sv[:, k // 128] * codes[:, k])
+    # x = 1 on one group: y = s * sum_{k in g} q
+    x = np.zeros((1, K)); x[0, 128:256] = 1.0
+    y = int4.gemm(_bf16(x), codes, scales)
+    assert np.array_equal(y[0], sv[:, 1] * codes[:, 128:256].sum(axis=1))
+    # zero scales give exact zeros
+    y = int4.gemm(_bf16(np.ones((1, K))), codes, np.zeros_like(scales))
+    assert np.all(y == 0)
+
+
+def test_int4_layout_positions_by_hand():
+    N, K = 40, 256
+    rows = []
+    with open(os.path.join(GOLDEN, "int4_layout_positions.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                n, k, byte, nib = line.split()
+                rows.append((int(n), int(k), int(byte), nib))
+    total, c_off, c_bytes, s_off, s_bytes = int4.packed_sizes(N, K)
+    assert (c_off, c_bytes, s_off) == (128, 8192, 8320)
+    for n, k, byte, nib in rows:
+        codes = np.zeros((N, K), dtype=np.int8)
+        codes[n, k] = 5                              # nibble u = 13, every other nibble 8
+        packed = int4.pack(codes, np.zeros((N, K // 128), dtype=np.uint16))
+        sec = packed[c_off:c_off + c_bytes]
+        lo, hi = sec & 0xF, sec >> 4
+        expect_lo = np.full(c_bytes, 8); expect_hi = np.full(c_bytes, 8)
+        (expect_lo if nib == "lo" else expect_hi)[byte] = 13
+        assert np.array_equal(lo, expect_lo) and np.array_equal(hi, expect_hi), (n, k)
+    scales = np.zeros((N, K // 128), dtype=np.uint16)
+    scales[33, 1] = 0x3C00
+    packed = int4.pack(np.zeros((N, K), dtype=np.int8), scales)
+    sec = packed[s_off:s_off + s_bytes].view("<u2")
+    assert sec[194 // 2] == 0x3C00 and np.count_nonzero(sec) == 1
+
+
+@pytest.mark.parametrize("N,K", [(40, 256), (256, 512), (33, 128)])
+def test_int4_pack_round_trip_and_header(N, K):
+    codes, scales, _ = synth.int4_problem(4, 1, N, K)
+    packed = int4.pack(codes, scales)
+    assert packed.size == int4.packed_sizes(N, K)[0]
+    c2, s2 = int4.unpack(packed)
+    assert np.array_equal(c2, codes) and np.array_equal(s2, scales)
+    hd = int4.parse_header(packed)
+    assert (hd["magic"], hd["format"], hd["N"], hd["K"], hd["group"]) == (int4.MAGIC, 1, N, K, 128)
+    # exactly N*K/2 + N*K/64 payload bytes when N is a multiple of the row tile
+    if N % 32 == 0:
+        assert hd["codes_bytes"] + hd["scales_bytes"] == N * K // 2 + N * K // 64
+
+
+# ------------------------------------------------------------------ binary planes
+
+@pytest.mark.parametrize("G", [4, 8])
+def test_binplane_hand_example(G):
+    fx = _read_fixture("binplane_hand_4x8.txt")
+    x = _bf16([float(v) for v in fx["x"]])[None, :]
+    bits = np.array([[[int(v, 16)] for v in fx["bits_p0"]],
+                     [[int(v, 16)] for v in fx["bits_p1"]]], dtype=np.uint8)   # [2][4][1]
+    a0 = np.array([float(v) for v in fx[f"G{G}_a_p0"]]).reshape(4, -1)
+    a1 = np.array([float(v) for v in fx[f"G{G}_a_p1"]]).reshape(4, -1)
+    alpha = _f16(np.stack([a0, a1]))
+    y = binplane.gemm(x, bits, alpha, group=G)
+    assert np.array_equal(y[0], np.array([float(v) for v in fx[f"G{G}_y"]]))
+
+
+def test_binplane_planes_are_exactly_pm1_and_identity():
+    bits, alpha, x = synth.binplane_problem(3, 3, 1, 8, 256)
+    b = binplane.signs(bits)
+    assert set(np.unique(b)) == {-1.0, 1.0}
+    # sum b*x = 2 * sum_{b=+1} x - sum x, on random data
+    xv = numerics.bf16_to_f64(x)[0]
+    lhs = b @ xv
+    rhs = 2 * ((b > 0) * xv).sum(axis=-1) - xv.sum()
+    assert np.allclose(lhs, rhs, rtol=0, atol=1e-12)
+
+
+def test_binplane_closed_forms():
+    P, N, K = 1, 5, 256
+    _, alpha, x = synth.binplane_problem(8, P, 1, N, K)
+    xv = numerics.bf16_to_f64(x)[0]
+    av = numerics.f16_to_f64(alpha)[0]
+    gsum = xv.reshape(2, 128).sum(axis=1)
+    ones = np.full((P, N, K // 8), 0xFF, dtype=np.uint8)
+    zeros = np.zeros((P, N, K // 8), dtype=np.uint8)
+    assert np.allclose(binplane.gemm(x, ones, alpha)[0], av @ gsum, rtol=1e-14, atol=0)
+    assert np.allclose(binplane.gemm(x, zeros, alpha)[0], -(av @ gsum), rtol=1e-14, atol=0)
+    # one-hot activation picks sum_p alpha_p b_p at that input
+    bits, alpha, _ = synth.binplane_problem(8, 4, 1, N, K)
+    for k in (0, 7, 8, 129, 255):
+        xo = np.zeros((1, K)); xo[0, k] = 1.0
+        y = binplane.gemm(_bf16(xo), bits, alpha)[0]
+        sgn = ((bits[:, :, k // 8] >> (k % 8)) & 1) * 2.0 - 1.0     # [P][N]
+        assert np.array_equal(y, (numerics.f16_to_f64(alpha)[:, :, k // 128] * sgn).sum(axis=0))
+
+
+def test_binplane_brute_force():
+    P, M, N, K = 3, 2, 3, 256
+    bits, alpha, x = synth.binplane_problem(21, P, M, N, K)
+    xv = numerics.bf16_to_f64(x)
+    av = numerics.f16_to_f64(alpha)
+    ref = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            tot = 0.0
+            for p in range(P):
+                for g in range(K // 128):
+                    s = 0.0
+                    for k in range(g * 128, (g + 1) * 128):
+                        bit = (int(bits[p, n, k // 8]) >> (k % 8)) & 1
+                        s += xv[m, k] if bit else -xv[m, k]
+                    tot += av[p, n, g] * s
+            ref[m, n] = tot
+    assert np.allclose(binplane.gemm(x, bits, alpha), ref, rtol=1e-12, atol=1e-14)
+
+
+def test_binplane_layout_positions_by_hand():
+    P, N, K = 2, 40, 256
+    total, c_off, c_bytes, a_off, a_bytes = binplane.packed_sizes(P, N, K)
+    with open(os.path.join(GOLDEN, "binplane_layout_positions.txt")) as f:
+        rows = [tuple(int(v) for v in line.split()) for line in f
+                if line.strip() and not line.startswith("#")]
+    for p, n, k, byte, bit in rows:
+        bits = np.zeros((P, N, K // 8), dtype=np.uint8)
+        bits[p, n, k // 8] = 1 << (k % 8)
+        packed = binplane.pack(bits, np.zeros((P, N, K // 128), dtype=np.uint16))
+        sec = packed[c_off:c_off + c_bytes]
+        expect = np.zeros(c_bytes, dtype=np.uint8)
+        expect[byte] = 1 << bit
+        assert np.array_equal(sec, expect), (p, n, k)
+
+
+@pytest.mark.parametrize("P,N,K", [(2, 40, 256), (3, 64, 512), (4, 33, 128)])
+def test_binplane_pack_round_trip(P, N, K):
+    bits, alpha, _ = synth.binplane_problem(6, P, 1, N, K)
+    packed = binplane.pack(bits, alpha)
+    b2, a2 = binplane.unpack(packed)
+    assert np.array_equal(b2, bits) and np.array_equal(a2, alpha)
+    if N % 32 == 0:
+        hd = int4.parse_header(packed)
+        assert hd["codes_bytes"] + hd["scales_bytes"] == P * N * K // 8 + P * N * K // 64
+
+
+# ------------------------------------------------------------------ argmax / acceptance
+
+def test_argmax_lowest_index_brute_force():
+    g = np.random.default_rng(3)
+    for _ in range(200):
+        L = g.integers(-3, 4, size=(3, 9)).astype(np.float64)   # many ties
+        a = verify.argmax_lowest(L)
+        for r in range(3):
+            best = max(L[r])
+            assert a[r] == min(i for i in range(9) if L[r, i] == best)
+
+
+def test_argmax_planted_maximum():
+    N, K = 300, 256
+    codes, scales, x = synth.int4_problem(17, 2, N, K)
+    # row 123 = +7 where x > 0 and -8 where x <= 0 with a large scale: it dominates every row
+    xv = numerics.bf16_to_f64(x)
+    codes[123] = np.where(xv[0] > 0, 7, -8)
+    scales[123] = _f16(np.full(K // 128, 4.0))
+    a = verify.argmax_lowest(int4.gemm(x, codes, scales))
+    assert a[0] == 123
+
+
+def test_top2_margin():
+    L = np.array([[1.0, 3.0, 2.5], [4.0, 4.0, 0.0]])
+    assert np.array_equal(verify.top2_margin(L), [0.5, 0.0])
+
+
+def test_acceptance_exhaustive_small_alphabet():
+    # every (a, d) over a 3-letter alphabet with M = 4 rows: compare with a direct count
+    import itertools
+    for a in itertools.product(range(3), repeat=4):
+        for d in itertools.product(range(3), repeat=3):
+            n, bonus = verify.accept(a, d)
+            k = 0
+            for i in range(3):
+                if all(d[j] == a[j] for j in range(i + 1)):
+                    k = i + 1
+            assert n == k and bonus == a[k] and 1 <= n + 1 <= 4
+
+
+def test_acceptance_planted_drafts():
+    a = np.arange(16) * 7 + 3
+    for j in range(16):
+        d, jj = synth.plant_drafts(5, a, 1000, j=j)
+        assert jj == j
+        n, bonus = verify.accept(a, d)
+        assert n == j and bonus == a[j]
+    d, j = synth.plant_drafts(5, a, 1000)
+    assert verify.accept(a, d)[0] == j

@@ -1,0 +1,155 @@
+"""ctypes marshalling for liblowbit.so (see the package docstring)."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblowbit.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python -m bit_weight_gemv_gb300.build`")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_sz = ctypes.c_size_t
+
+_SIGS = {
+    "lowbit_status_string": (ctypes.c_char_p, [_i]),
+    "lowbit_version": (_i, []),
+    "lowbit_int4_packed_bytes": (_sz, [_i, _i]),
+    "lowbit_binplane_packed_bytes": (_sz, [_i, _i, _i]),
+    "lmhead_workspace_bytes": (_sz, [_i, _i, _i]),
+    "lowbit_pack_int4": (_i, [_vp, _vp, _i, _i, _vp, _vp]),
+    "lowbit_pack_binplane": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp]),
+    "lowbit_validate_packed": (_i, [_vp, _i, _i, _i, _i, _vp]),
+    "lowbit_gemm_int4": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp]),
+    "lowbit_gemm_binplane": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp]),
+    "lmhead_argmax_verify": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "lowbit_device_error": (_i, [_vp, ctypes.POINTER(_i)]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _f = getattr(lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+
+class LowbitError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {lowbit_status_string(status)} (status {status})")
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise LowbitError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need(t, dtype, name):
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous CUDA tensor of dtype {dtype}")
+
+
+def lowbit_status_string(status: int) -> str:
+    return lib.lowbit_status_string(int(status)).decode()
+
+
+def lowbit_version() -> int:
+    return lib.lowbit_version()
+
+
+def lowbit_int4_packed_bytes(N: int, K: int) -> int:
+    return lib.lowbit_int4_packed_bytes(N, K)
+
+
+def lowbit_binplane_packed_bytes(P: int, N: int, K: int) -> int:
+    return lib.lowbit_binplane_packed_bytes(P, N, K)
+
+
+def lmhead_workspace_bytes(M: int, N: int, K: int) -> int:
+    return lib.lmhead_workspace_bytes(M, N, K)
+
+
+def lowbit_pack_int4(codes, scales, N, K, packed, stream=None):
+    """codes int8 [N][K], scales fp16 [N][K/128] -> packed uint8 [lowbit_int4_packed_bytes]."""
+    _need(codes, torch.int8, "codes")
+    _need(scales, torch.float16, "scales")
+    _need(packed, torch.uint8, "packed")
+    if packed.numel() < lowbit_int4_packed_bytes(N, K):
+        raise ValueError("packed buffer too small")
+    _check(lib.lowbit_pack_int4(_ptr(codes), _ptr(scales), N, K, _ptr(packed), _stream(stream)),
+           "lowbit_pack_int4")
+
+
+def lowbit_pack_binplane(signbits, alpha, P, N, K, packed, stream=None):
+    """signbits uint8 [P][N][K/8], alpha fp16 [P][N][K/128] -> packed uint8."""
+    _need(signbits, torch.uint8, "signbits")
+    _need(alpha, torch.float16, "alpha")
+    _need(packed, torch.uint8, "packed")
+    if packed.numel() < lowbit_binplane_packed_bytes(P, N, K):
+        raise ValueError("packed buffer too small")
+    _check(lib.lowbit_pack_binplane(_ptr(signbits), _ptr(alpha), P, N, K, _ptr(packed),
+                                    _stream(stream)), "lowbit_pack_binplane")
+
+
+def lowbit_validate_packed(packed, fmt, P, N, K, stream=None) -> int:
+    """Synchronous header check; returns the status code (0 = matches)."""
+    _need(packed, torch.uint8, "packed")
+    return lib.lowbit_validate_packed(_ptr(packed), fmt, P, N, K, _stream(stream))
+
+
+def lowbit_gemm_int4(X, packed, M, N, K, Y, stream=None):
+    """Y bf16 [M][N] = X bf16 [M][K] times the packed INT4 weights, transposed."""
+    _need(X, torch.bfloat16, "X")
+    _need(packed, torch.uint8, "packed")
+    _need(Y, torch.bfloat16, "Y")
+    if X.numel() < M * K or Y.numel() < M * N:
+        raise ValueError("X or Y too small")
+    _check(lib.lowbit_gemm_int4(_ptr(X), _ptr(packed), M, N, K, _ptr(Y), _stream(stream)),
+           "lowbit_gemm_int4")
+
+
+def lowbit_gemm_binplane(X, packed, P, M, N, K, Y, stream=None):
+    """Y bf16 [M][N] = X bf16 [M][K] times the packed binary-plane weights, transposed."""
+    _need(X, torch.bfloat16, "X")
+    _need(packed, torch.uint8, "packed")
+    _need(Y, torch.bfloat16, "Y")
+    if X.numel() < M * K or Y.numel() < M * N:
+        raise ValueError("X or Y too small")
+    _check(lib.lowbit_gemm_binplane(_ptr(X), _ptr(packed), P, M, N, K, _ptr(Y), _stream(stream)),
+           "lowbit_gemm_binplane")
+
+
+def lmhead_argmax_verify(H, packed_head, M, N, K, draft, argmax, n_accept, bonus, workspace,
+                         stream=None):
+    """Fused LM-head argmax over N vocabulary rows plus greedy prefix acceptance."""
+    _need(H, torch.bfloat16, "H")
+    _need(packed_head, torch.uint8, "packed_head")
+    for t, nm in ((draft, "draft"), (argmax, "argmax"), (n_accept, "n_accept"), (bonus, "bonus")):
+        _need(t, torch.int32, nm)
+    _need(workspace, torch.uint8, "workspace")
+    if H.numel() < M * K or draft.numel() < M - 1 or argmax.numel() < M:
+        raise ValueError("H, draft or argmax too small")
+    _check(lib.lmhead_argmax_verify(_ptr(H), _ptr(packed_head), M, N, K, _ptr(draft), _ptr(argmax),
+                                    _ptr(n_accept), _ptr(bonus), _ptr(workspace),
+                                    workspace.numel(), _stream(stream)), "lmhead_argmax_verify")
+
+
+def lowbit_device_error(stream=None) -> int:
+    """Synchronise and return (then clear) the device's recorded kernel-side error."""
+    out = ctypes.c_int(0)
+    _check(lib.lowbit_device_error(_stream(stream), ctypes.byref(out)), "lowbit_device_error")
+    return out.value

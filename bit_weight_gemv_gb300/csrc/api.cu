@@ -1,0 +1,166 @@
+// extern "C" entry points of liblowbit.so: host-side validation, then kernel dispatch.
+// Declarations and the full contract are in include/lowbit.h.
+#include <string.h>
+
+#include "common.cuh"
+
+namespace lowbit {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxK = 65536;
+
+// One error word per device (see lowbit_device_error).
+__device__ int g_device_error;
+int* g_err_ptr[kMaxDevices] = {nullptr};
+
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+inline lowbit_status check_shape(int M, int N, int K, int Mmax) {
+  if (K <= 0 || K % kGroup != 0 || K > kMaxK) return LOWBIT_ERR_SHAPE;
+  if (N < 1) return LOWBIT_ERR_SHAPE;
+  if (M < 1 || M > Mmax) return LOWBIT_ERR_SHAPE;
+  return LOWBIT_OK;
+}
+
+inline lowbit_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LOWBIT_OK : LOWBIT_ERR_CUDA; }
+
+}  // namespace
+
+int* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+}  // namespace lowbit
+
+using namespace lowbit;
+
+extern "C" {
+
+const char* lowbit_status_string(int status) {
+  switch (status) {
+    case LOWBIT_OK: return "ok";
+    case LOWBIT_ERR_INVALID_ARG: return "invalid argument";
+    case LOWBIT_ERR_SHAPE: return "unsupported shape";
+    case LOWBIT_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case LOWBIT_ERR_WORKSPACE: return "workspace missing or too small";
+    case LOWBIT_ERR_TIMEOUT: return "bounded in-kernel wait timed out";
+    case LOWBIT_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+int lowbit_version(void) { return 100; }
+
+size_t lowbit_int4_packed_bytes(int N, int K) {
+  if (check_shape(1, N, K, 1) != LOWBIT_OK) return 0;
+  return kHeaderBytes + int4_codes_bytes(N, K) + int4_scales_bytes(N, K);
+}
+
+size_t lowbit_binplane_packed_bytes(int P, int N, int K) {
+  if (check_shape(1, N, K, 1) != LOWBIT_OK || P < 1 || P > 8) return 0;
+  return kHeaderBytes + binplane_codes_bytes(P, N, K) + binplane_scales_bytes(P, N, K);
+}
+
+size_t lmhead_workspace_bytes(int M, int N, int K) {
+  if (M < 2 || M > 32 || N < 1 || K <= 0 || K % kGroup != 0) return 0;
+  return 512;
+}
+
+lowbit_status lowbit_pack_int4(const int8_t* codes, const uint16_t* scales, int N, int K,
+                               void* packed, void* stream) {
+  if (!codes || !scales || !packed) return LOWBIT_ERR_INVALID_ARG;
+  lowbit_status st = check_shape(1, N, K, 1);
+  if (st != LOWBIT_OK) return st;
+  if (!aligned16(codes) || !aligned16(packed)) return LOWBIT_ERR_ALIGN;
+  return from_cuda(launch_pack_int4(codes, scales, N, K, static_cast<uint8_t*>(packed),
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+lowbit_status lowbit_pack_binplane(const uint8_t* signbits, const uint16_t* alpha, int P, int N,
+                                   int K, void* packed, void* stream) {
+  if (!signbits || !alpha || !packed) return LOWBIT_ERR_INVALID_ARG;
+  lowbit_status st = check_shape(1, N, K, 1);
+  if (st != LOWBIT_OK) return st;
+  if (P < 1 || P > 8) return LOWBIT_ERR_SHAPE;
+  if (!aligned16(signbits) || !aligned16(packed)) return LOWBIT_ERR_ALIGN;
+  return from_cuda(launch_pack_binplane(signbits, alpha, P, N, K, static_cast<uint8_t*>(packed),
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+lowbit_status lowbit_validate_packed(const void* packed, int format, int P, int N, int K,
+                                     void* stream) {
+  if (!packed) return LOWBIT_ERR_INVALID_ARG;
+  PackedHeader h;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LOWBIT_ERR_CUDA;
+  if (cudaMemcpy(&h, packed, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return LOWBIT_ERR_CUDA;
+  const uint32_t want_p = (format == (int)kFormatInt4) ? 0u : (uint32_t)P;
+  const bool ok = h.magic == kMagic && h.format == (uint32_t)format && h.version == kVersion &&
+                  h.N == (uint32_t)N && h.K == (uint32_t)K && h.P == want_p &&
+                  h.group == (uint32_t)kGroup && h.row_tile == (uint32_t)kRowTile;
+  return ok ? LOWBIT_OK : LOWBIT_ERR_INVALID_ARG;
+}
+
+lowbit_status lowbit_gemm_int4(const uint16_t* X, const void* packed, int M, int N, int K,
+                               uint16_t* Y, void* stream) {
+  if (!X || !packed || !Y) return LOWBIT_ERR_INVALID_ARG;
+  lowbit_status st = check_shape(M, N, K, 32);
+  if (st != LOWBIT_OK) return st;
+  if (!aligned16(X) || !aligned16(packed)) return LOWBIT_ERR_ALIGN;
+  int* err = device_error_word();
+  if (!err) return LOWBIT_ERR_CUDA;
+  const uint8_t* pk = static_cast<const uint8_t*>(packed);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (M == 1) return from_cuda(launch_int4_gemv(X, pk, N, K, Y, err, s));
+  return from_cuda(launch_int4_gemm_cc(X, pk, M, N, K, Y, err, s));
+}
+
+lowbit_status lowbit_gemm_binplane(const uint16_t* X, const void* packed, int P, int M, int N,
+                                   int K, uint16_t* Y, void* stream) {
+  if (!X || !packed || !Y) return LOWBIT_ERR_INVALID_ARG;
+  lowbit_status st = check_shape(M, N, K, 32);
+  if (st != LOWBIT_OK) return st;
+  if (P < 1 || P > 8) return LOWBIT_ERR_SHAPE;
+  if (!aligned16(X) || !aligned16(packed)) return LOWBIT_ERR_ALIGN;
+  int* err = device_error_word();
+  if (!err) return LOWBIT_ERR_CUDA;
+  return from_cuda(launch_binplane_cc(X, static_cast<const uint8_t*>(packed), P, M, N, K, Y, err,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+lowbit_status lmhead_argmax_verify(const uint16_t* H, const void* packed_head, int M, int N,
+                                   int K, const int32_t* draft, int32_t* argmax,
+                                   int32_t* n_accept, int32_t* bonus, void* workspace,
+                                   size_t ws_bytes, void* stream) {
+  if (!H || !packed_head || !draft || !argmax || !n_accept || !bonus) return LOWBIT_ERR_INVALID_ARG;
+  lowbit_status st = check_shape(M, N, K, 32);
+  if (st != LOWBIT_OK) return st;
+  if (M < 2) return LOWBIT_ERR_SHAPE;
+  if (!workspace || ws_bytes < lmhead_workspace_bytes(M, N, K)) return LOWBIT_ERR_WORKSPACE;
+  if (!aligned16(H) || !aligned16(packed_head) || !aligned16(workspace)) return LOWBIT_ERR_ALIGN;
+  int* err = device_error_word();
+  if (!err) return LOWBIT_ERR_CUDA;
+  return from_cuda(launch_lmhead_cc(H, static_cast<const uint8_t*>(packed_head), M, N, K, draft,
+                                    argmax, n_accept, bonus, workspace, err,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+lowbit_status lowbit_device_error(void* stream, int* status_out) {
+  if (!status_out) return LOWBIT_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LOWBIT_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return LOWBIT_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return LOWBIT_ERR_CUDA;
+  *status_out = v;
+  return LOWBIT_OK;
+}
+
+}  // extern "C"

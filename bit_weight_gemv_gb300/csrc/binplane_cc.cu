@@ -1,0 +1,140 @@
+// Binary-plane (ShiftAdd) weight multiply on the CUDA cores.
+//
+//   y[m][n] = sum_p sum_g alpha[p][n][g] * sum_{k in g} b[p][n][k] * x[m][k],  b in {-1,+1}
+// (ShiftAddQwen README, introduction and "Method": a mat-vec is a sign-select-and-add per
+// plane plus one scale per group).
+//
+// Same work split as the INT4 CUDA-core kernel: one CTA per 32-row tile, warps split the
+// groups of a K segment, lane r owns row 32*tile + r and reads its 16 bytes of signs per
+// (group, plane) as part of one contiguous 512-byte warp load.  The sign select is an XOR
+// of the plane bit into the sign bit of the bf16 activation pair; the selected values are
+// added into fp32 and scaled once per (plane, group).
+#include "common.cuh"
+
+namespace lowbit {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+
+template <int MT>
+struct BpSeg {
+  static constexpr int kSeg = (MT <= 4) ? 16 : (MT <= 16 ? 8 : 4);
+};
+
+template <int MT>
+__global__ void __launch_bounds__(kThreads)
+binplane_cc_kernel(const uint16_t* __restrict__ X, const uint8_t* __restrict__ packed, int P,
+                   int M, int N, int K, uint16_t* __restrict__ Y, int* __restrict__ err) {
+  constexpr int SEG = BpSeg<MT>::kSeg;
+  __shared__ __align__(16) uint16_t xs[MT * SEG * kGroup];
+  __shared__ float red[kWarps * 32 * (MT < 8 ? MT : 8)];
+  __shared__ int ok;
+  const int G = K / kGroup;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x;
+
+  if (threadIdx.x == 0)
+    ok = header_matches(reinterpret_cast<const PackedHeader*>(packed), kFormatBinplane, P, N, K);
+  __syncthreads();
+  if (!ok) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) record_error(err, LOWBIT_ERR_INVALID_ARG);
+    return;
+  }
+  const uint4* codes = reinterpret_cast<const uint4*>(packed + kHeaderBytes) +
+                       (size_t)tile * G * P * kRowTile + lane;
+  const uint16_t* alphas = reinterpret_cast<const uint16_t*>(
+                               packed + kHeaderBytes + binplane_codes_bytes(P, N, K)) +
+                           (size_t)tile * G * P * kRowTile + lane;
+
+  float total[MT];
+#pragma unroll
+  for (int t = 0; t < MT; ++t) total[t] = 0.f;
+
+  for (int s0 = 0; s0 < G; s0 += SEG) {
+    const int sg = min(SEG, G - s0);
+    __syncthreads();
+    const int vec_per_row = sg * kGroup / 8;
+    for (int i = threadIdx.x; i < MT * vec_per_row; i += kThreads) {
+      const int t = i / vec_per_row, v = i % vec_per_row;
+      uint4 val = make_uint4(0, 0, 0, 0);
+      if (t < M) val = __ldg(reinterpret_cast<const uint4*>(X + (size_t)t * K + (size_t)s0 * kGroup) + v);
+      reinterpret_cast<uint4*>(xs + t * SEG * kGroup)[v] = val;
+    }
+    __syncthreads();
+    for (int gl = warp; gl < sg; gl += kWarps) {
+      const int g = s0 + gl;
+      for (int p = 0; p < P; ++p) {
+        const size_t unit = ((size_t)g * P + p) * kRowTile;
+        const uint4 wv = ld_stream(codes + unit);
+        const float a = half_bits_to_float(__ldg(alphas + unit));
+        const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
+        float acc[MT];
+#pragma unroll
+        for (int t = 0; t < MT; ++t) acc[t] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t nw = ~w4[j];
+#pragma unroll
+          for (int i4 = 0; i4 < 4; ++i4) {
+            uint32_t m[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int i = 4 * i4 + e;       // pair i: inputs k0 + 2i (low) and k0 + 2i + 1 (high)
+              m[e] = (nw << (15 - i)) & 0x80008000u;  // sign flip where the plane bit is 0
+            }
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+              const uint4 xp = *reinterpret_cast<const uint4*>(
+                  xs + t * SEG * kGroup + gl * kGroup + 32 * j + 8 * i4);
+              float lo = 0.f, hi = 0.f;
+              fma_bf16x2_f32(lo, hi, xp.x ^ m[0], 0x3F803F80u);
+              fma_bf16x2_f32(lo, hi, xp.y ^ m[1], 0x3F803F80u);
+              fma_bf16x2_f32(lo, hi, xp.z ^ m[2], 0x3F803F80u);
+              fma_bf16x2_f32(lo, hi, xp.w ^ m[3], 0x3F803F80u);
+              acc[t] += lo + hi;
+            }
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < MT; ++t) total[t] = fmaf(a, acc[t], total[t]);
+      }
+    }
+  }
+  constexpr int TB = MT < 8 ? MT : 8;
+  const int n = tile * kRowTile + lane;
+#pragma unroll
+  for (int t0 = 0; t0 < MT; t0 += TB) {
+    __syncthreads();
+#pragma unroll
+    for (int t = 0; t < TB; ++t) red[(t * kWarps + warp) * 32 + lane] = total[t0 + t];
+    __syncthreads();
+    for (int t = warp; t < TB; t += kWarps) {
+      float y = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) y += red[(t * kWarps + w) * 32 + lane];
+      if (n < N && t0 + t < M) Y[(size_t)(t0 + t) * N + n] = float_to_bf16_bits(y);
+    }
+  }
+}
+
+template <int MT>
+cudaError_t launch_bp(const uint16_t* X, const uint8_t* packed, int P, int M, int N, int K,
+                      uint16_t* Y, int* err, cudaStream_t s) {
+  binplane_cc_kernel<MT><<<(unsigned)row_tiles(N), kThreads, 0, s>>>(X, packed, P, M, N, K, Y, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_binplane_cc(const uint16_t* X, const uint8_t* packed, int P, int M, int N,
+                               int K, uint16_t* Y, int* err, cudaStream_t s) {
+  if (M <= 1) return launch_bp<1>(X, packed, P, M, N, K, Y, err, s);
+  if (M <= 2) return launch_bp<2>(X, packed, P, M, N, K, Y, err, s);
+  if (M <= 4) return launch_bp<4>(X, packed, P, M, N, K, Y, err, s);
+  if (M <= 8) return launch_bp<8>(X, packed, P, M, N, K, Y, err, s);
+  if (M <= 16) return launch_bp<16>(X, packed, P, M, N, K, Y, err, s);
+  return launch_bp<32>(X, packed, P, M, N, K, Y, err, s);
+}
+
+}  // namespace lowbit

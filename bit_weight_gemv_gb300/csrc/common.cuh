@@ -1,0 +1,119 @@
+// Internal definitions shared by the CUDA translation units of liblowbit.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/lowbit.h"
+
+namespace lowbit {
+
+// ------------------------------------------------------------------ packed layout
+constexpr uint32_t kMagic = 0x3142574Cu;  // "LWB1"
+constexpr uint32_t kFormatInt4 = 1;
+constexpr uint32_t kFormatBinplane = 2;
+constexpr uint32_t kVersion = 1;
+constexpr int kHeaderBytes = 128;
+constexpr int kGroup = 128;   // inputs per quantisation group
+constexpr int kRowTile = 32;  // weight rows per layout tile
+
+struct PackedHeader {
+  uint32_t magic, format, version, N, K, P, group, row_tile;
+  uint64_t codes_offset, codes_bytes, scales_offset, scales_bytes;
+};
+static_assert(sizeof(PackedHeader) == 64, "header layout");
+
+__host__ __device__ inline int row_tiles(int N) { return (N + kRowTile - 1) / kRowTile; }
+
+// INT4: codes [NT][K/32][32][16 B], scales [NT][K/128][32] fp16.
+__host__ __device__ inline uint64_t int4_codes_bytes(int N, int K) {
+  return (uint64_t)row_tiles(N) * kRowTile * (uint64_t)K / 2;
+}
+__host__ __device__ inline uint64_t int4_scales_bytes(int N, int K) {
+  return (uint64_t)row_tiles(N) * kRowTile * (uint64_t)(K / kGroup) * 2;
+}
+// Binary planes: codes [NT][K/128][P][32][16 B], alphas [NT][K/128][P][32] fp16.
+__host__ __device__ inline uint64_t binplane_codes_bytes(int P, int N, int K) {
+  return (uint64_t)row_tiles(N) * kRowTile * (uint64_t)P * K / 8;
+}
+__host__ __device__ inline uint64_t binplane_scales_bytes(int P, int N, int K) {
+  return (uint64_t)row_tiles(N) * kRowTile * (uint64_t)P * (K / kGroup) * 2;
+}
+
+// Kernel-side header check.  Returns true when the buffer holds (format, P, N, K).
+__device__ __forceinline__ bool header_matches(const PackedHeader* h, uint32_t format, int P,
+                                               int N, int K) {
+  const uint4 a = __ldg(reinterpret_cast<const uint4*>(h));
+  const uint4 b = __ldg(reinterpret_cast<const uint4*>(h) + 1);
+  return a.x == kMagic && a.y == format && a.z == kVersion && a.w == (uint32_t)N &&
+         b.x == (uint32_t)K && b.y == (uint32_t)P;
+}
+
+__device__ __forceinline__ void record_error(int* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+// ------------------------------------------------------------------ small device helpers
+
+// Streaming 16-byte load: weights are read once, so skip L1.
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// acc_lo += lo(a) * lo(b), acc_hi += hi(a) * hi(b): bf16 x bf16 products added into fp32
+// accumulators with one rounding each (sm_100+ mixed-precision fma).
+__device__ __forceinline__ void fma_bf16x2_f32(float& acc_lo, float& acc_hi, uint32_t a,
+                                               uint32_t b) {
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+      "mov.b32 {al, ah}, %2;\n\t"
+      "mov.b32 {bl, bh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, al, bl, %0;\n\t"
+      "fma.rn.f32.bf16 %1, ah, bh, %1;\n\t}"
+      : "+f"(acc_lo), "+f"(acc_hi)
+      : "r"(a), "r"(b));
+}
+
+// INT4 nibble pair -> bf16x2 of (128 + u_even, 128 + u_odd): the nibbles sit at bits
+// [4p, 4p+4) and [16+4p, 16+4p+4) of `word`; ORing a nibble into the low mantissa bits of
+// bf16 128.0 (0x4300) gives 128 + u exactly.
+template <int P>
+__device__ __forceinline__ uint32_t int4_pair_biased(uint32_t word) {
+  return ((word >> (4 * P)) & 0x000F000Fu) | 0x43004300u;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(((uint32_t)b) << 16);
+}
+__device__ __forceinline__ float half_bits_to_float(uint16_t h) {
+  return __half2float(__ushort_as_half(h));
+}
+// fp32 -> bf16 bits, round to nearest even.
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// ------------------------------------------------------------------ launchers (host side)
+
+int* device_error_word();  // address of the current device's error word (nullptr on failure)
+
+cudaError_t launch_pack_int4(const int8_t* codes, const uint16_t* scales, int N, int K,
+                             uint8_t* packed, cudaStream_t s);
+cudaError_t launch_pack_binplane(const uint8_t* bits, const uint16_t* alpha, int P, int N, int K,
+                                 uint8_t* packed, cudaStream_t s);
+cudaError_t launch_int4_gemv(const uint16_t* X, const uint8_t* packed, int N, int K, uint16_t* Y,
+                             int* err, cudaStream_t s);
+cudaError_t launch_int4_gemm_cc(const uint16_t* X, const uint8_t* packed, int M, int N, int K,
+                                uint16_t* Y, int* err, cudaStream_t s);
+cudaError_t launch_binplane_cc(const uint16_t* X, const uint8_t* packed, int P, int M, int N,
+                               int K, uint16_t* Y, int* err, cudaStream_t s);
+cudaError_t launch_lmhead_cc(const uint16_t* H, const uint8_t* packed, int M, int N, int K,
+                             const int32_t* draft, int32_t* argmax, int32_t* n_accept,
+                             int32_t* bonus, void* ws, int* err, cudaStream_t s);
+
+}  // namespace lowbit

@@ -1,0 +1,166 @@
+// Offline repack kernels: canonical INT4 codes / binary sign planes -> kernel layout.
+//
+// Efficient-Qwen report, section 2.1: INT4 codes under frozen symmetric per-group scales
+// (group 128), served as W4A16.  ShiftAddQwen README, "Format" and "Layout": sign planes
+// with per-group scales, written with bit-exact packing checks.  The layouts themselves are
+// this library's (see include/lowbit.h); they put the 32 rows of a tile side by side so one
+// warp's 16-byte-per-lane load of a tile chunk is a single contiguous 512-byte segment.
+#include "common.cuh"
+
+namespace lowbit {
+namespace {
+
+__device__ void write_header(uint8_t* packed, uint32_t format, int P, int N, int K,
+                             uint64_t codes_bytes, uint64_t scales_bytes) {
+  PackedHeader h;
+  h.magic = kMagic;
+  h.format = format;
+  h.version = kVersion;
+  h.N = (uint32_t)N;
+  h.K = (uint32_t)K;
+  h.P = (uint32_t)P;
+  h.group = kGroup;
+  h.row_tile = kRowTile;
+  h.codes_offset = kHeaderBytes;
+  h.codes_bytes = codes_bytes;
+  h.scales_offset = kHeaderBytes + codes_bytes;
+  h.scales_bytes = scales_bytes;
+  uint4* dst = reinterpret_cast<uint4*>(packed);
+  const uint4* src = reinterpret_cast<const uint4*>(&h);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) dst[i] = src[i];
+#pragma unroll
+  for (int i = 4; i < kHeaderBytes / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+}
+
+// One thread per 16-byte unit (tile t, chunk c, row r): 32 codes of row n, k = 32c..32c+31.
+__global__ void pack_int4_codes(const int8_t* __restrict__ codes, int N, int K,
+                                uint4* __restrict__ out, long long units) {
+  const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= units) return;
+  const int C = K / 32;
+  const int r = (int)(u % kRowTile);
+  const long long tc = u / kRowTile;
+  const int c = (int)(tc % C);
+  const long long t = tc / C;
+  const long long n = t * kRowTile + r;
+  uint32_t w[4] = {0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u};  // q = 0 padding
+  if (n < N) {
+    const uint4* src = reinterpret_cast<const uint4*>(codes + n * (long long)K + 32LL * c);
+    uint4 v0 = src[0], v1 = src[1];
+    const uint32_t b[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {  // k = 32c + 8i + e, e = 2p + o
+        const uint32_t byte = (b[(8 * i + e) / 4] >> (8 * ((8 * i + e) % 4))) & 0xFFu;
+        const uint32_t nib = (byte + 8u) & 0xFu;  // q + 8 (int8 two's complement)
+        const int p = e >> 1, o = e & 1;
+        word |= nib << (4 * p + 16 * o);
+      }
+      w[i] = word;
+    }
+  }
+  out[u] = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// One thread per (tile, group, row) scale.
+__global__ void pack_int4_scales(const uint16_t* __restrict__ scales, int N, int K,
+                                 uint16_t* __restrict__ out, long long units) {
+  const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= units) return;
+  const int G = K / kGroup;
+  const int r = (int)(u % kRowTile);
+  const long long tg = u / kRowTile;
+  const int g = (int)(tg % G);
+  const long long t = tg / G;
+  const long long n = t * kRowTile + r;
+  out[u] = (n < N) ? scales[n * G + g] : (uint16_t)0;
+}
+
+__global__ void pack_header(uint8_t* packed, uint32_t format, int P, int N, int K,
+                            unsigned long long codes_bytes, unsigned long long scales_bytes) {
+  if (threadIdx.x == 0 && blockIdx.x == 0)
+    write_header(packed, format, P, N, K, codes_bytes, scales_bytes);
+}
+
+// Even bits of a 32-bit word to its low half-word, odd bits to its high half-word.
+__device__ __forceinline__ uint32_t split_even_odd(uint32_t x) {
+  uint32_t e = x & 0x55555555u, o = (x >> 1) & 0x55555555u;
+  e = (e | (e >> 1)) & 0x33333333u;  o = (o | (o >> 1)) & 0x33333333u;
+  e = (e | (e >> 2)) & 0x0F0F0F0Fu;  o = (o | (o >> 2)) & 0x0F0F0F0Fu;
+  e = (e | (e >> 4)) & 0x00FF00FFu;  o = (o | (o >> 4)) & 0x00FF00FFu;
+  e = (e | (e >> 8)) & 0x0000FFFFu;  o = (o | (o >> 8)) & 0x0000FFFFu;
+  return e | (o << 16);
+}
+
+// One thread per 16-byte unit (tile t, group g, plane p, row r).
+__global__ void pack_binplane_codes(const uint8_t* __restrict__ bits, int P, int N, int K,
+                                    uint4* __restrict__ out, long long units) {
+  const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= units) return;
+  const int G = K / kGroup;
+  const int r = (int)(u % kRowTile);
+  long long rest = u / kRowTile;
+  const int p = (int)(rest % P);
+  rest /= P;
+  const int g = (int)(rest % G);
+  const long long t = rest / G;
+  const long long n = t * kRowTile + r;
+  uint4 v = make_uint4(0, 0, 0, 0);  // padding rows: all signs -1
+  if (n < N) {
+    const uint4 c = *reinterpret_cast<const uint4*>(bits + ((long long)p * N + n) * (K / 8) +
+                                                    16LL * g);
+    v = make_uint4(split_even_odd(c.x), split_even_odd(c.y), split_even_odd(c.z),
+                   split_even_odd(c.w));
+  }
+  out[u] = v;
+}
+
+__global__ void pack_binplane_alpha(const uint16_t* __restrict__ alpha, int P, int N, int K,
+                                    uint16_t* __restrict__ out, long long units) {
+  const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= units) return;
+  const int G = K / kGroup;
+  const int r = (int)(u % kRowTile);
+  long long rest = u / kRowTile;
+  const int p = (int)(rest % P);
+  rest /= P;
+  const int g = (int)(rest % G);
+  const long long t = rest / G;
+  const long long n = t * kRowTile + r;
+  out[u] = (n < N) ? alpha[((long long)p * N + n) * G + g] : (uint16_t)0;
+}
+
+inline unsigned blocks_for(long long units, int threads) {
+  return (unsigned)((units + threads - 1) / threads);
+}
+
+}  // namespace
+
+cudaError_t launch_pack_int4(const int8_t* codes, const uint16_t* scales, int N, int K,
+                             uint8_t* packed, cudaStream_t s) {
+  const uint64_t cb = int4_codes_bytes(N, K), sb = int4_scales_bytes(N, K);
+  const long long cu = (long long)(cb / 16), su = (long long)(sb / 2);
+  pack_header<<<1, 32, 0, s>>>(packed, kFormatInt4, 0, N, K, cb, sb);
+  pack_int4_codes<<<blocks_for(cu, 256), 256, 0, s>>>(
+      codes, N, K, reinterpret_cast<uint4*>(packed + kHeaderBytes), cu);
+  pack_int4_scales<<<blocks_for(su, 256), 256, 0, s>>>(
+      scales, N, K, reinterpret_cast<uint16_t*>(packed + kHeaderBytes + cb), su);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_binplane(const uint8_t* bits, const uint16_t* alpha, int P, int N, int K,
+                                 uint8_t* packed, cudaStream_t s) {
+  const uint64_t cb = binplane_codes_bytes(P, N, K), sb = binplane_scales_bytes(P, N, K);
+  const long long cu = (long long)(cb / 16), su = (long long)(sb / 2);
+  pack_header<<<1, 32, 0, s>>>(packed, kFormatBinplane, P, N, K, cb, sb);
+  pack_binplane_codes<<<blocks_for(cu, 256), 256, 0, s>>>(
+      bits, P, N, K, reinterpret_cast<uint4*>(packed + kHeaderBytes), cu);
+  pack_binplane_alpha<<<blocks_for(su, 256), 256, 0, s>>>(
+      alpha, P, N, K, reinterpret_cast<uint16_t*>(packed + kHeaderBytes + cb), su);
+  return cudaGetLastError();
+}
+
+}  // namespace lowbit

@@ -1,0 +1,76 @@
+// Vocabulary argmax and greedy prefix acceptance, fused into the LM-head multiply.
+//
+// Small-vocabulary MTP study, section 3.3: drafts are verified against the full vocabulary,
+// so outputs stay exact.  DFlash summary, section 4.1: a step accepts tau in [1, gamma+1]
+// tokens; section 6 item 2: the drafter conditions on the last target-verified ("bonus")
+// token.  Efficient-Qwen report, section 2.2: the target verifies the drafts in parallel.
+//
+// Reduction scheme (no spin-waits): each CTA reduces its rows to one (logit, row) key per
+// token and folds it into a 64-bit atomicMax; the last CTA to finish (an atomic counter)
+// reads the winners, applies the prefix rule and zeroes the workspace for the next call.
+#pragma once
+
+#include "common.cuh"
+
+namespace lowbit {
+
+struct LmheadWorkspace {
+  unsigned long long keys[32];  // per token: order-preserving logit bits << 32 | ~row
+  unsigned int counter;         // CTAs that have folded in their keys
+  unsigned int pad[63];
+};
+static_assert(sizeof(LmheadWorkspace) == 512, "workspace layout");
+
+// Larger key <=> larger logit; among equal logits, the lower row index wins.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int n) {
+  uint32_t u = __float_as_uint(v);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)n);
+}
+
+__device__ __forceinline__ int argmax_key_row(unsigned long long k) {
+  return (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
+}
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long k) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, k, o);
+    k = other > k ? other : k;
+  }
+  return k;
+}
+
+// Called by every thread of every CTA once the CTA's atomicMax calls have been issued.
+// The last CTA writes argmax[0..M), n_accept, bonus and resets the workspace.
+__device__ __forceinline__ void lmhead_finish(LmheadWorkspace* ws, int M,
+                                              const int32_t* __restrict__ draft,
+                                              int32_t* __restrict__ argmax,
+                                              int32_t* __restrict__ n_accept,
+                                              int32_t* __restrict__ bonus) {
+  __shared__ int is_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned int total = gridDim.x * gridDim.y * gridDim.z;
+    is_last = (atomicAdd(&ws->counter, 1u) == total - 1);
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  if (threadIdx.x == 0) {
+    int a[32];
+    for (int t = 0; t < M; ++t) {
+      const unsigned long long k = atomicExch(&ws->keys[t], 0ull);
+      a[t] = argmax_key_row(k);
+      argmax[t] = a[t];
+    }
+    int n = 0;
+    while (n < M - 1 && draft[n] == a[n]) ++n;
+    *n_accept = n;
+    *bonus = a[n];
+    atomicExch(&ws->counter, 0u);
+  }
+}
+
+}  // namespace lowbit

@@ -1,0 +1,152 @@
+/*
+ * lowbit.h -- C ABI of liblowbit.so: weight-only low-bit GEMV/GEMM for speculative decoding
+ * on GB300 (sm_103a).
+ *
+ * The library multiplies bf16 activation rows X[M][K] (M = 1 for plain decoding, M = 16 for
+ * verifying a 16-token draft block) by a weight matrix W[N][K] stored in one of two low-bit
+ * formats, and can fuse the vocabulary argmax and greedy draft acceptance into the LM-head
+ * multiply.  Y = X * W^T is bf16 [M][N], accumulated in fp32.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers are DEVICE pointers unless the comment says otherwise.  bf16 and fp16 arrays
+ *     are passed as uint16_t bit patterns.  Arrays are dense and row-major.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Every
+ *     call only enqueues work on `stream` and returns; results are ready when the stream is.
+ *   - The caller owns and allocates all memory; the library never allocates device memory.
+ *   - Arguments are validated on the host before anything is enqueued; on error nothing is
+ *     enqueued and no output is touched.  A CUDA launch error returns LOWBIT_ERR_CUDA.
+ *   - K must be a multiple of 128 (the quantisation group).  N >= 1 is arbitrary.
+ *   - Packed weight buffers start with a 128-byte header (magic, format, N, K, P).  Kernels
+ *     check it against the call's arguments; on a mismatch they touch nothing else, write
+ *     no output and record LOWBIT_ERR_INVALID_ARG in a per-device error word that
+ *     lowbit_device_error() returns.  lowbit_validate_packed() checks a header synchronously.
+ *   - No C++ exception crosses this interface.
+ */
+#ifndef LOWBIT_H
+#define LOWBIT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum lowbit_status {
+  LOWBIT_OK = 0,
+  LOWBIT_ERR_INVALID_ARG = 1, /* null pointer, negative size, wrong packed header */
+  LOWBIT_ERR_SHAPE = 2,       /* K % 128 != 0, M outside 1..32, P outside 1..8, N < 1 */
+  LOWBIT_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
+  LOWBIT_ERR_WORKSPACE = 4,   /* workspace missing or smaller than lmhead_workspace_bytes() */
+  LOWBIT_ERR_TIMEOUT = 5,     /* a bounded in-kernel wait gave up (recorded on the device) */
+  LOWBIT_ERR_CUDA = 6         /* a CUDA runtime call or launch failed */
+} lowbit_status;
+
+/* Short English description of a status code (static string, never NULL). */
+const char* lowbit_status_string(int status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int lowbit_version(void);
+
+/* ------------------------------------------------------------------------------------------
+ * Sizes (host-only, no CUDA call).  Return 0 for invalid shapes.
+ */
+
+/* Bytes of a packed INT4 buffer: 128-byte header + ceil(N/32)*32 rows of K/2 code bytes and
+ * K/64 scale bytes.  For N a multiple of 32 the payload is exactly N*K/2 + N*K/64 bytes. */
+size_t lowbit_int4_packed_bytes(int N, int K);
+
+/* Bytes of a packed binary-plane buffer: header + ceil(N/32)*32 rows of P*K/8 sign bytes and
+ * P*K/64 plane-scale bytes. */
+size_t lowbit_binplane_packed_bytes(int P, int N, int K);
+
+/* Bytes of the workspace lmhead_argmax_verify() needs (independent of N and K). */
+size_t lmhead_workspace_bytes(int M, int N, int K);
+
+/* ------------------------------------------------------------------------------------------
+ * Offline repack (Efficient-Qwen report, section 2.1: codes rounded onto the INT4 grid under
+ * frozen symmetric per-group scales, served as W4A16; ShiftAddQwen README, "Format" and
+ * "Layout": binary planes with per-group scales and bit-exact packing).
+ */
+
+/* Repack canonical INT4 weights into the kernel layout.
+ *   codes  : int8 [N][K], values in [-8, 7] (q of w = s*q); 16-byte aligned.  Values outside
+ *            the range are out of contract: they are stored modulo 16.
+ *   scales : fp16 [N][K/128], one symmetric scale per row and group of 128 inputs.
+ *   packed : lowbit_int4_packed_bytes(N, K) bytes, 16-byte aligned; fully overwritten.
+ * Layout of `packed` (little-endian): the header, then codes in row tiles of 32 rows (padding
+ * rows hold q = 0, scale 0): for tile t, 32-input chunk c and row r = n % 32 the 16 bytes at
+ * ((t*(K/32) + c)*32 + r)*16 hold k = 32c..32c+31 as four u32 words, word i holding
+ * k = 32c + 8i + 2p + o (p = 0..3, o = 0..1) as the nibble q + 8 at bit 4p + 16o; then the
+ * fp16 scales, s[n][g] at ((t*(K/128) + g)*32 + r)*2 after the codes. */
+lowbit_status lowbit_pack_int4(const int8_t* codes, const uint16_t* scales, int N, int K,
+                               void* packed, void* stream);
+
+/* Repack canonical binary planes (w = sum_p alpha_p * b_p, b in {-1,+1}).
+ *   signbits : uint8 [P][N][K/8]; bit j (LSB first) of byte i is input k = 8i + j; 1 = +1.
+ *   alpha    : fp16 [P][N][K/128], one scale per plane, row and group of 128 inputs.
+ *   packed   : lowbit_binplane_packed_bytes(P, N, K) bytes, 16-byte aligned.
+ * Layout: header, then for tile t, group g, plane p, row r the 16 bytes at
+ * (((t*(K/128) + g)*P + p)*32 + r)*16 hold the 128 signs of k = 128g.. as four u32 words;
+ * word w covers k0 = 128g + 32w with bit i = sign of k0 + 2i and bit 16 + i = sign of
+ * k0 + 2i + 1; then alpha[p][n][g] (fp16) at (((t*(K/128) + g)*P + p)*32 + r)*2. */
+lowbit_status lowbit_pack_binplane(const uint8_t* signbits, const uint16_t* alpha, int P, int N,
+                                   int K, void* packed, void* stream);
+
+/* Synchronous check (copies the 128-byte header to the host after synchronising `stream`)
+ * that `packed` holds format `format` (1 = INT4, 2 = binary planes) with these P, N, K.
+ * Returns LOWBIT_OK or LOWBIT_ERR_INVALID_ARG. */
+lowbit_status lowbit_validate_packed(const void* packed, int format, int P, int N, int K,
+                                     void* stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Multiplies.
+ */
+
+/* Y = X * W^T for symmetric per-group INT4 weights (Efficient-Qwen report, section 2.1):
+ *   y[m][n] = sum_g s[n][g] * sum_{k in g} q[n][k] * x[m][k], fp32 accumulation, each
+ *   output rounded once to bf16 (nearest, ties to even).
+ *   X : bf16 [M][K], 16-byte aligned.   packed : from lowbit_pack_int4(N, K).
+ *   Y : bf16 [M][N], written in full.   1 <= M <= 32.
+ * M = 1 runs the streaming GEMV; M >= 2 runs the tensor-core skinny GEMM. */
+lowbit_status lowbit_gemm_int4(const uint16_t* X, const void* packed, int M, int N, int K,
+                               uint16_t* Y, void* stream);
+
+/* Y = X * W^T for binary-plane weights (ShiftAddQwen README, "Method" and "Format"):
+ *   y[m][n] = sum_p sum_g alpha[p][n][g] * sum_{k in g} b[p][n][k] * x[m][k].
+ *   Shapes and rounding as lowbit_gemm_int4; packed from lowbit_pack_binplane(P, N, K). */
+lowbit_status lowbit_gemm_binplane(const uint16_t* X, const void* packed, int P, int M, int N,
+                                   int K, uint16_t* Y, void* stream);
+
+/* LM-head verify step (small-vocabulary MTP study, section 3.3: full-vocabulary verification;
+ * DFlash summary, section 4.1: tau in [1, gamma + 1]; Efficient-Qwen report, section 2.2).
+ *   H        : bf16 [M][K] hidden rows of one verify block, 2 <= M <= 32 (M - 1 drafts).
+ *   packed_head : INT4 head from lowbit_pack_int4(N, K), N = vocabulary rows.
+ *   draft    : int32 [M-1] draft token ids for positions 1..M-1 of the block.
+ *   argmax   : int32 [M] out: a[m] = argmax_n logit[m][n] over fp32 logits (never rounded),
+ *              lowest index on ties.  Logits are not written anywhere.
+ *   n_accept : int32 [1] out: n = largest j <= M-1 with draft[i] == a[i] for all i < j.
+ *   bonus    : int32 [1] out: a[n], the target's token after the accepted prefix.
+ *   workspace: lmhead_workspace_bytes(M, N, K) bytes, 16-byte aligned, ZERO-FILLED ONCE
+ *              before first use; every call leaves it zero again.  Calls that share a
+ *              workspace must not overlap on the GPU.  After a failed call, re-zero it. */
+lowbit_status lmhead_argmax_verify(const uint16_t* H, const void* packed_head, int M, int N,
+                                   int K, const int32_t* draft, int32_t* argmax,
+                                   int32_t* n_accept, int32_t* bonus, void* workspace,
+                                   size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Device-side error word.
+ */
+
+/* Synchronises `stream`, then returns (in *status_out) and clears the current device's
+ * error word: LOWBIT_OK, LOWBIT_ERR_INVALID_ARG (a kernel found a packed header that did not
+ * match its arguments) or LOWBIT_ERR_TIMEOUT (a bounded wait gave up).  The function's own
+ * return value reports failures of the query itself. */
+lowbit_status lowbit_device_error(void* stream, int* status_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LOWBIT_H */

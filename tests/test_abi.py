@@ -1,0 +1,80 @@
+"""CPU checks of the C ABI: the library loads, exports every function include/lowbit.h
+declares, and its host-only size/status queries behave as documented.  No kernel runs."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lowbit.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_weight_gemv_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M)
+    return sorted({n for n in names if n not in ("if", "defined")})
+
+
+def test_header_declares_the_five_entry_points():
+    names = declared_functions()
+    for n in ("lowbit_pack_int4", "lowbit_pack_binplane", "lowbit_gemm_int4",
+              "lowbit_gemm_binplane", "lmhead_argmax_verify"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_sizes_and_status_strings(lib):
+    lib.lowbit_int4_packed_bytes.restype = ctypes.c_size_t
+    lib.lowbit_binplane_packed_bytes.restype = ctypes.c_size_t
+    lib.lmhead_workspace_bytes.restype = ctypes.c_size_t
+    lib.lowbit_status_string.restype = ctypes.c_char_p
+    # one 4B-class layer's INT4 projections: 50,012,160 payload bytes + 7 headers
+    shapes = [(2560, 4096), (2560, 1024), (2560, 1024), (2560, 2560), (2560, 9728),
+              (2560, 9728), (9728, 2560)]
+    total = sum(lib.lowbit_int4_packed_bytes(n, k) - 128 for k, n in shapes)
+    assert total == 50_012_160
+    assert lib.lowbit_int4_packed_bytes(248_320, 4096) - 128 == 524_451_840
+    assert lib.lowbit_int4_packed_bytes(32_768, 4096) - 128 == 69_206_016
+    assert lib.lowbit_binplane_packed_bytes(3, 12288, 4096) - 128 == 21_233_664
+    assert lib.lowbit_binplane_packed_bytes(4, 4096, 12288) - 128 == 28_311_552
+    # ragged rows are padded to the 32-row tile
+    assert lib.lowbit_int4_packed_bytes(33, 128) == 128 + 64 * 64 + 64 * 2
+    assert lib.lowbit_int4_packed_bytes(10, 100) == 0          # K not a multiple of 128
+    assert lib.lowbit_binplane_packed_bytes(9, 32, 128) == 0   # P > 8
+    assert lib.lmhead_workspace_bytes(16, 248_320, 4096) == 512
+    assert lib.lmhead_workspace_bytes(1, 10, 128) == 0
+    for s in range(7):
+        assert lib.lowbit_status_string(s)
+    assert lib.lowbit_status_string(0) == b"ok"
+
+
+def test_host_validation_rejects_before_any_launch(lib):
+    # Null pointers and bad shapes are rejected on the host; nothing reaches the GPU.
+    vp = ctypes.c_void_p
+    f = lib.lowbit_gemm_int4
+    f.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp]
+    assert f(None, None, 1, 64, 128, None, None) == 1            # invalid argument
+    fake = vp(0x1000)
+    assert f(fake, fake, 1, 64, 100, fake, None) == 2            # K % 128
+    assert f(fake, fake, 33, 64, 128, fake, None) == 2           # M > 32
+    assert f(vp(0x1008), fake, 1, 64, 128, fake, None) == 3      # X misaligned
+    g = lib.lmhead_argmax_verify
+    g.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp,
+                  ctypes.c_size_t, vp]
+    assert g(fake, fake, 16, 64, 128, fake, fake, fake, fake, fake, 100, None) == 4  # workspace
+    assert g(fake, fake, 1, 64, 128, fake, fake, fake, fake, fake, 512, None) == 2   # M < 2

@@ -1,0 +1,227 @@
+"""GPU parity: every hot-path row through the C ABI against the CPU oracle.
+
+Inputs come from the seeded generators in ``synth``; expected values come only from
+``oracle``.  Sizes span several row tiles and a ragged tail; the full workload shapes are
+checked too (all outputs where the oracle finishes in seconds)."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import binplane as obp
+from oracle import int4 as oint4
+from oracle import verify as over
+from helpers import bf16_dev, check_argmax, check_gemm, dev, f16_dev, host_bits
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def lb():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import bit_weight_gemv_gb300 as lb
+    return lb
+
+
+def pack_int4_gpu(lb, codes, scales):
+    N, K = codes.shape
+    packed = torch.empty(lb.lowbit_int4_packed_bytes(N, K), dtype=torch.uint8, device="cuda")
+    lb.lowbit_pack_int4(dev(codes), f16_dev(scales), N, K, packed)
+    return packed
+
+
+def pack_bp_gpu(lb, bits, alpha):
+    P, N, KB = bits.shape
+    K = KB * 8
+    packed = torch.empty(lb.lowbit_binplane_packed_bytes(P, N, K), dtype=torch.uint8, device="cuda")
+    lb.lowbit_pack_binplane(dev(bits), f16_dev(alpha), P, N, K, packed)
+    return packed
+
+
+def gemm_int4_gpu(lb, x, packed, M, N, K):
+    Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lb.lowbit_gemm_int4(bf16_dev(x), packed, M, N, K, Y)
+    torch.cuda.synchronize()
+    return host_bits(Y)
+
+
+# ------------------------------------------------------------------------- packing
+
+@pytest.mark.parametrize("N,K", [(256, 512), (257, 384), (8, 128), (1, 128), (4096, 2560),
+                                 (2560, 9728)])
+def test_pack_int4_bit_exact(lb, N, K):
+    codes, scales, _ = synth.int4_problem(0, 1, N, K, 77)
+    got = pack_int4_gpu(lb, codes, scales).cpu().numpy()
+    ref = oint4.pack(codes, scales)
+    assert got.shape == ref.shape and np.array_equal(got, ref)
+    c2, s2 = oint4.unpack(got)
+    assert np.array_equal(c2, codes) and np.array_equal(s2, scales)
+    assert lb.lowbit_validate_packed(pack_int4_gpu(lb, codes, scales), 1, 0, N, K) == 0
+    assert lb.lowbit_validate_packed(pack_int4_gpu(lb, codes, scales), 1, 0, N + 1, K) == 1
+
+
+@pytest.mark.parametrize("P,N,K", [(3, 64, 256), (4, 33, 128), (1, 300, 512), (3, 12288, 4096),
+                                   (4, 4096, 12288)])
+def test_pack_binplane_bit_exact(lb, P, N, K):
+    bits, alpha, _ = synth.binplane_problem(3, P, 1, N, K, 78)
+    got = pack_bp_gpu(lb, bits, alpha).cpu().numpy()
+    ref = obp.pack(bits, alpha)
+    assert np.array_equal(got, ref)
+    b2, a2 = obp.unpack(got)
+    assert np.array_equal(b2, bits) and np.array_equal(a2, alpha)
+
+
+# ------------------------------------------------------------------------- INT4 GEMV / GEMM
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 512), (1, 257, 384), (1, 1, 128), (1, 8, 1024),
+                                   (1, 100, 12288), (2, 96, 256), (3, 65, 640), (16, 300, 1280),
+                                   (32, 33, 384), (5, 1, 128)])
+def test_int4_small_and_ragged(lb, M, N, K):
+    codes, scales, x = synth.int4_problem(0, M, N, K)
+    packed = pack_int4_gpu(lb, codes, scales)
+    y = gemm_int4_gpu(lb, x, packed, M, N, K)
+    check_gemm(y, oint4.gemm(x, codes, scales), f"int4 M={M} N={N} K={K}")
+
+
+def test_int4_config0_tiny_gemv(lb):
+    cfg = synth.CONFIGS[0]
+    (K, N), = cfg["shapes"]
+    codes, scales, x = synth.int4_problem(cfg["seed"], 1, N, K)
+    y = gemm_int4_gpu(lb, x, pack_int4_gpu(lb, codes, scales), 1, N, K)
+    check_gemm(y, oint4.gemm(x, codes, scales), "config 0")
+
+
+@pytest.mark.parametrize("proj", range(7))
+def test_int4_config1_decode_layer(lb, proj):
+    cfg = synth.CONFIGS[1]
+    K, N = cfg["shapes"][proj]
+    codes, scales, x = synth.int4_problem(cfg["seed"], 1, N, K, proj)
+    y = gemm_int4_gpu(lb, x, pack_int4_gpu(lb, codes, scales), 1, N, K)
+    check_gemm(y, oint4.gemm(x, codes, scales), f"config 1 proj {proj}")
+
+
+@pytest.mark.parametrize("M", synth.M_SWEEP)
+@pytest.mark.parametrize("proj", [0, 1, 6])
+def test_int4_config2_verify_sweep(lb, proj, M):
+    cfg = synth.CONFIGS[2]
+    K, N = cfg["shapes"][proj]
+    codes, scales, x = synth.int4_problem(cfg["seed"], M, N, K, proj)
+    y = gemm_int4_gpu(lb, x, pack_int4_gpu(lb, codes, scales), M, N, K)
+    check_gemm(y, oint4.gemm(x, codes, scales), f"config 2 proj {proj} M={M}")
+
+
+@pytest.mark.parametrize("proj", [2, 3, 4, 5])
+def test_int4_config2_remaining_projections(lb, proj):
+    cfg = synth.CONFIGS[2]
+    K, N = cfg["shapes"][proj]
+    codes, scales, x = synth.int4_problem(cfg["seed"], 16, N, K, proj)
+    y = gemm_int4_gpu(lb, x, pack_int4_gpu(lb, codes, scales), 16, N, K)
+    check_gemm(y, oint4.gemm(x, codes, scales), f"config 2 proj {proj}")
+
+
+# ------------------------------------------------------------------------- binary planes
+
+@pytest.mark.parametrize("P,M,N,K", [(3, 1, 64, 256), (4, 2, 33, 128), (1, 16, 300, 512),
+                                     (2, 5, 8, 1024), (3, 32, 40, 384)])
+def test_binplane_small_and_ragged(lb, P, M, N, K):
+    bits, alpha, x = synth.binplane_problem(3, P, M, N, K)
+    packed = pack_bp_gpu(lb, bits, alpha)
+    Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lb.lowbit_gemm_binplane(bf16_dev(x), packed, P, M, N, K, Y)
+    torch.cuda.synchronize()
+    check_gemm(host_bits(Y), obp.gemm(x, bits, alpha), f"binplane P={P} M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("shape", [0, 1])
+@pytest.mark.parametrize("P", synth.BINPLANE_PLANES)
+@pytest.mark.parametrize("M", (1, 16))
+def test_binplane_config3(lb, shape, P, M):
+    cfg = synth.CONFIGS[3]
+    K, N = cfg["shapes"][shape]
+    bits, alpha, x = synth.binplane_problem(cfg["seed"], P, M, N, K, shape)
+    packed = pack_bp_gpu(lb, bits, alpha)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    lb.lowbit_gemm_binplane(bf16_dev(x), packed, P, M, N, K, Y)
+    torch.cuda.synchronize()
+    check_gemm(host_bits(Y), obp.gemm(x, bits, alpha), f"config 3 K={K} N={N} P={P} M={M}")
+
+
+# ------------------------------------------------------------------------- LM head verify
+
+def run_lmhead(lb, h, packed, M, N, K, drafts, ws=None):
+    if ws is None:
+        ws = torch.zeros(lb.lmhead_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+    a = torch.full((M,), -1, dtype=torch.int32, device="cuda")
+    n = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    b = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    lb.lmhead_argmax_verify(bf16_dev(h), packed, M, N, K, dev(drafts.astype(np.int32)), a, n, b, ws)
+    torch.cuda.synchronize()
+    return a.cpu().numpy(), int(n.item()), int(b.item()), ws
+
+
+def check_lmhead(a, n, b, logits, drafts, j, what):
+    check_argmax(a, logits, what)
+    # acceptance is bit-exact against the prefix rule on the GPU's own argmax ...
+    assert (n, b) == over.accept(a, drafts), what
+    # ... and equals the planted j whenever rows 0..j are decided by a clear margin
+    margin = over.top2_margin(logits)
+    if np.all(margin[: j + 1] > 1e-2):
+        assert n == j, what
+
+
+@pytest.mark.parametrize("rows", synth.HEAD_ROWS)
+def test_lmhead_config4(lb, rows):
+    cfg = synth.CONFIGS[4]
+    M, K = cfg["M"], cfg["K"]
+    codes, scales, h = synth.int4_problem(cfg["seed"], M, rows, K)
+    packed = pack_int4_gpu(lb, codes, scales)
+    logits = oint4.gemm(h, codes, scales)
+    a_ref = over.argmax_lowest(logits)
+    ws = None
+    for trial, j in enumerate((None, 0, 15)):
+        drafts, jj = synth.plant_drafts(cfg["seed"] + trial, a_ref, rows, j)
+        a, n, b, ws = run_lmhead(lb, h, packed, M, rows, K, drafts, ws)
+        check_lmhead(a, n, b, logits, drafts, jj, f"config 4 N={rows} j={jj}")
+    # the workspace is left zeroed for the next call
+    assert int(ws.sum().item()) == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(2, 40, 128), (16, 1000, 512), (32, 257, 256), (7, 5, 128)])
+def test_lmhead_small_and_planted(lb, M, N, K):
+    codes, scales, h = synth.int4_problem(11, M, N, K)
+    # plant a dominant row for token 0 so at least one row is decided by construction
+    hv = h.view(np.uint16)
+    xv = (hv[0].astype(np.uint32) << 16).view(np.float32)
+    codes[N // 2] = np.where(xv > 0, 7, -8)
+    scales[N // 2] = np.float16(1.0).view(np.uint16)
+    logits = oint4.gemm(h, codes, scales)
+    a_ref = over.argmax_lowest(logits)
+    assert a_ref[0] == N // 2
+    drafts, j = synth.plant_drafts(2, a_ref, N)
+    a, n, b, _ = run_lmhead(lb, h, pack_int4_gpu(lb, codes, scales), M, N, K, drafts)
+    assert a[0] == N // 2
+    check_lmhead(a, n, b, logits, drafts, j, f"lmhead M={M} N={N}")
+
+
+# ------------------------------------------------------------------------- error paths
+
+def test_header_mismatch_is_recorded_and_nothing_written(lb):
+    codes, scales, x = synth.int4_problem(1, 1, 64, 256)
+    packed = pack_int4_gpu(lb, codes, scales)
+    assert lb.lowbit_device_error() == 0
+    Y = torch.full((1, 96), 7.0, dtype=torch.bfloat16, device="cuda")
+    lb.lowbit_gemm_int4(bf16_dev(x), packed, 1, 96, 256, Y)     # header says N = 64
+    assert lb.lowbit_device_error() == 1
+    assert torch.all(Y == 7.0)
+    assert lb.lowbit_device_error() == 0                        # cleared by the read
+
+
+def test_shape_errors_raise(lb):
+    codes, scales, x = synth.int4_problem(1, 1, 64, 256)
+    packed = pack_int4_gpu(lb, codes, scales)
+    Y = torch.empty((1, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(lb.LowbitError) as e:
+        lb.lowbit_gemm_int4(bf16_dev(x), packed, 1, 64, 200, Y)
+    assert e.value.status == 2

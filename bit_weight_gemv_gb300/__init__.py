@@ -13,6 +13,7 @@ __all__ = [
     "lowbit_binplane_packed_bytes", "lowbit_device_error", "lowbit_gemm_binplane",
     "lowbit_gemm_int4", "lowbit_int4_packed_bytes", "lowbit_pack_binplane", "lowbit_pack_int4",
     "lowbit_status_string", "lowbit_validate_packed", "lowbit_version",
+    "lowbit_gemm_int4_path", "lowbit_gemm_binplane_path", "lmhead_argmax_verify_path",
 ]
 
 

@@ -29,6 +29,9 @@ _SIGS = {
     "lowbit_gemm_int4": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp]),
     "lowbit_gemm_binplane": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp]),
     "lmhead_argmax_verify": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "lowbit_gemm_int4_path": (_i, [_vp, _vp, _i, _i, _i, _vp, _i, _vp]),
+    "lowbit_gemm_binplane_path": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _i, _vp]),
+    "lmhead_argmax_verify_path": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _sz, _i, _vp]),
     "lowbit_device_error": (_i, [_vp, ctypes.POINTER(_i)]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -111,31 +114,43 @@ def lowbit_validate_packed(packed, fmt, P, N, K, stream=None) -> int:
     return lib.lowbit_validate_packed(_ptr(packed), fmt, P, N, K, _stream(stream))
 
 
-def lowbit_gemm_int4(X, packed, M, N, K, Y, stream=None):
-    """Y bf16 [M][N] = X bf16 [M][K] times the packed INT4 weights, transposed."""
+def _gemm_args(X, packed, M, N, K, Y):
     _need(X, torch.bfloat16, "X")
     _need(packed, torch.uint8, "packed")
     _need(Y, torch.bfloat16, "Y")
     if X.numel() < M * K or Y.numel() < M * N:
         raise ValueError("X or Y too small")
+
+
+def lowbit_gemm_int4(X, packed, M, N, K, Y, stream=None):
+    """Y bf16 [M][N] = X bf16 [M][K] times the packed INT4 weights, transposed."""
+    _gemm_args(X, packed, M, N, K, Y)
     _check(lib.lowbit_gemm_int4(_ptr(X), _ptr(packed), M, N, K, _ptr(Y), _stream(stream)),
            "lowbit_gemm_int4")
 
 
+def lowbit_gemm_int4_path(X, packed, M, N, K, Y, path, stream=None):
+    """lowbit_gemm_int4 with the kernel family forced (1 = CUDA cores, 2 = tensor cores)."""
+    _gemm_args(X, packed, M, N, K, Y)
+    _check(lib.lowbit_gemm_int4_path(_ptr(X), _ptr(packed), M, N, K, _ptr(Y), path,
+                                     _stream(stream)), "lowbit_gemm_int4_path")
+
+
 def lowbit_gemm_binplane(X, packed, P, M, N, K, Y, stream=None):
     """Y bf16 [M][N] = X bf16 [M][K] times the packed binary-plane weights, transposed."""
-    _need(X, torch.bfloat16, "X")
-    _need(packed, torch.uint8, "packed")
-    _need(Y, torch.bfloat16, "Y")
-    if X.numel() < M * K or Y.numel() < M * N:
-        raise ValueError("X or Y too small")
+    _gemm_args(X, packed, M, N, K, Y)
     _check(lib.lowbit_gemm_binplane(_ptr(X), _ptr(packed), P, M, N, K, _ptr(Y), _stream(stream)),
            "lowbit_gemm_binplane")
 
 
-def lmhead_argmax_verify(H, packed_head, M, N, K, draft, argmax, n_accept, bonus, workspace,
-                         stream=None):
-    """Fused LM-head argmax over N vocabulary rows plus greedy prefix acceptance."""
+def lowbit_gemm_binplane_path(X, packed, P, M, N, K, Y, path, stream=None):
+    """lowbit_gemm_binplane with the kernel family forced (1 = CUDA cores, 2 = tensor cores)."""
+    _gemm_args(X, packed, M, N, K, Y)
+    _check(lib.lowbit_gemm_binplane_path(_ptr(X), _ptr(packed), P, M, N, K, _ptr(Y), path,
+                                         _stream(stream)), "lowbit_gemm_binplane_path")
+
+
+def _lmhead_args(H, packed_head, M, K, draft, argmax, n_accept, bonus, workspace):
     _need(H, torch.bfloat16, "H")
     _need(packed_head, torch.uint8, "packed_head")
     for t, nm in ((draft, "draft"), (argmax, "argmax"), (n_accept, "n_accept"), (bonus, "bonus")):
@@ -143,9 +158,25 @@ def lmhead_argmax_verify(H, packed_head, M, N, K, draft, argmax, n_accept, bonus
     _need(workspace, torch.uint8, "workspace")
     if H.numel() < M * K or draft.numel() < M - 1 or argmax.numel() < M:
         raise ValueError("H, draft or argmax too small")
+
+
+def lmhead_argmax_verify(H, packed_head, M, N, K, draft, argmax, n_accept, bonus, workspace,
+                         stream=None):
+    """Fused LM-head argmax over N vocabulary rows plus greedy prefix acceptance."""
+    _lmhead_args(H, packed_head, M, K, draft, argmax, n_accept, bonus, workspace)
     _check(lib.lmhead_argmax_verify(_ptr(H), _ptr(packed_head), M, N, K, _ptr(draft), _ptr(argmax),
                                     _ptr(n_accept), _ptr(bonus), _ptr(workspace),
                                     workspace.numel(), _stream(stream)), "lmhead_argmax_verify")
+
+
+def lmhead_argmax_verify_path(H, packed_head, M, N, K, draft, argmax, n_accept, bonus, workspace,
+                              path, stream=None):
+    """lmhead_argmax_verify with the kernel family forced (1 = CUDA cores, 2 = tensor cores)."""
+    _lmhead_args(H, packed_head, M, K, draft, argmax, n_accept, bonus, workspace)
+    _check(lib.lmhead_argmax_verify_path(_ptr(H), _ptr(packed_head), M, N, K, _ptr(draft),
+                                         _ptr(argmax), _ptr(n_accept), _ptr(bonus),
+                                         _ptr(workspace), workspace.numel(), path,
+                                         _stream(stream)), "lmhead_argmax_verify_path")
 
 
 def lowbit_device_error(stream=None) -> int:

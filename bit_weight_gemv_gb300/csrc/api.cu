@@ -110,7 +110,12 @@ lowbit_status lowbit_validate_packed(const void* packed, int format, int P, int 
 
 lowbit_status lowbit_gemm_int4(const uint16_t* X, const void* packed, int M, int N, int K,
                                uint16_t* Y, void* stream) {
-  if (!X || !packed || !Y) return LOWBIT_ERR_INVALID_ARG;
+  return lowbit_gemm_int4_path(X, packed, M, N, K, Y, 0, stream);
+}
+
+lowbit_status lowbit_gemm_int4_path(const uint16_t* X, const void* packed, int M, int N, int K,
+                                    uint16_t* Y, int path, void* stream) {
+  if (!X || !packed || !Y || path < 0 || path > 2) return LOWBIT_ERR_INVALID_ARG;
   lowbit_status st = check_shape(M, N, K, 32);
   if (st != LOWBIT_OK) return st;
   if (!aligned16(X) || !aligned16(packed)) return LOWBIT_ERR_ALIGN;
@@ -118,28 +123,48 @@ lowbit_status lowbit_gemm_int4(const uint16_t* X, const void* packed, int M, int
   if (!err) return LOWBIT_ERR_CUDA;
   const uint8_t* pk = static_cast<const uint8_t*>(packed);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (M == 1) return from_cuda(launch_int4_gemv(X, pk, N, K, Y, err, s));
-  return from_cuda(launch_int4_gemm_cc(X, pk, M, N, K, Y, err, s));
+  if (path == 0) path = (M == 1) ? 1 : 2;
+  if (path == 1)
+    return from_cuda(M == 1 ? launch_int4_gemv(X, pk, N, K, Y, err, s)
+                            : launch_int4_gemm_cc(X, pk, M, N, K, Y, err, s));
+  return from_cuda(launch_int4_gemm_tc(X, pk, M, N, K, Y, err, s));
 }
 
 lowbit_status lowbit_gemm_binplane(const uint16_t* X, const void* packed, int P, int M, int N,
                                    int K, uint16_t* Y, void* stream) {
-  if (!X || !packed || !Y) return LOWBIT_ERR_INVALID_ARG;
+  return lowbit_gemm_binplane_path(X, packed, P, M, N, K, Y, 0, stream);
+}
+
+lowbit_status lowbit_gemm_binplane_path(const uint16_t* X, const void* packed, int P, int M,
+                                        int N, int K, uint16_t* Y, int path, void* stream) {
+  if (!X || !packed || !Y || path < 0 || path > 2) return LOWBIT_ERR_INVALID_ARG;
   lowbit_status st = check_shape(M, N, K, 32);
   if (st != LOWBIT_OK) return st;
   if (P < 1 || P > 8) return LOWBIT_ERR_SHAPE;
   if (!aligned16(X) || !aligned16(packed)) return LOWBIT_ERR_ALIGN;
   int* err = device_error_word();
   if (!err) return LOWBIT_ERR_CUDA;
-  return from_cuda(launch_binplane_cc(X, static_cast<const uint8_t*>(packed), P, M, N, K, Y, err,
-                                      static_cast<cudaStream_t>(stream)));
+  const uint8_t* pk = static_cast<const uint8_t*>(packed);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (path == 0) path = (M == 1) ? 1 : 2;
+  if (path == 1) return from_cuda(launch_binplane_cc(X, pk, P, M, N, K, Y, err, s));
+  return from_cuda(launch_binplane_tc(X, pk, P, M, N, K, Y, err, s));
 }
 
 lowbit_status lmhead_argmax_verify(const uint16_t* H, const void* packed_head, int M, int N,
                                    int K, const int32_t* draft, int32_t* argmax,
                                    int32_t* n_accept, int32_t* bonus, void* workspace,
                                    size_t ws_bytes, void* stream) {
-  if (!H || !packed_head || !draft || !argmax || !n_accept || !bonus) return LOWBIT_ERR_INVALID_ARG;
+  return lmhead_argmax_verify_path(H, packed_head, M, N, K, draft, argmax, n_accept, bonus,
+                                   workspace, ws_bytes, 0, stream);
+}
+
+lowbit_status lmhead_argmax_verify_path(const uint16_t* H, const void* packed_head, int M, int N,
+                                        int K, const int32_t* draft, int32_t* argmax,
+                                        int32_t* n_accept, int32_t* bonus, void* workspace,
+                                        size_t ws_bytes, int path, void* stream) {
+  if (!H || !packed_head || !draft || !argmax || !n_accept || !bonus || path < 0 || path > 2)
+    return LOWBIT_ERR_INVALID_ARG;
   lowbit_status st = check_shape(M, N, K, 32);
   if (st != LOWBIT_OK) return st;
   if (M < 2) return LOWBIT_ERR_SHAPE;
@@ -147,9 +172,13 @@ lowbit_status lmhead_argmax_verify(const uint16_t* H, const void* packed_head, i
   if (!aligned16(H) || !aligned16(packed_head) || !aligned16(workspace)) return LOWBIT_ERR_ALIGN;
   int* err = device_error_word();
   if (!err) return LOWBIT_ERR_CUDA;
-  return from_cuda(launch_lmhead_cc(H, static_cast<const uint8_t*>(packed_head), M, N, K, draft,
-                                    argmax, n_accept, bonus, workspace, err,
-                                    static_cast<cudaStream_t>(stream)));
+  const uint8_t* pk = static_cast<const uint8_t*>(packed_head);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (path == 1)
+    return from_cuda(launch_lmhead_cc(H, pk, M, N, K, draft, argmax, n_accept, bonus, workspace,
+                                      err, s));
+  return from_cuda(launch_lmhead_tc(H, pk, M, N, K, draft, argmax, n_accept, bonus, workspace,
+                                    err, s));
 }
 
 lowbit_status lowbit_device_error(void* stream, int* status_out) {

@@ -112,6 +112,13 @@ cudaError_t launch_int4_gemm_cc(const uint16_t* X, const uint8_t* packed, int M,
                                 uint16_t* Y, int* err, cudaStream_t s);
 cudaError_t launch_binplane_cc(const uint16_t* X, const uint8_t* packed, int P, int M, int N,
                                int K, uint16_t* Y, int* err, cudaStream_t s);
+cudaError_t launch_int4_gemm_tc(const uint16_t* X, const uint8_t* packed, int M, int N, int K,
+                                uint16_t* Y, int* err, cudaStream_t s);
+cudaError_t launch_binplane_tc(const uint16_t* X, const uint8_t* packed, int P, int M, int N,
+                               int K, uint16_t* Y, int* err, cudaStream_t s);
+cudaError_t launch_lmhead_tc(const uint16_t* H, const uint8_t* packed, int M, int N, int K,
+                             const int32_t* draft, int32_t* argmax, int32_t* n_accept,
+                             int32_t* bonus, void* ws, int* err, cudaStream_t s);
 cudaError_t launch_lmhead_cc(const uint16_t* H, const uint8_t* packed, int M, int N, int K,
                              const int32_t* draft, int32_t* argmax, int32_t* n_accept,
                              int32_t* bonus, void* ws, int* err, cudaStream_t s);

@@ -136,6 +136,21 @@ lowbit_status lmhead_argmax_verify(const uint16_t* H, const void* packed_head, i
                                    size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Kernel-family selection (diagnostics and testing).  Same contract as the functions above,
+ * plus `path`: 0 = the library's choice, 1 = the CUDA-core streaming kernels (row per lane,
+ * in-register dequantisation, fp32 accumulation), 2 = the tensor-core kernels (dequantisation
+ * into tensor memory, tcgen05 MMA with fp32 accumulation).  Other values: INVALID_ARG.
+ */
+lowbit_status lowbit_gemm_int4_path(const uint16_t* X, const void* packed, int M, int N, int K,
+                                    uint16_t* Y, int path, void* stream);
+lowbit_status lowbit_gemm_binplane_path(const uint16_t* X, const void* packed, int P, int M,
+                                        int N, int K, uint16_t* Y, int path, void* stream);
+lowbit_status lmhead_argmax_verify_path(const uint16_t* H, const void* packed_head, int M, int N,
+                                        int K, const int32_t* draft, int32_t* argmax,
+                                        int32_t* n_accept, int32_t* bonus, void* workspace,
+                                        size_t ws_bytes, int path, void* stream);
+
+/* ------------------------------------------------------------------------------------------
  * Device-side error word.
  */
 

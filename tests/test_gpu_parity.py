@@ -40,11 +40,21 @@ def pack_bp_gpu(lb, bits, alpha):
     return packed
 
 
-def gemm_int4_gpu(lb, x, packed, M, N, K):
+def gemm_int4_gpu(lb, x, packed, M, N, K, path=0):
     Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
-    lb.lowbit_gemm_int4(bf16_dev(x), packed, M, N, K, Y)
+    lb.lowbit_gemm_int4_path(bf16_dev(x), packed, M, N, K, Y, path)
     torch.cuda.synchronize()
     return host_bits(Y)
+
+
+def gemm_bp_gpu(lb, x, packed, P, M, N, K, path=0):
+    Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lb.lowbit_gemm_binplane_path(bf16_dev(x), packed, P, M, N, K, Y, path)
+    torch.cuda.synchronize()
+    return host_bits(Y)
+
+
+PATHS = (1, 2)   # 1 = CUDA-core kernels, 2 = tensor-core kernels
 
 
 # ------------------------------------------------------------------------- packing
@@ -75,14 +85,15 @@ def test_pack_binplane_bit_exact(lb, P, N, K):
 
 # ------------------------------------------------------------------------- INT4 GEMV / GEMM
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("M,N,K", [(1, 256, 512), (1, 257, 384), (1, 1, 128), (1, 8, 1024),
                                    (1, 100, 12288), (2, 96, 256), (3, 65, 640), (16, 300, 1280),
-                                   (32, 33, 384), (5, 1, 128)])
-def test_int4_small_and_ragged(lb, M, N, K):
+                                   (32, 33, 384), (5, 1, 128), (17, 129, 2048), (16, 2000, 256)])
+def test_int4_small_and_ragged(lb, M, N, K, path):
     codes, scales, x = synth.int4_problem(0, M, N, K)
     packed = pack_int4_gpu(lb, codes, scales)
-    y = gemm_int4_gpu(lb, x, packed, M, N, K)
-    check_gemm(y, oint4.gemm(x, codes, scales), f"int4 M={M} N={N} K={K}")
+    y = gemm_int4_gpu(lb, x, packed, M, N, K, path)
+    check_gemm(y, oint4.gemm(x, codes, scales), f"int4 M={M} N={N} K={K} path={path}")
 
 
 def test_int4_config0_tiny_gemv(lb):
@@ -93,23 +104,25 @@ def test_int4_config0_tiny_gemv(lb):
     check_gemm(y, oint4.gemm(x, codes, scales), "config 0")
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("proj", range(7))
-def test_int4_config1_decode_layer(lb, proj):
+def test_int4_config1_decode_layer(lb, proj, path):
     cfg = synth.CONFIGS[1]
     K, N = cfg["shapes"][proj]
     codes, scales, x = synth.int4_problem(cfg["seed"], 1, N, K, proj)
-    y = gemm_int4_gpu(lb, x, pack_int4_gpu(lb, codes, scales), 1, N, K)
-    check_gemm(y, oint4.gemm(x, codes, scales), f"config 1 proj {proj}")
+    y = gemm_int4_gpu(lb, x, pack_int4_gpu(lb, codes, scales), 1, N, K, path)
+    check_gemm(y, oint4.gemm(x, codes, scales), f"config 1 proj {proj} path={path}")
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("M", synth.M_SWEEP)
 @pytest.mark.parametrize("proj", [0, 1, 6])
-def test_int4_config2_verify_sweep(lb, proj, M):
+def test_int4_config2_verify_sweep(lb, proj, M, path):
     cfg = synth.CONFIGS[2]
     K, N = cfg["shapes"][proj]
     codes, scales, x = synth.int4_problem(cfg["seed"], M, N, K, proj)
-    y = gemm_int4_gpu(lb, x, pack_int4_gpu(lb, codes, scales), M, N, K)
-    check_gemm(y, oint4.gemm(x, codes, scales), f"config 2 proj {proj} M={M}")
+    y = gemm_int4_gpu(lb, x, pack_int4_gpu(lb, codes, scales), M, N, K, path)
+    check_gemm(y, oint4.gemm(x, codes, scales), f"config 2 proj {proj} M={M} path={path}")
 
 
 @pytest.mark.parametrize("proj", [2, 3, 4, 5])
@@ -123,40 +136,39 @@ def test_int4_config2_remaining_projections(lb, proj):
 
 # ------------------------------------------------------------------------- binary planes
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("P,M,N,K", [(3, 1, 64, 256), (4, 2, 33, 128), (1, 16, 300, 512),
-                                     (2, 5, 8, 1024), (3, 32, 40, 384)])
-def test_binplane_small_and_ragged(lb, P, M, N, K):
+                                     (2, 5, 8, 1024), (3, 32, 40, 384), (8, 20, 130, 640)])
+def test_binplane_small_and_ragged(lb, P, M, N, K, path):
     bits, alpha, x = synth.binplane_problem(3, P, M, N, K)
     packed = pack_bp_gpu(lb, bits, alpha)
-    Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
-    lb.lowbit_gemm_binplane(bf16_dev(x), packed, P, M, N, K, Y)
-    torch.cuda.synchronize()
-    check_gemm(host_bits(Y), obp.gemm(x, bits, alpha), f"binplane P={P} M={M} N={N} K={K}")
+    y = gemm_bp_gpu(lb, x, packed, P, M, N, K, path)
+    check_gemm(y, obp.gemm(x, bits, alpha), f"binplane P={P} M={M} N={N} K={K} path={path}")
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("shape", [0, 1])
 @pytest.mark.parametrize("P", synth.BINPLANE_PLANES)
 @pytest.mark.parametrize("M", (1, 16))
-def test_binplane_config3(lb, shape, P, M):
+def test_binplane_config3(lb, shape, P, M, path):
     cfg = synth.CONFIGS[3]
     K, N = cfg["shapes"][shape]
     bits, alpha, x = synth.binplane_problem(cfg["seed"], P, M, N, K, shape)
     packed = pack_bp_gpu(lb, bits, alpha)
-    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    lb.lowbit_gemm_binplane(bf16_dev(x), packed, P, M, N, K, Y)
-    torch.cuda.synchronize()
-    check_gemm(host_bits(Y), obp.gemm(x, bits, alpha), f"config 3 K={K} N={N} P={P} M={M}")
+    y = gemm_bp_gpu(lb, x, packed, P, M, N, K, path)
+    check_gemm(y, obp.gemm(x, bits, alpha), f"config 3 K={K} N={N} P={P} M={M} path={path}")
 
 
 # ------------------------------------------------------------------------- LM head verify
 
-def run_lmhead(lb, h, packed, M, N, K, drafts, ws=None):
+def run_lmhead(lb, h, packed, M, N, K, drafts, ws=None, path=0):
     if ws is None:
         ws = torch.zeros(lb.lmhead_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
     a = torch.full((M,), -1, dtype=torch.int32, device="cuda")
     n = torch.full((1,), -1, dtype=torch.int32, device="cuda")
     b = torch.full((1,), -1, dtype=torch.int32, device="cuda")
-    lb.lmhead_argmax_verify(bf16_dev(h), packed, M, N, K, dev(drafts.astype(np.int32)), a, n, b, ws)
+    lb.lmhead_argmax_verify_path(bf16_dev(h), packed, M, N, K, dev(drafts.astype(np.int32)), a, n,
+                                 b, ws, path)
     torch.cuda.synchronize()
     return a.cpu().numpy(), int(n.item()), int(b.item()), ws
 
@@ -171,8 +183,9 @@ def check_lmhead(a, n, b, logits, drafts, j, what):
         assert n == j, what
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("rows", synth.HEAD_ROWS)
-def test_lmhead_config4(lb, rows):
+def test_lmhead_config4(lb, rows, path):
     cfg = synth.CONFIGS[4]
     M, K = cfg["M"], cfg["K"]
     codes, scales, h = synth.int4_problem(cfg["seed"], M, rows, K)
@@ -182,14 +195,16 @@ def test_lmhead_config4(lb, rows):
     ws = None
     for trial, j in enumerate((None, 0, 15)):
         drafts, jj = synth.plant_drafts(cfg["seed"] + trial, a_ref, rows, j)
-        a, n, b, ws = run_lmhead(lb, h, packed, M, rows, K, drafts, ws)
+        a, n, b, ws = run_lmhead(lb, h, packed, M, rows, K, drafts, ws, path)
         check_lmhead(a, n, b, logits, drafts, jj, f"config 4 N={rows} j={jj}")
     # the workspace is left zeroed for the next call
     assert int(ws.sum().item()) == 0
 
 
-@pytest.mark.parametrize("M,N,K", [(2, 40, 128), (16, 1000, 512), (32, 257, 256), (7, 5, 128)])
-def test_lmhead_small_and_planted(lb, M, N, K):
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("M,N,K", [(2, 40, 128), (16, 1000, 512), (32, 257, 256), (7, 5, 128),
+                                   (16, 300, 2048)])
+def test_lmhead_small_and_planted(lb, M, N, K, path):
     codes, scales, h = synth.int4_problem(11, M, N, K)
     # plant a dominant row for token 0 so at least one row is decided by construction
     hv = h.view(np.uint16)
@@ -200,19 +215,20 @@ def test_lmhead_small_and_planted(lb, M, N, K):
     a_ref = over.argmax_lowest(logits)
     assert a_ref[0] == N // 2
     drafts, j = synth.plant_drafts(2, a_ref, N)
-    a, n, b, _ = run_lmhead(lb, h, pack_int4_gpu(lb, codes, scales), M, N, K, drafts)
+    a, n, b, _ = run_lmhead(lb, h, pack_int4_gpu(lb, codes, scales), M, N, K, drafts, path=path)
     assert a[0] == N // 2
     check_lmhead(a, n, b, logits, drafts, j, f"lmhead M={M} N={N}")
 
 
 # ------------------------------------------------------------------------- error paths
 
-def test_header_mismatch_is_recorded_and_nothing_written(lb):
+@pytest.mark.parametrize("path", PATHS)
+def test_header_mismatch_is_recorded_and_nothing_written(lb, path):
     codes, scales, x = synth.int4_problem(1, 1, 64, 256)
     packed = pack_int4_gpu(lb, codes, scales)
     assert lb.lowbit_device_error() == 0
     Y = torch.full((1, 96), 7.0, dtype=torch.bfloat16, device="cuda")
-    lb.lowbit_gemm_int4(bf16_dev(x), packed, 1, 96, 256, Y)     # header says N = 64
+    lb.lowbit_gemm_int4_path(bf16_dev(x), packed, 1, 96, 256, Y, path)   # header says N = 64
     assert lb.lowbit_device_error() == 1
     assert torch.all(Y == 7.0)
     assert lb.lowbit_device_error() == 0                        # cleared by the read

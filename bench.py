@@ -153,44 +153,146 @@ def f16_dev(bits):
     return dev(bits.view(np.int16), torch.float16)
 
 
-class Layer:
-    """Packed INT4 projections of one 4B-class layer, replicated into C device copies."""
+class Workload:
+    """A timed step: a list of calls over one of C rotating device copies of the weights.
 
-    def __init__(self, lb, torch, copies: int, M: int, seed: int):
-        self.M = M
-        self.shapes = [(k, n) for _, k, n in synth.LAYER_4B]
-        self.packed = [[None] * len(self.shapes) for _ in range(copies)]
-        self.X, self.Y = [], []
-        for j, (K, N) in enumerate(self.shapes):
-            codes, scales, x = synth.int4_problem(seed, M, N, K, j)
-            p = torch.empty(lb.lowbit_int4_packed_bytes(N, K), dtype=torch.uint8, device="cuda")
-            lb.lowbit_pack_int4(dev(codes), f16_dev(scales), N, K, p)
-            for c in range(copies):
-                self.packed[c][j] = p if c == 0 else p.clone()
-            self.X.append(bf16_dev(x))
-            self.Y.append(torch.empty((M, N), dtype=torch.bfloat16, device="cuda"))
-        self.bytes = sum(algorithmic_int4_bytes(N, K) for K, N in self.shapes)
+    name, description, M, weight bytes per step, tokens per step, launches per step, the
+    dominant kernel's name, and C (copies) so that C * bytes >= 4x L2."""
 
-    def step(self, lb, c, M=None):
-        M = M or self.M
-        for j, (K, N) in enumerate(self.shapes):
-            lb.lowbit_gemm_int4(self.X[j], self.packed[c][j], M, N, K, self.Y[j])
+    def __init__(self, name, desc, kernel):
+        self.name, self.desc, self.kernel = name, desc, kernel
+        self.calls = []          # per copy: list of zero-arg callables
+        self.bytes = 0
+        self.tokens = 0
+        self.launches = 0
+        self.M = 0
+        self.host_io = None      # (inputs on device, outputs on device) for the e2e leg
+
+    def step(self, c):
+        for f in self.calls[c % len(self.calls)]:
+            f()
 
 
-def capture(torch, fn, n):
-    """One CUDA graph per rotation slot i (fn(i) enqueues one step)."""
+def _copies(p0, n, torch):
+    return [p0] + [p0.clone() for _ in range(n - 1)]
+
+
+def build_int4_layer(lb, torch, l2, M, path, seed, name, desc):
+    w = Workload(name, desc, "int4_gemv_kernel" if (M == 1 and path != 2) else "tc_gemm_kernel")
+    shapes = [(k, n) for _, k, n in synth.LAYER_4B]
+    w.bytes = sum(algorithmic_int4_bytes(N, K) for K, N in shapes)
+    C = copies_for(w.bytes, l2)
+    packs, X, Y = [], [], []
+    for j, (K, N) in enumerate(shapes):
+        codes, scales, x = synth.int4_problem(seed, M, N, K, j)
+        p = torch.empty(lb.lowbit_int4_packed_bytes(N, K), dtype=torch.uint8, device="cuda")
+        lb.lowbit_pack_int4(dev(codes), f16_dev(scales), N, K, p)
+        packs.append(_copies(p, C, torch))
+        X.append(bf16_dev(x))
+        Y.append(torch.empty((M, N), dtype=torch.bfloat16, device="cuda"))
+    for c in range(C):
+        w.calls.append([(lambda j=j, K=K, N=N, c=c: lb.lowbit_gemm_int4_path(
+            X[j], packs[j][c], M, N, K, Y[j], path)) for j, (K, N) in enumerate(shapes)])
+    w.M, w.tokens, w.launches = M, M, len(shapes)
+    w.host_io = (X, Y, lambda c, j: (packs[j][c], shapes[j]))
+    return w
+
+
+def build_binplane(lb, torch, l2, M, path, name, desc):
+    w = Workload(name, desc, "binplane_cc_kernel" if (M == 1 and path == 1) else "tc_gemm_kernel")
+    mats = []
+    for si, (K, N) in enumerate(synth.BINPLANE_SHAPES):
+        for P in synth.BINPLANE_PLANES:
+            bits, alpha, x = synth.binplane_problem(3, P, M, N, K, si)
+            p = torch.empty(lb.lowbit_binplane_packed_bytes(P, N, K), dtype=torch.uint8, device="cuda")
+            lb.lowbit_pack_binplane(dev(bits), f16_dev(alpha), P, N, K, p)
+            mats.append((P, K, N, p, bf16_dev(x), torch.empty((M, N), dtype=torch.bfloat16, device="cuda")))
+            w.bytes += algorithmic_binplane_bytes(P, N, K)
+    C = copies_for(w.bytes, l2)
+    copies = [_copies(m[3], C, torch) for m in mats]
+    for c in range(C):
+        w.calls.append([(lambda i=i, c=c: lb.lowbit_gemm_binplane_path(
+            mats[i][4], copies[i][c], mats[i][0], M, mats[i][2], mats[i][1], mats[i][5], path))
+            for i in range(len(mats))])
+    w.M, w.tokens, w.launches = M, M, len(mats)
+    return w
+
+
+def build_lmhead(lb, torch, l2, N, path, name, desc):
+    M, K = synth.VERIFY_BLOCK, synth.HEAD_K
+    w = Workload(name, desc, "tc_gemm_kernel" if path != 1 else "int4_gemm_cc_kernel")
+    codes, scales, h = synth.int4_problem(4, M, N, K)
+    p = torch.empty(lb.lowbit_int4_packed_bytes(N, K), dtype=torch.uint8, device="cuda")
+    lb.lowbit_pack_int4(dev(codes), f16_dev(scales), N, K, p)
+    del codes
+    w.bytes = algorithmic_int4_bytes(N, K)
+    C = copies_for(w.bytes, l2, 2)
+    packs = _copies(p, C, torch)
+    H = bf16_dev(h)
+    drafts = dev(np.arange(M - 1, dtype=np.int32))
+    a = torch.empty(M, dtype=torch.int32, device="cuda")
+    n1 = torch.empty(1, dtype=torch.int32, device="cuda")
+    b1 = torch.empty(1, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(lb.lmhead_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+    for c in range(C):
+        w.calls.append([lambda c=c: lb.lmhead_argmax_verify_path(H, packs[c], M, N, K, drafts, a, n1,
+                                                                 b1, ws, path)])
+    w.M, w.tokens, w.launches = M, M, 1
+    return w
+
+
+def build_workload(lb, torch, l2, name, path):
+    if name == "decode":
+        return build_int4_layer(lb, torch, l2, 1, path, 1, name,
+                                "decode W4A16 GEMV over one 4B-class layer: q,k,v,o,gate,up (K=2560) "
+                                "and down (K=9728), INT4 group 128, M=1")
+    if name == "verify":
+        return build_int4_layer(lb, torch, l2, 16, path, 2, name,
+                                "speculative-verify skinny GEMM over the same 4B-class layer, M=16")
+    if name.startswith("verify_m"):
+        M = int(name[len("verify_m"):])
+        return build_int4_layer(lb, torch, l2, M, path, 2, name,
+                                f"batch sweep: the 4B-class layer at M={M}")
+    if name == "tiny":
+        w = Workload(name, "tiny INT4 GEMV K=512 N=256 M=1", "int4_gemv_kernel")
+        codes, scales, x = synth.int4_problem(0, 1, 256, 512)
+        p = torch.empty(lb.lowbit_int4_packed_bytes(256, 512), dtype=torch.uint8, device="cuda")
+        lb.lowbit_pack_int4(dev(codes), f16_dev(scales), 256, 512, p)
+        X, Y = bf16_dev(x), torch.empty((1, 256), dtype=torch.bfloat16, device="cuda")
+        w.calls = [[lambda: lb.lowbit_gemm_int4_path(X, p, 1, 256, 512, Y, path)]]
+        w.bytes, w.M, w.tokens, w.launches = algorithmic_int4_bytes(256, 512), 1, 1, 1
+        return w
+    if name in ("binplane_m1", "binplane_m16"):
+        M = 1 if name == "binplane_m1" else 16
+        return build_binplane(lb, torch, l2, M, path, name,
+                              f"binary-plane GEMM: (K,N) in {{(4096,12288),(12288,4096)}} x P in {{3,4}}, "
+                              f"M={M}, group 128")
+    if name in ("lmhead_full", "lmhead_trim"):
+        N = synth.HEAD_ROWS[0] if name == "lmhead_full" else synth.HEAD_ROWS[1]
+        return build_lmhead(lb, torch, l2, N, path, name,
+                            f"LM-head verify: M=16, K=4096, INT4 head of N={N} rows, fused argmax + "
+                            "greedy acceptance of 15 drafts")
+    raise ValueError(name)
+
+
+WORKLOADS = ("decode", "verify", "binplane_m1", "binplane_m16", "lmhead_full", "lmhead_trim",
+             "tiny") + tuple(f"verify_m{m}" for m in synth.M_SWEEP if m not in (16,))
+
+
+def capture(torch, w, n):
+    """One CUDA graph per rotation slot (each replays one step over one weight copy)."""
     graphs = []
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
         for i in range(n):
-            fn(i)                      # eager warm-up outside capture
+            w.step(i)                  # eager warm-up outside capture
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
     for i in range(n):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, capture_error_mode="thread_local"):
-            fn(i)
+            w.step(i)
         graphs.append(g)
     torch.cuda.synchronize()
     return graphs
@@ -220,76 +322,23 @@ def copies_for(bytes_per_copy, l2_bytes, factor=4):
     return max(2, math.ceil(factor * l2_bytes / max(1, bytes_per_copy)))
 
 
-def measure_rows(lb, torch, peak, l2, budget_s=1.0):
-    """Secondary rows: M=16 verify GEMM + batch sweep, binary planes, LM head."""
+def measure_rows(lb, torch, peak, l2, names, budget_s=0.5):
+    """Secondary rows: every other workload, timed the same way (CUDA graphs, rotation)."""
     rows = {}
-
-    def run(name, bytes_per_call, calls_per_step, fns, tokens_per_step, kernel):  # noqa: E306
-        graphs = capture(torch, fns, fns.n)
+    for name, path in names:
+        w = build_workload(lb, torch, l2, name, path)
+        graphs = capture(torch, w, len(w.calls))
         t1 = time_graphs(torch, graphs, 3, 2)
         steps = max(10, int(budget_s / max(t1 / 3, 1e-6)))
         secs = time_graphs(torch, graphs, steps, 5)
         per = secs / steps
-        gbs = bytes_per_call * calls_per_step / per / 1e9
-        rows[name] = {"us_per_step": round(per * 1e6, 3), "GB_s": round(gbs, 1),
-                      "frac_of_hbm_peak": round(gbs / peak, 4), "tok_s": round(tokens_per_step / per, 1),
-                      "kernel": kernel, "steps": steps}
-        del graphs
-
-    class Fns:
-        def __init__(self, n, f):
-            self.n, self.f = n, f
-
-        def __call__(self, i):
-            self.f(i)
-
-    # config 2 and the batch sweep over the same layer
-    layer = Layer(lb, torch, copies_for(LAYER_BYTES, l2), 32, seed=2)
-    for M in synth.M_SWEEP:
-        run(f"int4_layer_M{M}", layer.bytes, 1,
-            Fns(len(layer.packed), lambda i, M=M: layer.step(lb, i, M)), M,
-            "int4_gemv" if M == 1 else "int4_gemm")
-    del layer
-    torch.cuda.empty_cache()
-
-    # config 3: binary planes
-    for (K, N) in synth.BINPLANE_SHAPES:
-        for P in synth.BINPLANE_PLANES:
-            bits, alpha, x = synth.binplane_problem(3, P, 16, N, K)
-            p0 = torch.empty(lb.lowbit_binplane_packed_bytes(P, N, K), dtype=torch.uint8, device="cuda")
-            lb.lowbit_pack_binplane(dev(bits), f16_dev(alpha), P, N, K, p0)
-            nb = algorithmic_binplane_bytes(P, N, K)
-            C = copies_for(nb, l2)
-            packs = [p0] + [p0.clone() for _ in range(C - 1)]
-            X = bf16_dev(x)
-            for M in (1, 16):
-                Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-                run(f"binplane_K{K}_N{N}_P{P}_M{M}", nb, 1,
-                    Fns(C, lambda i, M=M, Y=Y: lb.lowbit_gemm_binplane(X, packs[i], P, M, N, K, Y)),
-                    M, "binplane")
-            del packs, p0
-            torch.cuda.empty_cache()
-
-    # config 4: LM head verify
-    M, K = synth.VERIFY_BLOCK, synth.HEAD_K
-    for N in synth.HEAD_ROWS:
-        codes, scales, h = synth.int4_problem(4, M, N, K)
-        p0 = torch.empty(lb.lowbit_int4_packed_bytes(N, K), dtype=torch.uint8, device="cuda")
-        lb.lowbit_pack_int4(dev(codes), f16_dev(scales), N, K, p0)
-        del codes
-        nb = algorithmic_int4_bytes(N, K)
-        C = copies_for(nb, l2, 2)
-        packs = [p0] + [p0.clone() for _ in range(C - 1)]
-        H = bf16_dev(h)
-        drafts = dev(np.arange(M - 1, dtype=np.int32))
-        a = torch.empty(M, dtype=torch.int32, device="cuda")
-        n1 = torch.empty(1, dtype=torch.int32, device="cuda")
-        b1 = torch.empty(1, dtype=torch.int32, device="cuda")
-        ws = torch.zeros(lb.lmhead_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
-        run(f"lmhead_N{N}_M{M}", nb, 1,
-            Fns(C, lambda i: lb.lmhead_argmax_verify(H, packs[i], M, N, K, drafts, a, n1, b1, ws)),
-            M, "lmhead")
-        del packs, p0
+        gbs = w.bytes / per / 1e9
+        key = name if path == 0 else f"{name}@path{path}"
+        rows[key] = {"us_per_step": round(per * 1e6, 3), "GB_s": round(gbs, 1),
+                     "frac_of_hbm_peak": round(gbs / peak, 4), "tok_s": round(w.tokens / per, 1),
+                     "kernel": w.kernel, "launches_per_step": w.launches, "steps": steps,
+                     "weight_bytes_per_step": w.bytes}
+        del graphs, w
         torch.cuda.empty_cache()
     return rows
 
@@ -326,59 +375,68 @@ def run_ours(args):
 
     peak, peak_kind = read_peaks()
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
-    C = copies_for(LAYER_BYTES, l2)
-    layer = Layer(lb, torch, C, 1, seed=1)
-    assert layer.bytes == LAYER_BYTES
-    graphs = capture(torch, lambda i: layer.step(lb, i), C)
+    w = build_workload(lb, torch, l2, args.workload, args.path)
+    C = len(w.calls)
+    graphs = capture(torch, w, C)
 
     sampler = ClockSampler(local)
     sampler.start()
     secs = time_graphs(torch, graphs, args.steps, args.warmup, world)
     clocks = sampler.stop()
-    units = LAYER_BYTES * args.steps
+    units = w.bytes * args.steps
     rate, slowest = whole_job_rate(units, secs, world)
-    value = rate / 1e9
     per_rank_gbs = units / secs / 1e9
-    launches = 7 * args.steps
+    del graphs
 
-    # e2e through the public API with host buffers: H2D of X, 7 GEMVs, D2H of Y per step
-    Xh = [x.cpu().pin_memory() for x in layer.X]
-    Yh = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in layer.Y]
-    h2d = sum(x.numel() * 2 for x in Xh)
-    d2h = sum(y.numel() * 2 for y in Yh)
-    e2e_steps = max(20, min(args.steps, 2000))
+    # e2e through the public API with host buffers: every step copies the step's activations
+    # in from pinned host memory, runs the step's calls, and copies the outputs back.
+    e2e = None
+    if w.host_io is not None:
+        Xd, Yd, pk = w.host_io
+        Xh = [x.cpu().pin_memory() for x in Xd]
+        Yh = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in Yd]
+        h2d = sum(x.numel() * 2 for x in Xh)
+        d2h = sum(y.numel() * 2 for y in Yh)
+        e2e_steps = max(20, min(args.steps, 2000))
 
-    def e2e_step(i):
-        for j, (K, N) in enumerate(layer.shapes):
-            layer.X[j].copy_(Xh[j], non_blocking=True)
-            lb.lowbit_gemm_int4(layer.X[j], layer.packed[i % C][j], 1, N, K, layer.Y[j])
-            Yh[j].copy_(layer.Y[j], non_blocking=True)
+        def e2e_step(i):
+            for j in range(len(Xd)):
+                Xd[j].copy_(Xh[j], non_blocking=True)
+                packed, (K, N) = pk(i % C, j)
+                lb.lowbit_gemm_int4_path(Xd[j], packed, w.M, N, K, Yd[j], args.path)
+                Yh[j].copy_(Yd[j], non_blocking=True)
 
-    for i in range(5):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for i in range(e2e_steps):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    e2e_secs = time.perf_counter() - t0
-    e2e_rate, _ = whole_job_rate(LAYER_BYTES * e2e_steps, e2e_secs, world)
+        for i in range(5):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(e2e_steps):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        e2e_secs = time.perf_counter() - t0
+        e2e_rate, _ = whole_job_rate(w.bytes * e2e_steps, e2e_secs, world)
+        e2e = {"value": round(e2e_rate / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h,
+               "note": "eager API calls per step with pinned host activations/outputs"}
 
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
         with open(tpath) as f:
             tj = json.load(f)
-        ent = tj.get("int4_gemv_kernel@decode_layer")
-        if ent and ent.get("src_sha") == _src_sha("int4_cc.cu"):
+        ent = tj.get(f"{w.kernel}@{args.workload}")
+        if ent and ent.get("src_sha") == _src_sha():
             traffic = ent.get("bytes_per_launch")
 
     rows = {}
     if not args.no_rows and rank == 0:
-        rows = measure_rows(lb, torch, peak, l2)
+        names = [(n, 0) for n in WORKLOADS if n not in (args.workload, "tiny")]
+        names += [("decode", 1), ("decode", 2), ("binplane_m1", 1), ("binplane_m1", 2)]
+        names = [nm for nm in names if nm != (args.workload, args.path)]
+        rows = measure_rows(lb, torch, peak, l2, names)
 
     cpu = None
-    if rank == 0:
+    if rank == 0 and args.cpu_budget > 0:
         gbs, reps, nbytes, csecs = cpu_baseline_oracle(args.cpu_budget)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"{reps} passes of the oracle (numpy fp64 dequant + multiply) over the "
@@ -387,27 +445,24 @@ def run_ours(args):
 
     if rank == 0:
         out = {
-            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "metric": METRIC, "value": round(rate / 1e9, 2), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(slowest / args.steps * 1e3, 6), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": "decode W4A16 GEMV over one 4B-class layer: q,k,v,o,gate,up "
-                                   "(K=2560) and down (K=9728), INT4 group 128, M=1",
-                       "M": 1, "weight_bytes_per_step": LAYER_BYTES, "rotating_copies": C,
+            "config": {"workload": w.desc, "name": args.workload, "M": w.M,
+                       "weight_bytes_per_step": w.bytes, "rotating_copies": C,
                        "l2_policy": f"inputs larger than L2: {C} rotating weight copies, "
-                                    f"{C * LAYER_BYTES / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB",
-                       "replay": "per-copy CUDA graphs"},
-            "tok_s": round(args.steps * world / slowest, 1),
+                                    f"{C * w.bytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB",
+                       "replay": "per-copy CUDA graphs", "kernel_path": args.path},
+            "tok_s": round(w.tokens * args.steps * world / slowest, 1),
             "roofline": {"bound": "hbm", "achieved": round(per_rank_gbs, 2), "peak": peak,
                          "unit": "GB/s", "frac": round(per_rank_gbs / peak, 4),
-                         "peak_source": peak_kind, "traffic": traffic,
-                         "kernel": "int4_gemv_kernel",
-                         "algorithmic_bytes_per_launch": LAYER_BYTES / 7},
+                         "peak_source": peak_kind, "traffic": traffic, "kernel": w.kernel,
+                         "algorithmic_bytes_per_launch": w.bytes / w.launches,
+                         "launches_per_step": w.launches},
             "cpu_baseline": cpu,
-            "e2e": {"value": round(e2e_rate / 1e9, 2), "unit": "GB/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "note": "eager API calls per step with pinned host X/Y, 7 projections"},
-            "gpu_launches": launches,
+            "e2e": e2e,
+            "gpu_launches": w.launches * args.steps,
             "clocks": clocks,
             "rows": rows,
         }
@@ -417,11 +472,15 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def _src_sha(name):
+def _src_sha():
+    """Hash of the CUDA sources; stored traffic counters are void once it changes."""
+    import glob
     import hashlib
-    p = os.path.join(ROOT, "bit_weight_gemv_gb300", "csrc", name)
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "bit_weight_gemv_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -473,6 +532,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-rows", action="store_true", help="skip the secondary rows")
+    ap.add_argument("--workload", choices=WORKLOADS, default="decode",
+                    help="timed step (default: decode through one 4B-class layer, M=1)")
+    ap.add_argument("--path", type=int, choices=(0, 1, 2), default=0,
+                    help="kernel family: 0 library choice, 1 CUDA cores, 2 tensor cores")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing")
     args = ap.parse_args()
     if args.warmup < 3:

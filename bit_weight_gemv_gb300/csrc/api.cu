@@ -61,12 +61,12 @@ int lowbit_version(void) { return 100; }
 
 size_t lowbit_int4_packed_bytes(int N, int K) {
   if (check_shape(1, N, K, 1) != LOWBIT_OK) return 0;
-  return kHeaderBytes + int4_codes_bytes(N, K) + int4_scales_bytes(N, K);
+  return kHeaderBytes + int4_payload_bytes(N, K);
 }
 
 size_t lowbit_binplane_packed_bytes(int P, int N, int K) {
   if (check_shape(1, N, K, 1) != LOWBIT_OK || P < 1 || P > 8) return 0;
-  return kHeaderBytes + binplane_codes_bytes(P, N, K) + binplane_scales_bytes(P, N, K);
+  return kHeaderBytes + binplane_payload_bytes(P, N, K);
 }
 
 size_t lmhead_workspace_bytes(int M, int N, int K) {

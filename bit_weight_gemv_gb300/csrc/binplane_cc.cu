@@ -4,9 +4,9 @@
 // (ShiftAddQwen README, introduction and "Method": a mat-vec is a sign-select-and-add per
 // plane plus one scale per group).
 //
-// Same work split as the INT4 CUDA-core kernel: one CTA per 32-row tile, warps split the
-// groups of a K segment, lane r owns row 32*tile + r and reads its 16 bytes of signs per
-// (group, plane) as part of one contiguous 512-byte warp load.  The sign select is an XOR
+// Same work split as the INT4 CUDA-core kernel: one CTA per 32 rows (a quarter of a 128-row
+// layout tile), warps split the groups of a K segment, lane r owns row 32*cta + r and reads its
+// 16 bytes of signs per (group, plane) as part of one contiguous 512-byte warp load.  The sign select is an XOR
 // of the plane bit into the sign bit of the bf16 activation pair; the selected values are
 // added into fp32 and scaled once per (plane, group).
 #include "common.cuh"
@@ -32,7 +32,7 @@ binplane_cc_kernel(const uint16_t* __restrict__ X, const uint8_t* __restrict__ p
   __shared__ int ok;
   const int G = K / kGroup;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x;
+  const int tile = blockIdx.x;  // 32-row unit: layout tile blockIdx.x / 4, quarter blockIdx.x % 4
 
   if (threadIdx.x == 0)
     ok = header_matches(reinterpret_cast<const PackedHeader*>(packed), kFormatBinplane, P, N, K);
@@ -41,11 +41,9 @@ binplane_cc_kernel(const uint16_t* __restrict__ X, const uint8_t* __restrict__ p
     if (threadIdx.x == 0 && blockIdx.x == 0) record_error(err, LOWBIT_ERR_INVALID_ARG);
     return;
   }
-  const uint4* codes = reinterpret_cast<const uint4*>(packed + kHeaderBytes) +
-                       (size_t)tile * G * P * kRowTile + lane;
-  const uint16_t* alphas = reinterpret_cast<const uint16_t*>(
-                               packed + kHeaderBytes + binplane_codes_bytes(P, N, K)) +
-                           (size_t)tile * G * P * kRowTile + lane;
+  const int rit = (tile & 3) * 32 + lane;
+  const uint32_t BB = binplane_block(P);
+  const uint8_t* tbase = packed + kHeaderBytes + (size_t)(tile >> 2) * G * BB;
 
   float total[MT];
 #pragma unroll
@@ -65,9 +63,10 @@ binplane_cc_kernel(const uint16_t* __restrict__ X, const uint8_t* __restrict__ p
     for (int gl = warp; gl < sg; gl += kWarps) {
       const int g = s0 + gl;
       for (int p = 0; p < P; ++p) {
-        const size_t unit = ((size_t)g * P + p) * kRowTile;
-        const uint4 wv = ld_stream(codes + unit);
-        const float a = half_bits_to_float(__ldg(alphas + unit));
+        const uint8_t* blk = tbase + (size_t)g * BB;
+        const uint4 wv = ld_stream(reinterpret_cast<const uint4*>(blk + p * (kRowTile * 16) + rit * 16));
+        const float a = half_bits_to_float(__ldg(reinterpret_cast<const uint16_t*>(
+            blk + binplane_alpha_off(P) + (p * kRowTile + rit) * 2)));
         const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
         float acc[MT];
 #pragma unroll
@@ -102,7 +101,7 @@ binplane_cc_kernel(const uint16_t* __restrict__ X, const uint8_t* __restrict__ p
     }
   }
   constexpr int TB = MT < 8 ? MT : 8;
-  const int n = tile * kRowTile + lane;
+  const int n = tile * 32 + lane;
 #pragma unroll
   for (int t0 = 0; t0 < MT; t0 += TB) {
     __syncthreads();
@@ -121,7 +120,7 @@ binplane_cc_kernel(const uint16_t* __restrict__ X, const uint8_t* __restrict__ p
 template <int MT>
 cudaError_t launch_bp(const uint16_t* X, const uint8_t* packed, int P, int M, int N, int K,
                       uint16_t* Y, int* err, cudaStream_t s) {
-  binplane_cc_kernel<MT><<<(unsigned)row_tiles(N), kThreads, 0, s>>>(X, packed, P, M, N, K, Y, err);
+  binplane_cc_kernel<MT><<<(unsigned)row_tiles(N) * 4, kThreads, 0, s>>>(X, packed, P, M, N, K, Y, err);
   return cudaGetLastError();
 }
 

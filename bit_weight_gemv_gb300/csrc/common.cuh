@@ -11,35 +11,35 @@
 namespace lowbit {
 
 // ------------------------------------------------------------------ packed layout
-constexpr uint32_t kMagic = 0x3142574Cu;  // "LWB1"
+constexpr uint32_t kMagic = 0x3242574Cu;  // "LWB2"
 constexpr uint32_t kFormatInt4 = 1;
 constexpr uint32_t kFormatBinplane = 2;
-constexpr uint32_t kVersion = 1;
+constexpr uint32_t kVersion = 2;
 constexpr int kHeaderBytes = 128;
-constexpr int kGroup = 128;   // inputs per quantisation group
-constexpr int kRowTile = 32;  // weight rows per layout tile
+constexpr int kGroup = 128;    // inputs per quantisation group
+constexpr int kRowTile = 128;  // weight rows per layout tile
 
 struct PackedHeader {
   uint32_t magic, format, version, N, K, P, group, row_tile;
-  uint64_t codes_offset, codes_bytes, scales_offset, scales_bytes;
+  uint64_t payload_offset, payload_bytes, block_bytes, reserved;
 };
 static_assert(sizeof(PackedHeader) == 64, "header layout");
 
 __host__ __device__ inline int row_tiles(int N) { return (N + kRowTile - 1) / kRowTile; }
 
-// INT4: codes [NT][K/32][32][16 B], scales [NT][K/128][32] fp16.
-__host__ __device__ inline uint64_t int4_codes_bytes(int N, int K) {
-  return (uint64_t)row_tiles(N) * kRowTile * (uint64_t)K / 2;
+// The payload is one contiguous block per (128-row tile t, group g) at (t*(K/128) + g) * block.
+// INT4 block: codes [4 chunks][128 rows][16 B] then scales [128 rows] fp16 = 8448 bytes.
+constexpr uint32_t kInt4Block = 4 * kRowTile * 16 + kRowTile * 2;
+constexpr uint32_t kInt4ScaleOff = 4 * kRowTile * 16;
+// Binary-plane block: signs [P][128 rows][16 B] then alphas [P][128 rows] fp16.
+__host__ __device__ inline uint32_t binplane_block(int P) { return (uint32_t)P * (kRowTile * 16 + kRowTile * 2); }
+__host__ __device__ inline uint32_t binplane_alpha_off(int P) { return (uint32_t)P * kRowTile * 16; }
+
+__host__ __device__ inline uint64_t int4_payload_bytes(int N, int K) {
+  return (uint64_t)row_tiles(N) * (uint64_t)(K / kGroup) * kInt4Block;
 }
-__host__ __device__ inline uint64_t int4_scales_bytes(int N, int K) {
-  return (uint64_t)row_tiles(N) * kRowTile * (uint64_t)(K / kGroup) * 2;
-}
-// Binary planes: codes [NT][K/128][P][32][16 B], alphas [NT][K/128][P][32] fp16.
-__host__ __device__ inline uint64_t binplane_codes_bytes(int P, int N, int K) {
-  return (uint64_t)row_tiles(N) * kRowTile * (uint64_t)P * K / 8;
-}
-__host__ __device__ inline uint64_t binplane_scales_bytes(int P, int N, int K) {
-  return (uint64_t)row_tiles(N) * kRowTile * (uint64_t)P * (K / kGroup) * 2;
+__host__ __device__ inline uint64_t binplane_payload_bytes(int P, int N, int K) {
+  return (uint64_t)row_tiles(N) * (uint64_t)(K / kGroup) * binplane_block(P);
 }
 
 // Kernel-side header check.  Returns true when the buffer holds (format, P, N, K).

@@ -3,15 +3,17 @@
 // Efficient-Qwen report, section 2.1: INT4 codes under frozen symmetric per-group scales
 // (group 128), served as W4A16.  ShiftAddQwen README, "Format" and "Layout": sign planes
 // with per-group scales, written with bit-exact packing checks.  The layouts themselves are
-// this library's (see include/lowbit.h); they put the 32 rows of a tile side by side so one
-// warp's 16-byte-per-lane load of a tile chunk is a single contiguous 512-byte segment.
+// this library's (see include/lowbit.h): every (128-row tile, group of 128 inputs) is one
+// contiguous block holding the tile's codes (rows side by side, so a warp's 16-byte-per-lane
+// load of 32 rows is one 512-byte segment) followed by its scales, so a kernel can stage a
+// whole block with a single bulk copy.
 #include "common.cuh"
 
 namespace lowbit {
 namespace {
 
 __device__ void write_header(uint8_t* packed, uint32_t format, int P, int N, int K,
-                             uint64_t codes_bytes, uint64_t scales_bytes) {
+                             uint64_t payload_bytes, uint64_t block_bytes) {
   PackedHeader h;
   h.magic = kMagic;
   h.format = format;
@@ -21,10 +23,10 @@ __device__ void write_header(uint8_t* packed, uint32_t format, int P, int N, int
   h.P = (uint32_t)P;
   h.group = kGroup;
   h.row_tile = kRowTile;
-  h.codes_offset = kHeaderBytes;
-  h.codes_bytes = codes_bytes;
-  h.scales_offset = kHeaderBytes + codes_bytes;
-  h.scales_bytes = scales_bytes;
+  h.payload_offset = kHeaderBytes;
+  h.payload_bytes = payload_bytes;
+  h.block_bytes = block_bytes;
+  h.reserved = 0;
   uint4* dst = reinterpret_cast<uint4*>(packed);
   const uint4* src = reinterpret_cast<const uint4*>(&h);
 #pragma unroll
@@ -33,17 +35,21 @@ __device__ void write_header(uint8_t* packed, uint32_t format, int P, int N, int
   for (int i = 4; i < kHeaderBytes / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
 }
 
-// One thread per 16-byte unit (tile t, chunk c, row r): 32 codes of row n, k = 32c..32c+31.
+// One thread per 16-byte code unit (tile t, group g, chunk c, row r): 32 codes of row n,
+// k = 128g + 32c .. +31, stored at block(t, g) + c*2048 + r*16.
 __global__ void pack_int4_codes(const int8_t* __restrict__ codes, int N, int K,
-                                uint4* __restrict__ out, long long units) {
+                                uint8_t* __restrict__ payload, long long units) {
   const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (u >= units) return;
-  const int C = K / 32;
+  const int G = K / kGroup;
   const int r = (int)(u % kRowTile);
-  const long long tc = u / kRowTile;
-  const int c = (int)(tc % C);
-  const long long t = tc / C;
+  long long rest = u / kRowTile;
+  const int c4 = (int)(rest % 4);
+  rest /= 4;
+  const int g = (int)(rest % G);
+  const long long t = rest / G;
   const long long n = t * kRowTile + r;
+  const int c = 4 * g + c4;  // 32-input chunk index within the row
   uint32_t w[4] = {0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u};  // q = 0 padding
   if (n < N) {
     const uint4* src = reinterpret_cast<const uint4*>(codes + n * (long long)K + 32LL * c);
@@ -62,12 +68,13 @@ __global__ void pack_int4_codes(const int8_t* __restrict__ codes, int N, int K,
       w[i] = word;
     }
   }
-  out[u] = make_uint4(w[0], w[1], w[2], w[3]);
+  uint8_t* dst = payload + (size_t)(t * G + g) * kInt4Block + (size_t)c4 * kRowTile * 16 + r * 16;
+  *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// One thread per (tile, group, row) scale.
+// One thread per (tile, group, row) scale, stored at block(t, g) + 8192 + r*2.
 __global__ void pack_int4_scales(const uint16_t* __restrict__ scales, int N, int K,
-                                 uint16_t* __restrict__ out, long long units) {
+                                 uint8_t* __restrict__ payload, long long units) {
   const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (u >= units) return;
   const int G = K / kGroup;
@@ -76,13 +83,14 @@ __global__ void pack_int4_scales(const uint16_t* __restrict__ scales, int N, int
   const int g = (int)(tg % G);
   const long long t = tg / G;
   const long long n = t * kRowTile + r;
-  out[u] = (n < N) ? scales[n * G + g] : (uint16_t)0;
+  *reinterpret_cast<uint16_t*>(payload + (size_t)tg * kInt4Block + kInt4ScaleOff + r * 2) =
+      (n < N) ? scales[n * G + g] : (uint16_t)0;
 }
 
 __global__ void pack_header(uint8_t* packed, uint32_t format, int P, int N, int K,
-                            unsigned long long codes_bytes, unsigned long long scales_bytes) {
+                            unsigned long long payload_bytes, unsigned long long block_bytes) {
   if (threadIdx.x == 0 && blockIdx.x == 0)
-    write_header(packed, format, P, N, K, codes_bytes, scales_bytes);
+    write_header(packed, format, P, N, K, payload_bytes, block_bytes);
 }
 
 // Even bits of a 32-bit word to its low half-word, odd bits to its high half-word.
@@ -95,9 +103,9 @@ __device__ __forceinline__ uint32_t split_even_odd(uint32_t x) {
   return e | (o << 16);
 }
 
-// One thread per 16-byte unit (tile t, group g, plane p, row r).
+// One thread per 16-byte unit (tile t, group g, plane p, row r) at block(t, g) + p*2048 + r*16.
 __global__ void pack_binplane_codes(const uint8_t* __restrict__ bits, int P, int N, int K,
-                                    uint4* __restrict__ out, long long units) {
+                                    uint8_t* __restrict__ payload, long long units) {
   const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (u >= units) return;
   const int G = K / kGroup;
@@ -115,11 +123,13 @@ __global__ void pack_binplane_codes(const uint8_t* __restrict__ bits, int P, int
     v = make_uint4(split_even_odd(c.x), split_even_odd(c.y), split_even_odd(c.z),
                    split_even_odd(c.w));
   }
-  out[u] = v;
+  uint8_t* dst = payload + (size_t)(t * G + g) * binplane_block(P) + (size_t)p * kRowTile * 16 + r * 16;
+  *reinterpret_cast<uint4*>(dst) = v;
 }
 
+// One thread per (tile, group, plane, row) scale at block(t, g) + 2048P + (p*128 + r)*2.
 __global__ void pack_binplane_alpha(const uint16_t* __restrict__ alpha, int P, int N, int K,
-                                    uint16_t* __restrict__ out, long long units) {
+                                    uint8_t* __restrict__ payload, long long units) {
   const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (u >= units) return;
   const int G = K / kGroup;
@@ -130,7 +140,9 @@ __global__ void pack_binplane_alpha(const uint16_t* __restrict__ alpha, int P, i
   const int g = (int)(rest % G);
   const long long t = rest / G;
   const long long n = t * kRowTile + r;
-  out[u] = (n < N) ? alpha[((long long)p * N + n) * G + g] : (uint16_t)0;
+  uint8_t* dst = payload + (size_t)(t * G + g) * binplane_block(P) + binplane_alpha_off(P) +
+                 ((size_t)p * kRowTile + r) * 2;
+  *reinterpret_cast<uint16_t*>(dst) = (n < N) ? alpha[((long long)p * N + n) * G + g] : (uint16_t)0;
 }
 
 inline unsigned blocks_for(long long units, int threads) {
@@ -141,25 +153,21 @@ inline unsigned blocks_for(long long units, int threads) {
 
 cudaError_t launch_pack_int4(const int8_t* codes, const uint16_t* scales, int N, int K,
                              uint8_t* packed, cudaStream_t s) {
-  const uint64_t cb = int4_codes_bytes(N, K), sb = int4_scales_bytes(N, K);
-  const long long cu = (long long)(cb / 16), su = (long long)(sb / 2);
-  pack_header<<<1, 32, 0, s>>>(packed, kFormatInt4, 0, N, K, cb, sb);
-  pack_int4_codes<<<blocks_for(cu, 256), 256, 0, s>>>(
-      codes, N, K, reinterpret_cast<uint4*>(packed + kHeaderBytes), cu);
-  pack_int4_scales<<<blocks_for(su, 256), 256, 0, s>>>(
-      scales, N, K, reinterpret_cast<uint16_t*>(packed + kHeaderBytes + cb), su);
+  const long long blocks = (long long)row_tiles(N) * (K / kGroup);
+  const long long cu = blocks * 4 * kRowTile, su = blocks * kRowTile;
+  pack_header<<<1, 32, 0, s>>>(packed, kFormatInt4, 0, N, K, int4_payload_bytes(N, K), kInt4Block);
+  pack_int4_codes<<<blocks_for(cu, 256), 256, 0, s>>>(codes, N, K, packed + kHeaderBytes, cu);
+  pack_int4_scales<<<blocks_for(su, 256), 256, 0, s>>>(scales, N, K, packed + kHeaderBytes, su);
   return cudaGetLastError();
 }
 
 cudaError_t launch_pack_binplane(const uint8_t* bits, const uint16_t* alpha, int P, int N, int K,
                                  uint8_t* packed, cudaStream_t s) {
-  const uint64_t cb = binplane_codes_bytes(P, N, K), sb = binplane_scales_bytes(P, N, K);
-  const long long cu = (long long)(cb / 16), su = (long long)(sb / 2);
-  pack_header<<<1, 32, 0, s>>>(packed, kFormatBinplane, P, N, K, cb, sb);
-  pack_binplane_codes<<<blocks_for(cu, 256), 256, 0, s>>>(
-      bits, P, N, K, reinterpret_cast<uint4*>(packed + kHeaderBytes), cu);
-  pack_binplane_alpha<<<blocks_for(su, 256), 256, 0, s>>>(
-      alpha, P, N, K, reinterpret_cast<uint16_t*>(packed + kHeaderBytes + cb), su);
+  const long long units = (long long)row_tiles(N) * (K / kGroup) * P * kRowTile;
+  pack_header<<<1, 32, 0, s>>>(packed, kFormatBinplane, P, N, K, binplane_payload_bytes(P, N, K),
+                               binplane_block(P));
+  pack_binplane_codes<<<blocks_for(units, 256), 256, 0, s>>>(bits, P, N, K, packed + kHeaderBytes, units);
+  pack_binplane_alpha<<<blocks_for(units, 256), 256, 0, s>>>(alpha, P, N, K, packed + kHeaderBytes, units);
   return cudaGetLastError();
 }
 

@@ -52,11 +52,11 @@ int lowbit_version(void);
  * Sizes (host-only, no CUDA call).  Return 0 for invalid shapes.
  */
 
-/* Bytes of a packed INT4 buffer: 128-byte header + ceil(N/32)*32 rows of K/2 code bytes and
- * K/64 scale bytes.  For N a multiple of 32 the payload is exactly N*K/2 + N*K/64 bytes. */
+/* Bytes of a packed INT4 buffer: 128-byte header + ceil(N/128)*128 rows of K/2 code bytes and
+ * K/64 scale bytes.  For N a multiple of 128 the payload is exactly N*K/2 + N*K/64 bytes. */
 size_t lowbit_int4_packed_bytes(int N, int K);
 
-/* Bytes of a packed binary-plane buffer: header + ceil(N/32)*32 rows of P*K/8 sign bytes and
+/* Bytes of a packed binary-plane buffer: header + ceil(N/128)*128 rows of P*K/8 sign bytes and
  * P*K/64 plane-scale bytes. */
 size_t lowbit_binplane_packed_bytes(int P, int N, int K);
 
@@ -74,11 +74,12 @@ size_t lmhead_workspace_bytes(int M, int N, int K);
  *            the range are out of contract: they are stored modulo 16.
  *   scales : fp16 [N][K/128], one symmetric scale per row and group of 128 inputs.
  *   packed : lowbit_int4_packed_bytes(N, K) bytes, 16-byte aligned; fully overwritten.
- * Layout of `packed` (little-endian): the header, then codes in row tiles of 32 rows (padding
- * rows hold q = 0, scale 0): for tile t, 32-input chunk c and row r = n % 32 the 16 bytes at
- * ((t*(K/32) + c)*32 + r)*16 hold k = 32c..32c+31 as four u32 words, word i holding
- * k = 32c + 8i + 2p + o (p = 0..3, o = 0..1) as the nibble q + 8 at bit 4p + 16o; then the
- * fp16 scales, s[n][g] at ((t*(K/128) + g)*32 + r)*2 after the codes. */
+ * Layout of `packed` (little-endian): the header (magic 0x3242574C, format 1, version 2), then
+ * rows in tiles of 128 (padding rows hold q = 0, scale 0).  Tile t and group g (inputs
+ * 128g..128g+127) own one contiguous 8448-byte block at 128 + (t*(K/128) + g)*8448: for chunk
+ * c = 0..3 and row r = n % 128 the 16 bytes at c*2048 + r*16 are four u32 words, word i
+ * holding k = 128g + 32c + 8i + 2p + o (p = 0..3, o = 0..1) as the nibble q + 8 at bit
+ * 4p + 16o; the fp16 scale s[n][g] sits at 8192 + r*2. */
 lowbit_status lowbit_pack_int4(const int8_t* codes, const uint16_t* scales, int N, int K,
                                void* packed, void* stream);
 
@@ -86,10 +87,11 @@ lowbit_status lowbit_pack_int4(const int8_t* codes, const uint16_t* scales, int 
  *   signbits : uint8 [P][N][K/8]; bit j (LSB first) of byte i is input k = 8i + j; 1 = +1.
  *   alpha    : fp16 [P][N][K/128], one scale per plane, row and group of 128 inputs.
  *   packed   : lowbit_binplane_packed_bytes(P, N, K) bytes, 16-byte aligned.
- * Layout: header, then for tile t, group g, plane p, row r the 16 bytes at
- * (((t*(K/128) + g)*P + p)*32 + r)*16 hold the 128 signs of k = 128g.. as four u32 words;
- * word w covers k0 = 128g + 32w with bit i = sign of k0 + 2i and bit 16 + i = sign of
- * k0 + 2i + 1; then alpha[p][n][g] (fp16) at (((t*(K/128) + g)*P + p)*32 + r)*2. */
+ * Layout: header (format 2), then tiles of 128 rows; tile t and group g own one contiguous
+ * block of 2304*P bytes at 128 + (t*(K/128) + g)*2304*P: for plane p and row r = n % 128 the
+ * 16 bytes at p*2048 + r*16 hold the 128 signs of k = 128g.. as four u32 words, word w
+ * covering k0 = 128g + 32w with bit i = sign of k0 + 2i and bit 16 + i = sign of k0 + 2i + 1;
+ * alpha[p][n][g] (fp16) sits at 2048*P + (p*128 + r)*2. */
 lowbit_status lowbit_pack_binplane(const uint8_t* signbits, const uint16_t* alpha, int P, int N,
                                    int K, void* packed, void* stream);
 

@@ -13,20 +13,21 @@ Canonical sign-bit input: uint8 [P][N][K/8]; bit j (LSB first) of byte i is elem
 k = 8i + j, and a set bit means +1.
 
 Packed layout (this project's kernel layout, restated from its written description):
-  header as for INT4 (see ``oracle.int4``) with format 2 and P planes.
-  codes: row tiles of 32 (padding rows: all bits 0 and alpha 0).  For tile t, group g,
-    plane p and row r the 128 sign bits of k = 128g .. 128g+127 are 16 bytes at
-    (((t*(K/128) + g)*P + p)*32 + r)*16, as four little-endian u32 words.  Word w covers
-    k0 = 128g + 32w: bit i (i = 0..15) is the sign of k0 + 2i and bit 16 + i the sign of
-    k0 + 2i + 1 (even inputs in the low half-word, odd inputs in the high half-word).
-  alphas: fp16 bits of alpha[p][n][g] at alpha_offset + (((t*(K/128) + g)*P + p)*32 + r)*2.
+  header as for INT4 (see ``oracle.int4``) with format 2, P planes and block bytes 2304*P.
+  payload: row tiles of 128 (padding rows: all bits 0 and alpha 0).  Tile t and group g own
+    one contiguous block of 2304*P bytes at (t*(K/128) + g)*2304*P:
+      signs: for plane p and row r = n mod 128, 16 bytes at p*2048 + r*16 holding the 128
+        sign bits of k = 128g .. 128g+127 as four little-endian u32 words.  Word w covers
+        k0 = 128g + 32w: bit i (i = 0..15) is the sign of k0 + 2i and bit 16 + i the sign of
+        k0 + 2i + 1 (even inputs in the low half-word, odd inputs in the high half-word);
+      alphas: fp16 bits of alpha[p][n][g] at 2048*P + (p*128 + r)*2.
 """
 from __future__ import annotations
 
 import numpy as np
 
 from .numerics import bf16_to_f64, f16_to_f64
-from .int4 import HEADER_BYTES, MAGIC, ROW_TILE, GROUP, header_bytes, parse_header
+from .int4 import HEADER_BYTES, MAGIC, ROW_TILE, GROUP, VERSION, header_bytes, parse_header
 
 FORMAT_BINPLANE = 2
 
@@ -60,13 +61,15 @@ def gemm(x_bits: np.ndarray, bits: np.ndarray, alpha_bits: np.ndarray,
 
 # ----------------------------------------------------------------------------- layout
 
+def block_bytes(P: int) -> int:
+    return P * (ROW_TILE * 16 + ROW_TILE * 2)
+
+
 def packed_sizes(P: int, N: int, K: int):
+    """(total bytes, payload offset, payload bytes, block bytes)."""
     NT = -(-N // ROW_TILE)
-    codes_bytes = NT * ROW_TILE * P * K // 8
-    alpha_bytes = NT * ROW_TILE * P * (K // GROUP) * 2
-    codes_off = HEADER_BYTES
-    alpha_off = codes_off + codes_bytes
-    return alpha_off + alpha_bytes, codes_off, codes_bytes, alpha_off, alpha_bytes
+    payload = NT * (K // GROUP) * block_bytes(P)
+    return HEADER_BYTES + payload, HEADER_BYTES, payload, block_bytes(P)
 
 
 def pack(bits: np.ndarray, alpha_bits: np.ndarray) -> np.ndarray:
@@ -75,12 +78,12 @@ def pack(bits: np.ndarray, alpha_bits: np.ndarray) -> np.ndarray:
     K = KB * 8
     G = K // GROUP
     assert K % GROUP == 0 and alpha_bits.shape == (P, N, G)
-    total, c_off, c_bytes, a_off, a_bytes = packed_sizes(P, N, K)
+    total, off, payload, blk = packed_sizes(P, N, K)
     NT = -(-N // ROW_TILE)
     Np = NT * ROW_TILE
     beta = np.zeros((P, Np, K), dtype=np.uint32)
     beta[:, :N] = np.unpackbits(bits, axis=-1, bitorder="little")
-    # beta[p][t*32 + r][128g + 32w + 2i + o] -> axes [p][t][r][g][w][i][o]
+    # beta[p][t*128 + r][128g + 32w + 2i + o] -> axes [p][t][r][g][w][i][o]
     b7 = beta.reshape(P, NT, ROW_TILE, G, 4, 16, 2)
     shift = (np.arange(16, dtype=np.uint32)[:, None]
              + 16 * np.arange(2, dtype=np.uint32)[None, :])          # [i][o]
@@ -89,29 +92,33 @@ def pack(bits: np.ndarray, alpha_bits: np.ndarray) -> np.ndarray:
     words = np.ascontiguousarray(words.transpose(1, 3, 0, 2, 4)).astype("<u4")  # [t][g][p][r][w]
     a = np.zeros((P, Np, G), dtype=np.uint16)
     a[:, :N] = alpha_bits
-    a = np.ascontiguousarray(a.reshape(P, NT, ROW_TILE, G).transpose(1, 3, 0, 2)).astype("<u2")
+    a = np.ascontiguousarray(a.reshape(P, NT, ROW_TILE, G).transpose(1, 3, 0, 2)).astype("<u2")  # [t][g][p][r]
+    blocks = np.zeros((NT, G, blk), dtype=np.uint8)
+    blocks[:, :, :2048 * P] = words.reshape(NT, G, 512 * P).view(np.uint8)
+    blocks[:, :, 2048 * P:] = a.view(np.uint8).reshape(NT, G, 256 * P)
     out = np.zeros(total, dtype=np.uint8)
-    out[:HEADER_BYTES] = header_bytes(FORMAT_BINPLANE, N, K, P, c_off, c_bytes, a_off, a_bytes)
-    out[c_off:c_off + c_bytes] = words.reshape(-1).view(np.uint8)
-    out[a_off:a_off + a_bytes] = a.reshape(-1).view(np.uint8)
+    out[:HEADER_BYTES] = header_bytes(FORMAT_BINPLANE, N, K, P, payload, blk)
+    out[off:] = blocks.reshape(-1)
     return out
 
 
 def unpack(packed: np.ndarray):
     """Packed bytes -> (sign bits uint8 [P][N][K/8], fp16 alpha bits [P][N][K/128])."""
     hd = parse_header(packed)
-    assert hd["magic"] == MAGIC and hd["format"] == FORMAT_BINPLANE
+    assert hd["magic"] == MAGIC and hd["format"] == FORMAT_BINPLANE and hd["version"] == VERSION
     P, N, K = hd["P"], hd["N"], hd["K"]
     G = K // GROUP
     NT = -(-N // ROW_TILE)
-    c = packed[hd["codes_offset"]:hd["codes_offset"] + hd["codes_bytes"]]
-    words = np.ascontiguousarray(c).view("<u4").reshape(NT, G, P, ROW_TILE, 4)
+    blocks = np.ascontiguousarray(
+        packed[hd["payload_offset"]:hd["payload_offset"] + hd["payload_bytes"]]
+    ).reshape(NT, G, block_bytes(P))
+    words = np.ascontiguousarray(blocks[:, :, :2048 * P]).view("<u4").reshape(NT, G, P, ROW_TILE, 4)
     shift = (np.arange(16, dtype=np.uint32)[:, None]
              + 16 * np.arange(2, dtype=np.uint32)[None, :])
     b = (words[..., None, None] >> shift) & np.uint32(1)             # [t][g][p][r][w][i][o]
     b = b.transpose(2, 0, 3, 1, 4, 5, 6).reshape(P, NT * ROW_TILE, K)[:, :N]
     bits = np.packbits(b.astype(np.uint8), axis=-1, bitorder="little")
-    a = packed[hd["scales_offset"]:hd["scales_offset"] + hd["scales_bytes"]]
-    a = np.ascontiguousarray(a).view("<u2").reshape(NT, G, P, ROW_TILE).transpose(2, 0, 3, 1)
+    a = np.ascontiguousarray(blocks[:, :, 2048 * P:]).view("<u2").reshape(NT, G, P, ROW_TILE)
+    a = a.transpose(2, 0, 3, 1)
     alpha = np.ascontiguousarray(a.reshape(P, NT * ROW_TILE, G)[:, :N]).astype(np.uint16)
     return bits, alpha

@@ -52,8 +52,8 @@ def test_sizes_and_status_strings(lib):
     assert lib.lowbit_int4_packed_bytes(32_768, 4096) - 128 == 69_206_016
     assert lib.lowbit_binplane_packed_bytes(3, 12288, 4096) - 128 == 21_233_664
     assert lib.lowbit_binplane_packed_bytes(4, 4096, 12288) - 128 == 28_311_552
-    # ragged rows are padded to the 32-row tile
-    assert lib.lowbit_int4_packed_bytes(33, 128) == 128 + 64 * 64 + 64 * 2
+    # ragged rows are padded to the 128-row tile
+    assert lib.lowbit_int4_packed_bytes(33, 128) == 128 + 8448   # one 128-row tile, one group
     assert lib.lowbit_int4_packed_bytes(10, 100) == 0          # K not a multiple of 128
     assert lib.lowbit_binplane_packed_bytes(9, 32, 128) == 0   # P > 8
     assert lib.lmhead_workspace_bytes(16, 248_320, 4096) == 512

@@ -139,32 +139,37 @@ def test_int4_one_hot_and_group_closed_forms():
 
 
 def test_int4_layout_positions_by_hand():
-    N, K = 40, 256
+    N, K = 200, 256
     rows = []
     with open(os.path.join(GOLDEN, "int4_layout_positions.txt")) as f:
         for line in f:
             if line.strip() and not line.startswith("#"):
                 n, k, byte, nib = line.split()
                 rows.append((int(n), int(k), int(byte), nib))
-    total, c_off, c_bytes, s_off, s_bytes = int4.packed_sizes(N, K)
-    assert (c_off, c_bytes, s_off) == (128, 8192, 8320)
+    total, off, payload, block = int4.packed_sizes(N, K)
+    assert (off, payload, block) == (128, 33792, 8448)
+    code_bytes = np.zeros(payload, dtype=bool)      # which payload bytes hold codes
+    for b in range(4):
+        code_bytes[b * block:b * block + 8192] = True
     for n, k, byte, nib in rows:
         codes = np.zeros((N, K), dtype=np.int8)
         codes[n, k] = 5                              # nibble u = 13, every other nibble 8
         packed = int4.pack(codes, np.zeros((N, K // 128), dtype=np.uint16))
-        sec = packed[c_off:c_off + c_bytes]
+        sec = packed[off:off + payload]
         lo, hi = sec & 0xF, sec >> 4
-        expect_lo = np.full(c_bytes, 8); expect_hi = np.full(c_bytes, 8)
+        expect_lo = np.where(code_bytes, 8, 0); expect_hi = np.where(code_bytes, 8, 0)
         (expect_lo if nib == "lo" else expect_hi)[byte] = 13
         assert np.array_equal(lo, expect_lo) and np.array_equal(hi, expect_hi), (n, k)
     scales = np.zeros((N, K // 128), dtype=np.uint16)
-    scales[33, 1] = 0x3C00
+    scales[130, 1] = 0x3C00
     packed = int4.pack(np.zeros((N, K), dtype=np.int8), scales)
-    sec = packed[s_off:s_off + s_bytes].view("<u2")
-    assert sec[194 // 2] == 0x3C00 and np.count_nonzero(sec) == 1
+    sec = packed[off:off + payload].copy()
+    sec[code_bytes] = 0
+    sec = sec.view("<u2")
+    assert sec[33540 // 2] == 0x3C00 and np.count_nonzero(sec) == 1
 
 
-@pytest.mark.parametrize("N,K", [(40, 256), (256, 512), (33, 128)])
+@pytest.mark.parametrize("N,K", [(40, 256), (256, 512), (33, 128), (300, 384)])
 def test_int4_pack_round_trip_and_header(N, K):
     codes, scales, _ = synth.int4_problem(4, 1, N, K)
     packed = int4.pack(codes, scales)
@@ -173,9 +178,9 @@ def test_int4_pack_round_trip_and_header(N, K):
     assert np.array_equal(c2, codes) and np.array_equal(s2, scales)
     hd = int4.parse_header(packed)
     assert (hd["magic"], hd["format"], hd["N"], hd["K"], hd["group"]) == (int4.MAGIC, 1, N, K, 128)
-    # exactly N*K/2 + N*K/64 payload bytes when N is a multiple of the row tile
-    if N % 32 == 0:
-        assert hd["codes_bytes"] + hd["scales_bytes"] == N * K // 2 + N * K // 64
+    # exactly N*K/2 + N*K/64 payload bytes when N is a multiple of the 128-row tile
+    if N % 128 == 0:
+        assert hd["payload_bytes"] == N * K // 2 + N * K // 64
 
 
 # ------------------------------------------------------------------ binary planes
@@ -244,8 +249,9 @@ def test_binplane_brute_force():
 
 
 def test_binplane_layout_positions_by_hand():
-    P, N, K = 2, 40, 256
-    total, c_off, c_bytes, a_off, a_bytes = binplane.packed_sizes(P, N, K)
+    P, N, K = 2, 200, 256
+    total, off, payload, block = binplane.packed_sizes(P, N, K)
+    assert block == 4608
     with open(os.path.join(GOLDEN, "binplane_layout_positions.txt")) as f:
         rows = [tuple(int(v) for v in line.split()) for line in f
                 if line.strip() and not line.startswith("#")]
@@ -253,21 +259,21 @@ def test_binplane_layout_positions_by_hand():
         bits = np.zeros((P, N, K // 8), dtype=np.uint8)
         bits[p, n, k // 8] = 1 << (k % 8)
         packed = binplane.pack(bits, np.zeros((P, N, K // 128), dtype=np.uint16))
-        sec = packed[c_off:c_off + c_bytes]
-        expect = np.zeros(c_bytes, dtype=np.uint8)
+        sec = packed[off:off + payload]
+        expect = np.zeros(payload, dtype=np.uint8)
         expect[byte] = 1 << bit
         assert np.array_equal(sec, expect), (p, n, k)
 
 
-@pytest.mark.parametrize("P,N,K", [(2, 40, 256), (3, 64, 512), (4, 33, 128)])
+@pytest.mark.parametrize("P,N,K", [(2, 40, 256), (3, 128, 512), (4, 33, 128), (1, 256, 256)])
 def test_binplane_pack_round_trip(P, N, K):
     bits, alpha, _ = synth.binplane_problem(6, P, 1, N, K)
     packed = binplane.pack(bits, alpha)
     b2, a2 = binplane.unpack(packed)
     assert np.array_equal(b2, bits) and np.array_equal(a2, alpha)
-    if N % 32 == 0:
+    if N % 128 == 0:
         hd = int4.parse_header(packed)
-        assert hd["codes_bytes"] + hd["scales_bytes"] == P * N * K // 8 + P * N * K // 64
+        assert hd["payload_bytes"] == P * N * K // 8 + P * N * K // 64
 
 
 # ------------------------------------------------------------------ argmax / acceptance

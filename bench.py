@@ -5,7 +5,8 @@ Headline workload (one "step"): decode through one 4B-class dense decoder layer 
 INT4 group-128 W4A16 projections (q, k, v, o, gate, up with K=2560; down with K=9728) at
 M=1, 50,012,160 algorithmic weight bytes per step.  Every step reads a different copy of the
 layer's packed weights (copies totalling more than 4x the L2 size), so timed weights come
-from HBM.  Steps are replayed from per-copy CUDA graphs and timed with CUDA events.
+from HBM.  Steps are replayed from CUDA graphs (one per rotation of the weight copies) and
+timed with CUDA events.
 
 Also reported under "rows": the M=16 verify GEMM over the same layer and its batch sweep,
 binary-plane GEMV/GEMM, and the LM-head argmax+verify over 248,320 and 32,768 rows.
@@ -177,8 +178,17 @@ def _copies(p0, n, torch):
     return [p0] + [p0.clone() for _ in range(n - 1)]
 
 
-def build_int4_layer(lb, torch, l2, M, path, seed, name, desc):
-    w = Workload(name, desc, "int4_gemv_kernel" if (M == 1 and path != 2) else "tc_gemm_kernel")
+# Launch groupings of the layer's seven projections (q, k, v, o, gate, up, down):
+#   None   : one lowbit_gemm_int4 call per projection (7 launches);
+#   "deps" : what a decoder's data dependencies allow, one lowbit_gemm_int4_grouped call per
+#            set -- (q, k, v) read the same input, o follows attention, (gate, up) share the
+#            post-attention input, down follows the activation -- 4 launches;
+#   "all"  : all seven in one grouped call (1 launch).
+LAYER_GROUPS = {"deps": ((0, 1, 2), (3,), (4, 5), (6,)), "all": ((0, 1, 2, 3, 4, 5, 6),)}
+
+
+def build_int4_layer(lb, torch, l2, M, path, seed, name, desc, grouping=None):
+    w = Workload(name, desc, "int4_stream_kernel" if (M == 1 and path != 2) else "tc_gemm_kernel")
     shapes = [(k, n) for _, k, n in synth.LAYER_4B]
     w.bytes = sum(algorithmic_int4_bytes(N, K) for K, N in shapes)
     C = copies_for(w.bytes, l2)
@@ -190,11 +200,20 @@ def build_int4_layer(lb, torch, l2, M, path, seed, name, desc):
         packs.append(_copies(p, C, torch))
         X.append(bf16_dev(x))
         Y.append(torch.empty((M, N), dtype=torch.bfloat16, device="cuda"))
-    for c in range(C):
-        w.calls.append([(lambda j=j, K=K, N=N, c=c: lb.lowbit_gemm_int4_path(
-            X[j], packs[j][c], M, N, K, Y[j], path)) for j, (K, N) in enumerate(shapes)])
-    w.M, w.tokens, w.launches = M, M, len(shapes)
-    w.host_io = (X, Y, lambda c, j: (packs[j][c], shapes[j]))
+    if grouping is None:
+        for c in range(C):
+            w.calls.append([(lambda j=j, K=K, N=N, c=c: lb.lowbit_gemm_int4_path(
+                X[j], packs[j][c], M, N, K, Y[j], path)) for j, (K, N) in enumerate(shapes)])
+        w.launches = len(shapes)
+    else:
+        groups = LAYER_GROUPS[grouping]
+        for c in range(C):
+            w.calls.append([(lambda grp=grp, c=c: lb.lowbit_gemm_int4_grouped(
+                [(X[j], packs[j][c], shapes[j][1], shapes[j][0], Y[j]) for j in grp], M))
+                for grp in groups])
+        w.launches = len(groups) if M == 1 else len(shapes)
+    w.M, w.tokens = M, M
+    w.host_io = (X, Y)
     return w
 
 
@@ -246,6 +265,13 @@ def build_workload(lb, torch, l2, name, path):
         return build_int4_layer(lb, torch, l2, 1, path, 1, name,
                                 "decode W4A16 GEMV over one 4B-class layer: q,k,v,o,gate,up (K=2560) "
                                 "and down (K=9728), INT4 group 128, M=1")
+    if name in ("decode_deps", "decode_all"):
+        grouping = name.split("_")[1]
+        how = ("grouped as a decoder's dependencies allow: (q,k,v), (o), (gate,up), (down), "
+               "one launch each" if grouping == "deps" else "all seven in one grouped launch")
+        return build_int4_layer(lb, torch, l2, 1, path, 1, name,
+                                "decode W4A16 GEMV over one 4B-class layer, M=1, " + how,
+                                grouping=grouping)
     if name == "verify":
         return build_int4_layer(lb, torch, l2, 16, path, 2, name,
                                 "speculative-verify skinny GEMM over the same 4B-class layer, M=16")
@@ -254,7 +280,7 @@ def build_workload(lb, torch, l2, name, path):
         return build_int4_layer(lb, torch, l2, M, path, 2, name,
                                 f"batch sweep: the 4B-class layer at M={M}")
     if name == "tiny":
-        w = Workload(name, "tiny INT4 GEMV K=512 N=256 M=1", "int4_gemv_kernel")
+        w = Workload(name, "tiny INT4 GEMV K=512 N=256 M=1", "int4_stream_kernel")
         codes, scales, x = synth.int4_problem(0, 1, 256, 512)
         p = torch.empty(lb.lowbit_int4_packed_bytes(256, 512), dtype=torch.uint8, device="cuda")
         lb.lowbit_pack_int4(dev(codes), f16_dev(scales), 256, 512, p)
@@ -275,13 +301,33 @@ def build_workload(lb, torch, l2, name, path):
     raise ValueError(name)
 
 
-WORKLOADS = ("decode", "verify", "binplane_m1", "binplane_m16", "lmhead_full", "lmhead_trim",
+WORKLOADS = ("decode", "decode_deps", "decode_all", "verify", "binplane_m1", "binplane_m16", "lmhead_full", "lmhead_trim",
              "tiny") + tuple(f"verify_m{m}" for m in synth.M_SWEEP if m not in (16,))
 
 
+class Replay:
+    """CUDA graphs for a workload: `full` replays one whole rotation (n steps, one per weight
+    copy) so the host pays one graph launch per n steps; `single[i]` replays step i alone and
+    tops a timed run up to an exact step count."""
+
+    def __init__(self, full, single, n):
+        self.full, self.single, self.n = full, single, n
+
+    def run(self, steps, start=0):
+        i = start
+        while steps > 0:
+            if i % self.n == 0 and steps >= self.n:
+                self.full.replay()
+                steps -= self.n
+                i += self.n
+            else:
+                self.single[i % self.n].replay()
+                steps -= 1
+                i += 1
+        return i
+
+
 def capture(torch, w, n):
-    """One CUDA graph per rotation slot (each replays one step over one weight copy)."""
-    graphs = []
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
@@ -289,18 +335,24 @@ def capture(torch, w, n):
             w.step(i)                  # eager warm-up outside capture
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
+    single = []
     for i in range(n):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, capture_error_mode="thread_local"):
             w.step(i)
-        graphs.append(g)
+        single.append(g)
+    full = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(full, capture_error_mode="thread_local"):
+        for i in range(n):
+            w.step(i)
     torch.cuda.synchronize()
-    return graphs
+    return Replay(full, single, n)
 
 
-def time_graphs(torch, graphs, steps, warmup, world=1):
-    for i in range(warmup):
-        graphs[i % len(graphs)].replay()
+def time_graphs(torch, rep, steps, warmup, world=1):
+    """Device time of exactly `steps` steps after `warmup` untimed ones (CUDA events on the
+    launching stream, barrier + synchronize on both sides)."""
+    rep.run(warmup)
     torch.cuda.synchronize()
     if world > 1:
         import torch.distributed as dist
@@ -308,8 +360,7 @@ def time_graphs(torch, graphs, steps, warmup, world=1):
     st = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(st)
-    for i in range(steps):
-        graphs[i % len(graphs)].replay()
+    rep.run(steps)
     e1.record(st)
     torch.cuda.synchronize()
     if world > 1:
@@ -392,7 +443,7 @@ def run_ours(args):
     # in from pinned host memory, runs the step's calls, and copies the outputs back.
     e2e = None
     if w.host_io is not None:
-        Xd, Yd, pk = w.host_io
+        Xd, Yd = w.host_io
         Xh = [x.cpu().pin_memory() for x in Xd]
         Yh = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in Yd]
         h2d = sum(x.numel() * 2 for x in Xh)
@@ -402,8 +453,8 @@ def run_ours(args):
         def e2e_step(i):
             for j in range(len(Xd)):
                 Xd[j].copy_(Xh[j], non_blocking=True)
-                packed, (K, N) = pk(i % C, j)
-                lb.lowbit_gemm_int4_path(Xd[j], packed, w.M, N, K, Yd[j], args.path)
+            w.step(i)
+            for j in range(len(Yd)):
                 Yh[j].copy_(Yd[j], non_blocking=True)
 
         for i in range(5):
@@ -431,7 +482,7 @@ def run_ours(args):
     rows = {}
     if not args.no_rows and rank == 0:
         names = [(n, 0) for n in WORKLOADS if n not in (args.workload, "tiny")]
-        names += [("decode", 1), ("decode", 2), ("binplane_m1", 1), ("binplane_m1", 2)]
+        names += [("decode", 2), ("binplane_m1", 1), ("binplane_m1", 2)]
         names = [nm for nm in names if nm != (args.workload, args.path)]
         rows = measure_rows(lb, torch, peak, l2, names)
 
@@ -453,7 +504,7 @@ def run_ours(args):
                        "weight_bytes_per_step": w.bytes, "rotating_copies": C,
                        "l2_policy": f"inputs larger than L2: {C} rotating weight copies, "
                                     f"{C * w.bytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB",
-                       "replay": "per-copy CUDA graphs", "kernel_path": args.path},
+                       "replay": "one CUDA graph per rotation of the weight copies", "kernel_path": args.path},
             "tok_s": round(w.tokens * args.steps * world / slowest, 1),
             "roofline": {"bound": "hbm", "achieved": round(per_rank_gbs, 2), "peak": peak,
                          "unit": "GB/s", "frac": round(per_rank_gbs / peak, 4),

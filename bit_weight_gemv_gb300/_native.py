@@ -34,6 +34,14 @@ _SIGS = {
     "lmhead_argmax_verify_path": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _sz, _i, _vp]),
     "lowbit_device_error": (_i, [_vp, ctypes.POINTER(_i)]),
 }
+
+
+class lowbit_gemm_desc(ctypes.Structure):
+    """One multiply of lowbit_gemm_int4_grouped (mirrors the C struct)."""
+    _fields_ = [("X", _vp), ("packed", _vp), ("Y", _vp), ("N", _i), ("K", _i)]
+
+
+_SIGS["lowbit_gemm_int4_grouped"] = (_i, [ctypes.POINTER(lowbit_gemm_desc), _i, _i, _vp])
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(lib, _name)
     _f.restype = _res
@@ -134,6 +142,18 @@ def lowbit_gemm_int4_path(X, packed, M, N, K, Y, path, stream=None):
     _gemm_args(X, packed, M, N, K, Y)
     _check(lib.lowbit_gemm_int4_path(_ptr(X), _ptr(packed), M, N, K, _ptr(Y), path,
                                      _stream(stream)), "lowbit_gemm_int4_path")
+
+
+def lowbit_gemm_int4_grouped(problems, M, stream=None):
+    """Several independent INT4 multiplies with a common M in one call.
+
+    problems: sequence of (X, packed, N, K, Y) tuples, 1 to 8 of them."""
+    n = len(problems)
+    arr = (lowbit_gemm_desc * max(1, n))()
+    for i, (X, packed, N, K, Y) in enumerate(problems):
+        _gemm_args(X, packed, M, N, K, Y)
+        arr[i] = lowbit_gemm_desc(X.data_ptr(), packed.data_ptr(), Y.data_ptr(), N, K)
+    _check(lib.lowbit_gemm_int4_grouped(arr, n, M, _stream(stream)), "lowbit_gemm_int4_grouped")
 
 
 def lowbit_gemm_binplane(X, packed, P, M, N, K, Y, stream=None):

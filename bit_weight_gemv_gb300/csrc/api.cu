@@ -124,10 +124,41 @@ lowbit_status lowbit_gemm_int4_path(const uint16_t* X, const void* packed, int M
   const uint8_t* pk = static_cast<const uint8_t*>(packed);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (path == 0) path = (M == 1) ? 1 : 2;
-  if (path == 1)
-    return from_cuda(M == 1 ? launch_int4_gemv(X, pk, N, K, Y, err, s)
-                            : launch_int4_gemm_cc(X, pk, M, N, K, Y, err, s));
+  if (path == 1 && M == 1) {
+    GemvProblem p = {X, pk, Y, N, K, 0, 1};
+    return from_cuda(launch_int4_stream(&p, 1, err, s));
+  }
+  if (path == 1) return from_cuda(launch_int4_gemm_cc(X, pk, M, N, K, Y, err, s));
   return from_cuda(launch_int4_gemm_tc(X, pk, M, N, K, Y, err, s));
+}
+
+lowbit_status lowbit_gemm_int4_grouped(const lowbit_gemm_desc* descs, int count, int M,
+                                       void* stream) {
+  if (!descs || count < 1 || count > kMaxGemvProblems) return LOWBIT_ERR_INVALID_ARG;
+  for (int i = 0; i < count; ++i) {
+    const lowbit_gemm_desc& d = descs[i];
+    if (!d.X || !d.packed || !d.Y) return LOWBIT_ERR_INVALID_ARG;
+    lowbit_status st = check_shape(M, d.N, d.K, 32);
+    if (st != LOWBIT_OK) return st;
+    if (!aligned16(d.X) || !aligned16(d.packed)) return LOWBIT_ERR_ALIGN;
+  }
+  int* err = device_error_word();
+  if (!err) return LOWBIT_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (M == 1) {
+    GemvProblem p[kMaxGemvProblems];
+    for (int i = 0; i < count; ++i)
+      p[i] = GemvProblem{descs[i].X, static_cast<const uint8_t*>(descs[i].packed), descs[i].Y,
+                         descs[i].N, descs[i].K, 0, 1};
+    return from_cuda(launch_int4_stream(p, count, err, s));
+  }
+  for (int i = 0; i < count; ++i) {
+    const lowbit_gemm_desc& d = descs[i];
+    const cudaError_t e = launch_int4_gemm_tc(d.X, static_cast<const uint8_t*>(d.packed), M, d.N,
+                                              d.K, d.Y, err, s);
+    if (e != cudaSuccess) return LOWBIT_ERR_CUDA;
+  }
+  return LOWBIT_OK;
 }
 
 lowbit_status lowbit_gemm_binplane(const uint16_t* X, const void* packed, int P, int M, int N,

@@ -102,12 +102,22 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
 
 int* device_error_word();  // address of the current device's error word (nullptr on failure)
 
+// One matrix of a streaming mat-vec launch (M = 1).  The launcher fills in the schedule.
+struct GemvProblem {
+  const uint16_t* X;       // [K] bf16
+  const uint8_t* packed;   // header + INT4 payload for (N, K)
+  uint16_t* Y;             // [N] bf16
+  int N, K;
+  int cluster_begin;       // first cluster of this matrix
+  int ks;                  // CTAs that split one tile's groups (divides the cluster size)
+};
+constexpr int kMaxGemvProblems = 8;
+
 cudaError_t launch_pack_int4(const int8_t* codes, const uint16_t* scales, int N, int K,
                              uint8_t* packed, cudaStream_t s);
 cudaError_t launch_pack_binplane(const uint8_t* bits, const uint16_t* alpha, int P, int N, int K,
                                  uint8_t* packed, cudaStream_t s);
-cudaError_t launch_int4_gemv(const uint16_t* X, const uint8_t* packed, int N, int K, uint16_t* Y,
-                             int* err, cudaStream_t s);
+cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int* err, cudaStream_t s);
 cudaError_t launch_int4_gemm_cc(const uint16_t* X, const uint8_t* packed, int M, int N, int K,
                                 uint16_t* Y, int* err, cudaStream_t s);
 cudaError_t launch_binplane_cc(const uint16_t* X, const uint8_t* packed, int P, int M, int N,

@@ -145,6 +145,10 @@ __global__ void pack_binplane_alpha(const uint16_t* __restrict__ alpha, int P, i
   *reinterpret_cast<uint16_t*>(dst) = (n < N) ? alpha[((long long)p * N + n) * G + g] : (uint16_t)0;
 }
 
+// Launched last by every pack call: the multiplies read their weights before their
+// programmatic-dependency wait, so the kernel right before one must not be a weight writer.
+__global__ void pack_done() {}
+
 inline unsigned blocks_for(long long units, int threads) {
   return (unsigned)((units + threads - 1) / threads);
 }
@@ -158,6 +162,7 @@ cudaError_t launch_pack_int4(const int8_t* codes, const uint16_t* scales, int N,
   pack_header<<<1, 32, 0, s>>>(packed, kFormatInt4, 0, N, K, int4_payload_bytes(N, K), kInt4Block);
   pack_int4_codes<<<blocks_for(cu, 256), 256, 0, s>>>(codes, N, K, packed + kHeaderBytes, cu);
   pack_int4_scales<<<blocks_for(su, 256), 256, 0, s>>>(scales, N, K, packed + kHeaderBytes, su);
+  pack_done<<<1, 32, 0, s>>>();
   return cudaGetLastError();
 }
 
@@ -168,6 +173,7 @@ cudaError_t launch_pack_binplane(const uint8_t* bits, const uint16_t* alpha, int
                                binplane_block(P));
   pack_binplane_codes<<<blocks_for(units, 256), 256, 0, s>>>(bits, P, N, K, packed + kHeaderBytes, units);
   pack_binplane_alpha<<<blocks_for(units, 256), 256, 0, s>>>(alpha, P, N, K, packed + kHeaderBytes, units);
+  pack_done<<<1, 32, 0, s>>>();
   return cudaGetLastError();
 }
 

@@ -1,0 +1,298 @@
+// Streaming INT4 mat-vec (M = 1) over one or several weight matrices in a single launch.
+//
+//   y[n] = sum_g s[n][g] * sum_{k in g} q[n][k] * x[k]
+// (Efficient-Qwen report, section 2.1: W = s (.) W_q with frozen symmetric per-group scales,
+// group 128, served as W4A16; at one token per step the cost is streaming the packed weights
+// once.)
+//
+// Work unit: one 128-row layout tile x a contiguous range of its groups.  The blocks of that
+// range are adjacent in the packed payload, so a producer lane moves each (tile, group) block
+// with one bulk copy into a ring of shared-memory stages.  The weights never depend on the
+// preceding kernel, so the first ring's worth is requested before the programmatic-dependency
+// wait and streams in while the previous kernel is still finishing; the activations of each
+// group (256 bytes) follow into the same stage once that wait returns.
+//
+// Schedule: every matrix gets its own split of K (ks CTAs per tile) so that no CTA holds much
+// more than a handful of blocks, whatever the matrix's K; a thread-block cluster of C CTAs
+// (C = the largest ks) holds C / ks tiles of one matrix, and each tile's partial sums meet in
+// distributed shared memory.  Clusters of the matrices with the most blocks per CTA come
+// first in the grid, so the longest CTAs start in the first wave.
+//
+// Arithmetic (in registers, fp32 accumulation): a nibble pair ORed into bf16 128.0 is the
+// exact pair (128 + u) = (q + 136); a mixed-precision fma multiplies it with the bf16
+// activation pair into fp32.  Per half group the bias is removed with the activations' sum:
+// sum (q + 136) x - 136 sum x = sum q x.  Each output is rounded once to bf16.
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace lowbit {
+namespace {
+
+constexpr int kCWarps = 8;                          // compute warps: 4 row quarters x 2 K halves
+constexpr int kSThreads = (kCWarps + 1) * 32;       // plus one producer warp
+constexpr uint32_t kXBytes = kGroup * 2;            // one group's bf16 activations
+constexpr uint32_t kStage = kInt4Block + kXBytes;   // 8704 bytes, a multiple of 16
+constexpr int kMaxStages = 6;      // 52 KB of ring: four CTAs per SM
+constexpr int kTargetBlocks = 5;   // blocks per CTA the K split aims for
+
+struct StreamArgs {
+  GemvProblem p[kMaxGemvProblems];
+  int count;
+  int stages;
+  int cluster;  // C
+  int* err;
+};
+
+__device__ __forceinline__ void grid_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+// acc += (q + 136) * x for the 8 inputs of one code word.  Nibble e of the word sits at bits
+// 4(e/2) + 16(e%2); x8 holds the word's 8 activations as 4 bf16 pairs (even input low).
+__device__ __forceinline__ void dot8(uint32_t w, const uint4& x8, float (&acc)[4]) {
+  fma_bf16x2_f32(acc[0], acc[1], int4_pair_biased<0>(w), x8.x);
+  fma_bf16x2_f32(acc[2], acc[3], int4_pair_biased<1>(w), x8.y);
+  fma_bf16x2_f32(acc[0], acc[1], int4_pair_biased<2>(w), x8.z);
+  fma_bf16x2_f32(acc[2], acc[3], int4_pair_biased<3>(w), x8.w);
+}
+
+__global__ void __launch_bounds__(kSThreads)
+int4_stream_kernel(const __grid_constant__ StreamArgs a) {
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ __align__(8) uint64_t full[kMaxStages];
+  __shared__ __align__(8) uint64_t empty[kMaxStages];
+  __shared__ float red[kCWarps][32];
+  __shared__ float part[kRowTile];
+  __shared__ int ok;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int C = a.cluster;
+  const int cid = (int)blockIdx.x / C, crank = (int)blockIdx.x % C;  // cluster, rank in it
+  int pi = 0;
+  for (int i = 1; i < a.count; ++i)
+    if (cid >= a.p[i].cluster_begin) pi = i;
+  const GemvProblem& pr = a.p[pi];
+  const int ks = pr.ks, rank = crank % ks;  // this CTA's share of its tile's groups
+  const int tile = (cid - pr.cluster_begin) * (C / ks) + crank / ks;
+  const int G = pr.K / kGroup;
+  const bool live = tile < row_tiles(pr.N);  // the last cluster of a matrix may be partly idle
+  const int g0 = (int)((long long)rank * G / ks), g1 = (int)((long long)(rank + 1) * G / ks);
+  const int nb = live ? g1 - g0 : 0;
+  const int S = a.stages;
+
+  if (threadIdx.x == 0) {
+    ok = live && header_matches(reinterpret_cast<const PackedHeader*>(pr.packed), kFormatInt4, 0,
+                                pr.N, pr.K);
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&empty[s]), kCWarps);
+    }
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) grid_launch();  // dependents may begin their own weight prefetch
+  const bool hdr_ok = ok != 0;
+  if (!hdr_ok && live && threadIdx.x == 0 && rank == 0 && tile == 0)
+    record_error(a.err, LOWBIT_ERR_INVALID_ARG);
+
+  float total = 0.f;
+  if (warp == kCWarps) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0 && hdr_ok) {
+      const uint8_t* wsrc = pr.packed + kHeaderBytes + ((size_t)tile * G + g0) * kInt4Block;
+      const uint16_t* xsrc = pr.X + (size_t)g0 * kGroup;
+      const int pre = min(nb, S);
+      for (int b = 0; b < pre; ++b) {
+        const uint32_t bar = ptx::smem_addr(&full[b]);
+        ptx::mbar_arrive_expect_tx(bar, kStage);
+        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)b * kStage), wsrc + (size_t)b * kInt4Block,
+                      kInt4Block, bar);
+      }
+      grid_wait();  // the activations may be the previous kernel's output
+      for (int b = 0; b < pre; ++b)
+        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)b * kStage + kInt4Block), xsrc + (size_t)b * kGroup,
+                      kXBytes, ptx::smem_addr(&full[b]));
+      int issued = pre;
+      for (int b = pre; b < nb; ++b) {
+        const int s = b % S;
+        if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), ((b / S) - 1) & 1)) {
+          record_error(a.err, LOWBIT_ERR_TIMEOUT);
+          break;
+        }
+        const uint32_t bar = ptx::smem_addr(&full[s]);
+        ptx::mbar_arrive_expect_tx(bar, kStage);
+        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)s * kStage), wsrc + (size_t)b * kInt4Block,
+                      kInt4Block, bar);
+        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)s * kStage + kInt4Block),
+                      xsrc + (size_t)b * kGroup, kXBytes, bar);
+        issued = b + 1;
+      }
+      // Copies still in flight must land before the CTA may exit.
+      for (int b = max(0, issued - S); b < issued; ++b)
+        ptx::mbar_wait(ptx::smem_addr(&full[b % S]), (b / S) & 1);
+    }
+    __syncwarp();
+  } else if (hdr_ok) {
+    // ---------------------------------------------------------------- compute
+    const int q = warp & 3, h = warp >> 2;  // rows 32q..32q+31, inputs 64h..64h+63 of each group
+    const int row = 32 * q + lane;
+    for (int b = 0; b < nb; ++b) {
+      const int s = b % S;
+      const bool landed = ptx::mbar_wait(ptx::smem_addr(&full[s]), (b / S) & 1);
+      if (!__all_sync(0xFFFFFFFFu, landed)) {  // warp-uniform exit keeps the warp converged
+        if (lane == 0) record_error(a.err, LOWBIT_ERR_TIMEOUT);
+        break;
+      }
+      const uint8_t* st = ring + (size_t)s * kStage;
+      const uint4 c0 = *reinterpret_cast<const uint4*>(st + (2 * h) * (kRowTile * 16) + row * 16);
+      const uint4 c1 = *reinterpret_cast<const uint4*>(st + (2 * h + 1) * (kRowTile * 16) + row * 16);
+      const float sc = half_bits_to_float(*reinterpret_cast<const uint16_t*>(st + kInt4ScaleOff + row * 2));
+      const uint8_t* xh = st + kInt4Block + h * 128;
+      const uint32_t xpair = reinterpret_cast<const uint32_t*>(xh)[lane];
+      const float xsum = warp_sum(bf16_bits_to_float((uint16_t)(xpair & 0xFFFFu)) +
+                                  bf16_bits_to_float((uint16_t)(xpair >> 16)));
+      const uint4* x8 = reinterpret_cast<const uint4*>(xh);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      dot8(c0.x, x8[0], acc);
+      dot8(c0.y, x8[1], acc);
+      dot8(c0.z, x8[2], acc);
+      dot8(c0.w, x8[3], acc);
+      dot8(c1.x, x8[4], acc);
+      dot8(c1.y, x8[5], acc);
+      dot8(c1.z, x8[6], acc);
+      dot8(c1.w, x8[7], acc);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&empty[s]));
+      total = fmaf(sc, ((acc[0] + acc[1]) + (acc[2] + acc[3])) - 136.f * xsum, total);
+    }
+  }
+
+  // -------------------------------------------------------------------- reduction + store
+  if (warp < kCWarps) red[warp][lane] = total;
+  __syncthreads();
+  if (threadIdx.x < kRowTile) {
+    const int q = threadIdx.x >> 5, l = threadIdx.x & 31;
+    part[threadIdx.x] = red[q][l] + red[q + 4][l];
+  }
+  const int n = tile * kRowTile + (int)threadIdx.x;
+  if (C > 1) {  // every CTA of the cluster takes part in both cluster barriers
+    ptx::cluster_sync();
+    if (ks > 1 && rank == 0 && hdr_ok && threadIdx.x < kRowTile) {
+      float y = 0.f;
+      const uint32_t la = ptx::smem_addr(&part[threadIdx.x]);
+      for (int r = 0; r < ks; ++r) y += ptx::ld_dsmem_f32(la, (uint32_t)(crank + r));
+      grid_wait();
+      if (n < pr.N) pr.Y[n] = float_to_bf16_bits(y);
+    } else if (ks == 1 && hdr_ok && threadIdx.x < kRowTile) {
+      grid_wait();
+      if (n < pr.N) pr.Y[n] = float_to_bf16_bits(part[threadIdx.x]);
+    }
+    ptx::cluster_sync();  // keep every rank's partials alive until they have been read
+  } else {
+    __syncthreads();
+    if (hdr_ok && threadIdx.x < kRowTile) {
+      grid_wait();
+      if (n < pr.N) pr.Y[n] = float_to_bf16_bits(part[threadIdx.x]);
+    }
+  }
+}
+
+int sm_count() {
+  int dev = 0, nsm = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  return nsm;
+}
+
+}  // namespace
+
+// Schedule: ks per matrix aims at kTargetBlocks blocks per CTA, then all splits are doubled
+// while the grid holds fewer than two CTAs per SM (small launches).  Matrices are ordered by
+// blocks per CTA, longest first.
+cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int* err, cudaStream_t s) {
+  if (count < 1 || count > kMaxGemvProblems) return cudaErrorInvalidValue;
+  const int nsm = sm_count();
+  StreamArgs a = {};
+  int ks[kMaxGemvProblems];
+  long long ctas = 0;
+  for (int i = 0; i < count; ++i) {
+    const int G = probs[i].K / kGroup;
+    int k = 1;
+    while (k < 8 && k * 2 <= G && (G + k - 1) / k > kTargetBlocks) k *= 2;
+    ks[i] = k;
+    ctas += (long long)row_tiles(probs[i].N) * k;
+  }
+  for (bool grew = true; grew && ctas < 2LL * nsm;) {
+    grew = false;
+    ctas = 0;
+    for (int i = 0; i < count; ++i) {
+      if (ks[i] < 8 && ks[i] * 2 <= probs[i].K / kGroup) {
+        ks[i] *= 2;
+        grew = true;
+      }
+      ctas += (long long)row_tiles(probs[i].N) * ks[i];
+    }
+  }
+  int C = 1;
+  for (int i = 0; i < count; ++i) C = ks[i] > C ? ks[i] : C;
+  int order[kMaxGemvProblems];
+  for (int i = 0; i < count; ++i) order[i] = i;
+  auto per_cta = [&](int i) { return (probs[i].K / kGroup + ks[i] - 1) / ks[i]; };
+  for (int i = 1; i < count; ++i)  // stable insertion sort: most blocks per CTA first
+    for (int j = i; j > 0 && per_cta(order[j]) > per_cta(order[j - 1]); --j) {
+      const int t = order[j];
+      order[j] = order[j - 1];
+      order[j - 1] = t;
+    }
+  long long clusters = 0;
+  int maxnb = 1;
+  for (int i = 0; i < count; ++i) {
+    const int o = order[i];
+    a.p[i] = probs[o];
+    a.p[i].ks = ks[o];
+    a.p[i].cluster_begin = (int)clusters;
+    const int tpc = C / ks[o];
+    clusters += (row_tiles(probs[o].N) + tpc - 1) / tpc;
+    maxnb = per_cta(o) > maxnb ? per_cta(o) : maxnb;
+  }
+  if (clusters * C > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  a.count = count;
+  a.cluster = C;
+  a.err = err;
+  a.stages = maxnb < kMaxStages ? maxnb : kMaxStages;
+  const size_t smem = (size_t)a.stages * kStage;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(int4_stream_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(clusters * C), 1, 1);
+  cfg.blockDim = dim3(kSThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (C > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)C;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, int4_stream_kernel, a);
+}
+
+}  // namespace lowbit

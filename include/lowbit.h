@@ -20,6 +20,12 @@
  *     check it against the call's arguments; on a mismatch they touch nothing else, write
  *     no output and record LOWBIT_ERR_INVALID_ARG in a per-device error word that
  *     lowbit_device_error() returns.  lowbit_validate_packed() checks a header synchronously.
+ *   - Multiplies are launched with programmatic dependent launch: they request their packed
+ *     weights (header included) before waiting for the preceding kernel on the stream, and
+ *     read activations / write outputs only after that wait.  So the kernel immediately
+ *     before a multiply on the same stream must not write that multiply's packed buffer.
+ *     lowbit_pack_int4 and lowbit_pack_binplane end with an empty kernel, which makes
+ *     "pack, then multiply" on one stream safe.
  *   - No C++ exception crosses this interface.
  */
 #ifndef LOWBIT_H
@@ -113,6 +119,26 @@ lowbit_status lowbit_validate_packed(const void* packed, int format, int P, int 
  * M = 1 runs the streaming GEMV; M >= 2 runs the tensor-core skinny GEMM. */
 lowbit_status lowbit_gemm_int4(const uint16_t* X, const void* packed, int M, int N, int K,
                                uint16_t* Y, void* stream);
+
+/* One multiply of a grouped call: the arguments of lowbit_gemm_int4 other than M. */
+typedef struct lowbit_gemm_desc {
+  const uint16_t* X;    /* bf16 [M][K], device, 16-byte aligned */
+  const void* packed;   /* from lowbit_pack_int4(N, K), device, 16-byte aligned */
+  uint16_t* Y;          /* bf16 [M][N], device */
+  int N;
+  int K;
+} lowbit_gemm_desc;
+
+/* Several independent INT4 multiplies with a common M (for example the q, k and v projections
+ * of a decoder layer, which read the same activations), each with the contract and rounding
+ * of lowbit_gemm_int4.  At M = 1 all of them run in ONE launch of the streaming GEMV, so the
+ * launch, pipeline fill and drain are paid once for the group instead of once per matrix;
+ * at M >= 2 each runs its own tensor-core launch, in order.
+ *   descs : HOST array of `count` descriptors, 1 <= count <= 8; read during the call only.
+ *   The multiplies must be independent: no Y may overlap any X, packed buffer or other Y of
+ *   the group.  Every descriptor is validated before anything is enqueued. */
+lowbit_status lowbit_gemm_int4_grouped(const lowbit_gemm_desc* descs, int count, int M,
+                                       void* stream);
 
 /* Y = X * W^T for binary-plane weights (ShiftAddQwen README, "Method" and "Format"):
  *   y[m][n] = sum_p sum_g alpha[p][n][g] * sum_{k in g} b[p][n][k] * x[m][k].

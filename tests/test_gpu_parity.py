@@ -241,3 +241,64 @@ def test_shape_errors_raise(lb):
     with pytest.raises(lb.LowbitError) as e:
         lb.lowbit_gemm_int4(bf16_dev(x), packed, 1, 64, 200, Y)
     assert e.value.status == 2
+
+
+# ------------------------------------------------------------------------- grouped multiplies
+
+def _grouped(lb, M, shapes, seed):
+    probs, refs = [], []
+    for j, (K, N) in enumerate(shapes):
+        codes, scales, x = synth.int4_problem(seed, M, N, K, j)
+        Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        probs.append((bf16_dev(x), pack_int4_gpu(lb, codes, scales), N, K, Y))
+        refs.append(oint4.gemm(x, codes, scales))
+    lb.lowbit_gemm_int4_grouped(probs, M)
+    torch.cuda.synchronize()
+    return [host_bits(p[4]) for p in probs], refs
+
+
+@pytest.mark.parametrize("M", [1, 16])
+def test_grouped_config1_layer_in_one_call(lb, M):
+    """The seven projections of the 4B-class layer as one grouped call (one launch at M=1)."""
+    shapes = synth.CONFIGS[1]["shapes"]
+    ys, refs = _grouped(lb, M, shapes, synth.CONFIGS[1]["seed"] if M == 1 else synth.CONFIGS[2]["seed"])
+    for j, (y, r) in enumerate(zip(ys, refs)):
+        check_gemm(y, r, f"grouped M={M} proj {j}")
+
+
+@pytest.mark.parametrize("shapes", [
+    ((512, 256),),
+    ((384, 257), (128, 1), (1280, 300)),
+    ((2560, 4096), (2560, 1024), (2560, 1024)),          # q, k, v share one launch
+    ((2560, 9728), (2560, 9728)),                        # gate, up
+    ((12288, 100), (128, 8), (256, 129), (640, 65), (128, 2), (1024, 33), (384, 1000), (896, 7)),
+])
+def test_grouped_ragged_mixes(lb, shapes):
+    ys, refs = _grouped(lb, 1, shapes, 11)
+    for j, (y, r) in enumerate(zip(ys, refs)):
+        check_gemm(y, r, f"grouped mix {shapes} item {j}")
+
+
+def test_grouped_matches_single_calls_bit_for_bit(lb):
+    """A matrix gives the same bf16 outputs alone and inside a group (same K split)."""
+    shapes = ((2560, 1024), (2560, 1024))
+    ys, _ = _grouped(lb, 1, shapes, 12)
+    codes, scales, x = synth.int4_problem(12, 1, 1024, 2560, 0)
+    y1 = gemm_int4_gpu(lb, x, pack_int4_gpu(lb, codes, scales), 1, 1024, 2560, 1)
+    check_gemm(y1, oint4.gemm(x, codes, scales), "single")
+    assert np.array_equal(ys[0], y1)
+
+
+def test_grouped_validation(lb):
+    codes, scales, x = synth.int4_problem(0, 1, 64, 256)
+    X, P = bf16_dev(x), pack_int4_gpu(lb, codes, scales)
+    Y = torch.empty((1, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(lb.LowbitError) as e:
+        lb.lowbit_gemm_int4_grouped([(X, P, 64, 256, Y)] * 9, 1)
+    assert e.value.status == 1
+    with pytest.raises(lb.LowbitError) as e:
+        lb.lowbit_gemm_int4_grouped([(X, P, 64, 256, Y), (X, P, 64, 100, Y)], 1)
+    assert e.value.status == 2
+    with pytest.raises(lb.LowbitError) as e:
+        lb.lowbit_gemm_int4_grouped([], 1)
+    assert e.value.status == 1

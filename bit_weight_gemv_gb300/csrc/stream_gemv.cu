@@ -34,6 +34,7 @@ constexpr uint32_t kXBytes = kGroup * 2;            // one group's bf16 activati
 constexpr uint32_t kStage = kInt4Block + kXBytes;   // 8704 bytes, a multiple of 16
 constexpr int kMaxStages = 6;      // 52 KB of ring: four CTAs per SM
 constexpr int kTargetBlocks = 5;   // blocks per CTA the K split aims for
+constexpr int kMaxSplit = 16;      // cluster sizes above 8 need the non-portable opt-in
 
 struct StreamArgs {
   GemvProblem p[kMaxGemvProblems];
@@ -225,7 +226,7 @@ cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int* err, cu
   for (int i = 0; i < count; ++i) {
     const int G = probs[i].K / kGroup;
     int k = 1;
-    while (k < 8 && k * 2 <= G && (G + k - 1) / k > kTargetBlocks) k *= 2;
+    while (k < kMaxSplit && k * 2 <= G && (G + k - 1) / k > kTargetBlocks) k *= 2;
     ks[i] = k;
     ctas += (long long)row_tiles(probs[i].N) * k;
   }
@@ -233,7 +234,7 @@ cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int* err, cu
     grew = false;
     ctas = 0;
     for (int i = 0; i < count; ++i) {
-      if (ks[i] < 8 && ks[i] * 2 <= probs[i].K / kGroup) {
+      if (ks[i] < kMaxSplit && ks[i] * 2 <= probs[i].K / kGroup) {
         ks[i] *= 2;
         grew = true;
       }
@@ -271,6 +272,11 @@ cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int* err, cu
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(int4_stream_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  if (C > 8) {
+    cudaError_t e = cudaFuncSetAttribute(int4_stream_kernel,
+                                         cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};

@@ -14,7 +14,7 @@ __all__ = [
     "lowbit_gemm_int4", "lowbit_int4_packed_bytes", "lowbit_pack_binplane", "lowbit_pack_int4",
     "lowbit_status_string", "lowbit_validate_packed", "lowbit_version",
     "lowbit_gemm_int4_path", "lowbit_gemm_binplane_path", "lmhead_argmax_verify_path",
-    "lowbit_gemm_int4_grouped", "lowbit_gemm_desc",
+    "lowbit_gemm_int4_grouped", "lowbit_gemm_desc", "lmhead_argmax_verify_noalloc",
 ]
 
 

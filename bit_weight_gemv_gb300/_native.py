@@ -42,6 +42,7 @@ class lowbit_gemm_desc(ctypes.Structure):
 
 
 _SIGS["lowbit_gemm_int4_grouped"] = (_i, [ctypes.POINTER(lowbit_gemm_desc), _i, _i, _vp])
+_SIGS["lmhead_argmax_verify_noalloc"] = (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp])
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(lib, _name)
     _f.restype = _res
@@ -197,6 +198,21 @@ def lmhead_argmax_verify_path(H, packed_head, M, N, K, draft, argmax, n_accept, 
                                          _ptr(argmax), _ptr(n_accept), _ptr(bonus),
                                          _ptr(workspace), workspace.numel(), path,
                                          _stream(stream)), "lmhead_argmax_verify_path")
+
+
+def lmhead_argmax_verify_noalloc(H, packed_head, M, N, K, draft, argmax, n_accept, bonus,
+                                 stream=None):
+    """lmhead_argmax_verify using the library's per-device scratch instead of a workspace
+    (for callers that cannot allocate; concurrent calls on one device race)."""
+    _need(H, torch.bfloat16, "H")
+    _need(packed_head, torch.uint8, "packed_head")
+    for t, nm in ((draft, "draft"), (argmax, "argmax"), (n_accept, "n_accept"), (bonus, "bonus")):
+        _need(t, torch.int32, nm)
+    if H.numel() < M * K or draft.numel() < M - 1 or argmax.numel() < M:
+        raise ValueError("H, draft or argmax too small")
+    _check(lib.lmhead_argmax_verify_noalloc(_ptr(H), _ptr(packed_head), M, N, K, _ptr(draft),
+                                            _ptr(argmax), _ptr(n_accept), _ptr(bonus),
+                                            _stream(stream)), "lmhead_argmax_verify_noalloc")
 
 
 def lowbit_device_error(stream=None) -> int:

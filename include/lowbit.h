@@ -164,6 +164,30 @@ lowbit_status lmhead_argmax_verify(const uint16_t* H, const void* packed_head, i
                                    size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------------
+ * For callers that cannot allocate device memory.
+ */
+
+/* lmhead_argmax_verify without the `workspace` argument.  The method has no counterpart to this
+ * function: it is a library convenience for callers that own no device allocator and so cannot
+ * provide the 512-byte workspace -- for example a plugin whose device memory is planned ahead
+ * of time by its host engine, or a C caller that links only this library and the CUDA runtime
+ * and must not allocate on its serving path.
+ *   Arguments, shapes, results and rounding are those of lmhead_argmax_verify.
+ *   Scratch: the library holds one 512-byte scratch per device in place of `workspace`.  The
+ *     first call on a device looks up its address (cudaGetSymbolAddress); make that first call
+ *     before any stream capture on that device.  Nothing is allocated or freed, ever.
+ *   Zeroing: the scratch must be zero when the kernel starts; every call clears it on `stream`
+ *     itself (cudaMemsetAsync) before the kernel, so the caller never has to.
+ *   Limit: shapes whose workspace (lmhead_workspace_bytes) would exceed 512 bytes return
+ *     LOWBIT_ERR_WORKSPACE; every shape lmhead_argmax_verify accepts fits today.
+ *   Concurrency: all calls on one device share the one scratch, so two calls that may run at
+ *     the same time (for example on two streams with no ordering between them) race and give
+ *     wrong results.  Order such calls, or use lmhead_argmax_verify with one workspace each. */
+lowbit_status lmhead_argmax_verify_noalloc(const uint16_t* H, const void* packed_head, int M,
+                                           int N, int K, const int32_t* draft, int32_t* argmax,
+                                           int32_t* n_accept, int32_t* bonus, void* stream);
+
+/* ------------------------------------------------------------------------------------------
  * Kernel-family selection (diagnostics and testing).  Same contract as the functions above,
  * plus `path`: 0 = the library's choice, 1 = the CUDA-core streaming kernels (row per lane,
  * in-register dequantisation, fp32 accumulation), 2 = the tensor-core kernels (dequantisation

@@ -3,12 +3,14 @@
 
 Headline workload (one "step"): decode through one 4B-class dense decoder layer -- the seven
 INT4 group-128 W4A16 projections (q, k, v, o, gate, up with K=2560; down with K=9728) at
-M=1, 50,012,160 algorithmic weight bytes per step.  Every step reads a different copy of the
-layer's packed weights (copies totalling more than 4x the L2 size), so timed weights come
-from HBM.  Steps are replayed from CUDA graphs (one per rotation of the weight copies) and
-timed with CUDA events.
+M=1, 50,012,160 algorithmic weight bytes per step, issued the way a decoder's data
+dependencies allow: lowbit_gemm_int4_grouped over (q, k, v), then o, then (gate, up), then
+down -- four launches.  Every step reads a different copy of the layer's packed weights
+(copies totalling more than 4x the L2 size), so timed weights come from HBM.  Steps are
+replayed from CUDA graphs (one per rotation of the weight copies) and timed with CUDA events.
 
-Also reported under "rows": the M=16 verify GEMM over the same layer and its batch sweep,
+Also reported under "rows": the same layer as seven single-matrix calls ("decode") and as one
+grouped call ("decode_all"), the M=16 verify GEMM over the same layer and its batch sweep,
 binary-plane GEMV/GEMM, and the LM-head argmax+verify over 248,320 and 32,768 rows.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-rows]
@@ -476,7 +478,7 @@ def run_ours(args):
         with open(tpath) as f:
             tj = json.load(f)
         ent = tj.get(f"{w.kernel}@{args.workload}")
-        if ent and ent.get("src_sha") == _src_sha():
+        if ent and ent.get("src_sha") == _src_sha(ent.get("sources", ())):
             traffic = ent.get("bytes_per_launch")
 
     rows = {}
@@ -523,15 +525,18 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def _src_sha():
-    """Hash of the CUDA sources; stored traffic counters are void once it changes."""
-    import glob
+def _src_sha(sources=()):
+    """Hash of the CUDA sources a stored counter was taken with (file names under
+    bit_weight_gemv_gb300/csrc); the stored value is void once any of them changes."""
     import hashlib
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "bit_weight_gemv_gb300", "csrc", "*"))):
+    for name in sorted(sources):
+        p = os.path.join(ROOT, "bit_weight_gemv_gb300", "csrc", name)
+        if not os.path.exists(p):
+            return None
         with open(p, "rb") as f:
-            h.update(f.read())
-    return h.hexdigest()[:16]
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16] if sources else None
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -583,7 +588,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-rows", action="store_true", help="skip the secondary rows")
-    ap.add_argument("--workload", choices=WORKLOADS, default="decode",
+    ap.add_argument("--workload", choices=WORKLOADS, default="decode_deps",
                     help="timed step (default: decode through one 4B-class layer, M=1)")
     ap.add_argument("--path", type=int, choices=(0, 1, 2), default=0,
                     help="kernel family: 0 library choice, 1 CUDA cores, 2 tensor cores")

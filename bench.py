@@ -213,7 +213,7 @@ def build_int4_layer(lb, torch, l2, M, path, seed, name, desc, grouping=None):
             w.calls.append([(lambda grp=grp, c=c: lb.lowbit_gemm_int4_grouped(
                 [(X[j], packs[j][c], shapes[j][1], shapes[j][0], Y[j]) for j in grp], M))
                 for grp in groups])
-        w.launches = len(groups) if M == 1 else len(shapes)
+        w.launches = len(groups)
     w.M, w.tokens = M, M
     w.host_io = (X, Y)
     return w
@@ -274,6 +274,13 @@ def build_workload(lb, torch, l2, name, path):
         return build_int4_layer(lb, torch, l2, 1, path, 1, name,
                                 "decode W4A16 GEMV over one 4B-class layer, M=1, " + how,
                                 grouping=grouping)
+    if name in ("verify_deps", "verify_all"):
+        grouping = name.split("_")[1]
+        how = ("grouped as a decoder's dependencies allow: (q,k,v), (o), (gate,up), (down), "
+               "one launch each" if grouping == "deps" else "all seven in one grouped launch")
+        return build_int4_layer(lb, torch, l2, 16, path, 2, name,
+                                "speculative-verify skinny GEMM over the same 4B-class layer, M=16, "
+                                + how, grouping=grouping)
     if name == "verify":
         return build_int4_layer(lb, torch, l2, 16, path, 2, name,
                                 "speculative-verify skinny GEMM over the same 4B-class layer, M=16")
@@ -303,7 +310,7 @@ def build_workload(lb, torch, l2, name, path):
     raise ValueError(name)
 
 
-WORKLOADS = ("decode", "decode_deps", "decode_all", "verify", "binplane_m1", "binplane_m16", "lmhead_full", "lmhead_trim",
+WORKLOADS = ("decode", "decode_deps", "decode_all", "verify", "verify_deps", "verify_all", "binplane_m1", "binplane_m16", "lmhead_full", "lmhead_trim",
              "tiny") + tuple(f"verify_m{m}" for m in synth.M_SWEEP if m not in (16,))
 
 

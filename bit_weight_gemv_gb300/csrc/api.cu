@@ -152,13 +152,11 @@ lowbit_status lowbit_gemm_int4_grouped(const lowbit_gemm_desc* descs, int count,
                          descs[i].N, descs[i].K, 0, 1};
     return from_cuda(launch_int4_stream(p, count, err, s));
   }
-  for (int i = 0; i < count; ++i) {
-    const lowbit_gemm_desc& d = descs[i];
-    const cudaError_t e = launch_int4_gemm_tc(d.X, static_cast<const uint8_t*>(d.packed), M, d.N,
-                                              d.K, d.Y, err, s);
-    if (e != cudaSuccess) return LOWBIT_ERR_CUDA;
-  }
-  return LOWBIT_OK;
+  GemvProblem p[kMaxGemvProblems];
+  for (int i = 0; i < count; ++i)
+    p[i] = GemvProblem{descs[i].X, static_cast<const uint8_t*>(descs[i].packed), descs[i].Y,
+                       descs[i].N, descs[i].K, 0, 1};
+  return from_cuda(launch_int4_tc_grouped(p, count, M, err, s));
 }
 
 lowbit_status lowbit_gemm_binplane(const uint16_t* X, const void* packed, int P, int M, int N,

@@ -104,9 +104,9 @@ int* device_error_word();  // address of the current device's error word (nullpt
 
 // One matrix of a streaming mat-vec launch (M = 1).  The launcher fills in the schedule.
 struct GemvProblem {
-  const uint16_t* X;       // [K] bf16
+  const uint16_t* X;       // [M][K] bf16 (M = 1 for the streaming kernel)
   const uint8_t* packed;   // header + INT4 payload for (N, K)
-  uint16_t* Y;             // [N] bf16
+  uint16_t* Y;             // [M][N] bf16
   int N, K;
   int cluster_begin;       // first cluster of this matrix
   int ks;                  // CTAs that split one tile's groups (divides the cluster size)
@@ -118,6 +118,9 @@ cudaError_t launch_pack_int4(const int8_t* codes, const uint16_t* scales, int N,
 cudaError_t launch_pack_binplane(const uint8_t* bits, const uint16_t* alpha, int P, int N, int K,
                                  uint8_t* packed, cudaStream_t s);
 cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int* err, cudaStream_t s);
+// Several INT4 multiplies with a common M >= 2 in one tensor-core launch (X, Y are [M][K], [M][N]).
+cudaError_t launch_int4_tc_grouped(const GemvProblem* probs, int count, int M, int* err,
+                                   cudaStream_t s);
 cudaError_t launch_int4_gemm_cc(const uint16_t* X, const uint8_t* packed, int M, int N, int K,
                                 uint16_t* Y, int* err, cudaStream_t s);
 cudaError_t launch_binplane_cc(const uint16_t* X, const uint8_t* packed, int P, int M, int N,

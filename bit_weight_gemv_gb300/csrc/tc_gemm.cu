@@ -55,12 +55,24 @@ struct TcArgs {
   uint16_t* Y;
   int M, N, K, P;
   int groups_per_rank;
+  int ks;            // CTAs splitting one row block's groups (divides the cluster size)
+  int cl_begin;      // first cluster of this matrix
+  int ncl;           // clusters of this matrix (they walk its row blocks with stride ncl * C / ks)
   int* err;
   LmheadWorkspace* ws;
   const int32_t* draft;
   int32_t* argmax;
   int32_t* n_accept;
   int32_t* bonus;
+};
+
+// One launch: up to kMaxGemvProblems matrices sharing M, each with its activation tensor map.
+// A cluster of `cluster` CTAs holds cluster / ks row blocks of one matrix.
+struct TcBatch {
+  CUtensorMap maps[kMaxGemvProblems];
+  TcArgs p[kMaxGemvProblems];
+  int count;
+  int cluster;
 };
 
 template <int FMT, int NMMA>
@@ -124,12 +136,19 @@ __device__ __forceinline__ void grid_launch_dependents() {
 
 template <int FMT, int NMMA, int EPI>
 __global__ void __launch_bounds__(kThreads, 2)
-tc_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs args) {
+tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
   using L = TcLayout<FMT, NMMA>;
   constexpr int S = L::kStages;
   constexpr int TOK = NMMA / 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const int C = batch.cluster;
+  const int cid = (int)blockIdx.x / C, crank = (int)blockIdx.x % C;  // cluster, rank in it
+  int pi = 0;
+  for (int i = 1; i < batch.count; ++i)
+    if (cid >= batch.p[i].cl_begin) pi = i;
+  const TcArgs& args = batch.p[pi];
+  const CUtensorMap* xmap = &batch.maps[pi];
   const int P = (FMT == kFmtInt4) ? 1 : args.P;
   const uint32_t SB = L::stage(P), BB = L::block(P);
   constexpr int NB = L::NB;
@@ -144,13 +163,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs args) {
   volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] header ok, [1] abort
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rank = blockIdx.x, ks = gridDim.x;
+  const int ks = args.ks, rank = crank % ks;
   const int N = args.N, K = args.K, G = K / kGroup, RB = row_tiles(N);
+  const int tile0 = (cid - args.cl_begin) * (C / ks) + crank / ks;  // first row block
+  const int tstride = args.ncl * (C / ks);                            // row-block stride
   const int g0 = min(G, rank * args.groups_per_rank);
   const int g1 = min(G, g0 + args.groups_per_rank);
   const int ngroups = g1 - g0;
   const int upi = ngroups * P;  // units per item
-  const int nitems = (RB - (int)blockIdx.y + (int)gridDim.y - 1) / (int)gridDim.y;
+  const int nitems = tile0 < RB ? (RB - tile0 + tstride - 1) / tstride : 0;
   const int total_groups = nitems * ngroups;
   const int total_units = nitems * upi;
 
@@ -182,7 +203,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs args) {
   if (threadIdx.x == 0) grid_launch_dependents();
   const uint32_t tmem = *tmem_slot;
   const bool hdr_ok = flags[0] != 0;
-  if (!hdr_ok && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
+  if (!hdr_ok && threadIdx.x == 0 && rank == 0 && tile0 == 0)
     record_error(args.err, LOWBIT_ERR_INVALID_ARG);
 
   const uint8_t* payload = args.packed + kHeaderBytes;
@@ -194,7 +215,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs args) {
       record_error(args.err, LOWBIT_ERR_TIMEOUT);
     }
   };
-  auto item_rb = [&](int it) { return (int)blockIdx.y + it * (int)gridDim.y; };
+  auto item_rb = [&](int it) { return tile0 + it * tstride; };
 
   float acc[TOK];
 #pragma unroll
@@ -213,8 +234,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs args) {
       };
       auto issue_x = [&](int gi) {
         const int s = gi % S, g = g0 + gi % ngroups;
-        tma_load_2d(smem_addr(stage_x(s)), &xmap, g * kGroup, 0, smem_addr(&full[s]));
-        tma_load_2d(smem_addr(stage_x(s)) + L::kAtom, &xmap, g * kGroup + 64, 0, smem_addr(&full[s]));
+        tma_load_2d(smem_addr(stage_x(s)), xmap, g * kGroup, 0, smem_addr(&full[s]));
+        tma_load_2d(smem_addr(stage_x(s)) + L::kAtom, xmap, g * kGroup + 64, 0, smem_addr(&full[s]));
       };
       const int pre = min(S, total_groups);
       for (int gi = 0; gi < pre; ++gi) {
@@ -412,21 +433,22 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs args) {
   // ------------------------------------------------------------------ split-K reduction
   grid_dependency_wait();  // every thread that writes outputs has waited for the previous grid
   __syncthreads();
-  if (ks > 1) {
-    // One item per CTA; every rank's partial sums go through shared memory (the stage ring
-    // is free now) and each rank reduces a slice of the rows across the cluster.
+  if (C > 1) {  // every CTA of the cluster takes part in both cluster barriers
+    // With ks > 1 a CTA has one item; every rank's partial sums go through shared memory
+    // (the stage ring is free now) and each rank reduces a slice of the rows across the
+    // ks CTAs of its row block.
     float* red = reinterpret_cast<float*>(smem);  // [NMMA][128]
-    if (hdr_ok && warp < kDqWarps && epi_active) {
+    if (ks > 1 && hdr_ok && warp < kDqWarps && epi_active) {
 #pragma unroll
       for (int j = 0; j < TOK; ++j) red[(tok0 + j) * kBlockRows + r] = acc[j];
     }
     cluster_sync();
-    if (hdr_ok && nitems > 0) {
-      const int rows = kBlockRows / ks, r0 = rank * rows, rb = blockIdx.y;
+    if (ks > 1 && hdr_ok && nitems > 0) {
+      const int rows = kBlockRows / ks, r0 = rank * rows, rb = tile0, base = crank - rank;
       auto reduced = [&](int t, int rr) {
         const uint32_t la = smem_addr(&red[t * kBlockRows + rr]);
         float v = 0.f;
-        for (int qq = 0; qq < ks; ++qq) v += ld_dsmem_f32(la, qq);
+        for (int qq = 0; qq < ks; ++qq) v += ld_dsmem_f32(la, (uint32_t)(base + qq));
         return v;
       };
       if constexpr (EPI == kEpiStore) {
@@ -493,30 +515,72 @@ int sm_count() {
 }
 
 template <int FMT, int NMMA, int EPI>
-cudaError_t launch_tc(TcArgs args, cudaStream_t stream) {
+cudaError_t launch_tc_batch(const TcArgs* probs, int count, cudaStream_t stream) {
   using L = TcLayout<FMT, NMMA>;
+  if (count < 1 || count > kMaxGemvProblems) return cudaErrorInvalidValue;
   auto encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
-  // X [M][K] bf16; one box = one 64-input swizzle atom for NMMA rows (rows >= M read as 0).
-  CUtensorMap map;
-  cuuint64_t dims[2] = {(cuuint64_t)args.K, (cuuint64_t)args.M};
-  cuuint64_t strides[1] = {(cuuint64_t)args.K * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)NMMA};
-  cuuint32_t estr[2] = {1, 1};
-  if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(args.X), dims,
-             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-  const int RB = row_tiles(args.N), G = args.K / kGroup;
-  const int slots = 2 * sm_count();
-  // Split K across a cluster only when the row blocks alone cannot fill the GPU.
-  int ks = 1;
-  while (ks < 8 && RB * ks * 2 <= slots && ks * 2 <= G) ks *= 2;
-  args.groups_per_rank = (G + ks - 1) / ks;
-  // With one rank per row block the grid is persistent: at most two CTAs per SM, each
-  // walking row blocks blockIdx.y, blockIdx.y + gridDim.y, ...
-  const int gy = (ks == 1) ? (RB < slots ? RB : slots) : RB;
-  const int P = FMT == kFmtInt4 ? 1 : args.P;
+  TcBatch batch = {};
+  const int slots = 2 * sm_count();  // at most two CTAs per SM (tensor memory, shared memory)
+  int ks[kMaxGemvProblems];
+  if (count == 1) {
+    // Split K across a cluster only when the row blocks alone cannot fill the GPU.
+    const int RB = row_tiles(probs[0].N), G = probs[0].K / kGroup;
+    int k = 1;
+    while (k < 8 && RB * k * 2 <= slots && k * 2 <= G) k *= 2;
+    ks[0] = k;
+  } else {
+    // Several matrices: each takes the smallest power-of-two K split whose CTAs hold at most
+    // the launch's groups per slot (so tall-K matrices do not become the long pole).
+    long long units = 0;
+    for (int i = 0; i < count; ++i) units += (long long)row_tiles(probs[i].N) * (probs[i].K / kGroup);
+    long long target = (units + slots - 1) / slots;
+    if (target < 4) target = 4;
+    for (int i = 0; i < count; ++i) {
+      const int G = probs[i].K / kGroup;
+      int k = 1;
+      while (k < 8 && k * 2 <= G && (G + k - 1) / k > target) k *= 2;
+      ks[i] = k;
+    }
+  }
+  int C = 1;
+  for (int i = 0; i < count; ++i) C = ks[i] > C ? ks[i] : C;
+  int order[kMaxGemvProblems];
+  for (int i = 0; i < count; ++i) order[i] = i;
+  auto per_cta = [&](int i) { return (probs[i].K / kGroup + ks[i] - 1) / ks[i]; };
+  for (int i = 1; i < count; ++i)  // stable insertion sort: most groups per CTA first
+    for (int j = i; j > 0 && per_cta(order[j]) > per_cta(order[j - 1]); --j) {
+      const int t = order[j];
+      order[j] = order[j - 1];
+      order[j - 1] = t;
+    }
+  long long clusters = 0;
+  for (int i = 0; i < count; ++i) {
+    const int o = order[i];
+    TcArgs a = probs[o];
+    const int RB = row_tiles(a.N), G = a.K / kGroup, tpc = C / ks[o];
+    a.ks = ks[o];
+    a.groups_per_rank = (G + ks[o] - 1) / ks[o];
+    a.cl_begin = (int)clusters;
+    // A single matrix with no K split runs persistent (at most `slots` CTAs walking its row
+    // blocks); otherwise every row block gets its own CTAs.
+    a.ncl = (count == 1 && C == 1) ? (RB < slots ? RB : slots) : (RB + tpc - 1) / tpc;
+    clusters += a.ncl;
+    batch.p[i] = a;
+    // X [M][K] bf16; one box = one 64-input swizzle atom for NMMA rows (rows >= M read as 0).
+    cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
+    cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)NMMA};
+    cuuint32_t estr[2] = {1, 1};
+    if (encode(&batch.maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(a.X), dims,
+               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  if (clusters * C > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  batch.count = count;
+  batch.cluster = C;
+  const int P = FMT == kFmtInt4 ? 1 : probs[0].P;
   // At least 80 KB of shared memory per CTA keeps at most two CTAs on an SM, so their two
   // 256-column TMEM allocations always fit and tcgen05.alloc never has to wait.
   const size_t smem = L::smem(P) > 80 * 1024 ? L::smem(P) : 80 * 1024;
@@ -524,7 +588,7 @@ cudaError_t launch_tc(TcArgs args, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)ks, (unsigned)gy, 1);
+  cfg.gridDim = dim3((unsigned)(clusters * C), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -533,16 +597,21 @@ cudaError_t launch_tc(TcArgs args, cudaStream_t stream) {
   attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[na].val.programmaticStreamSerializationAllowed = 1;
   ++na;
-  if (ks > 1) {
+  if (C > 1) {
     attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = (unsigned)ks;
+    attr[na].val.clusterDim.x = (unsigned)C;
     attr[na].val.clusterDim.y = 1;
     attr[na].val.clusterDim.z = 1;
     ++na;
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, kern, map, args);
+  return cudaLaunchKernelEx(&cfg, kern, batch);
+}
+
+template <int FMT, int NMMA, int EPI>
+cudaError_t launch_tc(TcArgs args, cudaStream_t stream) {
+  return launch_tc_batch<FMT, NMMA, EPI>(&args, 1, stream);
 }
 
 TcArgs base_args(const uint16_t* X, const uint8_t* packed, int P, int M, int N, int K, int* err) {
@@ -565,6 +634,18 @@ cudaError_t launch_int4_gemm_tc(const uint16_t* X, const uint8_t* packed, int M,
   a.Y = Y;
   return M <= 16 ? launch_tc<kFmtInt4, 16, kEpiStore>(a, s)
                  : launch_tc<kFmtInt4, 32, kEpiStore>(a, s);
+}
+
+cudaError_t launch_int4_tc_grouped(const GemvProblem* probs, int count, int M, int* err,
+                                   cudaStream_t s) {
+  if (count < 1 || count > kMaxGemvProblems) return cudaErrorInvalidValue;
+  TcArgs a[kMaxGemvProblems];
+  for (int i = 0; i < count; ++i) {
+    a[i] = base_args(probs[i].X, probs[i].packed, 1, M, probs[i].N, probs[i].K, err);
+    a[i].Y = probs[i].Y;
+  }
+  return M <= 16 ? launch_tc_batch<kFmtInt4, 16, kEpiStore>(a, count, s)
+                 : launch_tc_batch<kFmtInt4, 32, kEpiStore>(a, count, s);
 }
 
 cudaError_t launch_binplane_tc(const uint16_t* X, const uint8_t* packed, int P, int M, int N,

@@ -273,10 +273,11 @@ def test_grouped_config1_layer_in_one_call(lb, M):
     ((2560, 9728), (2560, 9728)),                        # gate, up
     ((12288, 100), (128, 8), (256, 129), (640, 65), (128, 2), (1024, 33), (384, 1000), (896, 7)),
 ])
-def test_grouped_ragged_mixes(lb, shapes):
-    ys, refs = _grouped(lb, 1, shapes, 11)
+@pytest.mark.parametrize("M", [1, 2, 16, 32])
+def test_grouped_ragged_mixes(lb, shapes, M):
+    ys, refs = _grouped(lb, M, shapes, 11)
     for j, (y, r) in enumerate(zip(ys, refs)):
-        check_gemm(y, r, f"grouped mix {shapes} item {j}")
+        check_gemm(y, r, f"grouped M={M} mix {shapes} item {j}")
 
 
 def test_grouped_matches_single_calls_bit_for_bit(lb):

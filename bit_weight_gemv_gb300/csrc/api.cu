@@ -1,5 +1,6 @@
 // extern "C" entry points of liblowbit.so: host-side validation, then kernel dispatch.
 // Declarations and the full contract are in include/lowbit.h.
+#include <cudaTypedefs.h>
 #include <string.h>
 
 #include "common.cuh"
@@ -36,6 +37,27 @@ int* device_error_word() {
     g_err_ptr[dev] = static_cast<int*>(p);
   }
   return g_err_ptr[dev];
+}
+
+bool allocation_covers(const void* p, size_t bytes) {
+  static PFN_cuPointerGetAttribute_v4000 get_attr = nullptr;
+  static bool looked_up = false;
+  if (!looked_up) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &fn, 4000, cudaEnableDefault,
+                                         &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      get_attr = reinterpret_cast<PFN_cuPointerGetAttribute_v4000>(fn);
+    looked_up = true;
+  }
+  if (!get_attr || !p) return false;
+  CUdeviceptr start = 0;
+  size_t size = 0;
+  const CUdeviceptr dp = (CUdeviceptr)(uintptr_t)p;
+  if (get_attr(&start, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, dp) != CUDA_SUCCESS) return false;
+  if (get_attr(&size, CU_POINTER_ATTRIBUTE_RANGE_SIZE, dp) != CUDA_SUCCESS) return false;
+  return dp >= start && bytes <= size && dp - start <= size - bytes;
 }
 
 }  // namespace lowbit
@@ -125,7 +147,8 @@ lowbit_status lowbit_gemm_int4_path(const uint16_t* X, const void* packed, int M
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (path == 0) path = (M == 1) ? 1 : 2;
   if (path == 1 && M == 1) {
-    GemvProblem p = {X, pk, Y, N, K, 0, 1};
+    GemvProblem p = {X, pk, Y, N, K, 0, 1, 0, 0};
+    p.early = allocation_covers(pk, kHeaderBytes + int4_payload_bytes(N, K)) ? 1 : 0;
     return from_cuda(launch_int4_stream(&p, 1, err, s));
   }
   if (path == 1) return from_cuda(launch_int4_gemm_cc(X, pk, M, N, K, Y, err, s));
@@ -147,15 +170,18 @@ lowbit_status lowbit_gemm_int4_grouped(const lowbit_gemm_desc* descs, int count,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (M == 1) {
     GemvProblem p[kMaxGemvProblems];
-    for (int i = 0; i < count; ++i)
+    for (int i = 0; i < count; ++i) {
       p[i] = GemvProblem{descs[i].X, static_cast<const uint8_t*>(descs[i].packed), descs[i].Y,
-                         descs[i].N, descs[i].K, 0, 1};
+                         descs[i].N, descs[i].K, 0, 1, 0, 0};
+      p[i].early = allocation_covers(descs[i].packed,
+                                     kHeaderBytes + int4_payload_bytes(descs[i].N, descs[i].K)) ? 1 : 0;
+    }
     return from_cuda(launch_int4_stream(p, count, err, s));
   }
   GemvProblem p[kMaxGemvProblems];
   for (int i = 0; i < count; ++i)
     p[i] = GemvProblem{descs[i].X, static_cast<const uint8_t*>(descs[i].packed), descs[i].Y,
-                       descs[i].N, descs[i].K, 0, 1};
+                       descs[i].N, descs[i].K, 0, 1, 0, 0};
   return from_cuda(launch_int4_tc_grouped(p, count, M, err, s));
 }
 

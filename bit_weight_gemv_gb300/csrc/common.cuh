@@ -102,14 +102,22 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
 
 int* device_error_word();  // address of the current device's error word (nullptr on failure)
 
+// True when [p, p + bytes) lies inside one device allocation (driver range query); false when
+// it does not or when the query is unavailable.
+bool allocation_covers(const void* p, size_t bytes);
+
 // One matrix of a streaming mat-vec launch (M = 1).  The launcher fills in the schedule.
-struct GemvProblem {
+// 64-byte aligned: a kernel reads one problem's fields from one cache line of its parameters.
+struct alignas(64) GemvProblem {
   const uint16_t* X;       // [M][K] bf16 (M = 1 for the streaming kernel)
   const uint8_t* packed;   // header + INT4 payload for (N, K)
   uint16_t* Y;             // [M][N] bf16
   int N, K;
   int cluster_begin;       // first cluster of this matrix
   int ks;                  // CTAs that split one tile's groups (divides the cluster size)
+  int early;               // 1: the payload is known to lie inside packed's allocation, so
+                           //    weight copies may start before the header has been checked
+  int pad_;
 };
 constexpr int kMaxGemvProblems = 8;
 

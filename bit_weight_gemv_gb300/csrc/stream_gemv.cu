@@ -36,12 +36,16 @@ constexpr int kMaxStages = 6;      // 52 KB of ring: four CTAs per SM
 constexpr int kTargetBlocks = 5;   // blocks per CTA the K split aims for
 constexpr int kMaxSplit = 16;      // cluster sizes above 8 need the non-portable opt-in
 
+// The first cache line holds what every CTA reads first (to find its matrix); each matrix's
+// fields sit in their own 64-byte line after it.
 struct StreamArgs {
-  GemvProblem p[kMaxGemvProblems];
   int count;
   int stages;
   int cluster;  // C
+  int pad_;
+  int cl_begin[kMaxGemvProblems];  // copy of p[i].cluster_begin
   int* err;
+  GemvProblem p[kMaxGemvProblems];
 };
 
 __device__ __forceinline__ void grid_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -69,6 +73,7 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ __align__(8) uint64_t full[kMaxStages];
   __shared__ __align__(8) uint64_t empty[kMaxStages];
+  __shared__ __align__(8) uint64_t redbar;  // rank 0 of a split tile: partials have arrived
   __shared__ float red[kCWarps][32];
   __shared__ float part[kRowTile];
   __shared__ int ok;
@@ -78,7 +83,7 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
   const int cid = (int)blockIdx.x / C, crank = (int)blockIdx.x % C;  // cluster, rank in it
   int pi = 0;
   for (int i = 1; i < a.count; ++i)
-    if (cid >= a.p[i].cluster_begin) pi = i;
+    if (cid >= a.cl_begin[i]) pi = i;
   const GemvProblem& pr = a.p[pi];
   const int ks = pr.ks, rank = crank % ks;  // this CTA's share of its tile's groups
   const int tile = (cid - pr.cluster_begin) * (C / ks) + crank / ks;
@@ -89,19 +94,29 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
   const int S = a.stages;
 
   if (threadIdx.x == 0) {
-    ok = live && header_matches(reinterpret_cast<const PackedHeader*>(pr.packed), kFormatInt4, 0,
-                                pr.N, pr.K);
+    // With `early`, the header is checked in parallel with the first copies (it then gates
+    // only the outputs); otherwise it is checked before anything else is read.
+    ok = live && (pr.early || header_matches(reinterpret_cast<const PackedHeader*>(pr.packed),
+                                             kFormatInt4, 0, pr.N, pr.K));
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
       ptx::mbar_init(ptx::smem_addr(&empty[s]), kCWarps);
     }
+    // rank 0 of a split tile receives one arrival per row from each other rank
+    ptx::mbar_init(ptx::smem_addr(&redbar), (uint32_t)(kRowTile * (ks > 1 ? ks - 1 : 1)));
     ptx::fence_mbar_init();
   }
   __syncthreads();
+  // Half of a cluster barrier: its wait, just before the partial sums are exchanged, finds
+  // every CTA's barriers initialised (and returns at once, as all arrived long before).
+  if (C > 1) ptx::cluster_arrive();
   if (threadIdx.x == 0) grid_launch();  // dependents may begin their own weight prefetch
-  const bool hdr_ok = ok != 0;
-  if (!hdr_ok && live && threadIdx.x == 0 && rank == 0 && tile == 0)
-    record_error(a.err, LOWBIT_ERR_INVALID_ARG);
+  const bool hdr_ok = ok != 0;  // with `early`: only "this CTA has work"; see out_ok below
+  // A compute warp checks the header (it would only be waiting for its first stage); the
+  // producer warp must not wait on this load before issuing its copies.
+  if (pr.early && live && threadIdx.x == 0 &&
+      !header_matches(reinterpret_cast<const PackedHeader*>(pr.packed), kFormatInt4, 0, pr.N, pr.K))
+    ok = 0;  // read after the epilogue's barrier
 
   float total = 0.f;
   if (warp == kCWarps) {
@@ -178,27 +193,38 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
   // -------------------------------------------------------------------- reduction + store
   if (warp < kCWarps) red[warp][lane] = total;
   __syncthreads();
+  const bool out_ok = ok != 0;  // header verified (before or alongside the copies)
+  if (!out_ok && live && threadIdx.x == 0 && rank == 0 && tile == 0)
+    record_error(a.err, LOWBIT_ERR_INVALID_ARG);
   if (threadIdx.x < kRowTile) {
     const int q = threadIdx.x >> 5, l = threadIdx.x & 31;
     part[threadIdx.x] = red[q][l] + red[q + 4][l];
   }
   const int n = tile * kRowTile + (int)threadIdx.x;
-  if (C > 1) {  // every CTA of the cluster takes part in both cluster barriers
-    ptx::cluster_sync();
-    if (ks > 1 && rank == 0 && hdr_ok && threadIdx.x < kRowTile) {
-      float y = 0.f;
-      const uint32_t la = ptx::smem_addr(&part[threadIdx.x]);
-      for (int r = 0; r < ks; ++r) y += ptx::ld_dsmem_f32(la, (uint32_t)(crank + r));
-      grid_wait();
-      if (n < pr.N) pr.Y[n] = float_to_bf16_bits(y);
-    } else if (ks == 1 && hdr_ok && threadIdx.x < kRowTile) {
-      grid_wait();
-      if (n < pr.N) pr.Y[n] = float_to_bf16_bits(part[threadIdx.x]);
+  if (C > 1) ptx::cluster_wait();
+  if (ks > 1) {
+    // Ranks 1..ks-1 push their partial sums into rank 0's slots (one float per row, each
+    // followed by a remote arrival) and leave; rank 0 waits for them, adds them in rank
+    // order and stores.
+    float* slots = reinterpret_cast<float*>(ring + (size_t)S * kStage);  // [ks-1][128]
+    const uint32_t owner = (uint32_t)(crank - rank);                    // rank 0's CTA
+    if (live && threadIdx.x < kRowTile) {
+      if (rank != 0) {
+        const uint32_t la = ptx::smem_addr(&slots[(rank - 1) * kRowTile + threadIdx.x]);
+        ptx::st_dsmem_f32(ptx::map_to_rank(la, owner), part[threadIdx.x]);
+        ptx::mbar_arrive_remote(ptx::map_to_rank(ptx::smem_addr(&redbar), owner));
+      } else {
+        const bool got = ptx::mbar_wait_cluster(ptx::smem_addr(&redbar), 0);
+        if (!got) record_error(a.err, LOWBIT_ERR_TIMEOUT);
+        float y = part[threadIdx.x];
+        for (int r = 1; r < ks; ++r) y += slots[(r - 1) * kRowTile + threadIdx.x];
+        grid_wait();
+        if (got && out_ok && n < pr.N) pr.Y[n] = float_to_bf16_bits(y);
+      }
     }
-    ptx::cluster_sync();  // keep every rank's partials alive until they have been read
   } else {
     __syncthreads();
-    if (hdr_ok && threadIdx.x < kRowTile) {
+    if (out_ok && threadIdx.x < kRowTile) {
       grid_wait();
       if (n < pr.N) pr.Y[n] = float_to_bf16_bits(part[threadIdx.x]);
     }
@@ -259,6 +285,7 @@ cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int* err, cu
     a.p[i] = probs[o];
     a.p[i].ks = ks[o];
     a.p[i].cluster_begin = (int)clusters;
+    a.cl_begin[i] = (int)clusters;
     const int tpc = C / ks[o];
     clusters += (row_tiles(probs[o].N) + tpc - 1) / tpc;
     maxnb = per_cta(o) > maxnb ? per_cta(o) : maxnb;
@@ -268,7 +295,10 @@ cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int* err, cu
   a.cluster = C;
   a.err = err;
   a.stages = maxnb < kMaxStages ? maxnb : kMaxStages;
-  const size_t smem = (size_t)a.stages * kStage;
+  int kmax = 1;
+  for (int i = 0; i < count; ++i) kmax = ks[i] > kmax ? ks[i] : kmax;
+  // ring, then the partial-sum slots rank 0 of a split tile receives
+  const size_t smem = (size_t)a.stages * kStage + (size_t)(kmax - 1) * kRowTile * sizeof(float);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(int4_stream_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -220,7 +220,7 @@ def build_int4_layer(lb, torch, l2, M, path, seed, name, desc, grouping=None):
 
 
 def build_binplane(lb, torch, l2, M, path, name, desc):
-    w = Workload(name, desc, "binplane_cc_kernel" if (M == 1 and path == 1) else "tc_gemm_kernel")
+    w = Workload(name, desc, "bp_stream_kernel" if (M == 1 and path != 2) else "tc_gemm_kernel")
     mats = []
     for si, (K, N) in enumerate(synth.BINPLANE_SHAPES):
         for P in synth.BINPLANE_PLANES:

@@ -202,6 +202,11 @@ lowbit_status lowbit_gemm_binplane_path(const uint16_t* X, const void* packed, i
   const uint8_t* pk = static_cast<const uint8_t*>(packed);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (path == 0) path = (M == 1) ? 1 : 2;
+  if (path == 1 && M == 1) {
+    GemvProblem p = {X, pk, Y, N, K, 0, 1, 0, P};
+    p.early = allocation_covers(pk, kHeaderBytes + binplane_payload_bytes(P, N, K)) ? 1 : 0;
+    return from_cuda(launch_bp_stream(&p, 1, err, s));
+  }
   if (path == 1) return from_cuda(launch_binplane_cc(X, pk, P, M, N, K, Y, err, s));
   return from_cuda(launch_binplane_tc(X, pk, P, M, N, K, Y, err, s));
 }

@@ -117,7 +117,7 @@ struct alignas(64) GemvProblem {
   int ks;                  // CTAs that split one tile's groups (divides the cluster size)
   int early;               // 1: the payload is known to lie inside packed's allocation, so
                            //    weight copies may start before the header has been checked
-  int pad_;
+  int P;                   // binary planes per weight (0 for INT4)
 };
 constexpr int kMaxGemvProblems = 8;
 
@@ -126,6 +126,8 @@ cudaError_t launch_pack_int4(const int8_t* codes, const uint16_t* scales, int N,
 cudaError_t launch_pack_binplane(const uint8_t* bits, const uint16_t* alpha, int P, int N, int K,
                                  uint8_t* packed, cudaStream_t s);
 cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int* err, cudaStream_t s);
+// Binary-plane counterpart (M = 1); every problem carries its plane count P (1..8).
+cudaError_t launch_bp_stream(const GemvProblem* probs, int count, int* err, cudaStream_t s);
 // Several INT4 multiplies with a common M >= 2 in one tensor-core launch (X, Y are [M][K], [M][N]).
 cudaError_t launch_int4_tc_grouped(const GemvProblem* probs, int count, int M, int* err,
                                    cudaStream_t s);

@@ -231,6 +231,213 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
   }
 }
 
+// ------------------------------------------------------------------------------ binary planes
+// y[n] = sum_p sum_g alpha[p][n][g] * sum_{k in g} b[p][n][k] x[k],  b in {-1, +1}
+// (ShiftAddQwen README, "Method": per plane a sign-select-and-add, then one scale per group).
+//
+// Same stream, schedule and reduction as the INT4 kernel; a stage holds one (tile, group)
+// block of P sign planes plus alphas and the group's 256 bytes of activations.  The
+// sign-select-and-add runs as table lookups: for each set of 4 inputs that one nibble of a
+// sign word covers, a helper warp tabulates the 16 signed sums +-x0 +-x1 +-x2 +-x3 once per
+// stage (2 KB per group, shared by every row and plane); a row then adds one table entry per
+// nibble, so each 4 weights of a plane cost one shared-memory load and one add.
+constexpr int kLutWarp = kCWarps + 1;
+constexpr int kBpThreads = (kCWarps + 2) * 32;  // compute, producer, table warp
+constexpr uint32_t kLutBytes = 32 * 16 * sizeof(float);  // 32 nibble sets x 16 sums
+constexpr size_t kBpRingBudget = 56 * 1024;               // stages + tables per CTA
+
+__host__ __device__ inline uint32_t bp_stage_bytes(int P) { return binplane_block(P) + kXBytes; }
+
+// acc += sum over the 8 nibbles of one sign word of the tabulated signed sums; `tab` points
+// at the word's 8 tables of 16 floats (nibble n: inputs of pair slots 4n..4n+3).
+__device__ __forceinline__ void lut_word(uint32_t w, const float* tab, float (&acc)[2]) {
+#pragma unroll
+  for (int n = 0; n < 8; ++n) acc[n & 1] += tab[16 * n + ((w >> (4 * n)) & 0xFu)];
+}
+
+__global__ void __launch_bounds__(kBpThreads)
+bp_stream_kernel(const __grid_constant__ StreamArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full[kMaxStages];
+  __shared__ __align__(8) uint64_t tabready[kMaxStages];
+  __shared__ __align__(8) uint64_t empty[kMaxStages];
+  __shared__ __align__(8) uint64_t redbar;
+  __shared__ float red[kCWarps][32];
+  __shared__ float part[kRowTile];
+  __shared__ int ok;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int C = a.cluster;
+  const int cid = (int)blockIdx.x / C, crank = (int)blockIdx.x % C;
+  int pi = 0;
+  for (int i = 1; i < a.count; ++i)
+    if (cid >= a.cl_begin[i]) pi = i;
+  const GemvProblem& pr = a.p[pi];
+  const int ks = pr.ks, rank = crank % ks;
+  const int tile = (cid - pr.cluster_begin) * (C / ks) + crank / ks;
+  const int G = pr.K / kGroup, P = pr.P;
+  const bool live = tile < row_tiles(pr.N);
+  const int g0 = (int)((long long)rank * G / ks), g1 = (int)((long long)(rank + 1) * G / ks);
+  const int nb = live ? g1 - g0 : 0;
+  const int S = a.stages;
+  const uint32_t BB = binplane_block(P), SB = bp_stage_bytes(P) + kLutBytes;
+
+  if (threadIdx.x == 0) {
+    ok = live && (pr.early || header_matches(reinterpret_cast<const PackedHeader*>(pr.packed),
+                                             kFormatBinplane, P, pr.N, pr.K));
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&tabready[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&empty[s]), kCWarps);
+    }
+    ptx::mbar_init(ptx::smem_addr(&redbar), (uint32_t)(kRowTile * (ks > 1 ? ks - 1 : 1)));
+    ptx::fence_mbar_init();
+  }
+  if (warp < kCWarps) red[warp][lane] = 0.f;
+  __syncthreads();
+  if (C > 1) ptx::cluster_arrive();
+  if (threadIdx.x == 0) grid_launch();
+  const bool hdr_ok = ok != 0;
+  if (pr.early && live && threadIdx.x == 0 &&
+      !header_matches(reinterpret_cast<const PackedHeader*>(pr.packed), kFormatBinplane, P, pr.N, pr.K))
+    ok = 0;
+
+  // stage s: block | activations (256 B) | tables (2 KB)
+  auto stage = [&](int s) { return smem + (size_t)s * SB; };
+  if (warp == kCWarps) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0 && hdr_ok) {
+      const uint8_t* wsrc = pr.packed + kHeaderBytes + ((size_t)tile * G + g0) * BB;
+      const uint16_t* xsrc = pr.X + (size_t)g0 * kGroup;
+      const int pre = min(nb, S);
+      for (int b = 0; b < pre; ++b) {
+        const uint32_t bar = ptx::smem_addr(&full[b]);
+        ptx::mbar_arrive_expect_tx(bar, BB + kXBytes);
+        ptx::bulk_g2s(ptx::smem_addr(stage(b)), wsrc + (size_t)b * BB, BB, bar);
+      }
+      grid_wait();
+      for (int b = 0; b < pre; ++b)
+        ptx::bulk_g2s(ptx::smem_addr(stage(b) + BB), xsrc + (size_t)b * kGroup, kXBytes,
+                      ptx::smem_addr(&full[b]));
+      int issued = pre;
+      for (int b = pre; b < nb; ++b) {
+        const int s = b % S;
+        if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), ((b / S) - 1) & 1)) {
+          record_error(a.err, LOWBIT_ERR_TIMEOUT);
+          break;
+        }
+        const uint32_t bar = ptx::smem_addr(&full[s]);
+        ptx::mbar_arrive_expect_tx(bar, BB + kXBytes);
+        ptx::bulk_g2s(ptx::smem_addr(stage(s)), wsrc + (size_t)b * BB, BB, bar);
+        ptx::bulk_g2s(ptx::smem_addr(stage(s) + BB), xsrc + (size_t)b * kGroup, kXBytes, bar);
+        issued = b + 1;
+      }
+      for (int b = max(0, issued - S); b < issued; ++b)
+        ptx::mbar_wait(ptx::smem_addr(&full[b % S]), (b / S) & 1);
+    }
+    __syncwarp();
+  } else if (warp == kLutWarp) {
+    // ---------------------------------------------------------------- tables
+    // Lane c tabulates nibble set c = 8w + n of the group: inputs k0 + {0, 2, 4, 6} with
+    // k0 = 32w + 8n (n < 4, even inputs) or 32w + 8(n - 4) + 1 (n >= 4, odd inputs).
+    if (hdr_ok) {
+      const int w = lane >> 3, n = lane & 7;
+      const int k0 = 32 * w + (n < 4 ? 8 * n : 8 * (n - 4) + 1);
+      for (int b = 0; b < nb; ++b) {
+        const int s = b % S;
+        const bool landed = ptx::mbar_wait(ptx::smem_addr(&full[s]), (b / S) & 1);
+        if (!__all_sync(0xFFFFFFFFu, landed)) {
+          if (lane == 0) record_error(a.err, LOWBIT_ERR_TIMEOUT);
+          break;
+        }
+        const uint16_t* xr = reinterpret_cast<const uint16_t*>(stage(s) + BB);
+        const float x0 = bf16_bits_to_float(xr[k0]), x1 = bf16_bits_to_float(xr[k0 + 2]);
+        const float x2 = bf16_bits_to_float(xr[k0 + 4]), x3 = bf16_bits_to_float(xr[k0 + 6]);
+        float e[16];
+        e[0] = -((x0 + x1) + (x2 + x3));  // every sign -1
+        const float d0 = 2.f * x0, d1 = 2.f * x1, d2 = 2.f * x2, d3 = 2.f * x3;
+#pragma unroll
+        for (int m = 1; m < 16; ++m) {  // set bit j of m flips input j to +1
+          const int low = m & -m;
+          const float d = low == 1 ? d0 : (low == 2 ? d1 : (low == 4 ? d2 : d3));
+          e[m] = e[m & (m - 1)] + d;
+        }
+        float4* t = reinterpret_cast<float4*>(stage(s) + BB + kXBytes) + 4 * lane;
+        t[0] = make_float4(e[0], e[1], e[2], e[3]);
+        t[1] = make_float4(e[4], e[5], e[6], e[7]);
+        t[2] = make_float4(e[8], e[9], e[10], e[11]);
+        t[3] = make_float4(e[12], e[13], e[14], e[15]);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&tabready[s]));
+      }
+    }
+  } else if (hdr_ok) {
+    // ---------------------------------------------------------------- compute
+    // Warp (q, h): rows 32q..32q+31, sign words 2h and 2h+1 (inputs 64h..64h+63) of each plane.
+    const int q = warp & 3, h = warp >> 2;
+    const int row = 32 * q + lane;
+    float total = 0.f;
+    for (int b = 0; b < nb; ++b) {
+      const int s = b % S;
+      const bool ready = ptx::mbar_wait(ptx::smem_addr(&tabready[s]), (b / S) & 1);
+      if (!__all_sync(0xFFFFFFFFu, ready)) {
+        if (lane == 0) record_error(a.err, LOWBIT_ERR_TIMEOUT);
+        break;
+      }
+      const uint8_t* st = stage(s);
+      const float* tab = reinterpret_cast<const float*>(st + BB + kXBytes) + 16 * 16 * h;
+      for (int p = 0; p < P; ++p) {
+        const uint2 sw = *reinterpret_cast<const uint2*>(st + p * (kRowTile * 16) + row * 16 + h * 8);
+        const float al = half_bits_to_float(
+            *reinterpret_cast<const uint16_t*>(st + binplane_alpha_off(P) + (p * kRowTile + row) * 2));
+        float acc[2] = {0.f, 0.f};
+        lut_word(sw.x, tab, acc);
+        lut_word(sw.y, tab + 8 * 16, acc);
+        total = fmaf(al, acc[0] + acc[1], total);
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&empty[s]));
+    }
+    red[warp][lane] = total;
+  }
+
+  // -------------------------------------------------------------------- reduction + store
+  __syncthreads();
+  const bool out_ok = ok != 0;
+  if (!out_ok && live && threadIdx.x == 0 && rank == 0 && tile == 0)
+    record_error(a.err, LOWBIT_ERR_INVALID_ARG);
+  if (threadIdx.x < kRowTile) {
+    const int q = threadIdx.x >> 5, l = threadIdx.x & 31;
+    part[threadIdx.x] = red[q][l] + red[q + 4][l];
+  }
+  const int n = tile * kRowTile + (int)threadIdx.x;
+  if (C > 1) ptx::cluster_wait();
+  if (ks > 1) {
+    float* slots = reinterpret_cast<float*>(smem + (size_t)S * SB);  // [ks-1][128]
+    const uint32_t owner = (uint32_t)(crank - rank);
+    if (live && threadIdx.x < kRowTile) {
+      if (rank != 0) {
+        const uint32_t la = ptx::smem_addr(&slots[(rank - 1) * kRowTile + threadIdx.x]);
+        ptx::st_dsmem_f32(ptx::map_to_rank(la, owner), part[threadIdx.x]);
+        ptx::mbar_arrive_remote(ptx::map_to_rank(ptx::smem_addr(&redbar), owner));
+      } else {
+        const bool got = ptx::mbar_wait_cluster(ptx::smem_addr(&redbar), 0);
+        if (!got) record_error(a.err, LOWBIT_ERR_TIMEOUT);
+        float y = part[threadIdx.x];
+        for (int r = 1; r < ks; ++r) y += slots[(r - 1) * kRowTile + threadIdx.x];
+        grid_wait();
+        if (got && out_ok && n < pr.N) pr.Y[n] = float_to_bf16_bits(y);
+      }
+    }
+  } else {
+    __syncthreads();
+    if (out_ok && threadIdx.x < kRowTile) {
+      grid_wait();
+      if (n < pr.N) pr.Y[n] = float_to_bf16_bits(part[threadIdx.x]);
+    }
+  }
+}
+
 int sm_count() {
   int dev = 0, nsm = 148;
   cudaGetDevice(&dev);
@@ -238,15 +445,18 @@ int sm_count() {
   return nsm;
 }
 
-}  // namespace
 
-// Schedule: ks per matrix aims at kTargetBlocks blocks per CTA, then all splits are doubled
-// while the grid holds fewer than two CTAs per SM (small launches).  Matrices are ordered by
-// blocks per CTA, longest first.
-cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int* err, cudaStream_t s) {
-  if (count < 1 || count > kMaxGemvProblems) return cudaErrorInvalidValue;
+// Schedule shared by both streaming kernels: ks per matrix aims at kTargetBlocks blocks per
+// CTA, then all splits are doubled while the grid holds fewer than two CTAs per SM (small
+// launches).  Matrices are ordered by blocks per CTA, longest first.  Fills `a` and returns
+// the cluster size C, the number of clusters, the largest blocks-per-CTA and the largest ks.
+struct Schedule {
+  int C, maxnb, kmax;
+  long long clusters;
+};
+
+bool make_schedule(const GemvProblem* probs, int count, StreamArgs& a, Schedule& out) {
   const int nsm = sm_count();
-  StreamArgs a = {};
   int ks[kMaxGemvProblems];
   long long ctas = 0;
   for (int i = 0; i < count; ++i) {
@@ -279,7 +489,7 @@ cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int* err, cu
       order[j - 1] = t;
     }
   long long clusters = 0;
-  int maxnb = 1;
+  int maxnb = 1, kmax = 1;
   for (int i = 0; i < count; ++i) {
     const int o = order[i];
     a.p[i] = probs[o];
@@ -289,29 +499,32 @@ cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int* err, cu
     const int tpc = C / ks[o];
     clusters += (row_tiles(probs[o].N) + tpc - 1) / tpc;
     maxnb = per_cta(o) > maxnb ? per_cta(o) : maxnb;
+    kmax = ks[o] > kmax ? ks[o] : kmax;
   }
-  if (clusters * C > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  if (clusters * C > 0x7FFFFFFFLL) return false;
   a.count = count;
   a.cluster = C;
-  a.err = err;
-  a.stages = maxnb < kMaxStages ? maxnb : kMaxStages;
-  int kmax = 1;
-  for (int i = 0; i < count; ++i) kmax = ks[i] > kmax ? ks[i] : kmax;
-  // ring, then the partial-sum slots rank 0 of a split tile receives
-  const size_t smem = (size_t)a.stages * kStage + (size_t)(kmax - 1) * kRowTile * sizeof(float);
+  out.C = C;
+  out.clusters = clusters;
+  out.maxnb = maxnb;
+  out.kmax = kmax;
+  return true;
+}
+
+template <typename Kernel>
+cudaError_t launch_streaming(Kernel kern, const StreamArgs& a, const Schedule& sc, size_t smem,
+                             int threads, cudaStream_t s) {
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(int4_stream_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  if (C > 8) {
-    cudaError_t e = cudaFuncSetAttribute(int4_stream_kernel,
-                                         cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (sc.C > 8) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(clusters * C), 1, 1);
-  cfg.blockDim = dim3(kSThreads, 1, 1);
+  cfg.gridDim = dim3((unsigned)(sc.clusters * sc.C), 1, 1);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -319,16 +532,46 @@ cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int* err, cu
   attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[na].val.programmaticStreamSerializationAllowed = 1;
   ++na;
-  if (C > 1) {
+  if (sc.C > 1) {
     attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = (unsigned)C;
+    attr[na].val.clusterDim.x = (unsigned)sc.C;
     attr[na].val.clusterDim.y = 1;
     attr[na].val.clusterDim.z = 1;
     ++na;
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, int4_stream_kernel, a);
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+}  // namespace
+
+cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int* err, cudaStream_t s) {
+  if (count < 1 || count > kMaxGemvProblems) return cudaErrorInvalidValue;
+  StreamArgs a = {};
+  Schedule sc;
+  if (!make_schedule(probs, count, a, sc)) return cudaErrorInvalidValue;
+  a.err = err;
+  a.stages = sc.maxnb < kMaxStages ? sc.maxnb : kMaxStages;
+  // ring, then the partial-sum slots rank 0 of a split tile receives
+  const size_t smem = (size_t)a.stages * kStage + (size_t)(sc.kmax - 1) * kRowTile * sizeof(float);
+  return launch_streaming(int4_stream_kernel, a, sc, smem, kSThreads, s);
+}
+
+cudaError_t launch_bp_stream(const GemvProblem* probs, int count, int* err, cudaStream_t s) {
+  if (count < 1 || count > kMaxGemvProblems) return cudaErrorInvalidValue;
+  StreamArgs a = {};
+  Schedule sc;
+  if (!make_schedule(probs, count, a, sc)) return cudaErrorInvalidValue;
+  int pmax = 1;
+  for (int i = 0; i < count; ++i) pmax = probs[i].P > pmax ? probs[i].P : pmax;
+  const size_t stage = bp_stage_bytes(pmax) + kLutBytes;
+  int S = (int)(kBpRingBudget / stage);
+  S = S < 2 ? 2 : (S > kMaxStages ? kMaxStages : S);
+  a.err = err;
+  a.stages = sc.maxnb < S ? sc.maxnb : S;
+  const size_t smem = (size_t)a.stages * stage + (size_t)(sc.kmax - 1) * kRowTile * sizeof(float);
+  return launch_streaming(bp_stream_kernel, a, sc, smem, kBpThreads, s);
 }
 
 }  // namespace lowbit

@@ -32,7 +32,10 @@ constexpr int kCWarps = 8;                          // compute warps: 4 row quar
 constexpr int kSThreads = (kCWarps + 1) * 32;       // plus one producer warp
 constexpr uint32_t kXBytes = kGroup * 2;            // one group's bf16 activations
 constexpr uint32_t kStage = kInt4Block + kXBytes;   // 8704 bytes, a multiple of 16
-constexpr int kMaxStages = 6;      // 52 KB of ring: four CTAs per SM
+constexpr int kMaxStages = 6;
+// Dynamic shared memory per CTA (ring + reduction slots): with the static part, four CTAs fit
+// in an SM's 228 KB.
+constexpr size_t kSmemBudget = 53 * 1024;
 constexpr int kTargetBlocks = 5;   // blocks per CTA the K split aims for
 constexpr int kMaxSplit = 16;      // cluster sizes above 8 need the non-portable opt-in
 
@@ -244,7 +247,6 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
 constexpr int kLutWarp = kCWarps + 1;
 constexpr int kBpThreads = (kCWarps + 2) * 32;  // compute, producer, table warp
 constexpr uint32_t kLutBytes = 32 * 16 * sizeof(float);  // 32 nibble sets x 16 sums
-constexpr size_t kBpRingBudget = 56 * 1024;               // stages + tables per CTA
 
 __host__ __device__ inline uint32_t bp_stage_bytes(int P) { return binplane_block(P) + kXBytes; }
 
@@ -552,9 +554,13 @@ cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int* err, cu
   Schedule sc;
   if (!make_schedule(probs, count, a, sc)) return cudaErrorInvalidValue;
   a.err = err;
-  a.stages = sc.maxnb < kMaxStages ? sc.maxnb : kMaxStages;
-  // ring, then the partial-sum slots rank 0 of a split tile receives
-  const size_t smem = (size_t)a.stages * kStage + (size_t)(sc.kmax - 1) * kRowTile * sizeof(float);
+  // ring, then the partial-sum slots rank 0 of a split tile receives; the ring takes what the
+  // slots leave of the per-CTA budget (four CTAs per SM)
+  const size_t slots = (size_t)(sc.kmax - 1) * kRowTile * sizeof(float);
+  int S = (int)((kSmemBudget - slots) / kStage);
+  S = S > kMaxStages ? kMaxStages : (S < 2 ? 2 : S);
+  a.stages = sc.maxnb < S ? sc.maxnb : S;
+  const size_t smem = (size_t)a.stages * kStage + slots;
   return launch_streaming(int4_stream_kernel, a, sc, smem, kSThreads, s);
 }
 
@@ -566,11 +572,12 @@ cudaError_t launch_bp_stream(const GemvProblem* probs, int count, int* err, cuda
   int pmax = 1;
   for (int i = 0; i < count; ++i) pmax = probs[i].P > pmax ? probs[i].P : pmax;
   const size_t stage = bp_stage_bytes(pmax) + kLutBytes;
-  int S = (int)(kBpRingBudget / stage);
+  const size_t slots = (size_t)(sc.kmax - 1) * kRowTile * sizeof(float);
+  int S = (int)((kSmemBudget - slots) / stage);
   S = S < 2 ? 2 : (S > kMaxStages ? kMaxStages : S);
   a.err = err;
   a.stages = sc.maxnb < S ? sc.maxnb : S;
-  const size_t smem = (size_t)a.stages * stage + (size_t)(sc.kmax - 1) * kRowTile * sizeof(float);
+  const size_t smem = (size_t)a.stages * stage + slots;
   return launch_streaming(bp_stream_kernel, a, sc, smem, kBpThreads, s);
 }
 

@@ -17,9 +17,12 @@
  *     enqueued and no output is touched.  A CUDA launch error returns LOWBIT_ERR_CUDA.
  *   - K must be a multiple of 128 (the quantisation group).  N >= 1 is arbitrary.
  *   - Packed weight buffers start with a 128-byte header (magic, format, N, K, P).  Kernels
- *     check it against the call's arguments; on a mismatch they touch nothing else, write
- *     no output and record LOWBIT_ERR_INVALID_ARG in a per-device error word that
- *     lowbit_device_error() returns.  lowbit_validate_packed() checks a header synchronously.
+ *     check it against the call's arguments; on a mismatch they write no output and record
+ *     LOWBIT_ERR_INVALID_ARG in a per-device error word that lowbit_device_error() returns.
+ *     The M = 1 kernels may start reading weights before the header has been checked, but
+ *     only when the host has verified that the payload the arguments describe lies inside
+ *     the device allocation that contains `packed`; otherwise nothing but the header is read
+ *     on a mismatch.  lowbit_validate_packed() checks a header synchronously.
  *   - Multiplies are launched with programmatic dependent launch: they request their packed
  *     weights (header included) before waiting for the preceding kernel on the stream, and
  *     read activations / write outputs only after that wait.  So the kernel immediately

@@ -234,6 +234,35 @@ def test_header_mismatch_is_recorded_and_nothing_written(lb, path):
     assert lb.lowbit_device_error() == 0                        # cleared by the read
 
 
+@pytest.mark.parametrize("path", PATHS)
+def test_header_mismatch_beyond_the_allocation(lb, path):
+    """A claimed shape whose payload cannot lie inside the buffer's allocation: the kernels
+    check the header before reading any weight, record the mismatch and write nothing."""
+    codes, scales, x = synth.int4_problem(1, 1, 64, 256)
+    packed = pack_int4_gpu(lb, codes, scales)                  # 17 KB
+    N = 65536                                                  # claims 8.6 MB of payload
+    Y = torch.full((1, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    lb.lowbit_gemm_int4_path(bf16_dev(x), packed, 1, N, 256, Y, path)
+    assert lb.lowbit_device_error() == 1
+    assert torch.all(Y == 7.0)
+
+
+@pytest.mark.parametrize("N", [96, 65536])
+def test_binplane_header_mismatch_is_recorded_and_nothing_written(lb, N):
+    bits, alpha, x = synth.binplane_problem(3, 3, 1, 64, 256, 5)
+    packed = pack_bp_gpu(lb, bits, alpha)
+    assert lb.lowbit_device_error() == 0
+    Y = torch.full((1, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    lb.lowbit_gemm_binplane(bf16_dev(x), packed, 3, 1, N, 256, Y)
+    assert lb.lowbit_device_error() == 1
+    assert torch.all(Y == 7.0)
+    # a plane count that disagrees with the header is caught the same way
+    Y2 = torch.full((1, 64), 7.0, dtype=torch.bfloat16, device="cuda")
+    lb.lowbit_gemm_binplane(bf16_dev(x), packed, 2, 1, 64, 256, Y2)
+    assert lb.lowbit_device_error() == 1
+    assert torch.all(Y2 == 7.0)
+
+
 def test_shape_errors_raise(lb):
     codes, scales, x = synth.int4_problem(1, 1, 64, 256)
     packed = pack_int4_gpu(lb, codes, scales)

@@ -39,6 +39,8 @@ import synth  # noqa: E402
 
 METRIC = "weight-stream GB/s (% of HBM peak) and tok/s, low-bit GEMV/GEMM at M=1 and M=16"
 LAYER_BYTES = 50_012_160
+DEFAULT_WORKLOAD_DESC = ("decode W4A16 GEMV over one 4B-class layer, M=1, grouped as a decoder's "
+                         "dependencies allow: (q,k,v), (o), (gate,up), (down), one launch each")
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -269,11 +271,9 @@ def build_workload(lb, torch, l2, name, path):
                                 "and down (K=9728), INT4 group 128, M=1")
     if name in ("decode_deps", "decode_all"):
         grouping = name.split("_")[1]
-        how = ("grouped as a decoder's dependencies allow: (q,k,v), (o), (gate,up), (down), "
-               "one launch each" if grouping == "deps" else "all seven in one grouped launch")
-        return build_int4_layer(lb, torch, l2, 1, path, 1, name,
-                                "decode W4A16 GEMV over one 4B-class layer, M=1, " + how,
-                                grouping=grouping)
+        desc = (DEFAULT_WORKLOAD_DESC if grouping == "deps" else
+                "decode W4A16 GEMV over one 4B-class layer, M=1, all seven in one grouped launch")
+        return build_int4_layer(lb, torch, l2, 1, path, 1, name, desc, grouping=grouping)
     if name in ("verify_deps", "verify_all"):
         grouping = name.split("_")[1]
         how = ("grouped as a decoder's dependencies allow: (q,k,v), (o), (gate,up), (down), "
@@ -579,8 +579,8 @@ def run_reference(args):
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(secs / args.steps * 1e3, 4), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": "decode W4A16 GEMV over one 4B-class layer: q,k,v,o,gate,up "
-                                  "(K=2560) and down (K=9728), INT4 group 128, M=1", "M": 1},
+           "config": {"workload": DEFAULT_WORKLOAD_DESC, "name": "decode_deps", "M": 1,
+                      "weight_bytes_per_step": LAYER_BYTES},
            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": os.cpu_count(),
                             "kind": "oracle", "sample": sample},
            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,

@@ -18,10 +18,15 @@
 // distributed shared memory.  Clusters of the matrices with the most blocks per CTA come
 // first in the grid, so the longest CTAs start in the first wave.
 //
-// Arithmetic (in registers, fp32 accumulation): a nibble pair ORed into bf16 128.0 is the
-// exact pair (128 + u) = (q + 136); a mixed-precision fma multiplies it with the bf16
-// activation pair into fp32.  Per half group the bias is removed with the activations' sum:
-// sum (q + 136) x - 136 sum x = sum q x.  Each output is rounded once to bf16.
+// Arithmetic: a converter warp turns each group's 128 bf16 activations into int16 with one
+// power-of-two scale 2^sh, chosen so that the largest magnitude lands in [2^14, 2^15): every
+// activation within 2^7 of the group's largest keeps all 8 of its significant bits, smaller
+// ones are rounded to a multiple of 2^-sh (at most 2^-15 of the group's largest).  A code
+// word's 8 nibbles u = q + 8 are split into two words of 4 unsigned bytes with two masks, and
+// the integer dot-product instruction (two 16-bit x 8-bit products added into 32 bits) sums
+// u * X exactly; 8 * sum X is removed per half group in integers, the half group's integer
+// (below 2^24 in magnitude, so exact in fp32) is scaled by s * 2^-sh in fp32, and each output
+// is rounded once to bf16.  A group holding a non-finite activation makes its rows NaN.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -29,14 +34,18 @@ namespace lowbit {
 namespace {
 
 constexpr int kCWarps = 8;                          // compute warps: 4 row quarters x 2 K halves
-constexpr int kSThreads = (kCWarps + 1) * 32;       // plus one producer warp
+constexpr int kConvWarp = kCWarps + 1;              // after the producer warp
+constexpr int kSThreads = (kCWarps + 2) * 32;
 constexpr uint32_t kXBytes = kGroup * 2;            // one group's bf16 activations
 constexpr uint32_t kStage = kInt4Block + kXBytes;   // 8704 bytes, a multiple of 16
 constexpr int kMaxStages = 6;
 // Dynamic shared memory per CTA (ring + reduction slots): with the static part, four CTAs fit
 // in an SM's 228 KB.
 constexpr size_t kSmemBudget = 53 * 1024;
-constexpr int kTargetBlocks = 5;   // blocks per CTA the K split aims for
+// Blocks per CTA the K split aims for: long streams amortise each CTA's fixed costs (start,
+// first-copy latency, exchange) once a matrix fills the GPU several times over; small
+// matrices are split further by the schedule's occupancy rule.
+constexpr int kInt4TargetBlocks = 32;
 constexpr int kMaxSplit = 16;      // cluster sizes above 8 need the non-portable opt-in
 
 // The first cache line holds what every CTA reads first (to find its matrix); each matrix's
@@ -56,27 +65,32 @@ __device__ __forceinline__ void grid_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  return v;
+// Two-way dot product: c + a.lo16 * b.byte0 + a.hi16 * b.byte1 (lo) or with bytes 2 and 3
+// (hi); a's halves signed, b's bytes unsigned.
+__device__ __forceinline__ int dp2a_lo(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
 }
-
-// acc += (q + 136) * x for the 8 inputs of one code word.  Nibble e of the word sits at bits
-// 4(e/2) + 16(e%2); x8 holds the word's 8 activations as 4 bf16 pairs (even input low).
-__device__ __forceinline__ void dot8(uint32_t w, const uint4& x8, float (&acc)[4]) {
-  fma_bf16x2_f32(acc[0], acc[1], int4_pair_biased<0>(w), x8.x);
-  fma_bf16x2_f32(acc[2], acc[3], int4_pair_biased<1>(w), x8.y);
-  fma_bf16x2_f32(acc[0], acc[1], int4_pair_biased<2>(w), x8.z);
-  fma_bf16x2_f32(acc[2], acc[3], int4_pair_biased<3>(w), x8.w);
+__device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
 }
 
 __global__ void __launch_bounds__(kSThreads)
 int4_stream_kernel(const __grid_constant__ StreamArgs a) {
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ __align__(8) uint64_t full[kMaxStages];
+  __shared__ __align__(8) uint64_t xready[kMaxStages];  // the stage's int16 activations are set
   __shared__ __align__(8) uint64_t empty[kMaxStages];
   __shared__ __align__(8) uint64_t redbar;  // rank 0 of a split tile: partials have arrived
+  // Per stage: the int16 activations, one uint4 per code word j holding the 16-bit pairs
+  // (X[8j], X[8j+4]), (X[8j+1], X[8j+5]), (X[8j+2], X[8j+6]), (X[8j+3], X[8j+7]) -- the
+  // order in which the two byte words of code word j meet them -- and (2^-sh, sum X over
+  // inputs 0..63, sum X over inputs 64..127).
+  __shared__ __align__(16) uint4 xq[kMaxStages][kGroup / 8];
+  __shared__ __align__(16) float4 xmeta[kMaxStages];
   __shared__ float red[kCWarps][32];
   __shared__ float part[kRowTile];
   __shared__ int ok;
@@ -103,12 +117,14 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
                                              kFormatInt4, 0, pr.N, pr.K));
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&xready[s]), 1);
       ptx::mbar_init(ptx::smem_addr(&empty[s]), kCWarps);
     }
     // rank 0 of a split tile receives one arrival per row from each other rank
     ptx::mbar_init(ptx::smem_addr(&redbar), (uint32_t)(kRowTile * (ks > 1 ? ks - 1 : 1)));
     ptx::fence_mbar_init();
   }
+  if (warp < kCWarps) red[warp][lane] = 0.f;
   __syncthreads();
   // Half of a cluster barrier: its wait, just before the partial sums are exchanged, finds
   // every CTA's barriers initialised (and returns at once, as all arrived long before).
@@ -121,7 +137,6 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
       !header_matches(reinterpret_cast<const PackedHeader*>(pr.packed), kFormatInt4, 0, pr.N, pr.K))
     ok = 0;  // read after the epilogue's barrier
 
-  float total = 0.f;
   if (warp == kCWarps) {
     // ---------------------------------------------------------------- producer
     if (lane == 0 && hdr_ok) {
@@ -158,14 +173,56 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
         ptx::mbar_wait(ptx::smem_addr(&full[b % S]), (b / S) & 1);
     }
     __syncwarp();
-  } else if (hdr_ok) {
+  } else if (warp == kConvWarp) {
+    // ---------------------------------------------------------------- activation converter
+    if (hdr_ok) {
+      for (int b = 0; b < nb; ++b) {
+        const int s = b % S;
+        const bool landed = ptx::mbar_wait(ptx::smem_addr(&full[s]), (b / S) & 1);
+        if (!__all_sync(0xFFFFFFFFu, landed)) {
+          if (lane == 0) record_error(a.err, LOWBIT_ERR_TIMEOUT);
+          break;
+        }
+        // lane l holds inputs 4l..4l+3 (code word l/2, nibbles 4(l&1)..4(l&1)+3)
+        const uint2 raw = reinterpret_cast<const uint2*>(ring + (size_t)s * kStage + kInt4Block)[lane];
+        const uint32_t mag = max(max(raw.x & 0x7FFFu, (raw.x >> 16) & 0x7FFFu),
+                                 max(raw.y & 0x7FFFu, (raw.y >> 16) & 0x7FFFu));
+        const uint32_t mmax = __reduce_max_sync(0xFFFFFFFFu, mag);  // |x| bits order as |x|
+        const int e = max((int)(mmax >> 7), 1);                     // biased exponent of max|x|
+        const int sh = min(141 - e, 126);                           // max|x| * 2^sh < 2^15
+        const float up = __int_as_float((127 + sh) << 23);
+        const float down = mmax >= 0x7F80u ? __int_as_float(0x7FC00000)
+                                           : __int_as_float((127 - sh) << 23);
+        // x * 2^sh is exact; adding 1.5 * 2^23 rounds it to an integer (nearest, even on ties)
+        // and leaves that integer's two's complement in the low 16 bits.
+        constexpr float kRound = 12582912.f;
+        const uint32_t i0 = __float_as_uint(fmaf(__uint_as_float(raw.x << 16), up, kRound)) & 0xFFFFu;
+        const uint32_t i1 = __float_as_uint(fmaf(__uint_as_float(raw.x & 0xFFFF0000u), up, kRound)) & 0xFFFFu;
+        const uint32_t i2 = __float_as_uint(fmaf(__uint_as_float(raw.y << 16), up, kRound)) & 0xFFFFu;
+        const uint32_t i3 = __float_as_uint(fmaf(__uint_as_float(raw.y & 0xFFFF0000u), up, kRound)) & 0xFFFFu;
+        const int mine = (int)(int16_t)i0 + (int)(int16_t)i1 + (int)(int16_t)i2 + (int)(int16_t)i3;
+        const int sum_lo = __reduce_add_sync(0xFFFFFFFFu, lane < 16 ? mine : 0);
+        const int sum_hi = __reduce_add_sync(0xFFFFFFFFu, lane < 16 ? 0 : mine);
+        const uint32_t p01 = i0 | (i1 << 16), p23 = i2 | (i3 << 16);
+        const uint32_t o01 = __shfl_xor_sync(0xFFFFFFFFu, p01, 1);  // the word's other half
+        const uint32_t o23 = __shfl_xor_sync(0xFFFFFFFFu, p23, 1);
+        if ((lane & 1) == 0)
+          xq[s][lane >> 1] = make_uint4(__byte_perm(p01, o01, 0x5410), __byte_perm(p01, o01, 0x7632),
+                                        __byte_perm(p23, o23, 0x5410), __byte_perm(p23, o23, 0x7632));
+        if (lane == 0) xmeta[s] = make_float4(down, __int_as_float(sum_lo), __int_as_float(sum_hi), 0.f);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&xready[s]));
+      }
+    }
+  } else if (warp < kCWarps && hdr_ok) {
     // ---------------------------------------------------------------- compute
     const int q = warp & 3, h = warp >> 2;  // rows 32q..32q+31, inputs 64h..64h+63 of each group
     const int row = 32 * q + lane;
+    float total = 0.f;
     for (int b = 0; b < nb; ++b) {
       const int s = b % S;
-      const bool landed = ptx::mbar_wait(ptx::smem_addr(&full[s]), (b / S) & 1);
-      if (!__all_sync(0xFFFFFFFFu, landed)) {  // warp-uniform exit keeps the warp converged
+      const bool ready = ptx::mbar_wait(ptx::smem_addr(&xready[s]), (b / S) & 1);
+      if (!__all_sync(0xFFFFFFFFu, ready)) {  // warp-uniform exit keeps the warp converged
         if (lane == 0) record_error(a.err, LOWBIT_ERR_TIMEOUT);
         break;
       }
@@ -173,28 +230,30 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
       const uint4 c0 = *reinterpret_cast<const uint4*>(st + (2 * h) * (kRowTile * 16) + row * 16);
       const uint4 c1 = *reinterpret_cast<const uint4*>(st + (2 * h + 1) * (kRowTile * 16) + row * 16);
       const float sc = half_bits_to_float(*reinterpret_cast<const uint16_t*>(st + kInt4ScaleOff + row * 2));
-      const uint8_t* xh = st + kInt4Block + h * 128;
-      const uint32_t xpair = reinterpret_cast<const uint32_t*>(xh)[lane];
-      const float xsum = warp_sum(bf16_bits_to_float((uint16_t)(xpair & 0xFFFFu)) +
-                                  bf16_bits_to_float((uint16_t)(xpair >> 16)));
-      const uint4* x8 = reinterpret_cast<const uint4*>(xh);
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      dot8(c0.x, x8[0], acc);
-      dot8(c0.y, x8[1], acc);
-      dot8(c0.z, x8[2], acc);
-      dot8(c0.w, x8[3], acc);
-      dot8(c1.x, x8[4], acc);
-      dot8(c1.y, x8[5], acc);
-      dot8(c1.z, x8[6], acc);
-      dot8(c1.w, x8[7], acc);
+      const uint4* xw = xq[s] + 8 * h;
+      const float4 meta = xmeta[s];
+      const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      int acc[4] = {0, 0, 0, 0};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        // nibble e of a word sits at bits 4(e/2) + 16(e%2): the masked word holds nibbles
+        // (0, 4, 1, 5) in its bytes, the shifted one (2, 6, 3, 7)
+        const uint4 x = xw[i];
+        const uint32_t lo = w[i] & 0x0F0F0F0Fu, hi = (w[i] >> 4) & 0x0F0F0F0Fu;
+        acc[0] = dp2a_lo(x.x, lo, acc[0]);
+        acc[1] = dp2a_hi(x.y, lo, acc[1]);
+        acc[2] = dp2a_lo(x.z, hi, acc[2]);
+        acc[3] = dp2a_hi(x.w, hi, acc[3]);
+      }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&empty[s]));
-      total = fmaf(sc, ((acc[0] + acc[1]) + (acc[2] + acc[3])) - 136.f * xsum, total);
+      const int v = (acc[0] + acc[1]) + (acc[2] + acc[3]) - 8 * __float_as_int(h ? meta.z : meta.y);
+      total = fmaf(sc * meta.x, (float)v, total);
     }
+    red[warp][lane] = total;
   }
 
   // -------------------------------------------------------------------- reduction + store
-  if (warp < kCWarps) red[warp][lane] = total;
   __syncthreads();
   const bool out_ok = ok != 0;  // header verified (before or alongside the copies)
   if (!out_ok && live && threadIdx.x == 0 && rank == 0 && tile == 0)
@@ -247,6 +306,7 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
 constexpr int kLutWarp = kCWarps + 1;
 constexpr int kBpThreads = (kCWarps + 2) * 32;  // compute, producer, table warp
 constexpr uint32_t kLutBytes = 32 * 16 * sizeof(float);  // 32 nibble sets x 16 sums
+constexpr int kBpTargetBlocks = 5;
 
 __host__ __device__ inline uint32_t bp_stage_bytes(int P) { return binplane_block(P) + kXBytes; }
 
@@ -448,7 +508,7 @@ int sm_count() {
 }
 
 
-// Schedule shared by both streaming kernels: ks per matrix aims at kTargetBlocks blocks per
+// Schedule shared by both streaming kernels: ks per matrix aims at `target` blocks per
 // CTA, then all splits are doubled while the grid holds fewer than two CTAs per SM (small
 // launches).  Matrices are ordered by blocks per CTA, longest first.  Fills `a` and returns
 // the cluster size C, the number of clusters, the largest blocks-per-CTA and the largest ks.
@@ -457,14 +517,14 @@ struct Schedule {
   long long clusters;
 };
 
-bool make_schedule(const GemvProblem* probs, int count, StreamArgs& a, Schedule& out) {
+bool make_schedule(const GemvProblem* probs, int count, int target, StreamArgs& a, Schedule& out) {
   const int nsm = sm_count();
   int ks[kMaxGemvProblems];
   long long ctas = 0;
   for (int i = 0; i < count; ++i) {
     const int G = probs[i].K / kGroup;
     int k = 1;
-    while (k < kMaxSplit && k * 2 <= G && (G + k - 1) / k > kTargetBlocks) k *= 2;
+    while (k < kMaxSplit && k * 2 <= G && (G + k - 1) / k > target) k *= 2;
     ks[i] = k;
     ctas += (long long)row_tiles(probs[i].N) * k;
   }
@@ -552,7 +612,7 @@ cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int* err, cu
   if (count < 1 || count > kMaxGemvProblems) return cudaErrorInvalidValue;
   StreamArgs a = {};
   Schedule sc;
-  if (!make_schedule(probs, count, a, sc)) return cudaErrorInvalidValue;
+  if (!make_schedule(probs, count, kInt4TargetBlocks, a, sc)) return cudaErrorInvalidValue;
   a.err = err;
   // ring, then the partial-sum slots rank 0 of a split tile receives; the ring takes what the
   // slots leave of the per-CTA budget (four CTAs per SM)
@@ -568,7 +628,7 @@ cudaError_t launch_bp_stream(const GemvProblem* probs, int count, int* err, cuda
   if (count < 1 || count > kMaxGemvProblems) return cudaErrorInvalidValue;
   StreamArgs a = {};
   Schedule sc;
-  if (!make_schedule(probs, count, a, sc)) return cudaErrorInvalidValue;
+  if (!make_schedule(probs, count, kBpTargetBlocks, a, sc)) return cudaErrorInvalidValue;
   int pmax = 1;
   for (int i = 0; i < count; ++i) pmax = probs[i].P > pmax ? probs[i].P : pmax;
   const size_t stage = bp_stage_bytes(pmax) + kLutBytes;

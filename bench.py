@@ -11,7 +11,8 @@ replayed from CUDA graphs (one per rotation of the weight copies) and timed with
 
 Also reported under "rows": the same layer as seven single-matrix calls ("decode") and as one
 grouped call ("decode_all"), the M=16 verify GEMM over the same layer and its batch sweep,
-binary-plane GEMV/GEMM, and the LM-head argmax+verify over 248,320 and 32,768 rows.
+binary-plane GEMV/GEMM, the 248,320-row vocabulary head as one M=1 GEMV ("head_gemv"), and the
+LM-head argmax+verify over 248,320 and 32,768 rows.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-rows]
 
@@ -264,6 +265,23 @@ def build_lmhead(lb, torch, l2, N, path, name, desc):
     return w
 
 
+def build_head_gemv(lb, torch, l2, path, name, desc):
+    """One large INT4 matrix at M=1: the full vocabulary head's logits for one token."""
+    N, K = synth.HEAD_ROWS[0], synth.HEAD_K
+    w = Workload(name, desc, "int4_stream_kernel" if path != 2 else "tc_gemm_kernel")
+    codes, scales, x = synth.int4_problem(4, 1, N, K, 1)
+    p = torch.empty(lb.lowbit_int4_packed_bytes(N, K), dtype=torch.uint8, device="cuda")
+    lb.lowbit_pack_int4(dev(codes), f16_dev(scales), N, K, p)
+    del codes
+    w.bytes = algorithmic_int4_bytes(N, K)
+    packs = _copies(p, copies_for(w.bytes, l2, 2), torch)
+    X, Y = bf16_dev(x), torch.empty((1, N), dtype=torch.bfloat16, device="cuda")
+    for c in range(len(packs)):
+        w.calls.append([lambda c=c: lb.lowbit_gemm_int4_path(X, packs[c], 1, N, K, Y, path)])
+    w.M, w.tokens, w.launches = 1, 1, 1
+    return w
+
+
 def build_workload(lb, torch, l2, name, path):
     if name == "decode":
         return build_int4_layer(lb, torch, l2, 1, path, 1, name,
@@ -302,6 +320,10 @@ def build_workload(lb, torch, l2, name, path):
         return build_binplane(lb, torch, l2, M, path, name,
                               f"binary-plane GEMM: (K,N) in {{(4096,12288),(12288,4096)}} x P in {{3,4}}, "
                               f"M={M}, group 128")
+    if name == "head_gemv":
+        return build_head_gemv(lb, torch, l2, path, name,
+                               f"INT4 GEMV at M=1 over the {synth.HEAD_ROWS[0]}-row vocabulary head, "
+                               f"K={synth.HEAD_K}, group 128 (one 524 MB matrix)")
     if name in ("lmhead_full", "lmhead_trim"):
         N = synth.HEAD_ROWS[0] if name == "lmhead_full" else synth.HEAD_ROWS[1]
         return build_lmhead(lb, torch, l2, N, path, name,
@@ -310,7 +332,7 @@ def build_workload(lb, torch, l2, name, path):
     raise ValueError(name)
 
 
-WORKLOADS = ("decode", "decode_deps", "decode_all", "verify", "verify_deps", "verify_all", "binplane_m1", "binplane_m16", "lmhead_full", "lmhead_trim",
+WORKLOADS = ("decode", "decode_deps", "decode_all", "verify", "verify_deps", "verify_all", "binplane_m1", "binplane_m16", "head_gemv", "lmhead_full", "lmhead_trim",
              "tiny") + tuple(f"verify_m{m}" for m in synth.M_SWEEP if m not in (16,))
 
 

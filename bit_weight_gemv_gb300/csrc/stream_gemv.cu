@@ -18,15 +18,18 @@
 // distributed shared memory.  Clusters of the matrices with the most blocks per CTA come
 // first in the grid, so the longest CTAs start in the first wave.
 //
-// Arithmetic: a converter warp turns each group's 128 bf16 activations into int16 with one
-// power-of-two scale 2^sh, chosen so that the largest magnitude lands in [2^14, 2^15): every
-// activation within 2^7 of the group's largest keeps all 8 of its significant bits, smaller
-// ones are rounded to a multiple of 2^-sh (at most 2^-15 of the group's largest).  A code
-// word's 8 nibbles u = q + 8 are split into two words of 4 unsigned bytes with two masks, and
-// the integer dot-product instruction (two 16-bit x 8-bit products added into 32 bits) sums
-// u * X exactly; 8 * sum X is removed per half group in integers, the half group's integer
-// (below 2^24 in magnitude, so exact in fp32) is scaled by s * 2^-sh in fp32, and each output
-// is rounded once to bf16.  A group holding a non-finite activation makes its rows NaN.
+// Arithmetic: a converter warp turns each half group's 64 bf16 activations into int16 with
+// one power-of-two scale 2^sh, chosen so that the largest magnitude lands in [2^14, 2^15):
+// every activation within 2^7 of the half group's largest keeps all 8 of its significant
+// bits, smaller ones are rounded to a multiple of 2^-sh (at most 2^-15 of that largest).  A
+// code word's 8 nibbles u = q + 8 are split into two words of 4 unsigned bytes with two
+// masks, and the integer dot-product instruction (two 16-bit x 8-bit products added into 32
+// bits) sums u * X exactly; 8 * sum X is removed per half group in integers, the half group's
+// integer (below 2^24 in magnitude, so exact in fp32) is scaled by s * 2^-sh in fp32, and each
+// output is rounded once to bf16.  A half group holding a non-finite activation makes its
+// rows NaN.
+#include <atomic>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -87,8 +90,8 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
   __shared__ __align__(8) uint64_t redbar;  // rank 0 of a split tile: partials have arrived
   // Per stage: the int16 activations, one uint4 per code word j holding the 16-bit pairs
   // (X[8j], X[8j+4]), (X[8j+1], X[8j+5]), (X[8j+2], X[8j+6]), (X[8j+3], X[8j+7]) -- the
-  // order in which the two byte words of code word j meet them -- and (2^-sh, sum X over
-  // inputs 0..63, sum X over inputs 64..127).
+  // order in which the two byte words of code word j meet them -- and, for inputs 0..63 and
+  // 64..127, (2^-sh of the first, of the second, sum X of the first, of the second).
   __shared__ __align__(16) uint4 xq[kMaxStages][kGroup / 8];
   __shared__ __align__(16) float4 xmeta[kMaxStages];
   __shared__ float red[kCWarps][32];
@@ -187,9 +190,12 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
         const uint2 raw = reinterpret_cast<const uint2*>(ring + (size_t)s * kStage + kInt4Block)[lane];
         const uint32_t mag = max(max(raw.x & 0x7FFFu, (raw.x >> 16) & 0x7FFFu),
                                  max(raw.y & 0x7FFFu, (raw.y >> 16) & 0x7FFFu));
-        const uint32_t mmax = __reduce_max_sync(0xFFFFFFFFu, mag);  // |x| bits order as |x|
-        const int e = max((int)(mmax >> 7), 1);                     // biased exponent of max|x|
-        const int sh = min(141 - e, 126);                           // max|x| * 2^sh < 2^15
+        // lanes 0..15 hold inputs 0..63, lanes 16..31 inputs 64..127; |x| bits order as |x|
+        const uint32_t mlo = __reduce_max_sync(0xFFFFFFFFu, lane < 16 ? mag : 0u);
+        const uint32_t mhi = __reduce_max_sync(0xFFFFFFFFu, lane < 16 ? 0u : mag);
+        const uint32_t mmax = lane < 16 ? mlo : mhi;
+        const int e = max((int)(mmax >> 7), 1);  // biased exponent of the half group's max |x|
+        const int sh = min(141 - e, 126);        // max |x| * 2^sh < 2^15
         const float up = __int_as_float((127 + sh) << 23);
         const float down = mmax >= 0x7F80u ? __int_as_float(0x7FC00000)
                                            : __int_as_float((127 - sh) << 23);
@@ -209,7 +215,11 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
         if ((lane & 1) == 0)
           xq[s][lane >> 1] = make_uint4(__byte_perm(p01, o01, 0x5410), __byte_perm(p01, o01, 0x7632),
                                         __byte_perm(p23, o23, 0x5410), __byte_perm(p23, o23, 0x7632));
-        if (lane == 0) xmeta[s] = make_float4(down, __int_as_float(sum_lo), __int_as_float(sum_hi), 0.f);
+        float* meta = reinterpret_cast<float*>(&xmeta[s]);
+        if ((lane & 15) == 0) {
+          meta[lane >> 4] = down;
+          meta[2 + (lane >> 4)] = __int_as_float(lane < 16 ? sum_lo : sum_hi);
+        }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&xready[s]));
       }
@@ -247,8 +257,8 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&empty[s]));
-      const int v = (acc[0] + acc[1]) + (acc[2] + acc[3]) - 8 * __float_as_int(h ? meta.z : meta.y);
-      total = fmaf(sc * meta.x, (float)v, total);
+      const int v = (acc[0] + acc[1]) + (acc[2] + acc[3]) - 8 * __float_as_int(h ? meta.w : meta.z);
+      total = fmaf(sc * (h ? meta.y : meta.x), (float)v, total);
     }
     red[warp][lane] = total;
   }
@@ -573,17 +583,34 @@ bool make_schedule(const GemvProblem* probs, int count, int target, StreamArgs& 
   return true;
 }
 
+// Kernel attributes a launch may need: dynamic shared memory beyond the default (48 KB
+// minus the kernel's static shared memory) and clusters above 8 CTAs.  An attribute holds
+// for every later launch on the device, so each kernel asks once per device, for the whole
+// per-CTA budget.
+constexpr int kMaxDevices = 64;
+struct OptIns {
+  std::atomic<unsigned char> done[kMaxDevices];
+};
+OptIns g_int4_optins, g_bp_optins;
+
 template <typename Kernel>
-cudaError_t launch_streaming(Kernel kern, const StreamArgs& a, const Schedule& sc, size_t smem,
-                             int threads, cudaStream_t s) {
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
-  if (sc.C > 8) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-  }
+cudaError_t opt_in(Kernel kern, OptIns& o) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < kMaxDevices && o.done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess && dev < kMaxDevices) o.done[dev].store(1, std::memory_order_release);
+  return e;
+}
+
+template <typename Kernel>
+cudaError_t launch_streaming(Kernel kern, OptIns& o, const StreamArgs& a, const Schedule& sc,
+                             size_t smem, int threads, cudaStream_t s) {
+  if (smem > kSmemBudget) return cudaErrorInvalidValue;
+  cudaError_t e = opt_in(kern, o);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(sc.clusters * sc.C), 1, 1);
   cfg.blockDim = dim3((unsigned)threads, 1, 1);
@@ -621,7 +648,7 @@ cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int* err, cu
   S = S > kMaxStages ? kMaxStages : (S < 2 ? 2 : S);
   a.stages = sc.maxnb < S ? sc.maxnb : S;
   const size_t smem = (size_t)a.stages * kStage + slots;
-  return launch_streaming(int4_stream_kernel, a, sc, smem, kSThreads, s);
+  return launch_streaming(int4_stream_kernel, g_int4_optins, a, sc, smem, kSThreads, s);
 }
 
 cudaError_t launch_bp_stream(const GemvProblem* probs, int count, int* err, cudaStream_t s) {
@@ -638,7 +665,7 @@ cudaError_t launch_bp_stream(const GemvProblem* probs, int count, int* err, cuda
   a.err = err;
   a.stages = sc.maxnb < S ? sc.maxnb : S;
   const size_t smem = (size_t)a.stages * stage + slots;
-  return launch_streaming(bp_stream_kernel, a, sc, smem, kBpThreads, s);
+  return launch_streaming(bp_stream_kernel, g_bp_optins, a, sc, smem, kBpThreads, s);
 }
 
 }  // namespace lowbit

@@ -115,11 +115,15 @@ lowbit_status lowbit_validate_packed(const void* packed, int format, int P, int 
  */
 
 /* Y = X * W^T for symmetric per-group INT4 weights (Efficient-Qwen report, section 2.1):
- *   y[m][n] = sum_g s[n][g] * sum_{k in g} q[n][k] * x[m][k], fp32 accumulation, each
- *   output rounded once to bf16 (nearest, ties to even).
+ *   y[m][n] = sum_g s[n][g] * sum_{k in g} q[n][k] * x[m][k], fp32 accumulation across
+ *   groups, each output rounded once to bf16 (nearest, ties to even).
  *   X : bf16 [M][K], 16-byte aligned.   packed : from lowbit_pack_int4(N, K).
  *   Y : bf16 [M][N], written in full.   1 <= M <= 32.
- * M = 1 runs the streaming GEMV; M >= 2 runs the tensor-core skinny GEMM. */
+ * M = 1 runs the streaming GEMV: each run of 64 activations is held as int16 times one
+ * power of two (exact for every activation within a factor 2^7 of the run's largest,
+ * otherwise rounded to a multiple of 2^-15 of that largest) and the products within a run
+ * are summed exactly in integers; a non-finite activation makes every output NaN.
+ * M >= 2 runs the tensor-core skinny GEMM (exact bf16 products, fp32 sums per group). */
 lowbit_status lowbit_gemm_int4(const uint16_t* X, const void* packed, int M, int N, int K,
                                uint16_t* Y, void* stream);
 
@@ -136,7 +140,7 @@ typedef struct lowbit_gemm_desc {
  * of a decoder layer, which read the same activations), each with the contract and rounding
  * of lowbit_gemm_int4.  At M = 1 all of them run in ONE launch of the streaming GEMV, so the
  * launch, pipeline fill and drain are paid once for the group instead of once per matrix;
- * at M >= 2 each runs its own tensor-core launch, in order.
+ * at M >= 2 they share one launch of the tensor-core GEMM.
  *   descs : HOST array of `count` descriptors, 1 <= count <= 8; read during the call only.
  *   The multiplies must be independent: no Y may overlap any X, packed buffer or other Y of
  *   the group.  Every descriptor is validated before anything is enqueued. */

@@ -118,6 +118,37 @@ def activations(g: np.random.Generator, M: int, K: int) -> np.ndarray:
     return to_bf16_bits(g.standard_normal(size=(M, K)))
 
 
+ACTIVATION_KINDS = ("outlier", "mixed_scale", "tiny", "huge", "zero", "sparse")
+
+
+def activation_variant(g: np.random.Generator, M: int, K: int, kind: str) -> np.ndarray:
+    """bf16 activation rows X[M][K] (uint16 bits) with a magnitude structure other than
+    N(0, 1), drawn from one N(0, 1) matrix z and then, for each kind:
+      outlier     -- each channel is, with probability 1/256, multiplied by 1000 in every row
+                     (the few huge channels of decoder activations);
+      mixed_scale -- each run of 64 inputs of a row multiplied by 2^e, e ~ U{-30..30};
+      tiny / huge -- all of z times 2^-90 / 2^90;
+      zero        -- all zero;
+      sparse      -- each entry kept with probability 1/10, else zero (post-ReLU-like)."""
+    z = g.standard_normal(size=(M, K))
+    if kind == "outlier":
+        z = z * np.where(g.random(K) < 1 / 256, 1000.0, 1.0)[None, :]
+    elif kind == "mixed_scale":
+        e = g.integers(-30, 31, size=(M, (K + 63) // 64))
+        z = z * np.ldexp(1.0, np.repeat(e, 64, axis=1)[:, :K])
+    elif kind == "tiny":
+        z = np.ldexp(z, -90)
+    elif kind == "huge":
+        z = np.ldexp(z, 90)
+    elif kind == "zero":
+        z = np.zeros_like(z)
+    elif kind == "sparse":
+        z = np.where(g.random(size=(M, K)) < 0.1, z, 0.0)
+    else:
+        raise ValueError(kind)
+    return to_bf16_bits(z)
+
+
 def int4_problem(seed: int, M: int, N: int, K: int, *sub: int):
     """One INT4 problem: (codes, scales, X) drawn in that order."""
     g = generator(seed, M, N, K, *sub)

@@ -51,11 +51,16 @@ def host_bits(t):
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def check_gemm(y_gpu_bits: np.ndarray, Y64: np.ndarray, what: str = ""):
-    """Assert the GEMM parity criterion; returns (max normalised error, boundary cases)."""
+def check_gemm(y_gpu_bits: np.ndarray, Y64: np.ndarray, what: str = "", scale: float = 1.0):
+    """Assert the GEMM parity criterion; returns (max normalised error, boundary cases).
+
+    ``scale`` (a power of two) multiplies both sides before the comparison, so outputs of
+    inputs drawn at 2^-90 or 2^90 are held to the same relative bar; bf16 rounding commutes
+    with it while the values stay normal."""
     Y64 = np.atleast_2d(Y64)
-    g = numerics.bf16_to_f64(np.atleast_2d(y_gpu_bits))
-    r = numerics.round_to_bf16(Y64)
+    r = numerics.round_to_bf16(Y64) * scale
+    g = numerics.bf16_to_f64(np.atleast_2d(y_gpu_bits)) * scale
+    Y64 = Y64 * scale
     rms = np.sqrt(np.mean(Y64 ** 2, axis=1, keepdims=True))
     tol = REL_TOL * rms + ABS_TOL
     err = np.abs(g - r)

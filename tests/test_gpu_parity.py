@@ -96,6 +96,67 @@ def test_int4_small_and_ragged(lb, M, N, K, path):
     check_gemm(y, oint4.gemm(x, codes, scales), f"int4 M={M} N={N} K={K} path={path}")
 
 
+ACT_SCALE = {"tiny": 2.0 ** 90, "huge": 2.0 ** -90}
+
+
+@pytest.mark.parametrize("M,path", [(1, 1), (16, 1), (16, 2)])
+@pytest.mark.parametrize("kind", synth.ACTIVATION_KINDS)
+def test_int4_activation_structures(lb, kind, M, path):
+    """Outlier channels, per-run magnitude swings, extreme exponents, zeros and sparsity: the
+    M = 1 kernel holds each run of 64 activations as int16 under one power of two, so these
+    are the inputs that would expose a lost scale, a clipped outlier or a rounding bias."""
+    N, K = 645, 1408
+    g = synth.generator(91, M, N, K, synth.ACTIVATION_KINDS.index(kind))
+    codes, scales = synth.int4_weights(g, N, K)
+    x = synth.activation_variant(g, M, K, kind)
+    y = gemm_int4_gpu(lb, x, pack_int4_gpu(lb, codes, scales), M, N, K, path)
+    check_gemm(y, oint4.gemm(x, codes, scales), f"int4 {kind} M={M} path={path}",
+               scale=ACT_SCALE.get(kind, 1.0))
+
+
+@pytest.mark.parametrize("M,path", [(1, 1), (16, 1), (16, 2)])
+def test_int4_nan_activation(lb, M, path):
+    """A NaN activation in token 0 makes token 0's outputs NaN and leaves the others exact."""
+    N, K = 300, 640
+    codes, scales, x = synth.int4_problem(92, M, N, K)
+    x = x.copy()
+    x[0, 333] = 0x7FC0
+    y = gemm_int4_gpu(lb, x, pack_int4_gpu(lb, codes, scales), M, N, K, path)
+    from oracle import numerics
+    assert np.isnan(numerics.bf16_to_f64(y[0])).all()
+    if M > 1:
+        check_gemm(y[1:], oint4.gemm(x[1:], codes, scales), f"int4 NaN rows 1.. path={path}")
+
+
+@pytest.mark.parametrize("M,path", [(1, 1), (16, 2)])
+@pytest.mark.parametrize("kind", ("outlier", "mixed_scale", "tiny", "sparse"))
+def test_binplane_activation_structures(lb, kind, M, path):
+    P, N, K = 3, 260, 1024
+    g = synth.generator(93, P, M, N, K, synth.ACTIVATION_KINDS.index(kind))
+    bits, alpha = synth.binplane_weights(g, P, N, K)
+    x = synth.activation_variant(g, M, K, kind)
+    y = gemm_bp_gpu(lb, x, pack_bp_gpu(lb, bits, alpha), P, M, N, K, path)
+    check_gemm(y, obp.gemm(x, bits, alpha), f"binplane {kind} M={M} path={path}",
+               scale=ACT_SCALE.get(kind, 1.0))
+
+
+@pytest.mark.parametrize("N,K", [(5000, 5120), (4864, 8192)])
+def test_int4_m1_ring_at_default_smem_limit(lb, N, K):
+    """Shapes whose ring plus split-K slots (about 46-48 KB) fit under 48 KB while ring plus
+    the kernel's static shared memory does not: the launch needs the large-shared-memory
+    opt-in even though the dynamic size alone is below 48 KB."""
+    codes, scales, x = synth.int4_problem(94, 1, N, K)
+    y = gemm_int4_gpu(lb, x, pack_int4_gpu(lb, codes, scales), 1, N, K)
+    check_gemm(y, oint4.gemm(x, codes, scales), f"int4 M=1 N={N} K={K}")
+
+
+@pytest.mark.parametrize("P,N,K", [(5, 200, 5120), (5, 1300, 5120)])
+def test_binplane_m1_ring_at_default_smem_limit(lb, P, N, K):
+    bits, alpha, x = synth.binplane_problem(95, P, 1, N, K)
+    y = gemm_bp_gpu(lb, x, pack_bp_gpu(lb, bits, alpha), P, 1, N, K, 1)
+    check_gemm(y, obp.gemm(x, bits, alpha), f"binplane M=1 P={P} N={N} K={K}")
+
+
 def test_int4_config0_tiny_gemv(lb):
     cfg = synth.CONFIGS[0]
     (K, N), = cfg["shapes"]

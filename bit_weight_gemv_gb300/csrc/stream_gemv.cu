@@ -45,6 +45,7 @@ constexpr int kMaxStages = 6;
 // Dynamic shared memory per CTA (ring + reduction slots): with the static part, four CTAs fit
 // in an SM's 228 KB.
 constexpr size_t kSmemBudget = 53 * 1024;
+constexpr int kResidentPerSm = 4;  // CTAs per SM that the budget allows
 // Blocks per CTA the K split aims for: long streams amortise each CTA's fixed costs (start,
 // first-copy latency, exchange) once a matrix fills the GPU several times over; small
 // matrices are split further by the schedule's occupancy rule.
@@ -519,8 +520,8 @@ int sm_count() {
 
 
 // Schedule shared by both streaming kernels: ks per matrix aims at `target` blocks per
-// CTA, then all splits are doubled while the grid holds fewer than two CTAs per SM (small
-// launches).  Matrices are ordered by blocks per CTA, longest first.  Fills `a` and returns
+// CTA, then all splits are doubled while the doubled grid still fits the SMs' resident
+// capacity (small launches).  Matrices are ordered by blocks per CTA, longest first.  Fills `a` and returns
 // the cluster size C, the number of clusters, the largest blocks-per-CTA and the largest ks.
 struct Schedule {
   int C, maxnb, kmax;
@@ -538,16 +539,21 @@ bool make_schedule(const GemvProblem* probs, int count, int target, StreamArgs& 
     ks[i] = k;
     ctas += (long long)row_tiles(probs[i].N) * k;
   }
-  for (bool grew = true; grew && ctas < 2LL * nsm;) {
+  // Double every split while the doubled grid still fits the SMs' resident capacity: more
+  // concurrent streams, each with fewer blocks.
+  const long long resident = (long long)kResidentPerSm * nsm;
+  for (bool grew = true; grew;) {
     grew = false;
-    ctas = 0;
+    long long next = 0;
     for (int i = 0; i < count; ++i) {
-      if (ks[i] < kMaxSplit && ks[i] * 2 <= probs[i].K / kGroup) {
-        ks[i] *= 2;
-        grew = true;
-      }
-      ctas += (long long)row_tiles(probs[i].N) * ks[i];
+      const bool can = ks[i] < kMaxSplit && ks[i] * 2 <= probs[i].K / kGroup;
+      next += (long long)row_tiles(probs[i].N) * ks[i] * (can ? 2 : 1);
     }
+    if (next == ctas || next > resident) break;
+    for (int i = 0; i < count; ++i)
+      if (ks[i] < kMaxSplit && ks[i] * 2 <= probs[i].K / kGroup) ks[i] *= 2;
+    ctas = next;
+    grew = true;
   }
   int C = 1;
   for (int i = 0; i < count; ++i) C = ks[i] > C ? ks[i] : C;

@@ -9,10 +9,12 @@ Modules
   numerics  -- fp16/bf16 decoding and round-to-nearest-even into bf16.
   int4      -- symmetric per-group INT4: dequantise, multiply, pack/unpack the layout.
   binplane  -- ShiftAdd binary planes: dequantise, multiply, pack/unpack the layout.
+  sa        -- the deployed ShiftAdd format (u8 scale codes x one fp16 d per 256 inputs):
+               dequantise, multiply, pack/unpack the layout.
   verify    -- vocabulary argmax (lowest index on ties) and greedy prefix acceptance.
 
 Parity pins (tests/test_oracle_pins.py) tie every function to something other than
 itself: hand-worked 4x8 examples, brute force on tiny shapes, closed forms, invariants
 and library rounding routines.  No function here is "parity unpinned".
 """
-from . import numerics, int4, binplane, verify  # noqa: F401
+from . import numerics, int4, binplane, sa, verify  # noqa: F401

@@ -118,6 +118,36 @@ def activations(g: np.random.Generator, M: int, K: int) -> np.ndarray:
     return to_bf16_bits(g.standard_normal(size=(M, K)))
 
 
+# The deployed ShiftAdd format (ShiftAddQwen README, "Format"): Q sign planes per super-block
+# of 256 inputs, a u8 scale code per plane and group of G inputs, one fp16 d per super-block.
+SA_GROUPS = (64, 128, 256)
+SA_SHAPES = BINPLANE_SHAPES
+SA_TYPES = ((3, 64), (4, 128))   # (planes, group) of the benchmark rows: sa3 and sa4_128
+
+
+def sa_weights(g: np.random.Generator, P: int, N: int, K: int, G: int):
+    """sa-format weights: d fp16 bits [N][K/256] ~ |N(0, 0.02)| / 255; codes uint8
+    [P][N][K/G] with a_1 ~ U{128..255} and a_{p+1} = max(1, round(a_p * U(0.3, 0.6))) (the
+    plane-scale decay of the binary-plane configuration on the u8 grid); sign bits uint8
+    [P][N][K/8] uniform.  Draw order: d, codes, bits."""
+    d = to_f16_bits(np.abs(g.normal(0.0, 0.02, size=(N, K // 256))) / 255.0)
+    a = np.empty((P, N, K // G), dtype=np.float64)
+    a[0] = g.integers(128, 256, size=(N, K // G))
+    for p in range(1, P):
+        a[p] = np.maximum(1.0, np.rint(a[p - 1] * g.uniform(0.3, 0.6, size=(N, K // G))))
+    codes = a.astype(np.uint8)
+    bits = g.integers(0, 256, size=(P, N, K // 8), dtype=np.uint8)
+    return bits, codes, d
+
+
+def sa_problem(seed: int, P: int, G: int, M: int, N: int, K: int, *sub: int):
+    """One sa-format problem: (bits, codes, d, X)."""
+    g = generator(seed, 0x5A, P, G, M, N, K, *sub)
+    bits, codes, d = sa_weights(g, P, N, K, G)
+    x = activations(g, M, K)
+    return bits, codes, d, x
+
+
 ACTIVATION_KINDS = ("outlier", "mixed_scale", "tiny", "huge", "zero", "sparse")
 
 

@@ -10,7 +10,8 @@ import pytest
 import torch
 
 import synth
-from oracle import binplane, int4, numerics, verify
+from oracle import binplane, int4, numerics, sa, verify
+from oracle.numerics import bf16_to_f64, f16_to_f64
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -326,3 +327,140 @@ def test_acceptance_planted_drafts():
         assert n == j and bonus == a[j]
     d, j = synth.plant_drafts(5, a, 1000)
     assert verify.accept(a, d)[0] == j
+
+
+# ----------------------------------------------------------------------------- sa format
+# ShiftAddQwen README, "Format": per super-block of 256 inputs, Q sign planes, a u8 code per
+# plane and group of G inputs, one fp16 d; alpha = d * a.
+
+def _sa_hand_inputs():
+    P, N, K = 2, 2, 256
+    x = np.zeros((1, K))
+    x[0, :4] = [1, 2, 3, 4]
+    x[0, 128], x[0, 255] = 5, -1
+    bits = np.zeros((P, N, K // 8), dtype=np.uint8)
+    bits[0, 0, 0], bits[0, 0, 16], bits[0, 0, 31] = 0x05, 0x01, 0x80
+    bits[1, 0, 0] = 0x0F
+    bits[:, 1, :] = 0xFF
+    d = synth.to_f16_bits(np.array([[0.5], [0.25]]))
+    return synth.to_bf16_bits(x), bits, d
+
+
+def test_sa_hand_example():
+    x, bits, d = _sa_hand_inputs()
+    with open(os.path.join(GOLDEN, "sa_hand_2x256.txt")) as f:
+        rows = [line.split() for line in f if line.strip() and not line.startswith("#")]
+    assert len(rows) == 3
+    for G, c0, c1, y0, y1 in rows:
+        G = int(G)
+        a0 = [int(v) for v in c0.split(",")]
+        a1 = [int(v) for v in c1.split(",")]
+        codes = np.zeros((2, 2, 256 // G), dtype=np.uint8)
+        codes[0, :, :] = a0
+        codes[1, :, :] = a1
+        Y = sa.gemm(x, bits, codes, d, G)
+        assert Y[0, 0] == float(y0) and Y[0, 1] == float(y1), (G, Y)
+
+
+@pytest.mark.parametrize("G", sa.GROUPS)
+def test_sa_equals_fp16_alpha_planes_when_exact(G):
+    """With G = 128 and d * a exact in fp16, the sa weights are the fp16-alpha binary planes
+    with alpha = d * a; for G = 64 / 256 the same holds after expanding alpha to groups of 128
+    (G = 64: the two halves share one alpha only when their codes agree, so they are set equal)."""
+    P, N, K = 3, 40, 512
+    g = synth.generator(11, P, N, K, G)
+    bits = g.integers(0, 256, size=(P, N, K // 8), dtype=np.uint8)
+    codes = g.integers(1, 256, size=(P, N, K // G), dtype=np.uint8)
+    if G == 64:
+        codes[..., 1::2] = codes[..., 0::2]
+    d = synth.to_f16_bits(np.ldexp(g.integers(1, 8, size=(N, K // 256)).astype(float), -12))
+    x = synth.activations(g, 2, K)
+    dd = np.repeat(f16_to_f64(d), 2, axis=1)                                  # per group of 128
+    a128 = codes.astype(float)[..., ::2] if G == 64 else (
+        np.repeat(codes.astype(float), 2, axis=2) if G == 256 else codes.astype(float))
+    alpha = synth.to_f16_bits(dd[None] * a128)
+    assert np.array_equal(f16_to_f64(alpha), dd[None] * a128)               # exact in fp16
+    assert np.array_equal(sa.gemm(x, bits, codes, d, G), binplane.gemm(x, bits, alpha))
+
+
+@pytest.mark.parametrize("G", sa.GROUPS)
+def test_sa_brute_force(G):
+    P, N, K = 2, 3, 512
+    bits, codes, d, x = synth.sa_problem(12, P, G, 2, N, K)
+    X = bf16_to_f64(x)
+    dv = f16_to_f64(d)
+    ref = np.zeros((2, N))
+    for m in range(2):
+        for n in range(N):
+            acc = 0.0
+            for k in range(K):
+                w = 0.0
+                for p in range(P):
+                    sgn = 1.0 if (bits[p, n, k // 8] >> (k % 8)) & 1 else -1.0
+                    w += float(codes[p, n, k // G]) * sgn
+                acc += X[m, k] * dv[n, k // 256] * w
+            ref[m, n] = acc
+    Y = sa.gemm(x, bits, codes, d, G)
+    assert np.allclose(Y, ref, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("G", sa.GROUPS)
+def test_sa_group_and_superblock_locality(G):
+    """Only group g's code nonzero: the output depends on inputs of group g alone and scales
+    with that super-block's d; all signs +1 gives the closed form d * a * sum of the group."""
+    P, N, K = 2, 5, 768
+    g = synth.generator(13, G)
+    bits = np.full((P, N, K // 8), 0xFF, dtype=np.uint8)
+    d = synth.to_f16_bits(g.uniform(0.5, 2.0, size=(N, K // 256)))
+    x = synth.activations(g, 1, K)
+    X = bf16_to_f64(x)[0]
+    for grp in (0, K // G - 1, (K // G) // 2):
+        codes = np.zeros((P, N, K // G), dtype=np.uint8)
+        codes[0, :, grp], codes[1, :, grp] = 3, 5
+        Y = sa.gemm(x, bits, codes, d, G)[0]
+        ks = slice(grp * G, (grp + 1) * G)
+        expect = f16_to_f64(d)[:, (grp * G) // 256] * 8.0 * X[ks].sum()
+        assert np.allclose(Y, expect, rtol=1e-13, atol=0)
+        x2 = x.copy()
+        x2[0, ks] = 0
+        assert not np.any(sa.gemm(x2, bits, codes, d, G))
+
+
+def test_sa_layout_positions_by_hand():
+    P, N, K, G = 2, 200, 512, 64
+    total, off, payload, block = sa.packed_sizes(P, G, N, K)
+    assert block == 9472 and payload == 2 * 2 * 9472
+    with open(os.path.join(GOLDEN, "sa_layout_positions.txt")) as f:
+        rows = [line.split() for line in f if line.strip() and not line.startswith("#")]
+    zb = np.zeros((P, N, K // 8), dtype=np.uint8)
+    zc = np.zeros((P, N, K // G), dtype=np.uint8)
+    zd = np.zeros((N, K // 256), dtype=np.uint16)
+    for kind, p, n, kg, byte, bit in rows:
+        n, kg, byte = int(n), int(kg), int(byte)
+        bits, codes, d = zb.copy(), zc.copy(), zd.copy()
+        expect = np.zeros(payload, dtype=np.uint8)
+        if kind == "sign":
+            bits[int(p), n, kg // 8] = 1 << (kg % 8)
+            expect[byte] = 1 << int(bit)
+        elif kind == "code":
+            codes[int(p), n, kg] = 0xA5
+            expect[byte] = 0xA5
+        else:
+            d[n, kg] = 0x3C01
+            expect[byte], expect[byte + 1] = 0x01, 0x3C
+        sec = sa.pack(bits, codes, d, G)[off:off + payload]
+        assert np.array_equal(sec, expect), (kind, p, n, kg)
+
+
+@pytest.mark.parametrize("P,G,N,K", [(2, 64, 40, 256), (3, 128, 128, 512), (6, 64, 33, 256),
+                                     (1, 256, 256, 768), (4, 128, 129, 1024)])
+def test_sa_pack_round_trip(P, G, N, K):
+    bits, codes, d, _ = synth.sa_problem(14, P, G, 1, N, K)
+    packed = sa.pack(bits, codes, d, G)
+    b2, c2, d2, g2 = sa.unpack(packed)
+    assert g2 == G and np.array_equal(b2, bits) and np.array_equal(c2, codes) and np.array_equal(d2, d)
+    hd = int4.parse_header(packed)
+    assert hd["format"] == sa.FORMAT_SA and hd["group"] == G and hd["P"] == P
+    if N % 128 == 0:   # payload = sign bits + u8 codes + fp16 d, nothing else
+        assert hd["payload_bytes"] == P * N * K // 8 + P * N * K // G + 2 * N * K // 256
+

@@ -11,7 +11,8 @@ replayed from CUDA graphs (one per rotation of the weight copies) and timed with
 
 Also reported under "rows": the same layer as seven single-matrix calls ("decode") and as one
 grouped call ("decode_all"), the M=16 verify GEMM over the same layer and its batch sweep,
-binary-plane GEMV/GEMM, the 248,320-row vocabulary head as one M=1 GEMV ("head_gemv"), and the
+binary-plane GEMV/GEMM, the deployed ShiftAdd format (u8 scale codes, "sa_m1"/"sa_m16"), the
+248,320-row vocabulary head as one M=1 GEMV ("head_gemv"), and the
 LM-head argmax+verify over 248,320 and 32,768 rows.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-rows]
@@ -52,6 +53,11 @@ def algorithmic_int4_bytes(N, K):
 
 def algorithmic_binplane_bytes(P, N, K):
     return P * N * K // 8 + P * N * (K // 128) * 2
+
+
+def algorithmic_sa_bytes(P, G, N, K):
+    """Sign bits, u8 scale codes and one fp16 d per 256 inputs."""
+    return P * N * K // 8 + P * N * (K // G) + N * (K // 256) * 2
 
 
 def read_peaks():
@@ -242,6 +248,26 @@ def build_binplane(lb, torch, l2, M, path, name, desc):
     return w
 
 
+def build_sa(lb, torch, l2, M, name, desc):
+    w = Workload(name, desc, "sa_stream_kernel" if M == 1 else "binplane_cc_kernel")
+    mats = []
+    for si, (K, N) in enumerate(synth.SA_SHAPES):
+        for P, G in synth.SA_TYPES:
+            bits, codes, d, x = synth.sa_problem(3, P, G, M, N, K, si)
+            p = torch.empty(lb.lowbit_sa_packed_bytes(P, G, N, K), dtype=torch.uint8, device="cuda")
+            lb.lowbit_pack_sa(dev(bits), dev(codes), f16_dev(d), P, G, N, K, p)
+            mats.append((P, G, K, N, p, bf16_dev(x), torch.empty((M, N), dtype=torch.bfloat16, device="cuda")))
+            w.bytes += algorithmic_sa_bytes(P, G, N, K)
+    C = copies_for(w.bytes, l2)
+    copies = [_copies(m[4], C, torch) for m in mats]
+    for c in range(C):
+        w.calls.append([(lambda i=i, c=c: lb.lowbit_gemm_sa(
+            mats[i][5], copies[i][c], mats[i][0], mats[i][1], M, mats[i][3], mats[i][2], mats[i][6]))
+            for i in range(len(mats))])
+    w.M, w.tokens, w.launches = M, M, len(mats)
+    return w
+
+
 def build_lmhead(lb, torch, l2, N, path, name, desc):
     M, K = synth.VERIFY_BLOCK, synth.HEAD_K
     w = Workload(name, desc, "tc_gemm_kernel" if path != 1 else "int4_gemm_cc_kernel")
@@ -320,6 +346,12 @@ def build_workload(lb, torch, l2, name, path):
         return build_binplane(lb, torch, l2, M, path, name,
                               f"binary-plane GEMM: (K,N) in {{(4096,12288),(12288,4096)}} x P in {{3,4}}, "
                               f"M={M}, group 128")
+    if name in ("sa_m1", "sa_m16"):
+        M = 1 if name == "sa_m1" else 16
+        types = ", ".join(f"sa{P}{'' if G == 64 else '_' + str(G)}" for P, G in synth.SA_TYPES)
+        return build_sa(lb, torch, l2, M, name,
+                        f"deployed ShiftAdd format ({types}: u8 scale codes, fp16 d per 256 inputs): "
+                        f"(K,N) in {{(4096,12288),(12288,4096)}}, M={M}")
     if name == "head_gemv":
         return build_head_gemv(lb, torch, l2, path, name,
                                f"INT4 GEMV at M=1 over the {synth.HEAD_ROWS[0]}-row vocabulary head, "
@@ -332,7 +364,7 @@ def build_workload(lb, torch, l2, name, path):
     raise ValueError(name)
 
 
-WORKLOADS = ("decode", "decode_deps", "decode_all", "verify", "verify_deps", "verify_all", "binplane_m1", "binplane_m16", "head_gemv", "lmhead_full", "lmhead_trim",
+WORKLOADS = ("decode", "decode_deps", "decode_all", "verify", "verify_deps", "verify_all", "binplane_m1", "binplane_m16", "sa_m1", "sa_m16", "head_gemv", "lmhead_full", "lmhead_trim",
              "tiny") + tuple(f"verify_m{m}" for m in synth.M_SWEEP if m not in (16,))
 
 

@@ -15,6 +15,7 @@ __all__ = [
     "lowbit_status_string", "lowbit_validate_packed", "lowbit_version",
     "lowbit_gemm_int4_path", "lowbit_gemm_binplane_path", "lmhead_argmax_verify_path",
     "lowbit_gemm_int4_grouped", "lowbit_gemm_desc", "lmhead_argmax_verify_noalloc",
+    "lowbit_sa_packed_bytes", "lowbit_pack_sa", "lowbit_gemm_sa", "lowbit_gemm_sa_path",
 ]
 
 

@@ -33,6 +33,10 @@ _SIGS = {
     "lowbit_gemm_binplane_path": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _i, _vp]),
     "lmhead_argmax_verify_path": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _sz, _i, _vp]),
     "lowbit_device_error": (_i, [_vp, ctypes.POINTER(_i)]),
+    "lowbit_sa_packed_bytes": (_sz, [_i, _i, _i, _i]),
+    "lowbit_pack_sa": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp]),
+    "lowbit_gemm_sa": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
+    "lowbit_gemm_sa_path": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _i, _vp]),
 }
 
 
@@ -169,6 +173,36 @@ def lowbit_gemm_binplane_path(X, packed, P, M, N, K, Y, path, stream=None):
     _gemm_args(X, packed, M, N, K, Y)
     _check(lib.lowbit_gemm_binplane_path(_ptr(X), _ptr(packed), P, M, N, K, _ptr(Y), path,
                                          _stream(stream)), "lowbit_gemm_binplane_path")
+
+
+def lowbit_sa_packed_bytes(P: int, G: int, N: int, K: int) -> int:
+    return lib.lowbit_sa_packed_bytes(P, G, N, K)
+
+
+def lowbit_pack_sa(signbits, codes, d, P, G, N, K, packed, stream=None):
+    """signbits uint8 [P][N][K/8], codes uint8 [P][N][K/G], d fp16 [N][K/256] -> packed uint8."""
+    _need(signbits, torch.uint8, "signbits")
+    _need(codes, torch.uint8, "codes")
+    _need(d, torch.float16, "d")
+    _need(packed, torch.uint8, "packed")
+    if packed.numel() < lowbit_sa_packed_bytes(P, G, N, K):
+        raise ValueError("packed buffer too small")
+    _check(lib.lowbit_pack_sa(_ptr(signbits), _ptr(codes), _ptr(d), P, G, N, K, _ptr(packed),
+                              _stream(stream)), "lowbit_pack_sa")
+
+
+def lowbit_gemm_sa(X, packed, P, G, M, N, K, Y, stream=None):
+    """Y bf16 [M][N] = X bf16 [M][K] times the packed sa-format weights, transposed."""
+    _gemm_args(X, packed, M, N, K, Y)
+    _check(lib.lowbit_gemm_sa(_ptr(X), _ptr(packed), P, G, M, N, K, _ptr(Y), _stream(stream)),
+           "lowbit_gemm_sa")
+
+
+def lowbit_gemm_sa_path(X, packed, P, G, M, N, K, Y, path, stream=None):
+    """lowbit_gemm_sa with the kernel family forced (0 = default, 1 = CUDA cores)."""
+    _gemm_args(X, packed, M, N, K, Y)
+    _check(lib.lowbit_gemm_sa_path(_ptr(X), _ptr(packed), P, G, M, N, K, _ptr(Y), path,
+                                   _stream(stream)), "lowbit_gemm_sa_path")
 
 
 def _lmhead_args(H, packed_head, M, K, draft, argmax, n_accept, bonus, workspace):

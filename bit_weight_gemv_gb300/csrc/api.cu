@@ -24,6 +24,14 @@ inline lowbit_status check_shape(int M, int N, int K, int Mmax) {
   return LOWBIT_OK;
 }
 
+// The sa format: K a multiple of the 256-input super-block, 1..8 planes, G in {64, 128, 256}.
+inline lowbit_status check_sa(int P, int G, int M, int N, int K) {
+  const lowbit_status st = check_shape(M, N, K, 32);
+  if (st != LOWBIT_OK) return st;
+  if (K % kSuper != 0 || P < 1 || P > 8 || (G != 64 && G != 128 && G != 256)) return LOWBIT_ERR_SHAPE;
+  return LOWBIT_OK;
+}
+
 inline lowbit_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LOWBIT_OK : LOWBIT_ERR_CUDA; }
 
 }  // namespace
@@ -91,6 +99,11 @@ size_t lowbit_binplane_packed_bytes(int P, int N, int K) {
   return kHeaderBytes + binplane_payload_bytes(P, N, K);
 }
 
+size_t lowbit_sa_packed_bytes(int P, int G, int N, int K) {
+  if (check_sa(P, G, 1, N, K) != LOWBIT_OK) return 0;
+  return kHeaderBytes + sa_payload_bytes(P, G, N, K);
+}
+
 size_t lmhead_workspace_bytes(int M, int N, int K) {
   if (M < 2 || M > 32 || N < 1 || K <= 0 || K % kGroup != 0) return 0;
   return 512;
@@ -115,6 +128,16 @@ lowbit_status lowbit_pack_binplane(const uint8_t* signbits, const uint16_t* alph
   if (!aligned16(signbits) || !aligned16(packed)) return LOWBIT_ERR_ALIGN;
   return from_cuda(launch_pack_binplane(signbits, alpha, P, N, K, static_cast<uint8_t*>(packed),
                                         static_cast<cudaStream_t>(stream)));
+}
+
+lowbit_status lowbit_pack_sa(const uint8_t* signbits, const uint8_t* codes, const uint16_t* d,
+                             int P, int G, int N, int K, void* packed, void* stream) {
+  if (!signbits || !codes || !d || !packed) return LOWBIT_ERR_INVALID_ARG;
+  const lowbit_status st = check_sa(P, G, 1, N, K);
+  if (st != LOWBIT_OK) return st;
+  if (!aligned16(signbits) || !aligned16(packed)) return LOWBIT_ERR_ALIGN;
+  return from_cuda(launch_pack_sa(signbits, codes, d, P, G, N, K, static_cast<uint8_t*>(packed),
+                                  static_cast<cudaStream_t>(stream)));
 }
 
 lowbit_status lowbit_validate_packed(const void* packed, int format, int P, int N, int K,
@@ -209,6 +232,29 @@ lowbit_status lowbit_gemm_binplane_path(const uint16_t* X, const void* packed, i
   }
   if (path == 1) return from_cuda(launch_binplane_cc(X, pk, P, M, N, K, Y, err, s));
   return from_cuda(launch_binplane_tc(X, pk, P, M, N, K, Y, err, s));
+}
+
+lowbit_status lowbit_gemm_sa(const uint16_t* X, const void* packed, int P, int G, int M, int N,
+                             int K, uint16_t* Y, void* stream) {
+  return lowbit_gemm_sa_path(X, packed, P, G, M, N, K, Y, 0, stream);
+}
+
+lowbit_status lowbit_gemm_sa_path(const uint16_t* X, const void* packed, int P, int G, int M,
+                                  int N, int K, uint16_t* Y, int path, void* stream) {
+  if (!X || !packed || !Y || path < 0 || path > 1) return LOWBIT_ERR_INVALID_ARG;
+  const lowbit_status st = check_sa(P, G, M, N, K);
+  if (st != LOWBIT_OK) return st;
+  if (!aligned16(X) || !aligned16(packed)) return LOWBIT_ERR_ALIGN;
+  int* err = device_error_word();
+  if (!err) return LOWBIT_ERR_CUDA;
+  const uint8_t* pk = static_cast<const uint8_t*>(packed);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (M == 1) {
+    GemvProblem p = {X, pk, Y, N, K, 0, 1, 0, P, G};
+    p.early = allocation_covers(pk, kHeaderBytes + sa_payload_bytes(P, G, N, K)) ? 1 : 0;
+    return from_cuda(launch_sa_stream(&p, 1, err, s));
+  }
+  return from_cuda(launch_sa_cc(X, pk, P, G, M, N, K, Y, err, s));
 }
 
 lowbit_status lmhead_argmax_verify(const uint16_t* H, const void* packed_head, int M, int N,

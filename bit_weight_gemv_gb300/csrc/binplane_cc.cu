@@ -4,6 +4,11 @@
 // (ShiftAddQwen README, introduction and "Method": a mat-vec is a sign-select-and-add per
 // plane plus one scale per group).
 //
+// The SA instantiation reads the deployed ShiftAdd format (ShiftAddQwen README, "Format"): one
+// block per (tile, super-block of 256 inputs), alpha = d * a with a u8 code a per (plane, group
+// of G inputs) and one fp16 d per (row, super-block); its units of 128 inputs are the halves
+// of a super-block.
+//
 // Same work split as the INT4 CUDA-core kernel: one CTA per 32 rows (a quarter of a 128-row
 // layout tile), warps split the groups of a K segment, lane r owns row 32*cta + r and reads its
 // 16 bytes of signs per (group, plane) as part of one contiguous 512-byte warp load.  The sign select is an XOR
@@ -22,10 +27,10 @@ struct BpSeg {
   static constexpr int kSeg = (MT <= 4) ? 16 : (MT <= 16 ? 8 : 4);
 };
 
-template <int MT>
+template <int MT, bool SA>
 __global__ void __launch_bounds__(kThreads)
 binplane_cc_kernel(const uint16_t* __restrict__ X, const uint8_t* __restrict__ packed, int P,
-                   int M, int N, int K, uint16_t* __restrict__ Y, int* __restrict__ err) {
+                   int GS, int M, int N, int K, uint16_t* __restrict__ Y, int* __restrict__ err) {
   constexpr int SEG = BpSeg<MT>::kSeg;
   __shared__ __align__(16) uint16_t xs[MT * SEG * kGroup];
   __shared__ float red[kWarps * 32 * (MT < 8 ? MT : 8)];
@@ -34,16 +39,19 @@ binplane_cc_kernel(const uint16_t* __restrict__ X, const uint8_t* __restrict__ p
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x;  // 32-row unit: layout tile blockIdx.x / 4, quarter blockIdx.x % 4
 
-  if (threadIdx.x == 0)
-    ok = header_matches(reinterpret_cast<const PackedHeader*>(packed), kFormatBinplane, P, N, K);
+  if (threadIdx.x == 0) {
+    const PackedHeader* hp = reinterpret_cast<const PackedHeader*>(packed);
+    ok = SA ? header_matches_sa(hp, P, GS, N, K) : header_matches(hp, kFormatBinplane, P, N, K);
+  }
   __syncthreads();
   if (!ok) {
     if (threadIdx.x == 0 && blockIdx.x == 0) record_error(err, LOWBIT_ERR_INVALID_ARG);
     return;
   }
   const int rit = (tile & 3) * 32 + lane;
-  const uint32_t BB = binplane_block(P);
-  const uint8_t* tbase = packed + kHeaderBytes + (size_t)(tile >> 2) * G * BB;
+  // units of 128 inputs; SA: unit g is half g % 2 of super-block g / 2
+  const uint32_t BB = SA ? sa_block(P, GS) : binplane_block(P);
+  const uint8_t* tbase = packed + kHeaderBytes + (size_t)(tile >> 2) * (SA ? G / 2 : G) * BB;
 
   float total[MT];
 #pragma unroll
@@ -62,17 +70,40 @@ binplane_cc_kernel(const uint16_t* __restrict__ X, const uint8_t* __restrict__ p
     __syncthreads();
     for (int gl = warp; gl < sg; gl += kWarps) {
       const int g = s0 + gl;
+      const uint8_t* blk = tbase + (size_t)(SA ? g / 2 : g) * BB;
+      const int h = g & 1;
+      float dsa = 0.f;
+      if (SA) dsa = half_bits_to_float(__ldg(reinterpret_cast<const uint16_t*>(blk + sa_d_off(P, GS) + rit * 2)));
       for (int p = 0; p < P; ++p) {
-        const uint8_t* blk = tbase + (size_t)g * BB;
-        const uint4 wv = ld_stream(reinterpret_cast<const uint4*>(blk + p * (kRowTile * 16) + rit * 16));
-        const float a = half_bits_to_float(__ldg(reinterpret_cast<const uint16_t*>(
-            blk + binplane_alpha_off(P) + (p * kRowTile + rit) * 2)));
+        float a, a23;  // scale of words 0-1 and of words 2-3 of this unit
+        uint4 wv;
+        if (SA) {
+          wv = ld_stream(reinterpret_cast<const uint4*>(blk + (p * 2 + h) * (kRowTile * 16) + rit * 16));
+          const int GJ = kSuper / GS;
+          const int g01 = GS == 64 ? 2 * h : (GS == 128 ? h : 0), g23 = GS == 64 ? 2 * h + 1 : g01;
+          const uint8_t* ap = blk + sa_code_off(P) + (size_t)p * GJ * kRowTile + rit;
+          a = dsa * (float)__ldg(ap + g01 * kRowTile);
+          a23 = dsa * (float)__ldg(ap + g23 * kRowTile);
+        } else {
+          wv = ld_stream(reinterpret_cast<const uint4*>(blk + p * (kRowTile * 16) + rit * 16));
+          a = half_bits_to_float(__ldg(reinterpret_cast<const uint16_t*>(
+              blk + binplane_alpha_off(P) + (p * kRowTile + rit) * 2)));
+          a23 = a;
+        }
         const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
         float acc[MT];
 #pragma unroll
         for (int t = 0; t < MT; ++t) acc[t] = 0.f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
+          if (SA && j == 2 && GS == 64) {  // words 2-3 carry the next group's code
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+              total[t] = fmaf(a, acc[t], total[t]);
+              acc[t] = 0.f;
+            }
+            a = a23;
+          }
           const uint32_t nw = ~w4[j];
 #pragma unroll
           for (int i4 = 0; i4 < 4; ++i4) {
@@ -117,10 +148,11 @@ binplane_cc_kernel(const uint16_t* __restrict__ X, const uint8_t* __restrict__ p
   }
 }
 
-template <int MT>
-cudaError_t launch_bp(const uint16_t* X, const uint8_t* packed, int P, int M, int N, int K,
+template <int MT, bool SA = false>
+cudaError_t launch_bp(const uint16_t* X, const uint8_t* packed, int P, int GS, int M, int N, int K,
                       uint16_t* Y, int* err, cudaStream_t s) {
-  binplane_cc_kernel<MT><<<(unsigned)row_tiles(N) * 4, kThreads, 0, s>>>(X, packed, P, M, N, K, Y, err);
+  binplane_cc_kernel<MT, SA><<<(unsigned)row_tiles(N) * 4, kThreads, 0, s>>>(X, packed, P, GS, M, N,
+                                                                             K, Y, err);
   return cudaGetLastError();
 }
 
@@ -128,12 +160,22 @@ cudaError_t launch_bp(const uint16_t* X, const uint8_t* packed, int P, int M, in
 
 cudaError_t launch_binplane_cc(const uint16_t* X, const uint8_t* packed, int P, int M, int N,
                                int K, uint16_t* Y, int* err, cudaStream_t s) {
-  if (M <= 1) return launch_bp<1>(X, packed, P, M, N, K, Y, err, s);
-  if (M <= 2) return launch_bp<2>(X, packed, P, M, N, K, Y, err, s);
-  if (M <= 4) return launch_bp<4>(X, packed, P, M, N, K, Y, err, s);
-  if (M <= 8) return launch_bp<8>(X, packed, P, M, N, K, Y, err, s);
-  if (M <= 16) return launch_bp<16>(X, packed, P, M, N, K, Y, err, s);
-  return launch_bp<32>(X, packed, P, M, N, K, Y, err, s);
+  if (M <= 1) return launch_bp<1>(X, packed, P, 0, M, N, K, Y, err, s);
+  if (M <= 2) return launch_bp<2>(X, packed, P, 0, M, N, K, Y, err, s);
+  if (M <= 4) return launch_bp<4>(X, packed, P, 0, M, N, K, Y, err, s);
+  if (M <= 8) return launch_bp<8>(X, packed, P, 0, M, N, K, Y, err, s);
+  if (M <= 16) return launch_bp<16>(X, packed, P, 0, M, N, K, Y, err, s);
+  return launch_bp<32>(X, packed, P, 0, M, N, K, Y, err, s);
+}
+
+cudaError_t launch_sa_cc(const uint16_t* X, const uint8_t* packed, int P, int G, int M, int N,
+                         int K, uint16_t* Y, int* err, cudaStream_t s) {
+  if (M <= 1) return launch_bp<1, true>(X, packed, P, G, M, N, K, Y, err, s);
+  if (M <= 2) return launch_bp<2, true>(X, packed, P, G, M, N, K, Y, err, s);
+  if (M <= 4) return launch_bp<4, true>(X, packed, P, G, M, N, K, Y, err, s);
+  if (M <= 8) return launch_bp<8, true>(X, packed, P, G, M, N, K, Y, err, s);
+  if (M <= 16) return launch_bp<16, true>(X, packed, P, G, M, N, K, Y, err, s);
+  return launch_bp<32, true>(X, packed, P, G, M, N, K, Y, err, s);
 }
 
 }  // namespace lowbit

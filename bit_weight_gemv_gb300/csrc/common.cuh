@@ -14,6 +14,7 @@ namespace lowbit {
 constexpr uint32_t kMagic = 0x3242574Cu;  // "LWB2"
 constexpr uint32_t kFormatInt4 = 1;
 constexpr uint32_t kFormatBinplane = 2;
+constexpr uint32_t kFormatSa = 3;
 constexpr uint32_t kVersion = 2;
 constexpr int kHeaderBytes = 128;
 constexpr int kGroup = 128;    // inputs per quantisation group
@@ -42,6 +43,19 @@ __host__ __device__ inline uint64_t binplane_payload_bytes(int P, int N, int K) 
   return (uint64_t)row_tiles(N) * (uint64_t)(K / kGroup) * binplane_block(P);
 }
 
+// The deployed ShiftAdd format: one block per (128-row tile, super-block of 256 inputs) holding
+// signs [P][2 halves][128 rows][16 B], u8 scale codes [P][256/G groups][128 rows] and the
+// rows' fp16 d [128].  G (inputs per scale code) is 64, 128 or 256.
+constexpr int kSuper = 256;
+__host__ __device__ inline uint32_t sa_code_off(int P) { return (uint32_t)P * 2 * kRowTile * 16; }
+__host__ __device__ inline uint32_t sa_d_off(int P, int G) {
+  return sa_code_off(P) + (uint32_t)P * (kSuper / G) * kRowTile;
+}
+__host__ __device__ inline uint32_t sa_block(int P, int G) { return sa_d_off(P, G) + kRowTile * 2; }
+__host__ __device__ inline uint64_t sa_payload_bytes(int P, int G, int N, int K) {
+  return (uint64_t)row_tiles(N) * (uint64_t)(K / kSuper) * sa_block(P, G);
+}
+
 // Kernel-side header check.  Returns true when the buffer holds (format, P, N, K).
 __device__ __forceinline__ bool header_matches(const PackedHeader* h, uint32_t format, int P,
                                                int N, int K) {
@@ -49,6 +63,14 @@ __device__ __forceinline__ bool header_matches(const PackedHeader* h, uint32_t f
   const uint4 b = __ldg(reinterpret_cast<const uint4*>(h) + 1);
   return a.x == kMagic && a.y == format && a.z == kVersion && a.w == (uint32_t)N &&
          b.x == (uint32_t)K && b.y == (uint32_t)P;
+}
+
+// The same for the sa format, whose header also records the scale-code group G.
+__device__ __forceinline__ bool header_matches_sa(const PackedHeader* h, int P, int G, int N, int K) {
+  const uint4 a = __ldg(reinterpret_cast<const uint4*>(h));
+  const uint4 b = __ldg(reinterpret_cast<const uint4*>(h) + 1);
+  return a.x == kMagic && a.y == kFormatSa && a.z == kVersion && a.w == (uint32_t)N &&
+         b.x == (uint32_t)K && b.y == (uint32_t)P && b.z == (uint32_t)G;
 }
 
 __device__ __forceinline__ void record_error(int* err, int code) {
@@ -118,6 +140,7 @@ struct alignas(64) GemvProblem {
   int early;               // 1: the payload is known to lie inside packed's allocation, so
                            //    weight copies may start before the header has been checked
   int P;                   // binary planes per weight (0 for INT4)
+  int G;                   // sa format: inputs per scale code (64, 128 or 256)
 };
 constexpr int kMaxGemvProblems = 8;
 
@@ -128,6 +151,12 @@ cudaError_t launch_pack_binplane(const uint8_t* bits, const uint16_t* alpha, int
 cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int* err, cudaStream_t s);
 // Binary-plane counterpart (M = 1); every problem carries its plane count P (1..8).
 cudaError_t launch_bp_stream(const GemvProblem* probs, int count, int* err, cudaStream_t s);
+// sa-format counterpart (M = 1); every problem carries P (1..8) and G (64, 128, 256).
+cudaError_t launch_sa_stream(const GemvProblem* probs, int count, int* err, cudaStream_t s);
+cudaError_t launch_pack_sa(const uint8_t* bits, const uint8_t* codes, const uint16_t* d, int P,
+                           int G, int N, int K, uint8_t* packed, cudaStream_t s);
+cudaError_t launch_sa_cc(const uint16_t* X, const uint8_t* packed, int P, int G, int M, int N,
+                         int K, uint16_t* Y, int* err, cudaStream_t s);
 // Several INT4 multiplies with a common M >= 2 in one tensor-core launch (X, Y are [M][K], [M][N]).
 cudaError_t launch_int4_tc_grouped(const GemvProblem* probs, int count, int M, int* err,
                                    cudaStream_t s);

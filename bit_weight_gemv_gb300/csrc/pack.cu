@@ -1,4 +1,5 @@
-// Offline repack kernels: canonical INT4 codes / binary sign planes -> kernel layout.
+// Offline repack kernels: canonical INT4 codes / binary sign planes / the deployed ShiftAdd
+// format (sign planes with u8 scale codes and one fp16 d per 256 inputs) -> kernel layout.
 //
 // Efficient-Qwen report, section 2.1: INT4 codes under frozen symmetric per-group scales
 // (group 128), served as W4A16.  ShiftAddQwen README, "Format" and "Layout": sign planes
@@ -12,7 +13,7 @@
 namespace lowbit {
 namespace {
 
-__device__ void write_header(uint8_t* packed, uint32_t format, int P, int N, int K,
+__device__ void write_header(uint8_t* packed, uint32_t format, int P, int N, int K, int group,
                              uint64_t payload_bytes, uint64_t block_bytes) {
   PackedHeader h;
   h.magic = kMagic;
@@ -21,7 +22,7 @@ __device__ void write_header(uint8_t* packed, uint32_t format, int P, int N, int
   h.N = (uint32_t)N;
   h.K = (uint32_t)K;
   h.P = (uint32_t)P;
-  h.group = kGroup;
+  h.group = (uint32_t)group;
   h.row_tile = kRowTile;
   h.payload_offset = kHeaderBytes;
   h.payload_bytes = payload_bytes;
@@ -87,10 +88,10 @@ __global__ void pack_int4_scales(const uint16_t* __restrict__ scales, int N, int
       (n < N) ? scales[n * G + g] : (uint16_t)0;
 }
 
-__global__ void pack_header(uint8_t* packed, uint32_t format, int P, int N, int K,
+__global__ void pack_header(uint8_t* packed, uint32_t format, int P, int N, int K, int group,
                             unsigned long long payload_bytes, unsigned long long block_bytes) {
   if (threadIdx.x == 0 && blockIdx.x == 0)
-    write_header(packed, format, P, N, K, payload_bytes, block_bytes);
+    write_header(packed, format, P, N, K, group, payload_bytes, block_bytes);
 }
 
 // Even bits of a 32-bit word to its low half-word, odd bits to its high half-word.
@@ -145,6 +146,70 @@ __global__ void pack_binplane_alpha(const uint16_t* __restrict__ alpha, int P, i
   *reinterpret_cast<uint16_t*>(dst) = (n < N) ? alpha[((long long)p * N + n) * G + g] : (uint16_t)0;
 }
 
+// ---- sa format (ShiftAddQwen README, "Format"): block (t, j) per tile and super-block of 256.
+
+// One thread per 16-byte unit (tile t, super-block j, plane p, half h, row r): the 128 signs of
+// k = 256j + 128h .. +127, at block(t, j) + p*4096 + h*2048 + r*16, in the binary-plane word
+// order (even inputs in the low half-word, odd inputs in the high half-word).
+__global__ void pack_sa_signs(const uint8_t* __restrict__ bits, int P, int G, int N, int K,
+                              uint8_t* __restrict__ payload, long long units) {
+  const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= units) return;
+  const int J = K / kSuper;
+  const int r = (int)(u % kRowTile);
+  long long rest = u / kRowTile;
+  const int h = (int)(rest % 2);
+  rest /= 2;
+  const int p = (int)(rest % P);
+  rest /= P;
+  const int j = (int)(rest % J);
+  const long long t = rest / J;
+  const long long n = t * kRowTile + r;
+  uint4 v = make_uint4(0, 0, 0, 0);  // padding rows: all signs -1 (their d is 0)
+  if (n < N) {
+    const uint4 c = *reinterpret_cast<const uint4*>(bits + ((long long)p * N + n) * (K / 8) +
+                                                    32LL * j + 16 * h);
+    v = make_uint4(split_even_odd(c.x), split_even_odd(c.y), split_even_odd(c.z),
+                   split_even_odd(c.w));
+  }
+  uint8_t* dst = payload + (size_t)(t * J + j) * sa_block(P, G) + ((size_t)p * 2 + h) * kRowTile * 16 +
+                 r * 16;
+  *reinterpret_cast<uint4*>(dst) = v;
+}
+
+// One thread per scale code (tile t, super-block j, plane p, group gl of the super-block, row r)
+// at block(t, j) + 4096P + (p*(256/G) + gl)*128 + r.
+__global__ void pack_sa_codes(const uint8_t* __restrict__ codes, int P, int G, int N, int K,
+                              uint8_t* __restrict__ payload, long long units) {
+  const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= units) return;
+  const int J = K / kSuper, GJ = kSuper / G;
+  const int r = (int)(u % kRowTile);
+  long long rest = u / kRowTile;
+  const int gl = (int)(rest % GJ);
+  rest /= GJ;
+  const int p = (int)(rest % P);
+  rest /= P;
+  const int j = (int)(rest % J);
+  const long long t = rest / J;
+  const long long n = t * kRowTile + r;
+  payload[(size_t)(t * J + j) * sa_block(P, G) + sa_code_off(P) + ((size_t)p * GJ + gl) * kRowTile + r] =
+      (n < N) ? codes[((long long)p * N + n) * (K / G) + (long long)j * GJ + gl] : (uint8_t)0;
+}
+
+// One thread per (tile t, super-block j, row r) fp16 d at block(t, j) + sa_d_off + r*2.
+__global__ void pack_sa_d(const uint16_t* __restrict__ d, int P, int G, int N, int K,
+                          uint8_t* __restrict__ payload, long long units) {
+  const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= units) return;
+  const int J = K / kSuper;
+  const int r = (int)(u % kRowTile);
+  const long long tj = u / kRowTile;
+  const long long n = (tj / J) * kRowTile + r;
+  *reinterpret_cast<uint16_t*>(payload + (size_t)tj * sa_block(P, G) + sa_d_off(P, G) + r * 2) =
+      (n < N) ? d[n * J + tj % J] : (uint16_t)0;
+}
+
 // Launched last by every pack call: the multiplies read their weights before their
 // programmatic-dependency wait, so the kernel right before one must not be a weight writer.
 __global__ void pack_done() {}
@@ -159,7 +224,8 @@ cudaError_t launch_pack_int4(const int8_t* codes, const uint16_t* scales, int N,
                              uint8_t* packed, cudaStream_t s) {
   const long long blocks = (long long)row_tiles(N) * (K / kGroup);
   const long long cu = blocks * 4 * kRowTile, su = blocks * kRowTile;
-  pack_header<<<1, 32, 0, s>>>(packed, kFormatInt4, 0, N, K, int4_payload_bytes(N, K), kInt4Block);
+  pack_header<<<1, 32, 0, s>>>(packed, kFormatInt4, 0, N, K, kGroup, int4_payload_bytes(N, K),
+                               kInt4Block);
   pack_int4_codes<<<blocks_for(cu, 256), 256, 0, s>>>(codes, N, K, packed + kHeaderBytes, cu);
   pack_int4_scales<<<blocks_for(su, 256), 256, 0, s>>>(scales, N, K, packed + kHeaderBytes, su);
   pack_done<<<1, 32, 0, s>>>();
@@ -169,10 +235,23 @@ cudaError_t launch_pack_int4(const int8_t* codes, const uint16_t* scales, int N,
 cudaError_t launch_pack_binplane(const uint8_t* bits, const uint16_t* alpha, int P, int N, int K,
                                  uint8_t* packed, cudaStream_t s) {
   const long long units = (long long)row_tiles(N) * (K / kGroup) * P * kRowTile;
-  pack_header<<<1, 32, 0, s>>>(packed, kFormatBinplane, P, N, K, binplane_payload_bytes(P, N, K),
-                               binplane_block(P));
+  pack_header<<<1, 32, 0, s>>>(packed, kFormatBinplane, P, N, K, kGroup,
+                               binplane_payload_bytes(P, N, K), binplane_block(P));
   pack_binplane_codes<<<blocks_for(units, 256), 256, 0, s>>>(bits, P, N, K, packed + kHeaderBytes, units);
   pack_binplane_alpha<<<blocks_for(units, 256), 256, 0, s>>>(alpha, P, N, K, packed + kHeaderBytes, units);
+  pack_done<<<1, 32, 0, s>>>();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_sa(const uint8_t* bits, const uint8_t* codes, const uint16_t* d, int P,
+                           int G, int N, int K, uint8_t* packed, cudaStream_t s) {
+  const long long tj = (long long)row_tiles(N) * (K / kSuper);
+  const long long su = tj * P * 2 * kRowTile, cu = tj * P * (kSuper / G) * kRowTile, du = tj * kRowTile;
+  pack_header<<<1, 32, 0, s>>>(packed, kFormatSa, P, N, K, G, sa_payload_bytes(P, G, N, K),
+                               sa_block(P, G));
+  pack_sa_signs<<<blocks_for(su, 256), 256, 0, s>>>(bits, P, G, N, K, packed + kHeaderBytes, su);
+  pack_sa_codes<<<blocks_for(cu, 256), 256, 0, s>>>(codes, P, G, N, K, packed + kHeaderBytes, cu);
+  pack_sa_d<<<blocks_for(du, 256), 256, 0, s>>>(d, P, G, N, K, packed + kHeaderBytes, du);
   pack_done<<<1, 32, 0, s>>>();
   return cudaGetLastError();
 }

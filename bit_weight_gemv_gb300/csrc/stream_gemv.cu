@@ -318,8 +318,11 @@ constexpr int kLutWarp = kCWarps + 1;
 constexpr int kBpThreads = (kCWarps + 2) * 32;  // compute, producer, table warp
 constexpr uint32_t kLutBytes = 32 * 16 * sizeof(float);  // 32 nibble sets x 16 sums
 constexpr int kBpTargetBlocks = 5;
+constexpr int kSaTargetBlocks = 3;  // blocks of 256 inputs
+// sa stages are up to 41 KB (8 planes, G = 64): two of them and the split-K slots may exceed
+// the four-per-SM budget, so the sa kernel may use up to this much.
+constexpr size_t kSaSmemMax = 96 * 1024;
 
-__host__ __device__ inline uint32_t bp_stage_bytes(int P) { return binplane_block(P) + kXBytes; }
 
 // acc += sum over the 8 nibbles of one sign word of the tabulated signed sums; `tab` points
 // at the word's 8 tables of 16 floats (nibble n: inputs of pair slots 4n..4n+3).
@@ -328,8 +331,11 @@ __device__ __forceinline__ void lut_word(uint32_t w, const float* tab, float (&a
   for (int n = 0; n < 8; ++n) acc[n & 1] += tab[16 * n + ((w >> (4 * n)) & 0xFu)];
 }
 
-__global__ void __launch_bounds__(kBpThreads)
-bp_stream_kernel(const __grid_constant__ StreamArgs a) {
+// Body of both plane kernels.  SA = false: fp16-alpha planes, one block per (tile, group of
+// 128 inputs).  SA = true: the deployed format, one block per (tile, super-block of 256 inputs)
+// with u8 codes a per (plane, group of G) and one fp16 d per row (alpha = d * a).
+template <bool SA>
+__device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full[kMaxStages];
   __shared__ __align__(8) uint64_t tabready[kMaxStages];
@@ -348,16 +354,21 @@ bp_stream_kernel(const __grid_constant__ StreamArgs a) {
   const GemvProblem& pr = a.p[pi];
   const int ks = pr.ks, rank = crank % ks;
   const int tile = (cid - pr.cluster_begin) * (C / ks) + crank / ks;
-  const int G = pr.K / kGroup, P = pr.P;
+  constexpr int KIN = SA ? kSuper : kGroup;  // inputs per block
+  constexpr uint32_t XB = KIN * 2, LUT = (KIN / 4) * 16 * sizeof(float);  // activations, tables
+  const int G = pr.K / KIN, P = pr.P, GS = pr.G;
   const bool live = tile < row_tiles(pr.N);
   const int g0 = (int)((long long)rank * G / ks), g1 = (int)((long long)(rank + 1) * G / ks);
   const int nb = live ? g1 - g0 : 0;
   const int S = a.stages;
-  const uint32_t BB = binplane_block(P), SB = bp_stage_bytes(P) + kLutBytes;
+  const uint32_t BB = SA ? sa_block(P, GS) : binplane_block(P), SB = BB + XB + LUT;
+  auto header_ok = [&]() {
+    const PackedHeader* hp = reinterpret_cast<const PackedHeader*>(pr.packed);
+    return SA ? header_matches_sa(hp, P, GS, pr.N, pr.K) : header_matches(hp, kFormatBinplane, P, pr.N, pr.K);
+  };
 
   if (threadIdx.x == 0) {
-    ok = live && (pr.early || header_matches(reinterpret_cast<const PackedHeader*>(pr.packed),
-                                             kFormatBinplane, P, pr.N, pr.K));
+    ok = live && (pr.early || header_ok());
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
       ptx::mbar_init(ptx::smem_addr(&tabready[s]), 1);
@@ -371,26 +382,24 @@ bp_stream_kernel(const __grid_constant__ StreamArgs a) {
   if (C > 1) ptx::cluster_arrive();
   if (threadIdx.x == 0) grid_launch();
   const bool hdr_ok = ok != 0;
-  if (pr.early && live && threadIdx.x == 0 &&
-      !header_matches(reinterpret_cast<const PackedHeader*>(pr.packed), kFormatBinplane, P, pr.N, pr.K))
-    ok = 0;
+  if (pr.early && live && threadIdx.x == 0 && !header_ok()) ok = 0;
 
-  // stage s: block | activations (256 B) | tables (2 KB)
+  // stage s: block | activations (2 bytes per input) | tables (16 floats per 4 inputs)
   auto stage = [&](int s) { return smem + (size_t)s * SB; };
   if (warp == kCWarps) {
     // ---------------------------------------------------------------- producer
     if (lane == 0 && hdr_ok) {
       const uint8_t* wsrc = pr.packed + kHeaderBytes + ((size_t)tile * G + g0) * BB;
-      const uint16_t* xsrc = pr.X + (size_t)g0 * kGroup;
+      const uint16_t* xsrc = pr.X + (size_t)g0 * KIN;
       const int pre = min(nb, S);
       for (int b = 0; b < pre; ++b) {
         const uint32_t bar = ptx::smem_addr(&full[b]);
-        ptx::mbar_arrive_expect_tx(bar, BB + kXBytes);
+        ptx::mbar_arrive_expect_tx(bar, BB + XB);
         ptx::bulk_g2s(ptx::smem_addr(stage(b)), wsrc + (size_t)b * BB, BB, bar);
       }
       grid_wait();
       for (int b = 0; b < pre; ++b)
-        ptx::bulk_g2s(ptx::smem_addr(stage(b) + BB), xsrc + (size_t)b * kGroup, kXBytes,
+        ptx::bulk_g2s(ptx::smem_addr(stage(b) + BB), xsrc + (size_t)b * KIN, XB,
                       ptx::smem_addr(&full[b]));
       int issued = pre;
       for (int b = pre; b < nb; ++b) {
@@ -400,9 +409,9 @@ bp_stream_kernel(const __grid_constant__ StreamArgs a) {
           break;
         }
         const uint32_t bar = ptx::smem_addr(&full[s]);
-        ptx::mbar_arrive_expect_tx(bar, BB + kXBytes);
+        ptx::mbar_arrive_expect_tx(bar, BB + XB);
         ptx::bulk_g2s(ptx::smem_addr(stage(s)), wsrc + (size_t)b * BB, BB, bar);
-        ptx::bulk_g2s(ptx::smem_addr(stage(s) + BB), xsrc + (size_t)b * kGroup, kXBytes, bar);
+        ptx::bulk_g2s(ptx::smem_addr(stage(s) + BB), xsrc + (size_t)b * KIN, XB, bar);
         issued = b + 1;
       }
       for (int b = max(0, issued - S); b < issued; ++b)
@@ -411,11 +420,10 @@ bp_stream_kernel(const __grid_constant__ StreamArgs a) {
     __syncwarp();
   } else if (warp == kLutWarp) {
     // ---------------------------------------------------------------- tables
-    // Lane c tabulates nibble set c = 8w + n of the group: inputs k0 + {0, 2, 4, 6} with
-    // k0 = 32w + 8n (n < 4, even inputs) or 32w + 8(n - 4) + 1 (n >= 4, odd inputs).
+    // Nibble set c = 8w + n of a block (w = 32-input word, n = nibble): inputs k0 + {0, 2, 4, 6}
+    // with k0 = 32w + 8n (n < 4, even inputs) or 32w + 8(n - 4) + 1 (n >= 4, odd inputs).
+    // Lane l tabulates sets l, l + 32, ... (one per 128 inputs of the block).
     if (hdr_ok) {
-      const int w = lane >> 3, n = lane & 7;
-      const int k0 = 32 * w + (n < 4 ? 8 * n : 8 * (n - 4) + 1);
       for (int b = 0; b < nb; ++b) {
         const int s = b % S;
         const bool landed = ptx::mbar_wait(ptx::smem_addr(&full[s]), (b / S) & 1);
@@ -424,22 +432,27 @@ bp_stream_kernel(const __grid_constant__ StreamArgs a) {
           break;
         }
         const uint16_t* xr = reinterpret_cast<const uint16_t*>(stage(s) + BB);
-        const float x0 = bf16_bits_to_float(xr[k0]), x1 = bf16_bits_to_float(xr[k0 + 2]);
-        const float x2 = bf16_bits_to_float(xr[k0 + 4]), x3 = bf16_bits_to_float(xr[k0 + 6]);
-        float e[16];
-        e[0] = -((x0 + x1) + (x2 + x3));  // every sign -1
-        const float d0 = 2.f * x0, d1 = 2.f * x1, d2 = 2.f * x2, d3 = 2.f * x3;
 #pragma unroll
-        for (int m = 1; m < 16; ++m) {  // set bit j of m flips input j to +1
-          const int low = m & -m;
-          const float d = low == 1 ? d0 : (low == 2 ? d1 : (low == 4 ? d2 : d3));
-          e[m] = e[m & (m - 1)] + d;
+        for (int half = 0; half < KIN / kGroup; ++half) {
+          const int c = lane + 32 * half, w = c >> 3, n = c & 7;
+          const int k0 = 32 * w + (n < 4 ? 8 * n : 8 * (n - 4) + 1);
+          const float x0 = bf16_bits_to_float(xr[k0]), x1 = bf16_bits_to_float(xr[k0 + 2]);
+          const float x2 = bf16_bits_to_float(xr[k0 + 4]), x3 = bf16_bits_to_float(xr[k0 + 6]);
+          float e[16];
+          e[0] = -((x0 + x1) + (x2 + x3));  // every sign -1
+          const float d0 = 2.f * x0, d1 = 2.f * x1, d2 = 2.f * x2, d3 = 2.f * x3;
+#pragma unroll
+          for (int m = 1; m < 16; ++m) {  // set bit j of m flips input j to +1
+            const int low = m & -m;
+            const float d = low == 1 ? d0 : (low == 2 ? d1 : (low == 4 ? d2 : d3));
+            e[m] = e[m & (m - 1)] + d;
+          }
+          float4* t = reinterpret_cast<float4*>(stage(s) + BB + XB) + 4 * c;
+          t[0] = make_float4(e[0], e[1], e[2], e[3]);
+          t[1] = make_float4(e[4], e[5], e[6], e[7]);
+          t[2] = make_float4(e[8], e[9], e[10], e[11]);
+          t[3] = make_float4(e[12], e[13], e[14], e[15]);
         }
-        float4* t = reinterpret_cast<float4*>(stage(s) + BB + kXBytes) + 4 * lane;
-        t[0] = make_float4(e[0], e[1], e[2], e[3]);
-        t[1] = make_float4(e[4], e[5], e[6], e[7]);
-        t[2] = make_float4(e[8], e[9], e[10], e[11]);
-        t[3] = make_float4(e[12], e[13], e[14], e[15]);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&tabready[s]));
       }
@@ -458,15 +471,42 @@ bp_stream_kernel(const __grid_constant__ StreamArgs a) {
         break;
       }
       const uint8_t* st = stage(s);
-      const float* tab = reinterpret_cast<const float*>(st + BB + kXBytes) + 16 * 16 * h;
-      for (int p = 0; p < P; ++p) {
-        const uint2 sw = *reinterpret_cast<const uint2*>(st + p * (kRowTile * 16) + row * 16 + h * 8);
-        const float al = half_bits_to_float(
-            *reinterpret_cast<const uint16_t*>(st + binplane_alpha_off(P) + (p * kRowTile + row) * 2));
-        float acc[2] = {0.f, 0.f};
-        lut_word(sw.x, tab, acc);
-        lut_word(sw.y, tab + 8 * 16, acc);
-        total = fmaf(al, acc[0] + acc[1], total);
+      if constexpr (!SA) {
+        // inputs 64h..64h+63: sign words 2h, 2h+1 of each plane, nibble sets 16h..16h+15
+        const float* tab = reinterpret_cast<const float*>(st + BB + XB) + 16 * 16 * h;
+        for (int p = 0; p < P; ++p) {
+          const uint2 sw = *reinterpret_cast<const uint2*>(st + p * (kRowTile * 16) + row * 16 + h * 8);
+          const float al = half_bits_to_float(
+              *reinterpret_cast<const uint16_t*>(st + binplane_alpha_off(P) + (p * kRowTile + row) * 2));
+          float acc[2] = {0.f, 0.f};
+          lut_word(sw.x, tab, acc);
+          lut_word(sw.y, tab + 8 * 16, acc);
+          total = fmaf(al, acc[0] + acc[1], total);
+        }
+      } else {
+        // inputs 128h..128h+127: sign words 4h..4h+3 of each plane (the 16 bytes of half h),
+        // nibble sets 32h..32h+31; code group of word w is (128h + 32w) / G.
+        const float* tab = reinterpret_cast<const float*>(st + BB + XB) + 32 * 16 * h;
+        const uint8_t* codes = st + sa_code_off(P) + row;
+        const int GJ = kSuper / GS;
+        float sb = 0.f;  // sum_p sum_g a[p][g] * (sum of the selected activations of group g)
+        for (int p = 0; p < P; ++p) {
+          const uint4 sw = *reinterpret_cast<const uint4*>(st + (p * 2 + h) * (kRowTile * 16) + row * 16);
+          const uint8_t* ap = codes + p * GJ * kRowTile;
+          float acc[2] = {0.f, 0.f};
+          lut_word(sw.x, tab, acc);
+          lut_word(sw.y, tab + 8 * 16, acc);
+          if (GS == 64) {  // words 0-1 and 2-3 of the half carry different codes
+            sb = fmaf((float)ap[(2 * h) * kRowTile], acc[0] + acc[1], sb);
+            acc[0] = acc[1] = 0.f;
+          }
+          lut_word(sw.z, tab + 16 * 16, acc);
+          lut_word(sw.w, tab + 24 * 16, acc);
+          const int gl = GS == 64 ? 2 * h + 1 : (GS == 128 ? h : 0);
+          sb = fmaf((float)ap[gl * kRowTile], acc[0] + acc[1], sb);
+        }
+        total = fmaf(half_bits_to_float(*reinterpret_cast<const uint16_t*>(st + sa_d_off(P, GS) + row * 2)),
+                     sb, total);
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&empty[s]));
@@ -511,6 +551,17 @@ bp_stream_kernel(const __grid_constant__ StreamArgs a) {
   }
 }
 
+__global__ void __launch_bounds__(kBpThreads)
+bp_stream_kernel(const __grid_constant__ StreamArgs a) {
+  plane_stream_body<false>(a);
+}
+
+// The deployed ShiftAdd format at M = 1 (ShiftAddQwen README, "Format": alpha = d * a).
+__global__ void __launch_bounds__(kBpThreads)
+sa_stream_kernel(const __grid_constant__ StreamArgs a) {
+  plane_stream_body<true>(a);
+}
+
 int sm_count() {
   int dev = 0, nsm = 148;
   cudaGetDevice(&dev);
@@ -519,7 +570,8 @@ int sm_count() {
 }
 
 
-// Schedule shared by both streaming kernels: ks per matrix aims at `target` blocks per
+// Schedule shared by the streaming kernels (blocks of `kin` inputs): ks per matrix aims at
+// `target` blocks per
 // CTA, then all splits are doubled while the doubled grid still fits the SMs' resident
 // capacity (small launches).  Matrices are ordered by blocks per CTA, longest first.  Fills `a` and returns
 // the cluster size C, the number of clusters, the largest blocks-per-CTA and the largest ks.
@@ -528,12 +580,13 @@ struct Schedule {
   long long clusters;
 };
 
-bool make_schedule(const GemvProblem* probs, int count, int target, StreamArgs& a, Schedule& out) {
+bool make_schedule(const GemvProblem* probs, int count, int kin, int target, StreamArgs& a,
+                   Schedule& out) {
   const int nsm = sm_count();
   int ks[kMaxGemvProblems];
   long long ctas = 0;
   for (int i = 0; i < count; ++i) {
-    const int G = probs[i].K / kGroup;
+    const int G = probs[i].K / kin;
     int k = 1;
     while (k < kMaxSplit && k * 2 <= G && (G + k - 1) / k > target) k *= 2;
     ks[i] = k;
@@ -546,12 +599,12 @@ bool make_schedule(const GemvProblem* probs, int count, int target, StreamArgs& 
     grew = false;
     long long next = 0;
     for (int i = 0; i < count; ++i) {
-      const bool can = ks[i] < kMaxSplit && ks[i] * 2 <= probs[i].K / kGroup;
+      const bool can = ks[i] < kMaxSplit && ks[i] * 2 <= probs[i].K / kin;
       next += (long long)row_tiles(probs[i].N) * ks[i] * (can ? 2 : 1);
     }
     if (next == ctas || next > resident) break;
     for (int i = 0; i < count; ++i)
-      if (ks[i] < kMaxSplit && ks[i] * 2 <= probs[i].K / kGroup) ks[i] *= 2;
+      if (ks[i] < kMaxSplit && ks[i] * 2 <= probs[i].K / kin) ks[i] *= 2;
     ctas = next;
     grew = true;
   }
@@ -559,7 +612,7 @@ bool make_schedule(const GemvProblem* probs, int count, int target, StreamArgs& 
   for (int i = 0; i < count; ++i) C = ks[i] > C ? ks[i] : C;
   int order[kMaxGemvProblems];
   for (int i = 0; i < count; ++i) order[i] = i;
-  auto per_cta = [&](int i) { return (probs[i].K / kGroup + ks[i] - 1) / ks[i]; };
+  auto per_cta = [&](int i) { return (probs[i].K / kin + ks[i] - 1) / ks[i]; };
   for (int i = 1; i < count; ++i)  // stable insertion sort: most blocks per CTA first
     for (int j = i; j > 0 && per_cta(order[j]) > per_cta(order[j - 1]); --j) {
       const int t = order[j];
@@ -597,25 +650,25 @@ constexpr int kMaxDevices = 64;
 struct OptIns {
   std::atomic<unsigned char> done[kMaxDevices];
 };
-OptIns g_int4_optins, g_bp_optins;
+OptIns g_int4_optins, g_bp_optins, g_sa_optins;
 
 template <typename Kernel>
-cudaError_t opt_in(Kernel kern, OptIns& o) {
+cudaError_t opt_in(Kernel kern, OptIns& o, size_t budget) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < kMaxDevices && o.done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e == cudaSuccess && dev < kMaxDevices) o.done[dev].store(1, std::memory_order_release);
   return e;
 }
 
 template <typename Kernel>
-cudaError_t launch_streaming(Kernel kern, OptIns& o, const StreamArgs& a, const Schedule& sc,
-                             size_t smem, int threads, cudaStream_t s) {
-  if (smem > kSmemBudget) return cudaErrorInvalidValue;
-  cudaError_t e = opt_in(kern, o);
+cudaError_t launch_streaming(Kernel kern, OptIns& o, size_t budget, const StreamArgs& a,
+                             const Schedule& sc, size_t smem, int threads, cudaStream_t s) {
+  if (smem > budget) return cudaErrorInvalidValue;
+  cudaError_t e = opt_in(kern, o, budget);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(sc.clusters * sc.C), 1, 1);
@@ -645,7 +698,7 @@ cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int* err, cu
   if (count < 1 || count > kMaxGemvProblems) return cudaErrorInvalidValue;
   StreamArgs a = {};
   Schedule sc;
-  if (!make_schedule(probs, count, kInt4TargetBlocks, a, sc)) return cudaErrorInvalidValue;
+  if (!make_schedule(probs, count, kGroup, kInt4TargetBlocks, a, sc)) return cudaErrorInvalidValue;
   a.err = err;
   // ring, then the partial-sum slots rank 0 of a split tile receives; the ring takes what the
   // slots leave of the per-CTA budget (four CTAs per SM)
@@ -654,24 +707,43 @@ cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int* err, cu
   S = S > kMaxStages ? kMaxStages : (S < 2 ? 2 : S);
   a.stages = sc.maxnb < S ? sc.maxnb : S;
   const size_t smem = (size_t)a.stages * kStage + slots;
-  return launch_streaming(int4_stream_kernel, g_int4_optins, a, sc, smem, kSThreads, s);
+  return launch_streaming(int4_stream_kernel, g_int4_optins, kSmemBudget, a, sc, smem, kSThreads, s);
 }
 
 cudaError_t launch_bp_stream(const GemvProblem* probs, int count, int* err, cudaStream_t s) {
   if (count < 1 || count > kMaxGemvProblems) return cudaErrorInvalidValue;
   StreamArgs a = {};
   Schedule sc;
-  if (!make_schedule(probs, count, kBpTargetBlocks, a, sc)) return cudaErrorInvalidValue;
+  if (!make_schedule(probs, count, kGroup, kBpTargetBlocks, a, sc)) return cudaErrorInvalidValue;
   int pmax = 1;
   for (int i = 0; i < count; ++i) pmax = probs[i].P > pmax ? probs[i].P : pmax;
-  const size_t stage = bp_stage_bytes(pmax) + kLutBytes;
+  const size_t stage = binplane_block(pmax) + kXBytes + kLutBytes;
   const size_t slots = (size_t)(sc.kmax - 1) * kRowTile * sizeof(float);
   int S = (int)((kSmemBudget - slots) / stage);
   S = S < 2 ? 2 : (S > kMaxStages ? kMaxStages : S);
   a.err = err;
   a.stages = sc.maxnb < S ? sc.maxnb : S;
   const size_t smem = (size_t)a.stages * stage + slots;
-  return launch_streaming(bp_stream_kernel, g_bp_optins, a, sc, smem, kBpThreads, s);
+  return launch_streaming(bp_stream_kernel, g_bp_optins, kSmemBudget, a, sc, smem, kBpThreads, s);
+}
+
+cudaError_t launch_sa_stream(const GemvProblem* probs, int count, int* err, cudaStream_t s) {
+  if (count < 1 || count > kMaxGemvProblems) return cudaErrorInvalidValue;
+  StreamArgs a = {};
+  Schedule sc;
+  if (!make_schedule(probs, count, kSuper, kSaTargetBlocks, a, sc)) return cudaErrorInvalidValue;
+  size_t stage = 0;  // largest stage of the launch: block + activations + tables
+  for (int i = 0; i < count; ++i) {
+    const size_t st = sa_block(probs[i].P, probs[i].G) + kSuper * 2 + (kSuper / 4) * 16 * sizeof(float);
+    stage = st > stage ? st : stage;
+  }
+  const size_t slots = (size_t)(sc.kmax - 1) * kRowTile * sizeof(float);
+  int S = (int)((kSmemBudget > slots ? kSmemBudget - slots : 0) / stage);
+  S = S < 2 ? 2 : (S > kMaxStages ? kMaxStages : S);
+  a.err = err;
+  a.stages = sc.maxnb < S ? sc.maxnb : S;
+  const size_t smem = (size_t)a.stages * stage + slots;
+  return launch_streaming(sa_stream_kernel, g_sa_optins, kSaSmemMax, a, sc, smem, kBpThreads, s);
 }
 
 }  // namespace lowbit

@@ -27,8 +27,8 @@
  *     weights (header included) before waiting for the preceding kernel on the stream, and
  *     read activations / write outputs only after that wait.  So the kernel immediately
  *     before a multiply on the same stream must not write that multiply's packed buffer.
- *     lowbit_pack_int4 and lowbit_pack_binplane end with an empty kernel, which makes
- *     "pack, then multiply" on one stream safe.
+ *     lowbit_pack_int4, lowbit_pack_binplane and lowbit_pack_sa end with an empty kernel,
+ *     which makes "pack, then multiply" on one stream safe.
  *   - No C++ exception crosses this interface.
  */
 #ifndef LOWBIT_H
@@ -69,6 +69,11 @@ size_t lowbit_int4_packed_bytes(int N, int K);
  * P*K/64 plane-scale bytes. */
 size_t lowbit_binplane_packed_bytes(int P, int N, int K);
 
+/* Bytes of a packed buffer of the deployed ShiftAdd format (lowbit_pack_sa): header +
+ * ceil(N/128)*128 rows of P*K/8 sign bytes, P*K/G code bytes and K/128 bytes of d.  0 unless
+ * K % 256 == 0, 1 <= P <= 8 and G is 64, 128 or 256. */
+size_t lowbit_sa_packed_bytes(int P, int G, int N, int K);
+
 /* Bytes of the workspace lmhead_argmax_verify() needs (independent of N and K). */
 size_t lmhead_workspace_bytes(int M, int N, int K);
 
@@ -103,6 +108,26 @@ lowbit_status lowbit_pack_int4(const int8_t* codes, const uint16_t* scales, int 
  * alpha[p][n][g] (fp16) sits at 2048*P + (p*128 + r)*2. */
 lowbit_status lowbit_pack_binplane(const uint8_t* signbits, const uint16_t* alpha, int P, int N,
                                    int K, void* packed, void* stream);
+
+/* Repack the deployed ShiftAdd format (ShiftAddQwen README, "Format": per super-block of 256
+ * weights along the input dimension, Q sign planes, one u8 scale code per plane and group of G
+ * weights, one fp16 scale d; alpha = d * a), so that
+ *   w[n][k] = d[n][k/256] * sum_p a[p][n][k/G] * b[p][n][k],   b in {-1, +1}.
+ *   signbits : uint8 [P][N][K/8], 16-byte aligned; bit j (LSB first) of byte i is input 8i + j;
+ *              1 = +1.
+ *   codes    : uint8 [P][N][K/G], the scale codes a (any alignment).
+ *   d        : fp16 [N][K/256] (2-byte aligned).
+ *   packed   : lowbit_sa_packed_bytes(P, G, N, K) bytes, 16-byte aligned; fully overwritten.
+ *   1 <= P <= 8, G in {64, 128, 256}, K % 256 == 0 (else LOWBIT_ERR_SHAPE).
+ * Layout: header (format 3, group field = G), then tiles of 128 rows; tile t and super-block
+ * j (inputs 256j..256j+255) own one contiguous block of B = 4096P + 128P(256/G) + 256 bytes at
+ * 128 + (t*(K/256) + j)*B: for plane p, half h and row r = n % 128 the 16 bytes at
+ * p*4096 + h*2048 + r*16 hold the signs of k = 256j + 128h.. as four u32 words (word w covers
+ * k0 = 256j + 128h + 32w: bit i = sign of k0 + 2i, bit 16 + i = sign of k0 + 2i + 1); the code
+ * a[p][n][g] sits at 4096P + (p*(256/G) + g - j*(256/G))*128 + r, and d[n][j] (fp16) at
+ * 4096P + 128P(256/G) + r*2.  Padding rows hold zero signs, codes and d. */
+lowbit_status lowbit_pack_sa(const uint8_t* signbits, const uint8_t* codes, const uint16_t* d,
+                             int P, int G, int N, int K, void* packed, void* stream);
 
 /* Synchronous check (copies the 128-byte header to the host after synchronising `stream`)
  * that `packed` holds format `format` (1 = INT4, 2 = binary planes) with these P, N, K.
@@ -152,6 +177,16 @@ lowbit_status lowbit_gemm_int4_grouped(const lowbit_gemm_desc* descs, int count,
  *   Shapes and rounding as lowbit_gemm_int4; packed from lowbit_pack_binplane(P, N, K). */
 lowbit_status lowbit_gemm_binplane(const uint16_t* X, const void* packed, int P, int M, int N,
                                    int K, uint16_t* Y, void* stream);
+
+/* Y = X * W^T for the deployed ShiftAdd format (ShiftAddQwen README, "Format"):
+ *   y[m][n] = sum_j d[n][j] * sum_p sum_{g in j} a[p][n][g] * sum_{k in g} b[p][n][k] * x[m][k],
+ *   fp32 accumulation, each output rounded once to bf16.  X, Y as lowbit_gemm_int4,
+ *   1 <= M <= 32; packed from lowbit_pack_sa(P, G, N, K); K % 256 == 0.  M = 1 runs the
+ *   streaming mat-vec (per plane a table-driven sign-select-and-add, one scale per group);
+ *   M >= 2 runs the CUDA-core kernel (sign select by XOR into the activation's sign bit).
+ *   The header (format 3, P, N, K, G) is checked on the device as for the other formats. */
+lowbit_status lowbit_gemm_sa(const uint16_t* X, const void* packed, int P, int G, int M, int N,
+                             int K, uint16_t* Y, void* stream);
 
 /* LM-head verify step (small-vocabulary MTP study, section 3.3: full-vocabulary verification;
  * DFlash summary, section 4.1: tau in [1, gamma + 1]; Efficient-Qwen report, section 2.2).
@@ -208,6 +243,9 @@ lowbit_status lmhead_argmax_verify_path(const uint16_t* H, const void* packed_he
                                         int K, const int32_t* draft, int32_t* argmax,
                                         int32_t* n_accept, int32_t* bonus, void* workspace,
                                         size_t ws_bytes, int path, void* stream);
+/* The sa format has CUDA-core kernels only: path 0 or 1; 2 returns INVALID_ARG. */
+lowbit_status lowbit_gemm_sa_path(const uint16_t* X, const void* packed, int P, int G, int M,
+                                  int N, int K, uint16_t* Y, int path, void* stream);
 
 /* ------------------------------------------------------------------------------------------
  * Device-side error word.

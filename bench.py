@@ -249,7 +249,7 @@ def build_binplane(lb, torch, l2, M, path, name, desc):
 
 
 def build_sa(lb, torch, l2, M, name, desc):
-    w = Workload(name, desc, "sa_stream_kernel" if M == 1 else "binplane_cc_kernel")
+    w = Workload(name, desc, "sa_stream_kernel" if M == 1 else "tc_gemm_kernel")
     mats = []
     for si, (K, N) in enumerate(synth.SA_SHAPES):
         for P, G in synth.SA_TYPES:

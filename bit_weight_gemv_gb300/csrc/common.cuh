@@ -157,6 +157,8 @@ cudaError_t launch_pack_sa(const uint8_t* bits, const uint8_t* codes, const uint
                            int G, int N, int K, uint8_t* packed, cudaStream_t s);
 cudaError_t launch_sa_cc(const uint16_t* X, const uint8_t* packed, int P, int G, int M, int N,
                          int K, uint16_t* Y, int* err, cudaStream_t s);
+cudaError_t launch_sa_tc(const uint16_t* X, const uint8_t* packed, int P, int G, int M, int N,
+                         int K, uint16_t* Y, int* err, cudaStream_t s);
 // Several INT4 multiplies with a common M >= 2 in one tensor-core launch (X, Y are [M][K], [M][N]).
 cudaError_t launch_int4_tc_grouped(const GemvProblem* probs, int count, int M, int* err,
                                    cudaStream_t s);

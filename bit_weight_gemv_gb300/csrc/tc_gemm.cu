@@ -23,6 +23,10 @@
 // Exactness of the operands (all bf16 arithmetic below is exact):
 //   INT4: a nibble ORed into bf16 128.0 is 128 + u (u = q + 8); subtracting 136 leaves q, so a
 //     group's accumulator is D = sum q x and the epilogue adds s * D.
+//   sa format (ShiftAddQwen README, "Format": alpha = d * a, u8 code a per plane and group of G
+//     inputs, one fp16 d per 256 inputs): a thread's 64 inputs share one code a (G >= 64), so
+//     it writes +-a (exact in bf16) by XORing the sign into the bf16 pair (a, a); a unit is
+//     one (half of a 256-input super-block, plane) and the epilogue adds d * D.
 //   Binary planes: the plane bit of pair i of a 32-input word, ORed into mantissa bit j(i) in
 //     1..6 of bf16 1.0, gives 1 + beta * 2^(j-7) (beta in {0,1}); subtracting 1 + 2^(j-8)
 //     leaves b * 2^(j-8) with b = 2 beta - 1 in {-1, +1}.  The activation of that input is
@@ -46,7 +50,7 @@ constexpr int kMmaWarp = 9;
 constexpr int kXWarp = 10;
 constexpr int kThreads = 352;
 constexpr uint32_t kTmemCols = 256;
-constexpr int kFmtInt4 = 0, kFmtBinplane = 1;
+constexpr int kFmtInt4 = 0, kFmtBinplane = 1, kFmtSa = 2;
 constexpr int kEpiStore = 0, kEpiArgmax = 1;
 
 struct TcArgs {
@@ -54,7 +58,8 @@ struct TcArgs {
   const uint16_t* X;
   uint16_t* Y;
   int M, N, K, P;
-  int groups_per_rank;
+  int GS;            // sa format: inputs per scale code (64, 128, 256)
+  int groups_per_rank;  // blocks (groups of 128 inputs; sa: super-blocks of 256) per K rank
   int ks;            // CTAs splitting one row block's groups (divides the cluster size)
   int cl_begin;      // first cluster of this matrix
   int ncl;           // clusters of this matrix (they walk its row blocks with stride ncl * C / ks)
@@ -73,23 +78,27 @@ struct TcBatch {
   TcArgs p[kMaxGemvProblems];
   int count;
   int cluster;
+  int stages;  // sa format: ring stages (its blocks vary with P and G)
 };
 
 template <int FMT, int NMMA>
 struct TcLayout {
-  static constexpr int kStages = NMMA <= 16 ? 6 : 5;
+  static constexpr int kStages = NMMA <= 16 ? 6 : 5;   // sa: chosen per launch (TcBatch::stages)
   static constexpr int NB = NMMA <= 16 ? 3 : 2;        // A/D buffers in tensor memory
   static constexpr uint32_t kColA = 0;                  // A[NB]: 64 columns each
   static constexpr uint32_t kColD = 64 * NB;            // D[NB]: NMMA columns each
   static_assert(64 * NB + NMMA * NB <= (int)kTmemCols, "tensor memory budget");
+  static constexpr int KIN = FMT == kFmtSa ? kSuper : kGroup;  // inputs per block
   static constexpr uint32_t kAtom = NMMA * 128;  // one 64-input swizzle atom of the X tile
-  static constexpr uint32_t kX = 2 * kAtom;      // X tile for one group of 128 inputs
-  __host__ __device__ static uint32_t block(int P) {
-    return FMT == kFmtInt4 ? kInt4Block : binplane_block(P);
+  static constexpr uint32_t kX = (KIN / 64) * kAtom;  // X tile for one block
+  __host__ __device__ static uint32_t block(int P, int GS) {
+    return FMT == kFmtInt4 ? kInt4Block : (FMT == kFmtSa ? sa_block(P, GS) : binplane_block(P));
   }
-  __host__ __device__ static uint32_t stage(int P) { return (kX + block(P) + 1023u) / 1024u * 1024u; }
+  __host__ __device__ static uint32_t stage(int P, int GS) {
+    return (kX + block(P, GS) + 1023u) / 1024u * 1024u;
+  }
   static constexpr uint32_t kCtrl = 1024;
-  __host__ static size_t smem(int P) { return 1024 + (size_t)kStages * stage(P) + kCtrl; }
+  __host__ static size_t smem(int P, int GS, int S) { return 1024 + (size_t)S * stage(P, GS) + kCtrl; }
 };
 
 // j(i): the mantissa bit (1..6) that carries pair i of a 32-input plane word.  Pairs 0-5 are
@@ -134,11 +143,19 @@ __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// sa: the bf16 pair (a, a) with the signs of inputs 2i, 2i+1 of word w taken from bits i and
+// 16 + i (bit set = +1, so the sign bit is set where the plane bit is 0).
+__device__ __forceinline__ void dequant_sa_word(uint32_t w, uint32_t apair, uint32_t (&v)[16]) {
+  const uint32_t nw = ~w;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = apair ^ ((nw << (15 - i)) & 0x80008000u);
+}
+
 template <int FMT, int NMMA, int EPI>
 __global__ void __launch_bounds__(kThreads, 2)
 tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
   using L = TcLayout<FMT, NMMA>;
-  constexpr int S = L::kStages;
+  const int S = FMT == kFmtSa ? batch.stages : L::kStages;
   constexpr int TOK = NMMA / 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -149,8 +166,9 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
     if (cid >= batch.p[i].cl_begin) pi = i;
   const TcArgs& args = batch.p[pi];
   const CUtensorMap* xmap = &batch.maps[pi];
-  const int P = (FMT == kFmtInt4) ? 1 : args.P;
-  const uint32_t SB = L::stage(P), BB = L::block(P);
+  const int P = (FMT == kFmtInt4) ? 1 : args.P, GS = args.GS;
+  const uint32_t SB = L::stage(P, GS), BB = L::block(P, GS);
+  const int UB = FMT == kFmtSa ? 2 * P : P;  // MMA units per block: (half, plane) for sa
   constexpr int NB = L::NB;
   uint8_t* ctrl = smem + (size_t)S * SB;
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
@@ -164,21 +182,22 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ks = args.ks, rank = crank % ks;
-  const int N = args.N, K = args.K, G = K / kGroup, RB = row_tiles(N);
+  const int N = args.N, K = args.K, G = K / L::KIN, RB = row_tiles(N);
   const int tile0 = (cid - args.cl_begin) * (C / ks) + crank / ks;  // first row block
   const int tstride = args.ncl * (C / ks);                            // row-block stride
   const int g0 = min(G, rank * args.groups_per_rank);
   const int g1 = min(G, g0 + args.groups_per_rank);
   const int ngroups = g1 - g0;
-  const int upi = ngroups * P;  // units per item
+  const int upi = ngroups * UB;  // units per item
   const int nitems = tile0 < RB ? (RB - tile0 + tstride - 1) / tstride : 0;
   const int total_groups = nitems * ngroups;
   const int total_units = nitems * upi;
 
   if (threadIdx.x == 0) {
-    flags[0] = header_matches(reinterpret_cast<const PackedHeader*>(args.packed),
-                              FMT == kFmtInt4 ? kFormatInt4 : kFormatBinplane,
-                              FMT == kFmtInt4 ? 0 : P, N, K);
+    const PackedHeader* hp = reinterpret_cast<const PackedHeader*>(args.packed);
+    flags[0] = FMT == kFmtSa ? header_matches_sa(hp, P, GS, N, K)
+                             : header_matches(hp, FMT == kFmtInt4 ? kFormatInt4 : kFormatBinplane,
+                                              FMT == kFmtInt4 ? 0 : P, N, K);
     flags[1] = 0;
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_addr(&full[s]), 1);
@@ -234,8 +253,10 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
       };
       auto issue_x = [&](int gi) {
         const int s = gi % S, g = g0 + gi % ngroups;
-        tma_load_2d(smem_addr(stage_x(s)), xmap, g * kGroup, 0, smem_addr(&full[s]));
-        tma_load_2d(smem_addr(stage_x(s)) + L::kAtom, xmap, g * kGroup + 64, 0, smem_addr(&full[s]));
+#pragma unroll
+        for (int at = 0; at < L::KIN / 64; ++at)
+          tma_load_2d(smem_addr(stage_x(s)) + at * L::kAtom, xmap, g * L::KIN + 64 * at, 0,
+                      smem_addr(&full[s]));
       };
       const int pre = min(S, total_groups);
       for (int gi = 0; gi < pre; ++gi) {
@@ -265,7 +286,7 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
     if (lane == 0) {
       constexpr uint32_t idesc = umma_idesc_bf16(kBlockRows, NMMA);
       for (int u = 0; u < total_units; ++u) {
-        const int lu = u % upi, i = lu / P, p = lu % P, a = u % NB;
+        const int lu = u % upi, i = lu / UB, ub = lu % UB, p = ub % P, a = u % NB;
         const int gi = (u / upi) * ngroups + i, s = gi % S;
         if (!mbar_wait(smem_addr(&aready[a]), (u / NB) & 1)) {
           fail();
@@ -279,14 +300,14 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
         tc_fence_after();
         const uint32_t d_tmem = tmem + L::kColD + a * NMMA;
         const uint32_t a_tmem = tmem + L::kColA + a * 64;
-        const uint32_t xs = smem_addr(stage_x(s));
+        const uint32_t xs = smem_addr(stage_x(s)) + (FMT == kFmtSa ? (ub / P) * 2 * L::kAtom : 0);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t bdesc = smem_desc_sw128(xs + (kk >> 2) * L::kAtom + (kk & 3) * 32);
           umma_ts(d_tmem, a_tmem + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
         }
         umma_commit(smem_addr(&mmadone[a]));
-        if (p == P - 1) umma_commit(smem_addr(&empty[s]));
+        if (ub == UB - 1) umma_commit(smem_addr(&empty[s]));
       }
       umma_commit(smem_addr(mmafinal));
       mbar_wait(smem_addr(mmafinal), 0, 200000000LL);
@@ -376,7 +397,7 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
 #pragma unroll
     for (int b = 0; b < NB; ++b) scq[b] = 0.f;
     for (int u = 0; u < total_units; ++u) {
-      const int lu = u % upi, i = lu / P, p = lu % P, a = u % NB;
+      const int lu = u % upi, i = lu / UB, ub = lu % UB, p = ub % P, a = u % NB;
       const int gi = (u / upi) * ngroups + i, s = gi % S;
       if (u >= NB) {
         float scv = 0.f;
@@ -385,7 +406,7 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
           if (b == a) scv = scq[b];
         epilogue(u - NB, scv);
       }
-      if (p == 0) wait_or_fail(smem_addr(&full[s]), (gi / S) & 1);
+      if (ub == 0) wait_or_fail(smem_addr(&full[s]), (gi / S) & 1);
       // Dequantise this thread's 64 inputs of unit u into TMEM columns of A[a].
       float sc;
       uint32_t v[16];
@@ -400,6 +421,22 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
         dequant_int4_chunk(c0, v);
         tmem_st16(acol, v);
         dequant_int4_chunk(c1, v);
+        tmem_st16(acol + 16, v);
+      } else if constexpr (FMT == kFmtSa) {
+        // unit (half hb, plane p); this thread's inputs 128hb + 64h .. +63 share code group
+        // (128hb + 64h) / GS of the super-block
+        const int hb = ub / P;
+        const uint2 wv = *reinterpret_cast<const uint2*>(blk + (p * 2 + hb) * 2048 + r * 16 + h * 8);
+        const int gl = (128 * hb + 64 * h) / GS;
+        const uint32_t ab = __float_as_uint((float)blk[sa_code_off(P) + (p * (kSuper / GS) + gl) * kBlockRows + r]) >> 16;
+        sc = half_bits_to_float(*reinterpret_cast<const uint16_t*>(blk + sa_d_off(P, GS) + r * 2));
+        if (ub == UB - 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+        }
+        dequant_sa_word(wv.x, ab * 0x00010001u, v);
+        tmem_st16(acol, v);
+        dequant_sa_word(wv.y, ab * 0x00010001u, v);
         tmem_st16(acol + 16, v);
       } else {
         const uint2 wv = *reinterpret_cast<const uint2*>(blk + p * 2048 + r * 16 + h * 8);
@@ -525,7 +562,7 @@ cudaError_t launch_tc_batch(const TcArgs* probs, int count, cudaStream_t stream)
   int ks[kMaxGemvProblems];
   if (count == 1) {
     // Split K across a cluster only when the row blocks alone cannot fill the GPU.
-    const int RB = row_tiles(probs[0].N), G = probs[0].K / kGroup;
+    const int RB = row_tiles(probs[0].N), G = probs[0].K / L::KIN;
     int k = 1;
     while (k < 8 && RB * k * 2 <= slots && k * 2 <= G) k *= 2;
     ks[0] = k;
@@ -533,11 +570,11 @@ cudaError_t launch_tc_batch(const TcArgs* probs, int count, cudaStream_t stream)
     // Several matrices: each takes the smallest power-of-two K split whose CTAs hold at most
     // the launch's groups per slot (so tall-K matrices do not become the long pole).
     long long units = 0;
-    for (int i = 0; i < count; ++i) units += (long long)row_tiles(probs[i].N) * (probs[i].K / kGroup);
+    for (int i = 0; i < count; ++i) units += (long long)row_tiles(probs[i].N) * (probs[i].K / L::KIN);
     long long target = (units + slots - 1) / slots;
     if (target < 4) target = 4;
     for (int i = 0; i < count; ++i) {
-      const int G = probs[i].K / kGroup;
+      const int G = probs[i].K / L::KIN;
       int k = 1;
       while (k < 8 && k * 2 <= G && (G + k - 1) / k > target) k *= 2;
       ks[i] = k;
@@ -547,7 +584,7 @@ cudaError_t launch_tc_batch(const TcArgs* probs, int count, cudaStream_t stream)
   for (int i = 0; i < count; ++i) C = ks[i] > C ? ks[i] : C;
   int order[kMaxGemvProblems];
   for (int i = 0; i < count; ++i) order[i] = i;
-  auto per_cta = [&](int i) { return (probs[i].K / kGroup + ks[i] - 1) / ks[i]; };
+  auto per_cta = [&](int i) { return (probs[i].K / L::KIN + ks[i] - 1) / ks[i]; };
   for (int i = 1; i < count; ++i)  // stable insertion sort: most groups per CTA first
     for (int j = i; j > 0 && per_cta(order[j]) > per_cta(order[j - 1]); --j) {
       const int t = order[j];
@@ -558,7 +595,7 @@ cudaError_t launch_tc_batch(const TcArgs* probs, int count, cudaStream_t stream)
   for (int i = 0; i < count; ++i) {
     const int o = order[i];
     TcArgs a = probs[o];
-    const int RB = row_tiles(a.N), G = a.K / kGroup, tpc = C / ks[o];
+    const int RB = row_tiles(a.N), G = a.K / L::KIN, tpc = C / ks[o];
     a.ks = ks[o];
     a.groups_per_rank = (G + ks[o] - 1) / ks[o];
     a.cl_begin = (int)clusters;
@@ -580,10 +617,17 @@ cudaError_t launch_tc_batch(const TcArgs* probs, int count, cudaStream_t stream)
   if (clusters * C > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   batch.count = count;
   batch.cluster = C;
-  const int P = FMT == kFmtInt4 ? 1 : probs[0].P;
+  const int P = FMT == kFmtInt4 ? 1 : probs[0].P, GS = probs[0].GS;
+  // sa blocks grow with P and G: as many stages (2..6) as keep two CTAs on an SM.
+  int S = L::kStages;
+  if (FMT == kFmtSa) {
+    S = (int)((110 * 1024 - 2048) / L::stage(P, GS));
+    S = S < 2 ? 2 : (S > 6 ? 6 : S);
+  }
+  batch.stages = S;
   // At least 80 KB of shared memory per CTA keeps at most two CTAs on an SM, so their two
   // 256-column TMEM allocations always fit and tcgen05.alloc never has to wait.
-  const size_t smem = L::smem(P) > 80 * 1024 ? L::smem(P) : 80 * 1024;
+  const size_t smem = L::smem(P, GS, S) > 80 * 1024 ? L::smem(P, GS, S) : 80 * 1024;
   auto kern = tc_gemm_kernel<FMT, NMMA, EPI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -654,6 +698,14 @@ cudaError_t launch_binplane_tc(const uint16_t* X, const uint8_t* packed, int P, 
   a.Y = Y;
   return M <= 16 ? launch_tc<kFmtBinplane, 16, kEpiStore>(a, s)
                  : launch_tc<kFmtBinplane, 32, kEpiStore>(a, s);
+}
+
+cudaError_t launch_sa_tc(const uint16_t* X, const uint8_t* packed, int P, int G, int M, int N,
+                         int K, uint16_t* Y, int* err, cudaStream_t s) {
+  TcArgs a = base_args(X, packed, P, M, N, K, err);
+  a.GS = G;
+  a.Y = Y;
+  return M <= 16 ? launch_tc<kFmtSa, 16, kEpiStore>(a, s) : launch_tc<kFmtSa, 32, kEpiStore>(a, s);
 }
 
 cudaError_t launch_lmhead_tc(const uint16_t* H, const uint8_t* packed, int M, int N, int K,

@@ -183,7 +183,8 @@ lowbit_status lowbit_gemm_binplane(const uint16_t* X, const void* packed, int P,
  *   fp32 accumulation, each output rounded once to bf16.  X, Y as lowbit_gemm_int4,
  *   1 <= M <= 32; packed from lowbit_pack_sa(P, G, N, K); K % 256 == 0.  M = 1 runs the
  *   streaming mat-vec (per plane a table-driven sign-select-and-add, one scale per group);
- *   M >= 2 runs the CUDA-core kernel (sign select by XOR into the activation's sign bit).
+ *   M >= 2 runs the tensor-core GEMM (weights written as +-a in bf16, d applied per 256
+ *   inputs in fp32).
  *   The header (format 3, P, N, K, G) is checked on the device as for the other formats. */
 lowbit_status lowbit_gemm_sa(const uint16_t* X, const void* packed, int P, int G, int M, int N,
                              int K, uint16_t* Y, void* stream);
@@ -243,7 +244,7 @@ lowbit_status lmhead_argmax_verify_path(const uint16_t* H, const void* packed_he
                                         int K, const int32_t* draft, int32_t* argmax,
                                         int32_t* n_accept, int32_t* bonus, void* workspace,
                                         size_t ws_bytes, int path, void* stream);
-/* The sa format has CUDA-core kernels only: path 0 or 1; 2 returns INVALID_ARG. */
+/* path 1 at M >= 2: CUDA-core kernel (sign select by XOR into the activation's sign bit). */
 lowbit_status lowbit_gemm_sa_path(const uint16_t* X, const void* packed, int P, int G, int M,
                                   int N, int K, uint16_t* Y, int path, void* stream);
 

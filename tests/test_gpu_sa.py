@@ -30,9 +30,9 @@ def pack_sa_gpu(lb, bits, codes, d, G):
     return packed
 
 
-def gemm_sa_gpu(lb, x, packed, P, G, M, N, K):
+def gemm_sa_gpu(lb, x, packed, P, G, M, N, K, path=0):
     Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
-    lb.lowbit_gemm_sa(bf16_dev(x), packed, P, G, M, N, K, Y)
+    lb.lowbit_gemm_sa_path(bf16_dev(x), packed, P, G, M, N, K, Y, path)
     torch.cuda.synchronize()
     return host_bits(Y)
 
@@ -49,25 +49,26 @@ def test_pack_sa_bit_exact(lb, P, G, N, K):
     assert g2 == G and np.array_equal(b2, bits) and np.array_equal(c2, codes) and np.array_equal(d2, d)
 
 
+@pytest.mark.parametrize("path", [1, 2])
 @pytest.mark.parametrize("M", [1, 2, 3, 16, 32])
 @pytest.mark.parametrize("P,G,N,K", [(1, 64, 1, 256), (2, 64, 65, 512), (3, 128, 257, 1280),
                                      (4, 256, 300, 768), (6, 64, 130, 256), (8, 128, 100, 512),
-                                     (3, 256, 2000, 2048)])
-def test_sa_small_and_ragged(lb, P, G, N, K, M):
+                                     (8, 64, 129, 512), (3, 256, 2000, 2048)])
+def test_sa_small_and_ragged(lb, P, G, N, K, M, path):
     bits, codes, d, x = synth.sa_problem(21, P, G, M, N, K)
-    y = gemm_sa_gpu(lb, x, pack_sa_gpu(lb, bits, codes, d, G), P, G, M, N, K)
-    check_gemm(y, osa.gemm(x, bits, codes, d, G), f"sa P={P} G={G} M={M} N={N} K={K}")
+    y = gemm_sa_gpu(lb, x, pack_sa_gpu(lb, bits, codes, d, G), P, G, M, N, K, path)
+    check_gemm(y, osa.gemm(x, bits, codes, d, G), f"sa P={P} G={G} M={M} N={N} K={K} path={path}")
 
 
-@pytest.mark.parametrize("M", [1, 16])
+@pytest.mark.parametrize("M,path", [(1, 0), (16, 0), (16, 1)])
 @pytest.mark.parametrize("P,G", synth.SA_TYPES)
 @pytest.mark.parametrize("shape", range(len(synth.SA_SHAPES)))
-def test_sa_config3_shapes(lb, shape, P, G, M):
+def test_sa_config3_shapes(lb, shape, P, G, M, path):
     """The binary-plane configuration's matrices (K, N) in {(4096, 12288), (12288, 4096)} in
     the deployed format; every output at M = 1, every output of 1024 sampled rows at M = 16."""
     K, N = synth.SA_SHAPES[shape]
     bits, codes, d, x = synth.sa_problem(3, P, G, M, N, K, shape)
-    y = gemm_sa_gpu(lb, x, pack_sa_gpu(lb, bits, codes, d, G), P, G, M, N, K)
+    y = gemm_sa_gpu(lb, x, pack_sa_gpu(lb, bits, codes, d, G), P, G, M, N, K, path)
     if M == 1:
         check_gemm(y, osa.gemm(x, bits, codes, d, G), f"sa config 3 shape {shape} M=1")
     else:
@@ -87,9 +88,9 @@ def test_sa_m1_activation_structures(lb, kind):
                scale=2.0 ** 90 if kind == "tiny" else 1.0)
 
 
-@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("M,path", [(1, 0), (4, 1), (4, 2)])
 @pytest.mark.parametrize("wrong", ["G", "P", "N"])
-def test_sa_header_mismatch_leaves_outputs(lb, wrong, M):
+def test_sa_header_mismatch_leaves_outputs(lb, wrong, M, path):
     """A buffer packed for other (P, G, N) is rejected on the device: the error word is set and
     no output is written."""
     P, G, N, K = 3, 128, 200, 512
@@ -100,7 +101,7 @@ def test_sa_header_mismatch_leaves_outputs(lb, wrong, M):
     if wrong == "N":
         N2 = N - 128
     Y = torch.full((M, N2), 7.0, dtype=torch.bfloat16, device="cuda")
-    lb.lowbit_gemm_sa(bf16_dev(x), packed, P2, G2, M, N2, K, Y)
+    lb.lowbit_gemm_sa_path(bf16_dev(x), packed, P2, G2, M, N2, K, Y, path)
     assert lb.lowbit_device_error() == 1
     assert bool((Y == 7.0).all())
 
@@ -120,5 +121,5 @@ def test_sa_validation(lb):
             lb.lowbit_gemm_sa(X, packed, P2, G2, M2, N, K2, Y)
         assert e.value.status == 2, (P2, G2, M2, K2)
     with pytest.raises(lb.LowbitError) as e:
-        lb.lowbit_gemm_sa_path(X, packed, P, G, 1, N, K, Y, 2)
+        lb.lowbit_gemm_sa_path(X, packed, P, G, 1, N, K, Y, 3)
     assert e.value.status == 1

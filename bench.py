@@ -199,7 +199,8 @@ LAYER_GROUPS = {"deps": ((0, 1, 2), (3,), (4, 5), (6,)), "all": ((0, 1, 2, 3, 4,
 
 
 def build_int4_layer(lb, torch, l2, M, path, seed, name, desc, grouping=None):
-    w = Workload(name, desc, "int4_stream_kernel" if (M == 1 and path != 2) else "tc_gemm_kernel")
+    w = Workload(name, desc, "int4_stream_kernel" if ((M <= 2 and path == 0) or (M <= 4 and path == 1))
+                 else ("int4_gemm_cc_kernel" if path == 1 else "tc_gemm_kernel"))
     shapes = [(k, n) for _, k, n in synth.LAYER_4B]
     w.bytes = sum(algorithmic_int4_bytes(N, K) for K, N in shapes)
     C = copies_for(w.bytes, l2)

@@ -168,11 +168,11 @@ lowbit_status lowbit_gemm_int4_path(const uint16_t* X, const void* packed, int M
   if (!err) return LOWBIT_ERR_CUDA;
   const uint8_t* pk = static_cast<const uint8_t*>(packed);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (path == 0) path = (M == 1) ? 1 : 2;
-  if (path == 1 && M == 1) {
+  if (path == 0) path = (M <= kStreamDefaultRows) ? 1 : 2;
+  if (path == 1 && M <= kStreamMaxRows) {
     GemvProblem p = {X, pk, Y, N, K, 0, 1, 0, 0};
     p.early = allocation_covers(pk, kHeaderBytes + int4_payload_bytes(N, K)) ? 1 : 0;
-    return from_cuda(launch_int4_stream(&p, 1, err, s));
+    return from_cuda(launch_int4_stream(&p, 1, M, err, s));
   }
   if (path == 1) return from_cuda(launch_int4_gemm_cc(X, pk, M, N, K, Y, err, s));
   return from_cuda(launch_int4_gemm_tc(X, pk, M, N, K, Y, err, s));
@@ -191,7 +191,7 @@ lowbit_status lowbit_gemm_int4_grouped(const lowbit_gemm_desc* descs, int count,
   int* err = device_error_word();
   if (!err) return LOWBIT_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (M == 1) {
+  if (M <= kStreamDefaultRows) {
     GemvProblem p[kMaxGemvProblems];
     for (int i = 0; i < count; ++i) {
       p[i] = GemvProblem{descs[i].X, static_cast<const uint8_t*>(descs[i].packed), descs[i].Y,
@@ -199,7 +199,7 @@ lowbit_status lowbit_gemm_int4_grouped(const lowbit_gemm_desc* descs, int count,
       p[i].early = allocation_covers(descs[i].packed,
                                      kHeaderBytes + int4_payload_bytes(descs[i].N, descs[i].K)) ? 1 : 0;
     }
-    return from_cuda(launch_int4_stream(p, count, err, s));
+    return from_cuda(launch_int4_stream(p, count, M, err, s));
   }
   GemvProblem p[kMaxGemvProblems];
   for (int i = 0; i < count; ++i)

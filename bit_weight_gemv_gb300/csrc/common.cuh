@@ -131,7 +131,7 @@ bool allocation_covers(const void* p, size_t bytes);
 // One matrix of a streaming mat-vec launch (M = 1).  The launcher fills in the schedule.
 // 64-byte aligned: a kernel reads one problem's fields from one cache line of its parameters.
 struct alignas(64) GemvProblem {
-  const uint16_t* X;       // [M][K] bf16 (M = 1 for the streaming kernel)
+  const uint16_t* X;       // [M][K] bf16
   const uint8_t* packed;   // header + INT4 payload for (N, K)
   uint16_t* Y;             // [M][N] bf16
   int N, K;
@@ -148,7 +148,12 @@ cudaError_t launch_pack_int4(const int8_t* codes, const uint16_t* scales, int N,
                              uint8_t* packed, cudaStream_t s);
 cudaError_t launch_pack_binplane(const uint8_t* bits, const uint16_t* alpha, int P, int N, int K,
                                  uint8_t* packed, cudaStream_t s);
-cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int* err, cudaStream_t s);
+// INT4 streaming mat-vec for 1 <= M <= kStreamMaxRows activation rows (X [M][K], Y [M][N]).
+// The library's default uses it up to kStreamDefaultRows rows (measured: at M = 2 it beats the
+// tensor-core GEMM, at M = 4 it does not); path 1 reaches it up to kStreamMaxRows.
+constexpr int kStreamMaxRows = 4;
+constexpr int kStreamDefaultRows = 2;
+cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int M, int* err, cudaStream_t s);
 // Binary-plane counterpart (M = 1); every problem carries its plane count P (1..8).
 cudaError_t launch_bp_stream(const GemvProblem* probs, int count, int* err, cudaStream_t s);
 // sa-format counterpart (M = 1); every problem carries P (1..8) and G (64, 128, 256).

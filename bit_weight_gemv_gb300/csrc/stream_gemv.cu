@@ -40,7 +40,6 @@ constexpr int kCWarps = 8;                          // compute warps: 4 row quar
 constexpr int kConvWarp = kCWarps + 1;              // after the producer warp
 constexpr int kSThreads = (kCWarps + 2) * 32;
 constexpr uint32_t kXBytes = kGroup * 2;            // one group's bf16 activations
-constexpr uint32_t kStage = kInt4Block + kXBytes;   // 8704 bytes, a multiple of 16
 constexpr int kMaxStages = 6;
 // Dynamic shared memory per CTA (ring + reduction slots): with the static part, four CTAs fit
 // in an SM's 228 KB.
@@ -58,7 +57,7 @@ struct StreamArgs {
   int count;
   int stages;
   int cluster;  // C
-  int pad_;
+  int m;        // activation rows (INT4 kernel; 1 for the plane kernels)
   int cl_begin[kMaxGemvProblems];  // copy of p[i].cluster_begin
   int* err;
   GemvProblem p[kMaxGemvProblems];
@@ -82,8 +81,12 @@ __device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
   return d;
 }
 
+// MT: activation rows the kernel is built for (1, 2 or 4); a.m <= MT rows are present.  Each
+// unpacked code word serves every row, so the bytes streamed per output stay those of M = 1.
+template <int MT>
 __global__ void __launch_bounds__(kSThreads)
 int4_stream_kernel(const __grid_constant__ StreamArgs a) {
+  constexpr uint32_t STG = kInt4Block + MT * kXBytes;  // stage: block, then MT activation rows
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ __align__(8) uint64_t full[kMaxStages];
   __shared__ __align__(8) uint64_t xready[kMaxStages];  // the stage's int16 activations are set
@@ -93,10 +96,10 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
   // (X[8j], X[8j+4]), (X[8j+1], X[8j+5]), (X[8j+2], X[8j+6]), (X[8j+3], X[8j+7]) -- the
   // order in which the two byte words of code word j meet them -- and, for inputs 0..63 and
   // 64..127, (2^-sh of the first, of the second, sum X of the first, of the second).
-  __shared__ __align__(16) uint4 xq[kMaxStages][kGroup / 8];
-  __shared__ __align__(16) float4 xmeta[kMaxStages];
-  __shared__ float red[kCWarps][32];
-  __shared__ float part[kRowTile];
+  __shared__ __align__(16) uint4 xq[kMaxStages][MT][kGroup / 8];
+  __shared__ __align__(16) float4 xmeta[kMaxStages][MT];
+  __shared__ float red[kCWarps][MT][32];
+  __shared__ float part[MT][kRowTile];
   __shared__ int ok;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -112,7 +115,7 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
   const bool live = tile < row_tiles(pr.N);  // the last cluster of a matrix may be partly idle
   const int g0 = (int)((long long)rank * G / ks), g1 = (int)((long long)(rank + 1) * G / ks);
   const int nb = live ? g1 - g0 : 0;
-  const int S = a.stages;
+  const int S = a.stages, M = MT == 1 ? 1 : a.m;
 
   if (threadIdx.x == 0) {
     // With `early`, the header is checked in parallel with the first copies (it then gates
@@ -128,7 +131,10 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
     ptx::mbar_init(ptx::smem_addr(&redbar), (uint32_t)(kRowTile * (ks > 1 ? ks - 1 : 1)));
     ptx::fence_mbar_init();
   }
-  if (warp < kCWarps) red[warp][lane] = 0.f;
+  if (warp < kCWarps) {
+#pragma unroll
+    for (int m = 0; m < MT; ++m) red[warp][m][lane] = 0.f;
+  }
   __syncthreads();
   // Half of a cluster barrier: its wait, just before the partial sums are exchanged, finds
   // every CTA's barriers initialised (and returns at once, as all arrived long before).
@@ -146,17 +152,22 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
     if (lane == 0 && hdr_ok) {
       const uint8_t* wsrc = pr.packed + kHeaderBytes + ((size_t)tile * G + g0) * kInt4Block;
       const uint16_t* xsrc = pr.X + (size_t)g0 * kGroup;
+      const uint32_t tx = kInt4Block + (uint32_t)M * kXBytes;
+      // activation row m of block b -> its slot in the stage
+      auto copy_x = [&](int b, int s, uint32_t bar) {
+        for (int m = 0; m < M; ++m)
+          ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)s * STG + kInt4Block + m * kXBytes),
+                        xsrc + (size_t)m * pr.K + (size_t)b * kGroup, kXBytes, bar);
+      };
       const int pre = min(nb, S);
       for (int b = 0; b < pre; ++b) {
         const uint32_t bar = ptx::smem_addr(&full[b]);
-        ptx::mbar_arrive_expect_tx(bar, kStage);
-        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)b * kStage), wsrc + (size_t)b * kInt4Block,
+        ptx::mbar_arrive_expect_tx(bar, tx);
+        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)b * STG), wsrc + (size_t)b * kInt4Block,
                       kInt4Block, bar);
       }
       grid_wait();  // the activations may be the previous kernel's output
-      for (int b = 0; b < pre; ++b)
-        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)b * kStage + kInt4Block), xsrc + (size_t)b * kGroup,
-                      kXBytes, ptx::smem_addr(&full[b]));
+      for (int b = 0; b < pre; ++b) copy_x(b, b, ptx::smem_addr(&full[b]));
       int issued = pre;
       for (int b = pre; b < nb; ++b) {
         const int s = b % S;
@@ -165,11 +176,10 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
           break;
         }
         const uint32_t bar = ptx::smem_addr(&full[s]);
-        ptx::mbar_arrive_expect_tx(bar, kStage);
-        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)s * kStage), wsrc + (size_t)b * kInt4Block,
+        ptx::mbar_arrive_expect_tx(bar, tx);
+        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)s * STG), wsrc + (size_t)b * kInt4Block,
                       kInt4Block, bar);
-        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)s * kStage + kInt4Block),
-                      xsrc + (size_t)b * kGroup, kXBytes, bar);
+        copy_x(b, s, bar);
         issued = b + 1;
       }
       // Copies still in flight must land before the CTA may exit.
@@ -187,8 +197,12 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
           if (lane == 0) record_error(a.err, LOWBIT_ERR_TIMEOUT);
           break;
         }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {  // rows are independent: unrolled, their chains interleave
+        if (m >= M) break;
         // lane l holds inputs 4l..4l+3 (code word l/2, nibbles 4(l&1)..4(l&1)+3)
-        const uint2 raw = reinterpret_cast<const uint2*>(ring + (size_t)s * kStage + kInt4Block)[lane];
+        const uint2 raw =
+            reinterpret_cast<const uint2*>(ring + (size_t)s * STG + kInt4Block + m * kXBytes)[lane];
         const uint32_t mag = max(max(raw.x & 0x7FFFu, (raw.x >> 16) & 0x7FFFu),
                                  max(raw.y & 0x7FFFu, (raw.y >> 16) & 0x7FFFu));
         // lanes 0..15 hold inputs 0..63, lanes 16..31 inputs 64..127; |x| bits order as |x|
@@ -214,12 +228,13 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
         const uint32_t o01 = __shfl_xor_sync(0xFFFFFFFFu, p01, 1);  // the word's other half
         const uint32_t o23 = __shfl_xor_sync(0xFFFFFFFFu, p23, 1);
         if ((lane & 1) == 0)
-          xq[s][lane >> 1] = make_uint4(__byte_perm(p01, o01, 0x5410), __byte_perm(p01, o01, 0x7632),
+          xq[s][m][lane >> 1] = make_uint4(__byte_perm(p01, o01, 0x5410), __byte_perm(p01, o01, 0x7632),
                                         __byte_perm(p23, o23, 0x5410), __byte_perm(p23, o23, 0x7632));
-        float* meta = reinterpret_cast<float*>(&xmeta[s]);
+        float* meta = reinterpret_cast<float*>(&xmeta[s][m]);
         if ((lane & 15) == 0) {
           meta[lane >> 4] = down;
           meta[2 + (lane >> 4)] = __int_as_float(lane < 16 ? sum_lo : sum_hi);
+        }
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&xready[s]));
@@ -229,7 +244,9 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
     // ---------------------------------------------------------------- compute
     const int q = warp & 3, h = warp >> 2;  // rows 32q..32q+31, inputs 64h..64h+63 of each group
     const int row = 32 * q + lane;
-    float total = 0.f;
+    float total[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) total[m] = 0.f;
     for (int b = 0; b < nb; ++b) {
       const int s = b % S;
       const bool ready = ptx::mbar_wait(ptx::smem_addr(&xready[s]), (b / S) & 1);
@@ -237,31 +254,47 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
         if (lane == 0) record_error(a.err, LOWBIT_ERR_TIMEOUT);
         break;
       }
-      const uint8_t* st = ring + (size_t)s * kStage;
+      const uint8_t* st = ring + (size_t)s * STG;
       const uint4 c0 = *reinterpret_cast<const uint4*>(st + (2 * h) * (kRowTile * 16) + row * 16);
       const uint4 c1 = *reinterpret_cast<const uint4*>(st + (2 * h + 1) * (kRowTile * 16) + row * 16);
       const float sc = half_bits_to_float(*reinterpret_cast<const uint16_t*>(st + kInt4ScaleOff + row * 2));
-      const uint4* xw = xq[s] + 8 * h;
-      const float4 meta = xmeta[s];
       const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-      int acc[4] = {0, 0, 0, 0};
+      int acc[MT][4];
+#pragma unroll
+      for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         // nibble e of a word sits at bits 4(e/2) + 16(e%2): the masked word holds nibbles
         // (0, 4, 1, 5) in its bytes, the shifted one (2, 6, 3, 7)
-        const uint4 x = xw[i];
         const uint32_t lo = w[i] & 0x0F0F0F0Fu, hi = (w[i] >> 4) & 0x0F0F0F0Fu;
-        acc[0] = dp2a_lo(x.x, lo, acc[0]);
-        acc[1] = dp2a_hi(x.y, lo, acc[1]);
-        acc[2] = dp2a_lo(x.z, hi, acc[2]);
-        acc[3] = dp2a_hi(x.w, hi, acc[3]);
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          if (m < M) {
+            const uint4 x = xq[s][m][8 * h + i];
+            acc[m][0] = dp2a_lo(x.x, lo, acc[m][0]);
+            acc[m][1] = dp2a_hi(x.y, lo, acc[m][1]);
+            acc[m][2] = dp2a_lo(x.z, hi, acc[m][2]);
+            acc[m][3] = dp2a_hi(x.w, hi, acc[m][3]);
+          }
+        }
       }
+      float4 meta[MT];
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+        if (m < M) meta[m] = xmeta[s][m];
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&empty[s]));
-      const int v = (acc[0] + acc[1]) + (acc[2] + acc[3]) - 8 * __float_as_int(h ? meta.w : meta.z);
-      total = fmaf(sc * (h ? meta.y : meta.x), (float)v, total);
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        if (m < M) {
+          const int v = (acc[m][0] + acc[m][1]) + (acc[m][2] + acc[m][3]) -
+                        8 * __float_as_int(h ? meta[m].w : meta[m].z);
+          total[m] = fmaf(sc * (h ? meta[m].y : meta[m].x), (float)v, total[m]);
+        }
+      }
     }
-    red[warp][lane] = total;
+#pragma unroll
+    for (int m = 0; m < MT; ++m) red[warp][m][lane] = total[m];
   }
 
   // -------------------------------------------------------------------- reduction + store
@@ -271,35 +304,41 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
     record_error(a.err, LOWBIT_ERR_INVALID_ARG);
   if (threadIdx.x < kRowTile) {
     const int q = threadIdx.x >> 5, l = threadIdx.x & 31;
-    part[threadIdx.x] = red[q][l] + red[q + 4][l];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) part[m][threadIdx.x] = red[q][m][l] + red[q + 4][m][l];
   }
   const int n = tile * kRowTile + (int)threadIdx.x;
   if (C > 1) ptx::cluster_wait();
   if (ks > 1) {
-    // Ranks 1..ks-1 push their partial sums into rank 0's slots (one float per row, each
-    // followed by a remote arrival) and leave; rank 0 waits for them, adds them in rank
-    // order and stores.
-    float* slots = reinterpret_cast<float*>(ring + (size_t)S * kStage);  // [ks-1][128]
-    const uint32_t owner = (uint32_t)(crank - rank);                    // rank 0's CTA
+    // Ranks 1..ks-1 push their partial sums into rank 0's slots (one float per row and
+    // activation row; each row's values followed by a remote arrival) and leave; rank 0 waits
+    // for them, adds them in rank order and stores.
+    float* slots = reinterpret_cast<float*>(ring + (size_t)S * STG);  // [ks-1][MT][128]
+    const uint32_t owner = (uint32_t)(crank - rank);                 // rank 0's CTA
     if (live && threadIdx.x < kRowTile) {
       if (rank != 0) {
-        const uint32_t la = ptx::smem_addr(&slots[(rank - 1) * kRowTile + threadIdx.x]);
-        ptx::st_dsmem_f32(ptx::map_to_rank(la, owner), part[threadIdx.x]);
+        for (int m = 0; m < M; ++m) {
+          const uint32_t la = ptx::smem_addr(&slots[((rank - 1) * MT + m) * kRowTile + threadIdx.x]);
+          ptx::st_dsmem_f32(ptx::map_to_rank(la, owner), part[m][threadIdx.x]);
+        }
         ptx::mbar_arrive_remote(ptx::map_to_rank(ptx::smem_addr(&redbar), owner));
       } else {
         const bool got = ptx::mbar_wait_cluster(ptx::smem_addr(&redbar), 0);
         if (!got) record_error(a.err, LOWBIT_ERR_TIMEOUT);
-        float y = part[threadIdx.x];
-        for (int r = 1; r < ks; ++r) y += slots[(r - 1) * kRowTile + threadIdx.x];
         grid_wait();
-        if (got && out_ok && n < pr.N) pr.Y[n] = float_to_bf16_bits(y);
+        for (int m = 0; m < M; ++m) {
+          float y = part[m][threadIdx.x];
+          for (int r = 1; r < ks; ++r) y += slots[((r - 1) * MT + m) * kRowTile + threadIdx.x];
+          if (got && out_ok && n < pr.N) pr.Y[(size_t)m * pr.N + n] = float_to_bf16_bits(y);
+        }
       }
     }
   } else {
     __syncthreads();
     if (out_ok && threadIdx.x < kRowTile) {
       grid_wait();
-      if (n < pr.N) pr.Y[n] = float_to_bf16_bits(part[threadIdx.x]);
+      if (n < pr.N)
+        for (int m = 0; m < M; ++m) pr.Y[(size_t)m * pr.N + n] = float_to_bf16_bits(part[m][threadIdx.x]);
     }
   }
 }
@@ -580,15 +619,15 @@ struct Schedule {
   long long clusters;
 };
 
-bool make_schedule(const GemvProblem* probs, int count, int kin, int target, StreamArgs& a,
-                   Schedule& out) {
+bool make_schedule(const GemvProblem* probs, int count, int kin, int target, int max_split,
+                   StreamArgs& a, Schedule& out) {
   const int nsm = sm_count();
   int ks[kMaxGemvProblems];
   long long ctas = 0;
   for (int i = 0; i < count; ++i) {
     const int G = probs[i].K / kin;
     int k = 1;
-    while (k < kMaxSplit && k * 2 <= G && (G + k - 1) / k > target) k *= 2;
+    while (k < max_split && k * 2 <= G && (G + k - 1) / k > target) k *= 2;
     ks[i] = k;
     ctas += (long long)row_tiles(probs[i].N) * k;
   }
@@ -599,12 +638,12 @@ bool make_schedule(const GemvProblem* probs, int count, int kin, int target, Str
     grew = false;
     long long next = 0;
     for (int i = 0; i < count; ++i) {
-      const bool can = ks[i] < kMaxSplit && ks[i] * 2 <= probs[i].K / kin;
+      const bool can = ks[i] < max_split && ks[i] * 2 <= probs[i].K / kin;
       next += (long long)row_tiles(probs[i].N) * ks[i] * (can ? 2 : 1);
     }
     if (next == ctas || next > resident) break;
     for (int i = 0; i < count; ++i)
-      if (ks[i] < kMaxSplit && ks[i] * 2 <= probs[i].K / kin) ks[i] *= 2;
+      if (ks[i] < max_split && ks[i] * 2 <= probs[i].K / kin) ks[i] *= 2;
     ctas = next;
     grew = true;
   }
@@ -650,7 +689,7 @@ constexpr int kMaxDevices = 64;
 struct OptIns {
   std::atomic<unsigned char> done[kMaxDevices];
 };
-OptIns g_int4_optins, g_bp_optins, g_sa_optins;
+OptIns g_int4_optins[3], g_bp_optins, g_sa_optins;  // INT4: one per row count built
 
 template <typename Kernel>
 cudaError_t opt_in(Kernel kern, OptIns& o, size_t budget) {
@@ -694,27 +733,47 @@ cudaError_t launch_streaming(Kernel kern, OptIns& o, size_t budget, const Stream
 
 }  // namespace
 
-cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int* err, cudaStream_t s) {
-  if (count < 1 || count > kMaxGemvProblems) return cudaErrorInvalidValue;
+namespace {
+
+template <int MT>
+cudaError_t launch_int4_stream_mt(const GemvProblem* probs, int count, int M, int* err,
+                                  cudaStream_t s) {
+  constexpr uint32_t stage = kInt4Block + MT * kXBytes;
+  // Shared memory a row beyond the first adds to the kernel's static part (converted
+  // activations, reduction buffers): the ring's budget shrinks by as much.  The split-K slots
+  // grow with the rows; the ring keeps what they leave (at least two stages).
+  constexpr size_t budget = kSmemBudget - (size_t)(MT - 1) * 3200;
   StreamArgs a = {};
   Schedule sc;
-  if (!make_schedule(probs, count, kGroup, kInt4TargetBlocks, a, sc)) return cudaErrorInvalidValue;
+  if (!make_schedule(probs, count, kGroup, kInt4TargetBlocks, kMaxSplit, a, sc))
+    return cudaErrorInvalidValue;
   a.err = err;
-  // ring, then the partial-sum slots rank 0 of a split tile receives; the ring takes what the
-  // slots leave of the per-CTA budget (four CTAs per SM)
-  const size_t slots = (size_t)(sc.kmax - 1) * kRowTile * sizeof(float);
-  int S = (int)((kSmemBudget - slots) / kStage);
+  a.m = M;
+  // ring, then the partial-sum slots rank 0 of a split tile receives
+  const size_t slots = (size_t)(sc.kmax - 1) * MT * kRowTile * sizeof(float);
+  int S = slots < budget ? (int)((budget - slots) / stage) : 0;
   S = S > kMaxStages ? kMaxStages : (S < 2 ? 2 : S);
   a.stages = sc.maxnb < S ? sc.maxnb : S;
-  const size_t smem = (size_t)a.stages * kStage + slots;
-  return launch_streaming(int4_stream_kernel, g_int4_optins, kSmemBudget, a, sc, smem, kSThreads, s);
+  const size_t smem = (size_t)a.stages * stage + slots;  // at most 2 * 9472 + 30720 bytes
+  return launch_streaming(int4_stream_kernel<MT>, g_int4_optins[MT == 1 ? 0 : (MT == 2 ? 1 : 2)],
+                          kSmemBudget, a, sc, smem, kSThreads, s);
+}
+
+}  // namespace
+
+cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int M, int* err, cudaStream_t s) {
+  if (count < 1 || count > kMaxGemvProblems || M < 1 || M > kStreamMaxRows) return cudaErrorInvalidValue;
+  if (M == 1) return launch_int4_stream_mt<1>(probs, count, M, err, s);
+  if (M == 2) return launch_int4_stream_mt<2>(probs, count, M, err, s);
+  return launch_int4_stream_mt<4>(probs, count, M, err, s);
 }
 
 cudaError_t launch_bp_stream(const GemvProblem* probs, int count, int* err, cudaStream_t s) {
   if (count < 1 || count > kMaxGemvProblems) return cudaErrorInvalidValue;
   StreamArgs a = {};
   Schedule sc;
-  if (!make_schedule(probs, count, kGroup, kBpTargetBlocks, a, sc)) return cudaErrorInvalidValue;
+  if (!make_schedule(probs, count, kGroup, kBpTargetBlocks, kMaxSplit, a, sc))
+    return cudaErrorInvalidValue;
   int pmax = 1;
   for (int i = 0; i < count; ++i) pmax = probs[i].P > pmax ? probs[i].P : pmax;
   const size_t stage = binplane_block(pmax) + kXBytes + kLutBytes;
@@ -731,7 +790,8 @@ cudaError_t launch_sa_stream(const GemvProblem* probs, int count, int* err, cuda
   if (count < 1 || count > kMaxGemvProblems) return cudaErrorInvalidValue;
   StreamArgs a = {};
   Schedule sc;
-  if (!make_schedule(probs, count, kSuper, kSaTargetBlocks, a, sc)) return cudaErrorInvalidValue;
+  if (!make_schedule(probs, count, kSuper, kSaTargetBlocks, kMaxSplit, a, sc))
+    return cudaErrorInvalidValue;
   size_t stage = 0;  // largest stage of the launch: block + activations + tables
   for (int i = 0; i < count; ++i) {
     const size_t st = sa_block(probs[i].P, probs[i].G) + kSuper * 2 + (kSuper / 4) * 16 * sizeof(float);

@@ -144,11 +144,12 @@ lowbit_status lowbit_validate_packed(const void* packed, int format, int P, int 
  *   groups, each output rounded once to bf16 (nearest, ties to even).
  *   X : bf16 [M][K], 16-byte aligned.   packed : from lowbit_pack_int4(N, K).
  *   Y : bf16 [M][N], written in full.   1 <= M <= 32.
- * M = 1 runs the streaming GEMV: each run of 64 activations is held as int16 times one
- * power of two (exact for every activation within a factor 2^7 of the run's largest,
- * otherwise rounded to a multiple of 2^-15 of that largest) and the products within a run
- * are summed exactly in integers; a non-finite activation makes every output NaN.
- * M >= 2 runs the tensor-core skinny GEMM (exact bf16 products, fp32 sums per group). */
+ * M <= 2 runs the streaming kernel (path 1 also at M = 3, 4): each run of 64 activations of a
+ * row is held as int16 times one power of two (exact for every activation within a factor 2^7
+ * of the run's largest, otherwise rounded to a multiple of 2^-15 of that largest) and the
+ * products within a run are summed exactly in integers; a non-finite activation makes every
+ * output of its row NaN.
+ * M >= 3 runs the tensor-core skinny GEMM (exact bf16 products, fp32 sums per group). */
 lowbit_status lowbit_gemm_int4(const uint16_t* X, const void* packed, int M, int N, int K,
                                uint16_t* Y, void* stream);
 
@@ -163,9 +164,9 @@ typedef struct lowbit_gemm_desc {
 
 /* Several independent INT4 multiplies with a common M (for example the q, k and v projections
  * of a decoder layer, which read the same activations), each with the contract and rounding
- * of lowbit_gemm_int4.  At M = 1 all of them run in ONE launch of the streaming GEMV, so the
- * launch, pipeline fill and drain are paid once for the group instead of once per matrix;
- * at M >= 2 they share one launch of the tensor-core GEMM.
+ * of lowbit_gemm_int4.  They share ONE launch (the streaming kernel at M <= 2, the tensor-core
+ * GEMM above), so the launch, pipeline fill and drain are paid once for the group instead of
+ * once per matrix.
  *   descs : HOST array of `count` descriptors, 1 <= count <= 8; read during the call only.
  *   The multiplies must be independent: no Y may overlap any X, packed buffer or other Y of
  *   the group.  Every descriptor is validated before anything is enqueued. */
@@ -232,9 +233,12 @@ lowbit_status lmhead_argmax_verify_noalloc(const uint16_t* H, const void* packed
 
 /* ------------------------------------------------------------------------------------------
  * Kernel-family selection (diagnostics and testing).  Same contract as the functions above,
- * plus `path`: 0 = the library's choice, 1 = the CUDA-core streaming kernels (row per lane,
- * in-register dequantisation, fp32 accumulation), 2 = the tensor-core kernels (dequantisation
- * into tensor memory, tcgen05 MMA with fp32 accumulation).  Other values: INVALID_ARG.
+ * plus `path`: 0 = the library's choice; 1 = the CUDA-core kernels (INT4: the streaming
+ * kernel up to M = 4, integer dot products on block-scaled int16 activations, and a
+ * row-per-lane bf16 kernel above; planes: the table-driven streaming kernel at M = 1 and a
+ * sign-XOR kernel above; LM head: the row-per-lane kernel); 2 = the tensor-core kernels
+ * (dequantisation into tensor memory, tcgen05 MMA with fp32 accumulation).  Other values:
+ * INVALID_ARG.
  */
 lowbit_status lowbit_gemm_int4_path(const uint16_t* X, const void* packed, int M, int N, int K,
                                     uint16_t* Y, int path, void* stream);

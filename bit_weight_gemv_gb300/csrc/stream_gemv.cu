@@ -38,7 +38,10 @@ namespace {
 
 constexpr int kCWarps = 8;                          // compute warps: 4 row quarters x 2 K halves
 constexpr int kConvWarp = kCWarps + 1;              // after the producer warp
-constexpr int kSThreads = (kCWarps + 2) * 32;
+// Activation converters of the INT4 kernel: at one row, two (even and odd blocks) measured
+// faster than one; with two or four rows, one.
+template <int MT> __host__ __device__ constexpr int conv_warps() { return MT == 1 ? 2 : 1; }
+template <int MT> __host__ __device__ constexpr int stream_threads() { return (kCWarps + 1 + conv_warps<MT>()) * 32; }
 constexpr uint32_t kXBytes = kGroup * 2;            // one group's bf16 activations
 constexpr int kMaxStages = 6;
 // Dynamic shared memory per CTA (ring + reduction slots): with the static part, four CTAs fit
@@ -84,7 +87,7 @@ __device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
 // MT: activation rows the kernel is built for (1, 2 or 4); a.m <= MT rows are present.  Each
 // unpacked code word serves every row, so the bytes streamed per output stay those of M = 1.
 template <int MT>
-__global__ void __launch_bounds__(kSThreads)
+__global__ void __launch_bounds__(stream_threads<MT>())
 int4_stream_kernel(const __grid_constant__ StreamArgs a) {
   constexpr uint32_t STG = kInt4Block + MT * kXBytes;  // stage: block, then MT activation rows
   extern __shared__ __align__(128) uint8_t ring[];
@@ -101,6 +104,7 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
   __shared__ float red[kCWarps][MT][32];
   __shared__ float part[MT][kRowTile];
   __shared__ int ok;
+  __shared__ int gave_up;  // some wait of this CTA timed out
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int C = a.cluster;
@@ -122,6 +126,7 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
     // only the outputs); otherwise it is checked before anything else is read.
     ok = live && (pr.early || header_matches(reinterpret_cast<const PackedHeader*>(pr.packed),
                                              kFormatInt4, 0, pr.N, pr.K));
+    gave_up = 0;
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
       ptx::mbar_init(ptx::smem_addr(&xready[s]), 1);
@@ -173,6 +178,7 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
         const int s = b % S;
         if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), ((b / S) - 1) & 1)) {
           record_error(a.err, LOWBIT_ERR_TIMEOUT);
+          gave_up = 1;
           break;
         }
         const uint32_t bar = ptx::smem_addr(&full[s]);
@@ -187,14 +193,22 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
         ptx::mbar_wait(ptx::smem_addr(&full[b % S]), (b / S) & 1);
     }
     __syncwarp();
-  } else if (warp == kConvWarp) {
-    // ---------------------------------------------------------------- activation converter
+  } else if (warp >= kConvWarp) {
+    // ---------------------------------------------------------------- activation converters
+    // Converter c owns the stages s with s % conv_warps == c: a block's conversion is a chain
+    // of dependent reductions and shuffles, so two warps double the rate a CTA can convert
+    // at.  Owning whole stages keeps each stage's phases in order for its one converter (a
+    // parity wait can never meet a phase two behind), whatever the stage count.
     if (hdr_ok) {
       for (int b = 0; b < nb; ++b) {
         const int s = b % S;
+        if (s % conv_warps<MT>() != warp - kConvWarp) continue;
         const bool landed = ptx::mbar_wait(ptx::smem_addr(&full[s]), (b / S) & 1);
         if (!__all_sync(0xFFFFFFFFu, landed)) {
-          if (lane == 0) record_error(a.err, LOWBIT_ERR_TIMEOUT);
+          if (lane == 0) {
+            record_error(a.err, LOWBIT_ERR_TIMEOUT);
+            gave_up = 1;
+          }
           break;
         }
 #pragma unroll
@@ -251,7 +265,10 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
       const int s = b % S;
       const bool ready = ptx::mbar_wait(ptx::smem_addr(&xready[s]), (b / S) & 1);
       if (!__all_sync(0xFFFFFFFFu, ready)) {  // warp-uniform exit keeps the warp converged
-        if (lane == 0) record_error(a.err, LOWBIT_ERR_TIMEOUT);
+        if (lane == 0) {
+          record_error(a.err, LOWBIT_ERR_TIMEOUT);
+          gave_up = 1;
+        }
         break;
       }
       const uint8_t* st = ring + (size_t)s * STG;
@@ -317,6 +334,9 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
     const uint32_t owner = (uint32_t)(crank - rank);                 // rank 0's CTA
     if (live && threadIdx.x < kRowTile) {
       if (rank != 0) {
+        // A CTA that gave up on a wait stays out of rank 0's shared memory: rank 0 may have
+        // stopped waiting for it and exited.
+        if (gave_up) return;
         for (int m = 0; m < M; ++m) {
           const uint32_t la = ptx::smem_addr(&slots[((rank - 1) * MT + m) * kRowTile + threadIdx.x]);
           ptx::st_dsmem_f32(ptx::map_to_rank(la, owner), part[m][threadIdx.x]);
@@ -383,6 +403,7 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
   __shared__ float red[kCWarps][32];
   __shared__ float part[kRowTile];
   __shared__ int ok;
+  __shared__ int gave_up;  // some wait of this CTA timed out
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int C = a.cluster;
@@ -408,6 +429,7 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
 
   if (threadIdx.x == 0) {
     ok = live && (pr.early || header_ok());
+    gave_up = 0;
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
       ptx::mbar_init(ptx::smem_addr(&tabready[s]), 1);
@@ -445,6 +467,7 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
         const int s = b % S;
         if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), ((b / S) - 1) & 1)) {
           record_error(a.err, LOWBIT_ERR_TIMEOUT);
+          gave_up = 1;
           break;
         }
         const uint32_t bar = ptx::smem_addr(&full[s]);
@@ -467,7 +490,10 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
         const int s = b % S;
         const bool landed = ptx::mbar_wait(ptx::smem_addr(&full[s]), (b / S) & 1);
         if (!__all_sync(0xFFFFFFFFu, landed)) {
-          if (lane == 0) record_error(a.err, LOWBIT_ERR_TIMEOUT);
+          if (lane == 0) {
+            record_error(a.err, LOWBIT_ERR_TIMEOUT);
+            gave_up = 1;
+          }
           break;
         }
         const uint16_t* xr = reinterpret_cast<const uint16_t*>(stage(s) + BB);
@@ -506,7 +532,10 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
       const int s = b % S;
       const bool ready = ptx::mbar_wait(ptx::smem_addr(&tabready[s]), (b / S) & 1);
       if (!__all_sync(0xFFFFFFFFu, ready)) {
-        if (lane == 0) record_error(a.err, LOWBIT_ERR_TIMEOUT);
+        if (lane == 0) {
+          record_error(a.err, LOWBIT_ERR_TIMEOUT);
+          gave_up = 1;
+        }
         break;
       }
       const uint8_t* st = stage(s);
@@ -569,6 +598,9 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
     const uint32_t owner = (uint32_t)(crank - rank);
     if (live && threadIdx.x < kRowTile) {
       if (rank != 0) {
+        // A CTA that gave up on a wait stays out of rank 0's shared memory: rank 0 may have
+        // stopped waiting for it and exited.
+        if (gave_up) return;
         const uint32_t la = ptx::smem_addr(&slots[(rank - 1) * kRowTile + threadIdx.x]);
         ptx::st_dsmem_f32(ptx::map_to_rank(la, owner), part[threadIdx.x]);
         ptx::mbar_arrive_remote(ptx::map_to_rank(ptx::smem_addr(&redbar), owner));
@@ -756,7 +788,7 @@ cudaError_t launch_int4_stream_mt(const GemvProblem* probs, int count, int M, in
   a.stages = sc.maxnb < S ? sc.maxnb : S;
   const size_t smem = (size_t)a.stages * stage + slots;  // at most 2 * 9472 + 30720 bytes
   return launch_streaming(int4_stream_kernel<MT>, g_int4_optins[MT == 1 ? 0 : (MT == 2 ? 1 : 2)],
-                          kSmemBudget, a, sc, smem, kSThreads, s);
+                          kSmemBudget, a, sc, smem, stream_threads<MT>(), s);
 }
 
 }  // namespace

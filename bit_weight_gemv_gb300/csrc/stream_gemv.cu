@@ -376,7 +376,8 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
 // stage (2 KB per group, shared by every row and plane); a row then adds one table entry per
 // nibble, so each 4 weights of a plane cost one shared-memory load and one add.
 constexpr int kLutWarp = kCWarps + 1;
-constexpr int kBpThreads = (kCWarps + 2) * 32;  // compute, producer, table warp
+constexpr int kLutWarps = 2;  // table builders, each owning alternate ring stages
+constexpr int kBpThreads = (kCWarps + 1 + kLutWarps) * 32;  // compute, producer, table warps
 constexpr uint32_t kLutBytes = 32 * 16 * sizeof(float);  // 32 nibble sets x 16 sums
 constexpr int kBpTargetBlocks = 5;
 constexpr int kSaTargetBlocks = 3;  // blocks of 256 inputs
@@ -482,13 +483,14 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
         ptx::mbar_wait(ptx::smem_addr(&full[b % S]), (b / S) & 1);
     }
     __syncwarp();
-  } else if (warp == kLutWarp) {
+  } else if (warp >= kLutWarp) {
     // ---------------------------------------------------------------- tables
     // Nibble set c = 8w + n of a block (w = 32-input word, n = nibble): inputs k0 + {0, 2, 4, 6}
     // with k0 = 32w + 8n (n < 4, even inputs) or 32w + 8(n - 4) + 1 (n >= 4, odd inputs).
     // Lane l tabulates sets l, l + 32, ... (one per 128 inputs of the block).
     if (hdr_ok) {
       for (int b = 0; b < nb; ++b) {
+        if ((b % S) % kLutWarps != warp - kLutWarp) continue;  // this warp's stages only
         const int s = b % S;
         const bool landed = ptx::mbar_wait(ptx::smem_addr(&full[s]), (b / S) & 1);
         if (!__all_sync(0xFFFFFFFFu, landed)) {
@@ -815,6 +817,7 @@ cudaError_t launch_bp_stream(const GemvProblem* probs, int count, int* err, cuda
   const size_t slots = (size_t)(sc.kmax - 1) * kRowTile * sizeof(float);
   int S = (int)((kSmemBudget - slots) / stage);
   S = S < 2 ? 2 : (S > kMaxStages ? kMaxStages : S);
+  S -= S % kLutWarps;  // the table warps share the stages evenly
   a.err = err;
   a.stages = sc.maxnb < S ? sc.maxnb : S;
   const size_t smem = (size_t)a.stages * stage + slots;
@@ -835,6 +838,7 @@ cudaError_t launch_sa_stream(const GemvProblem* probs, int count, int* err, cuda
   const size_t slots = (size_t)(sc.kmax - 1) * kRowTile * sizeof(float);
   int S = (int)((kSmemBudget > slots ? kSmemBudget - slots : 0) / stage);
   S = S < 2 ? 2 : (S > kMaxStages ? kMaxStages : S);
+  S -= S % kLutWarps;  // the table warps share the stages evenly
   a.err = err;
   a.stages = sc.maxnb < S ? sc.maxnb : S;
   const size_t smem = (size_t)a.stages * stage + slots;

@@ -11,10 +11,12 @@ Modules
   binplane  -- ShiftAdd binary planes: dequantise, multiply, pack/unpack the layout.
   sa        -- the deployed ShiftAdd format (u8 scale codes x one fp16 d per 256 inputs):
                dequantise, multiply, pack/unpack the layout.
+  nvfp4     -- NVFP4 weights (E2M1 x E4M3 per 16 x fp32) and the trimmed draft head's
+               argmax through an id map: dequantise, multiply, pack/unpack the layout.
   verify    -- vocabulary argmax (lowest index on ties) and greedy prefix acceptance.
 
 Parity pins (tests/test_oracle_pins.py) tie every function to something other than
 itself: hand-worked 4x8 examples, brute force on tiny shapes, closed forms, invariants
 and library rounding routines.  No function here is "parity unpinned".
 """
-from . import numerics, int4, binplane, sa, verify  # noqa: F401
+from . import numerics, int4, binplane, sa, nvfp4, verify  # noqa: F401

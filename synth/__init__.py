@@ -148,6 +148,37 @@ def sa_problem(seed: int, P: int, G: int, M: int, N: int, K: int, *sub: int):
     return bits, codes, d, x
 
 
+# The trimmed draft head (Small-vocabulary MTP study, section 3.3): the 32,768 most used rows of
+# the 248,320-row vocabulary, in NVFP4.
+DRAFT_ROWS = HEAD_ROWS[1]
+
+
+def nvfp4_weights(g: np.random.Generator, N: int, K: int):
+    """NVFP4 weights: codes uint8 [N][K/2] (two 4-bit E2M1 codes per byte, each uniform over
+    the 16 codes), E4M3 scale bytes uint8 [N][K/16] with exponent field uniform in 4..8 and
+    mantissa uniform (normal values 2^-3 .. 3.75), tensor scale 0.01.  Draw order: codes,
+    scales."""
+    codes = g.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    e = g.integers(4, 9, size=(N, K // 16))
+    m = g.integers(0, 8, size=(N, K // 16))
+    scales = ((e << 3) | m).astype(np.uint8)
+    return codes, scales, 0.01
+
+
+def id_map(g: np.random.Generator, rows: int, vocab: int = HEAD_ROWS[0]) -> np.ndarray:
+    """int32 [rows]: distinct full-vocabulary ids for the rows of a trimmed head."""
+    return np.sort(g.choice(vocab, size=rows, replace=False)).astype(np.int32)
+
+
+def nvfp4_problem(seed: int, M: int, N: int, K: int, *sub: int):
+    """One draft-head problem: (codes, scales, g, id_map, H)."""
+    gen = generator(seed, 0xF4, M, N, K, *sub)
+    codes, scales, gs = nvfp4_weights(gen, N, K)
+    ids = id_map(gen, N)
+    h = activations(gen, M, K)
+    return codes, scales, gs, ids, h
+
+
 ACTIVATION_KINDS = ("outlier", "mixed_scale", "tiny", "huge", "zero", "sparse")
 
 

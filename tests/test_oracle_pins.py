@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import synth
-from oracle import binplane, int4, numerics, sa, verify
+from oracle import binplane, int4, numerics, nvfp4, sa, verify
 from oracle.numerics import bf16_to_f64, f16_to_f64
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -463,4 +463,104 @@ def test_sa_pack_round_trip(P, G, N, K):
     assert hd["format"] == sa.FORMAT_SA and hd["group"] == G and hd["P"] == P
     if N % 128 == 0:   # payload = sign bits + u8 codes + fp16 d, nothing else
         assert hd["payload_bytes"] == P * N * K // 8 + P * N * K // G + 2 * N * K // 256
+
+
+# ----------------------------------------------------------------------------- NVFP4 head
+# Small-vocabulary MTP study, section 3.3: the trimmed draft head in NVFP4 (E2M1 weights, an
+# E4M3 scale per 16, an fp32 tensor scale), draft ids mapped to the full vocabulary.
+
+def test_e2m1_values_are_the_published_list():
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert list(nvfp4.e2m1_to_f64(np.arange(8))) == mags
+    assert list(nvfp4.e2m1_to_f64(np.arange(8, 16))) == [-m for m in mags]
+
+
+def test_e4m3_decode_matches_torch():
+    b = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(b).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = nvfp4.e4m3_to_f64(b)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+
+
+def test_nvfp4_hand_example():
+    rows = _read_fixture("nvfp4_hand_1x32.txt")
+    K = 32
+    codes = np.zeros((1, K // 2), dtype=np.uint8)
+    for kv in rows["codes"]:
+        i, v = kv.split(":")
+        codes[0, int(i)] = int(v, 16)
+    scales = np.array([[int(v, 16) for v in rows["scales"]]], dtype=np.uint8)
+    x = np.zeros((1, K))
+    for kv in rows["x"]:
+        i, v = kv.split(":")
+        x[0, int(i)] = float(v)
+    y = nvfp4.gemm(synth.to_bf16_bits(x), codes, scales, float(rows["g"][0]))
+    assert y[0, 0] == float(rows["y"][0])
+
+
+def test_nvfp4_brute_force():
+    codes, scales, g, _, h = synth.nvfp4_problem(30, 2, 5, 128)
+    H = numerics.bf16_to_f64(h)
+    ref = np.zeros((2, 5))
+    for m in range(2):
+        for n in range(5):
+            acc = 0.0
+            for k in range(128):
+                c = (codes[n, k // 2] >> (4 * (k % 2))) & 15
+                sgn = -1.0 if c & 8 else 1.0
+                e, mm = (c >> 1) & 3, c & 1
+                v = sgn * (mm * 0.5 if e == 0 else 2.0 ** (e - 1) * (1 + mm / 2))
+                sb = int(scales[n, k // 16])
+                se, sm = (sb >> 3) & 15, sb & 7
+                sv = (sm / 8.0) * 2.0 ** -6 if se == 0 else 2.0 ** (se - 7) * (1 + sm / 8)
+                acc += H[m, k] * np.float32(g) * sv * v
+            ref[m, n] = acc
+    assert np.allclose(nvfp4.gemm(h, codes, scales, g), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_nvfp4_layout_positions_by_hand():
+    N, K = 200, 256
+    total, off, payload, block = nvfp4.packed_sizes(N, K)
+    assert block == 9216 and payload == 2 * 2 * 9216
+    with open(os.path.join(GOLDEN, "nvfp4_layout_positions.txt")) as f:
+        rows = [line.split() for line in f if line.strip() and not line.startswith("#")]
+    for kind, n, kj, byte, nib in rows:
+        n, kj, byte = int(n), int(kj), int(byte)
+        codes = np.zeros((N, K // 2), dtype=np.uint8)
+        scales = np.zeros((N, K // 16), dtype=np.uint8)
+        expect = np.zeros(payload, dtype=np.uint8)
+        if kind == "code":
+            codes[n, kj // 2] = 0x5 << (4 * (kj % 2))
+            expect[byte] = 0x5 << (4 * int(nib))
+        else:
+            scales[n, kj] = 0x3A
+            expect[byte] = 0x3A
+        sec = nvfp4.pack(codes, scales, 1.0)[off:off + payload]
+        assert np.array_equal(sec, expect), (kind, n, kj)
+
+
+@pytest.mark.parametrize("N,K", [(1, 128), (130, 256), (256, 512)])
+def test_nvfp4_pack_round_trip(N, K):
+    codes, scales, g, _, _ = synth.nvfp4_problem(31, 1, N, K)
+    packed = nvfp4.pack(codes, scales, g)
+    c2, s2, g2 = nvfp4.unpack(packed)
+    assert np.array_equal(c2, codes) and np.array_equal(s2, scales) and g2 == np.float32(g)
+    hd = int4.parse_header(packed)
+    assert hd["format"] == nvfp4.FORMAT_NVFP4 and hd["block_bytes"] == 9216
+    if N % 128 == 0:
+        assert hd["payload_bytes"] == N * K // 2 + N * K // 16
+
+
+def test_draft_ids_map_and_ties():
+    logits = np.array([[1.0, 3.0, 3.0, -2.0], [0.0, -1.0, -5.0, 0.0]])
+    ids = np.array([70, 11, 4, 9], dtype=np.int32)
+    assert list(nvfp4.draft_ids(logits)) == [1, 0]          # lowest row among equal maxima
+    assert list(nvfp4.draft_ids(logits, ids)) == [11, 70]
+    g = synth.generator(32)
+    L = g.standard_normal((5, 1000))
+    m = synth.id_map(g, 1000)
+    assert len(set(m.tolist())) == 1000
+    assert np.array_equal(nvfp4.draft_ids(L, m), m[np.argmax(L, axis=1)])
 

@@ -12,7 +12,8 @@ replayed from CUDA graphs (one per rotation of the weight copies) and timed with
 Also reported under "rows": the same layer as seven single-matrix calls ("decode") and as one
 grouped call ("decode_all"), the M=16 verify GEMM over the same layer and its batch sweep,
 binary-plane GEMV/GEMM, the deployed ShiftAdd format (u8 scale codes, "sa_m1"/"sa_m16"), the
-248,320-row vocabulary head as one M=1 GEMV ("head_gemv"), and the
+248,320-row vocabulary head as one M=1 GEMV ("head_gemv"), the trimmed NVFP4 draft head with its
+id-mapped argmax ("draft_m1"/"draft_m16"), and the
 LM-head argmax+verify over 248,320 and 32,768 rows.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-rows]
@@ -58,6 +59,11 @@ def algorithmic_binplane_bytes(P, N, K):
 def algorithmic_sa_bytes(P, G, N, K):
     """Sign bits, u8 scale codes and one fp16 d per 256 inputs."""
     return P * N * K // 8 + P * N * (K // G) + N * (K // 256) * 2
+
+
+def algorithmic_nvfp4_bytes(N, K):
+    """E2M1 codes and one E4M3 scale per 16 inputs."""
+    return N * K // 2 + N * K // 16
 
 
 def read_peaks():
@@ -269,6 +275,24 @@ def build_sa(lb, torch, l2, M, name, desc):
     return w
 
 
+def build_draft_head(lb, torch, l2, M, name, desc):
+    """The trimmed NVFP4 draft head: argmax over its rows, mapped to full-vocabulary ids."""
+    N, K = synth.DRAFT_ROWS, synth.HEAD_K
+    w = Workload(name, desc, "tc_gemm_kernel")
+    codes, scales, g, ids, h = synth.nvfp4_problem(4, M, N, K)
+    p = torch.empty(lb.lowbit_nvfp4_packed_bytes(N, K), dtype=torch.uint8, device="cuda")
+    lb.lowbit_pack_nvfp4(dev(codes), dev(scales), g, N, K, p)
+    w.bytes = algorithmic_nvfp4_bytes(N, K)
+    packs = _copies(p, copies_for(w.bytes, l2), torch)
+    H, idm = bf16_dev(h), dev(ids)
+    out = torch.empty(M, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(lb.lmhead_workspace_bytes(2, N, K), dtype=torch.uint8, device="cuda")
+    for c in range(len(packs)):
+        w.calls.append([lambda c=c: lb.lowbit_draft_argmax(H, packs[c], M, N, K, idm, out, ws)])
+    w.M, w.tokens, w.launches = M, M, 1
+    return w
+
+
 def build_lmhead(lb, torch, l2, N, path, name, desc):
     M, K = synth.VERIFY_BLOCK, synth.HEAD_K
     w = Workload(name, desc, "tc_gemm_kernel" if path != 1 else "int4_gemm_cc_kernel")
@@ -353,6 +377,11 @@ def build_workload(lb, torch, l2, name, path):
         return build_sa(lb, torch, l2, M, name,
                         f"deployed ShiftAdd format ({types}: u8 scale codes, fp16 d per 256 inputs): "
                         f"(K,N) in {{(4096,12288),(12288,4096)}}, M={M}")
+    if name in ("draft_m1", "draft_m16"):
+        M = 1 if name == "draft_m1" else 16
+        return build_draft_head(lb, torch, l2, M, name,
+                                f"trimmed NVFP4 draft head: {synth.DRAFT_ROWS} rows x K={synth.HEAD_K}, "
+                                f"M={M}, fused argmax mapped to full-vocabulary ids")
     if name == "head_gemv":
         return build_head_gemv(lb, torch, l2, path, name,
                                f"INT4 GEMV at M=1 over the {synth.HEAD_ROWS[0]}-row vocabulary head, "
@@ -365,7 +394,7 @@ def build_workload(lb, torch, l2, name, path):
     raise ValueError(name)
 
 
-WORKLOADS = ("decode", "decode_deps", "decode_all", "verify", "verify_deps", "verify_all", "binplane_m1", "binplane_m16", "sa_m1", "sa_m16", "head_gemv", "lmhead_full", "lmhead_trim",
+WORKLOADS = ("decode", "decode_deps", "decode_all", "verify", "verify_deps", "verify_all", "binplane_m1", "binplane_m16", "sa_m1", "sa_m16", "draft_m1", "draft_m16", "head_gemv", "lmhead_full", "lmhead_trim",
              "tiny") + tuple(f"verify_m{m}" for m in synth.M_SWEEP if m not in (16,))
 
 

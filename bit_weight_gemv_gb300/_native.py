@@ -37,6 +37,10 @@ _SIGS = {
     "lowbit_pack_sa": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp]),
     "lowbit_gemm_sa": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
     "lowbit_gemm_sa_path": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _i, _vp]),
+    "lowbit_nvfp4_packed_bytes": (_sz, [_i, _i]),
+    "lowbit_pack_nvfp4": (_i, [_vp, _vp, ctypes.c_float, _i, _i, _vp, _vp]),
+    "lowbit_gemm_nvfp4": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp]),
+    "lowbit_draft_argmax": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
 }
 
 
@@ -203,6 +207,45 @@ def lowbit_gemm_sa_path(X, packed, P, G, M, N, K, Y, path, stream=None):
     _gemm_args(X, packed, M, N, K, Y)
     _check(lib.lowbit_gemm_sa_path(_ptr(X), _ptr(packed), P, G, M, N, K, _ptr(Y), path,
                                    _stream(stream)), "lowbit_gemm_sa_path")
+
+
+def lowbit_nvfp4_packed_bytes(N: int, K: int) -> int:
+    return lib.lowbit_nvfp4_packed_bytes(N, K)
+
+
+def lowbit_pack_nvfp4(codes, scales, g, N, K, packed, stream=None):
+    """codes uint8 [N][K/2] (E2M1 pairs), scales uint8 [N][K/16] (E4M3), g float -> packed."""
+    _need(codes, torch.uint8, "codes")
+    _need(scales, torch.uint8, "scales")
+    _need(packed, torch.uint8, "packed")
+    if packed.numel() < lowbit_nvfp4_packed_bytes(N, K):
+        raise ValueError("packed buffer too small")
+    _check(lib.lowbit_pack_nvfp4(_ptr(codes), _ptr(scales), float(g), N, K, _ptr(packed),
+                                 _stream(stream)), "lowbit_pack_nvfp4")
+
+
+def lowbit_gemm_nvfp4(X, packed, M, N, K, Y, stream=None):
+    """Y bf16 [M][N] = X bf16 [M][K] times the packed NVFP4 weights, transposed."""
+    _gemm_args(X, packed, M, N, K, Y)
+    _check(lib.lowbit_gemm_nvfp4(_ptr(X), _ptr(packed), M, N, K, _ptr(Y), _stream(stream)),
+           "lowbit_gemm_nvfp4")
+
+
+def lowbit_draft_argmax(H, packed_head, M, N, K, id_map, ids, workspace, stream=None):
+    """ids int32 [M] = id_map[argmax over the N rows of an NVFP4 draft head] (id_map may be None)."""
+    _need(H, torch.bfloat16, "H")
+    _need(packed_head, torch.uint8, "packed_head")
+    _need(ids, torch.int32, "ids")
+    _need(workspace, torch.uint8, "workspace")
+    if id_map is not None:
+        _need(id_map, torch.int32, "id_map")
+        if id_map.numel() < N:
+            raise ValueError("id_map too small")
+    if H.numel() < M * K or ids.numel() < M:
+        raise ValueError("H or ids too small")
+    _check(lib.lowbit_draft_argmax(_ptr(H), _ptr(packed_head), M, N, K, _ptr(id_map), _ptr(ids),
+                                   _ptr(workspace), workspace.numel(), _stream(stream)),
+           "lowbit_draft_argmax")
 
 
 def _lmhead_args(H, packed_head, M, K, draft, argmax, n_accept, bonus, workspace):

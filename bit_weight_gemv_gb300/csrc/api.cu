@@ -104,6 +104,11 @@ size_t lowbit_sa_packed_bytes(int P, int G, int N, int K) {
   return kHeaderBytes + sa_payload_bytes(P, G, N, K);
 }
 
+size_t lowbit_nvfp4_packed_bytes(int N, int K) {
+  if (check_shape(1, N, K, 1) != LOWBIT_OK) return 0;
+  return kHeaderBytes + nvfp4_payload_bytes(N, K);
+}
+
 size_t lmhead_workspace_bytes(int M, int N, int K) {
   if (M < 2 || M > 32 || N < 1 || K <= 0 || K % kGroup != 0) return 0;
   return 512;
@@ -138,6 +143,16 @@ lowbit_status lowbit_pack_sa(const uint8_t* signbits, const uint8_t* codes, cons
   if (!aligned16(signbits) || !aligned16(packed)) return LOWBIT_ERR_ALIGN;
   return from_cuda(launch_pack_sa(signbits, codes, d, P, G, N, K, static_cast<uint8_t*>(packed),
                                   static_cast<cudaStream_t>(stream)));
+}
+
+lowbit_status lowbit_pack_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, int N, int K,
+                                void* packed, void* stream) {
+  if (!codes || !scales || !packed) return LOWBIT_ERR_INVALID_ARG;
+  const lowbit_status st = check_shape(1, N, K, 1);
+  if (st != LOWBIT_OK) return st;
+  if (!aligned16(codes) || !aligned16(packed)) return LOWBIT_ERR_ALIGN;
+  return from_cuda(launch_pack_nvfp4(codes, scales, g, N, K, static_cast<uint8_t*>(packed),
+                                     static_cast<cudaStream_t>(stream)));
 }
 
 lowbit_status lowbit_validate_packed(const void* packed, int format, int P, int N, int K,
@@ -257,6 +272,33 @@ lowbit_status lowbit_gemm_sa_path(const uint16_t* X, const void* packed, int P, 
   }
   if (path == 1) return from_cuda(launch_sa_cc(X, pk, P, G, M, N, K, Y, err, s));
   return from_cuda(launch_sa_tc(X, pk, P, G, M, N, K, Y, err, s));
+}
+
+lowbit_status lowbit_gemm_nvfp4(const uint16_t* X, const void* packed, int M, int N, int K,
+                                uint16_t* Y, void* stream) {
+  if (!X || !packed || !Y) return LOWBIT_ERR_INVALID_ARG;
+  const lowbit_status st = check_shape(M, N, K, 32);
+  if (st != LOWBIT_OK) return st;
+  if (!aligned16(X) || !aligned16(packed)) return LOWBIT_ERR_ALIGN;
+  int* err = device_error_word();
+  if (!err) return LOWBIT_ERR_CUDA;
+  return from_cuda(launch_nvfp4_tc(X, static_cast<const uint8_t*>(packed), M, N, K, Y, err,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+lowbit_status lowbit_draft_argmax(const uint16_t* H, const void* packed_head, int M, int N, int K,
+                                  const int32_t* id_map, int32_t* ids, void* workspace,
+                                  size_t ws_bytes, void* stream) {
+  if (!H || !packed_head || !ids) return LOWBIT_ERR_INVALID_ARG;
+  const lowbit_status st = check_shape(M, N, K, 32);
+  if (st != LOWBIT_OK) return st;
+  if (!workspace || ws_bytes < lmhead_workspace_bytes(2, N, K)) return LOWBIT_ERR_WORKSPACE;
+  if (!aligned16(H) || !aligned16(packed_head) || !aligned16(workspace)) return LOWBIT_ERR_ALIGN;
+  int* err = device_error_word();
+  if (!err) return LOWBIT_ERR_CUDA;
+  return from_cuda(launch_draft_argmax_tc(H, static_cast<const uint8_t*>(packed_head), M, N, K,
+                                          id_map, ids, workspace, err,
+                                          static_cast<cudaStream_t>(stream)));
 }
 
 lowbit_status lmhead_argmax_verify(const uint16_t* H, const void* packed_head, int M, int N,

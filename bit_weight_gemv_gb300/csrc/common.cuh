@@ -15,6 +15,7 @@ constexpr uint32_t kMagic = 0x3242574Cu;  // "LWB2"
 constexpr uint32_t kFormatInt4 = 1;
 constexpr uint32_t kFormatBinplane = 2;
 constexpr uint32_t kFormatSa = 3;
+constexpr uint32_t kFormatNvfp4 = 4;
 constexpr uint32_t kVersion = 2;
 constexpr int kHeaderBytes = 128;
 constexpr int kGroup = 128;    // inputs per quantisation group
@@ -41,6 +42,15 @@ __host__ __device__ inline uint64_t int4_payload_bytes(int N, int K) {
 }
 __host__ __device__ inline uint64_t binplane_payload_bytes(int P, int N, int K) {
   return (uint64_t)row_tiles(N) * (uint64_t)(K / kGroup) * binplane_block(P);
+}
+
+// NVFP4: one block per (128-row tile, group of 128 inputs): the canonical code bytes (two E2M1
+// codes per byte, low nibble = even input) [4 chunks][128 rows][16 B], then the E4M3 scales
+// [8 per group][128 rows]; the fp32 tensor scale sits in the header's last u64 field.
+constexpr uint32_t kNvfp4Block = 4 * kRowTile * 16 + 8 * kRowTile;
+constexpr uint32_t kNvfp4ScaleOff = 4 * kRowTile * 16;
+__host__ __device__ inline uint64_t nvfp4_payload_bytes(int N, int K) {
+  return (uint64_t)row_tiles(N) * (uint64_t)(K / kGroup) * kNvfp4Block;
 }
 
 // The deployed ShiftAdd format: one block per (128-row tile, super-block of 256 inputs) holding
@@ -162,6 +172,14 @@ cudaError_t launch_pack_sa(const uint8_t* bits, const uint8_t* codes, const uint
                            int G, int N, int K, uint8_t* packed, cudaStream_t s);
 cudaError_t launch_sa_cc(const uint16_t* X, const uint8_t* packed, int P, int G, int M, int N,
                          int K, uint16_t* Y, int* err, cudaStream_t s);
+cudaError_t launch_pack_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, int N, int K,
+                             uint8_t* packed, cudaStream_t s);
+cudaError_t launch_nvfp4_tc(const uint16_t* X, const uint8_t* packed, int M, int N, int K,
+                            uint16_t* Y, int* err, cudaStream_t s);
+// Draft head: ids[m] = id_map[argmax_n logit[m][n]] (the row when id_map is null).
+cudaError_t launch_draft_argmax_tc(const uint16_t* H, const uint8_t* packed, int M, int N, int K,
+                                   const int32_t* id_map, int32_t* ids, void* ws, int* err,
+                                   cudaStream_t s);
 cudaError_t launch_sa_tc(const uint16_t* X, const uint8_t* packed, int P, int G, int M, int N,
                          int K, uint16_t* Y, int* err, cudaStream_t s);
 // Several INT4 multiplies with a common M >= 2 in one tensor-core launch (X, Y are [M][K], [M][N]).

@@ -8,13 +8,15 @@
 // contiguous block holding the tile's codes (rows side by side, so a warp's 16-byte-per-lane
 // load of 32 rows is one 512-byte segment) followed by its scales, so a kernel can stage a
 // whole block with a single bulk copy.
+#include <string.h>
+
 #include "common.cuh"
 
 namespace lowbit {
 namespace {
 
 __device__ void write_header(uint8_t* packed, uint32_t format, int P, int N, int K, int group,
-                             uint64_t payload_bytes, uint64_t block_bytes) {
+                             uint64_t payload_bytes, uint64_t block_bytes, uint64_t reserved) {
   PackedHeader h;
   h.magic = kMagic;
   h.format = format;
@@ -27,7 +29,7 @@ __device__ void write_header(uint8_t* packed, uint32_t format, int P, int N, int
   h.payload_offset = kHeaderBytes;
   h.payload_bytes = payload_bytes;
   h.block_bytes = block_bytes;
-  h.reserved = 0;
+  h.reserved = reserved;
   uint4* dst = reinterpret_cast<uint4*>(packed);
   const uint4* src = reinterpret_cast<const uint4*>(&h);
 #pragma unroll
@@ -89,9 +91,10 @@ __global__ void pack_int4_scales(const uint16_t* __restrict__ scales, int N, int
 }
 
 __global__ void pack_header(uint8_t* packed, uint32_t format, int P, int N, int K, int group,
-                            unsigned long long payload_bytes, unsigned long long block_bytes) {
+                            unsigned long long payload_bytes, unsigned long long block_bytes,
+                            unsigned long long reserved = 0) {
   if (threadIdx.x == 0 && blockIdx.x == 0)
-    write_header(packed, format, P, N, K, group, payload_bytes, block_bytes);
+    write_header(packed, format, P, N, K, group, payload_bytes, block_bytes, reserved);
 }
 
 // Even bits of a 32-bit word to its low half-word, odd bits to its high half-word.
@@ -210,6 +213,45 @@ __global__ void pack_sa_d(const uint16_t* __restrict__ d, int P, int G, int N, i
       (n < N) ? d[n * J + tj % J] : (uint16_t)0;
 }
 
+// ---- NVFP4 (E2M1 codes, an E4M3 scale per 16 inputs, an fp32 tensor scale).
+
+// One thread per 16-byte unit (tile t, group g, chunk c, row r): the canonical code bytes of
+// k = 128g + 32c .. +31 copied to block(t, g) + c*2048 + r*16.
+__global__ void pack_nvfp4_codes(const uint8_t* __restrict__ codes, int N, int K,
+                                 uint8_t* __restrict__ payload, long long units) {
+  const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= units) return;
+  const int G = K / kGroup;
+  const int r = (int)(u % kRowTile);
+  long long rest = u / kRowTile;
+  const int c = (int)(rest % 4);
+  rest /= 4;
+  const int g = (int)(rest % G);
+  const long long t = rest / G;
+  const long long n = t * kRowTile + r;
+  uint4 v = make_uint4(0, 0, 0, 0);  // padding rows: code 0 (+0)
+  if (n < N) v = *reinterpret_cast<const uint4*>(codes + n * (long long)(K / 2) + 64LL * g + 16 * c);
+  *reinterpret_cast<uint4*>(payload + (size_t)(t * G + g) * kNvfp4Block + (size_t)c * kRowTile * 16 +
+                            r * 16) = v;
+}
+
+// One thread per scale byte (tile t, group g, sub-group j, row r) at block(t, g) + 8192 + j*128 + r.
+__global__ void pack_nvfp4_scales(const uint8_t* __restrict__ scales, int N, int K,
+                                  uint8_t* __restrict__ payload, long long units) {
+  const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= units) return;
+  const int G = K / kGroup;
+  const int r = (int)(u % kRowTile);
+  long long rest = u / kRowTile;
+  const int j = (int)(rest % 8);
+  rest /= 8;
+  const int g = (int)(rest % G);
+  const long long t = rest / G;
+  const long long n = t * kRowTile + r;
+  payload[(size_t)(t * G + g) * kNvfp4Block + kNvfp4ScaleOff + j * kRowTile + r] =
+      (n < N) ? scales[n * (long long)(K / 16) + 8 * g + j] : (uint8_t)0;
+}
+
 // Launched last by every pack call: the multiplies read their weights before their
 // programmatic-dependency wait, so the kernel right before one must not be a weight writer.
 __global__ void pack_done() {}
@@ -252,6 +294,20 @@ cudaError_t launch_pack_sa(const uint8_t* bits, const uint8_t* codes, const uint
   pack_sa_signs<<<blocks_for(su, 256), 256, 0, s>>>(bits, P, G, N, K, packed + kHeaderBytes, su);
   pack_sa_codes<<<blocks_for(cu, 256), 256, 0, s>>>(codes, P, G, N, K, packed + kHeaderBytes, cu);
   pack_sa_d<<<blocks_for(du, 256), 256, 0, s>>>(d, P, G, N, K, packed + kHeaderBytes, du);
+  pack_done<<<1, 32, 0, s>>>();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, int N, int K,
+                             uint8_t* packed, cudaStream_t s) {
+  const long long blocks = (long long)row_tiles(N) * (K / kGroup);
+  const long long cu = blocks * 4 * kRowTile, su = blocks * 8 * kRowTile;
+  uint32_t gbits;
+  memcpy(&gbits, &g, sizeof(gbits));
+  pack_header<<<1, 32, 0, s>>>(packed, kFormatNvfp4, 0, N, K, kGroup, nvfp4_payload_bytes(N, K),
+                               kNvfp4Block, gbits);
+  pack_nvfp4_codes<<<blocks_for(cu, 256), 256, 0, s>>>(codes, N, K, packed + kHeaderBytes, cu);
+  pack_nvfp4_scales<<<blocks_for(su, 256), 256, 0, s>>>(scales, N, K, packed + kHeaderBytes, su);
   pack_done<<<1, 32, 0, s>>>();
   return cudaGetLastError();
 }

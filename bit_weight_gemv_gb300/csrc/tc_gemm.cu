@@ -50,7 +50,7 @@ constexpr int kMmaWarp = 9;
 constexpr int kXWarp = 10;
 constexpr int kThreads = 352;
 constexpr uint32_t kTmemCols = 256;
-constexpr int kFmtInt4 = 0, kFmtBinplane = 1, kFmtSa = 2;
+constexpr int kFmtInt4 = 0, kFmtBinplane = 1, kFmtSa = 2, kFmtNvfp4 = 3;
 constexpr int kEpiStore = 0, kEpiArgmax = 1;
 
 struct TcArgs {
@@ -66,7 +66,8 @@ struct TcArgs {
   int* err;
   LmheadWorkspace* ws;
   const int32_t* draft;
-  int32_t* argmax;
+  int32_t* argmax;       // ARGMAX epilogue: per-token winners (draft head: the mapped ids)
+  const int32_t* id_map; // draft head: full-vocabulary id of each row (may be null)
   int32_t* n_accept;
   int32_t* bonus;
 };
@@ -92,13 +93,18 @@ struct TcLayout {
   static constexpr uint32_t kAtom = NMMA * 128;  // one 64-input swizzle atom of the X tile
   static constexpr uint32_t kX = (KIN / 64) * kAtom;  // X tile for one block
   __host__ __device__ static uint32_t block(int P, int GS) {
-    return FMT == kFmtInt4 ? kInt4Block : (FMT == kFmtSa ? sa_block(P, GS) : binplane_block(P));
+    return FMT == kFmtInt4 ? kInt4Block
+         : FMT == kFmtNvfp4 ? kNvfp4Block
+         : (FMT == kFmtSa ? sa_block(P, GS) : binplane_block(P));
   }
   __host__ __device__ static uint32_t stage(int P, int GS) {
     return (kX + block(P, GS) + 1023u) / 1024u * 1024u;
   }
   static constexpr uint32_t kCtrl = 1024;
-  __host__ static size_t smem(int P, int GS, int S) { return 1024 + (size_t)S * stage(P, GS) + kCtrl; }
+  static constexpr uint32_t kLut = FMT == kFmtNvfp4 ? 256 * 4 : 0;  // NVFP4 code-byte table
+  __host__ static size_t smem(int P, int GS, int S) {
+    return 1024 + (size_t)S * stage(P, GS) + kCtrl + kLut;
+  }
 };
 
 // j(i): the mantissa bit (1..6) that carries pair i of a 32-input plane word.  Pairs 0-5 are
@@ -151,6 +157,37 @@ __device__ __forceinline__ void dequant_sa_word(uint32_t w, uint32_t apair, uint
   for (int i = 0; i < 16; ++i) v[i] = apair ^ ((nw << (15 - i)) & 0x80008000u);
 }
 
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// NVFP4: E2M1 code (0..15) -> bf16 bits, from the fields (sign, two exponent bits with bias
+// 1, one mantissa bit); every value has at most 2 significant bits, so bf16 holds it exactly.
+__device__ __forceinline__ uint32_t e2m1_bf16(uint32_t c) {
+  const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+  const float mag = e == 0 ? 0.5f * (float)m : __uint_as_float((126u + e) << 23 | m << 22);
+  return (__float_as_uint(mag) >> 16) | ((c & 8u) << 12);
+}
+// E4M3 byte -> bf16 pair (b, b): sign, four exponent bits with bias 7, three mantissa bits;
+// exponent 0 is subnormal, 0x7F / 0xFF NaN.  At most 4 significant bits: exact in bf16.
+__device__ __forceinline__ uint32_t e4m3_bf16x2(uint32_t b) {
+  float v = (b & 0x78u) ? __uint_as_float(((b & 0x7Fu) << 20) + (120u << 23)) : (float)(b & 7u) * 0x1p-9f;
+  if ((b & 0x7Fu) == 0x7Fu) v = __uint_as_float(0x7FC00000u);
+  const uint32_t h = (__float_as_uint(v) >> 16) | ((b & 0x80u) << 8);
+  return h | (h << 16);
+}
+// One 16-byte NVFP4 chunk (32 inputs, code byte j = inputs 2j and 2j+1) -> 16 bf16 pairs
+// w = e2m1 * e4m3 (exact: at most 6 significant bits); bytes 0-7 take scale pair sa, 8-15 sb.
+__device__ __forceinline__ void dequant_nvfp4_chunk(const uint4 c, uint32_t sa, uint32_t sb,
+                                                    const uint32_t* lut, uint32_t (&v)[16]) {
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    v[j] = bf16x2_mul(lut[(w[j >> 2] >> (8 * (j & 3))) & 0xFFu], j < 8 ? sa : sb);
+}
+
 template <int FMT, int NMMA, int EPI>
 __global__ void __launch_bounds__(kThreads, 2)
 tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
@@ -166,7 +203,7 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
     if (cid >= batch.p[i].cl_begin) pi = i;
   const TcArgs& args = batch.p[pi];
   const CUtensorMap* xmap = &batch.maps[pi];
-  const int P = (FMT == kFmtInt4) ? 1 : args.P, GS = args.GS;
+  const int P = (FMT == kFmtInt4 || FMT == kFmtNvfp4) ? 1 : args.P, GS = args.GS;
   const uint32_t SB = L::stage(P, GS), BB = L::block(P, GS);
   const int UB = FMT == kFmtSa ? 2 * P : P;  // MMA units per block: (half, plane) for sa
   constexpr int NB = L::NB;
@@ -178,7 +215,9 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
   uint64_t* mmadone = aready + NB;      // [NB]
   uint64_t* mmafinal = mmadone + NB;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mmafinal + 1);
-  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] header ok, [1] abort
+  // [0] header ok, [1] abort, [2] NVFP4 tensor scale (fp32 bits, from the header)
+  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint32_t* lut = reinterpret_cast<uint32_t*>(ctrl + L::kCtrl);  // NVFP4: code byte -> bf16 pair
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ks = args.ks, rank = crank % ks;
@@ -196,9 +235,11 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
   if (threadIdx.x == 0) {
     const PackedHeader* hp = reinterpret_cast<const PackedHeader*>(args.packed);
     flags[0] = FMT == kFmtSa ? header_matches_sa(hp, P, GS, N, K)
-                             : header_matches(hp, FMT == kFmtInt4 ? kFormatInt4 : kFormatBinplane,
-                                              FMT == kFmtInt4 ? 0 : P, N, K);
+             : FMT == kFmtNvfp4 ? header_matches(hp, kFormatNvfp4, 0, N, K)
+             : header_matches(hp, FMT == kFmtInt4 ? kFormatInt4 : kFormatBinplane,
+                              FMT == kFmtInt4 ? 0 : P, N, K);
     flags[1] = 0;
+    if (FMT == kFmtNvfp4 && flags[0]) flags[2] = (int)__ldg(reinterpret_cast<const uint32_t*>(hp) + 14);
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_addr(&full[s]), 1);
       // dequant warps, MMA commit and (binary planes) the X warp release a stage
@@ -216,6 +257,8 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  if (FMT == kFmtNvfp4 && threadIdx.x < 256)  // byte j: inputs (2j, 2j+1) -> bf16 pair
+    lut[threadIdx.x] = e2m1_bf16(threadIdx.x & 15u) | (e2m1_bf16(threadIdx.x >> 4) << 16);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -422,6 +465,20 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
         tmem_st16(acol, v);
         dequant_int4_chunk(c1, v);
         tmem_st16(acol + 16, v);
+      } else if constexpr (FMT == kFmtNvfp4) {
+        const uint4 c0 = *reinterpret_cast<const uint4*>(blk + (2 * h) * 2048 + r * 16);
+        const uint4 c1 = *reinterpret_cast<const uint4*>(blk + (2 * h + 1) * 2048 + r * 16);
+        // scales of the thread's four runs of 16 inputs (runs 4h .. 4h+3 of the group)
+        uint32_t sp[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sp[j] = e4m3_bf16x2(blk[kNvfp4ScaleOff + (4 * h + j) * kBlockRows + r]);
+        sc = __int_as_float(flags[2]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+        dequant_nvfp4_chunk(c0, sp[0], sp[1], lut, v);
+        tmem_st16(acol, v);
+        dequant_nvfp4_chunk(c1, sp[2], sp[3], lut, v);
+        tmem_st16(acol + 16, v);
       } else if constexpr (FMT == kFmtSa) {
         // unit (half hb, plane p); this thread's inputs 128hb + 64h .. +63 share code group
         // (128hb + 64h) / GS of the super-block
@@ -519,7 +576,10 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
     tmem_dealloc(tmem, kTmemCols);
   }
   if constexpr (EPI == kEpiArgmax) {
-    if (hdr_ok) lmhead_finish(args.ws, args.M, args.draft, args.argmax, args.n_accept, args.bonus);
+    if (hdr_ok) {
+      if (args.n_accept) lmhead_finish(args.ws, args.M, args.draft, args.argmax, args.n_accept, args.bonus);
+      else draft_finish(args.ws, args.M, args.id_map, args.argmax);
+    }
   }
 }
 
@@ -617,7 +677,7 @@ cudaError_t launch_tc_batch(const TcArgs* probs, int count, cudaStream_t stream)
   if (clusters * C > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   batch.count = count;
   batch.cluster = C;
-  const int P = FMT == kFmtInt4 ? 1 : probs[0].P, GS = probs[0].GS;
+  const int P = (FMT == kFmtInt4 || FMT == kFmtNvfp4) ? 1 : probs[0].P, GS = probs[0].GS;
   // sa blocks grow with P and G: as many stages (2..6) as keep two CTAs on an SM.
   int S = L::kStages;
   if (FMT == kFmtSa) {
@@ -706,6 +766,23 @@ cudaError_t launch_sa_tc(const uint16_t* X, const uint8_t* packed, int P, int G,
   a.GS = G;
   a.Y = Y;
   return M <= 16 ? launch_tc<kFmtSa, 16, kEpiStore>(a, s) : launch_tc<kFmtSa, 32, kEpiStore>(a, s);
+}
+
+cudaError_t launch_nvfp4_tc(const uint16_t* X, const uint8_t* packed, int M, int N, int K,
+                            uint16_t* Y, int* err, cudaStream_t s) {
+  TcArgs a = base_args(X, packed, 1, M, N, K, err);
+  a.Y = Y;
+  return M <= 16 ? launch_tc<kFmtNvfp4, 16, kEpiStore>(a, s) : launch_tc<kFmtNvfp4, 32, kEpiStore>(a, s);
+}
+
+cudaError_t launch_draft_argmax_tc(const uint16_t* H, const uint8_t* packed, int M, int N, int K,
+                                   const int32_t* id_map, int32_t* ids, void* ws, int* err,
+                                   cudaStream_t s) {
+  TcArgs a = base_args(H, packed, 1, M, N, K, err);
+  a.ws = reinterpret_cast<LmheadWorkspace*>(ws);
+  a.id_map = id_map;
+  a.argmax = ids;
+  return M <= 16 ? launch_tc<kFmtNvfp4, 16, kEpiArgmax>(a, s) : launch_tc<kFmtNvfp4, 32, kEpiArgmax>(a, s);
 }
 
 cudaError_t launch_lmhead_tc(const uint16_t* H, const uint8_t* packed, int M, int N, int K,

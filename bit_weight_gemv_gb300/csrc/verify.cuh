@@ -73,4 +73,28 @@ __device__ __forceinline__ void lmhead_finish(LmheadWorkspace* ws, int M,
   }
 }
 
+// The draft head's finish (small-vocabulary MTP study, section 3.3: a trimmed head's rows are
+// mapped back to full-vocabulary ids): the last CTA writes ids[t] = id_map[winner] (the
+// winning row itself when id_map is null) and resets the workspace.
+__device__ __forceinline__ void draft_finish(LmheadWorkspace* ws, int M,
+                                             const int32_t* __restrict__ id_map,
+                                             int32_t* __restrict__ ids) {
+  __shared__ int is_last_d;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned int total = gridDim.x * gridDim.y * gridDim.z;
+    is_last_d = (atomicAdd(&ws->counter, 1u) == total - 1);
+  }
+  __syncthreads();
+  if (!is_last_d) return;
+  __threadfence();
+  if (threadIdx.x < M) {
+    const int row = argmax_key_row(atomicExch(&ws->keys[threadIdx.x], 0ull));
+    ids[threadIdx.x] = id_map ? id_map[row] : row;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) atomicExch(&ws->counter, 0u);
+}
+
 }  // namespace lowbit

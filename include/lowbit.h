@@ -74,6 +74,10 @@ size_t lowbit_binplane_packed_bytes(int P, int N, int K);
  * K % 256 == 0, 1 <= P <= 8 and G is 64, 128 or 256. */
 size_t lowbit_sa_packed_bytes(int P, int G, int N, int K);
 
+/* Bytes of a packed NVFP4 buffer (lowbit_pack_nvfp4): header + ceil(N/128)*128 rows of K/2
+ * code bytes and K/16 scale bytes. */
+size_t lowbit_nvfp4_packed_bytes(int N, int K);
+
 /* Bytes of the workspace lmhead_argmax_verify() needs (independent of N and K). */
 size_t lmhead_workspace_bytes(int M, int N, int K);
 
@@ -128,6 +132,21 @@ lowbit_status lowbit_pack_binplane(const uint8_t* signbits, const uint16_t* alph
  * 4096P + 128P(256/G) + r*2.  Padding rows hold zero signs, codes and d. */
 lowbit_status lowbit_pack_sa(const uint8_t* signbits, const uint8_t* codes, const uint16_t* d,
                              int P, int G, int N, int K, void* packed, void* stream);
+
+/* Repack NVFP4 weights, the draft-head format of the small-vocabulary MTP study (section 3.3:
+ * trim the head to the most used 32,768 tokens, quantise to NVFP4):
+ *   w[n][k] = g * e4m3(scales[n][k/16]) * e2m1(code of k in row n).
+ *   codes  : uint8 [N][K/2], 16-byte aligned; byte i holds inputs 2i (low nibble) and 2i + 1
+ *            as 4-bit E2M1 codes (sign, two exponent bits with bias 1, one mantissa bit).
+ *   scales : uint8 [N][K/16], E4M3 bytes (sign, four exponent bits with bias 7, three mantissa
+ *            bits; 0x7F / 0xFF are NaN).       g : the fp32 tensor scale.
+ *   packed : lowbit_nvfp4_packed_bytes(N, K) bytes, 16-byte aligned; fully overwritten.
+ * Layout: header (format 4, the fp32 bits of g at byte 56), then per (tile t of 128 rows, group
+ * j of 128 inputs) one block of 9216 bytes at 128 + (t*(K/128) + j)*9216: for chunk c = 0..3 and
+ * row r the 16 code bytes of inputs 128j + 32c .. +31 at c*2048 + r*16, then the scale byte of
+ * inputs 128j + 16i .. +15 at 8192 + i*128 + r (i = 0..7). */
+lowbit_status lowbit_pack_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, int N, int K,
+                                void* packed, void* stream);
 
 /* Synchronous check (copies the 128-byte header to the host after synchronising `stream`)
  * that `packed` holds format `format` (1 = INT4, 2 = binary planes) with these P, N, K.
@@ -189,6 +208,26 @@ lowbit_status lowbit_gemm_binplane(const uint16_t* X, const void* packed, int P,
  *   The header (format 3, P, N, K, G) is checked on the device as for the other formats. */
 lowbit_status lowbit_gemm_sa(const uint16_t* X, const void* packed, int P, int G, int M, int N,
                              int K, uint16_t* Y, void* stream);
+
+/* Y = X * W^T for NVFP4 weights (packed by lowbit_pack_nvfp4), 1 <= M <= 32, on the tensor
+ * cores: each weight written to tensor memory as the exact bf16 of e2m1 * e4m3, g applied in
+ * fp32 per output, each output rounded once to bf16.  (The draft step itself needs only the
+ * argmax: lowbit_draft_argmax.) */
+lowbit_status lowbit_gemm_nvfp4(const uint16_t* X, const void* packed, int M, int N, int K,
+                                uint16_t* Y, void* stream);
+
+/* Draft step of a trimmed NVFP4 head (small-vocabulary MTP study, section 3.3: the draft head
+ * keeps the 32,768 most used rows of the vocabulary; its winners are mapped back to the full
+ * vocabulary before verification):
+ *   H      : bf16 [M][K] hidden rows, 1 <= M <= 32.   packed_head : from lowbit_pack_nvfp4.
+ *   id_map : int32 [N], the full-vocabulary id of each head row, or NULL (ids are rows).
+ *   ids    : int32 [M] out: id_map[argmax_n logit[m][n]], argmax over fp32 logits (never
+ *            rounded), lowest row on ties.  Logits are not written anywhere.
+ *   workspace : as lmhead_argmax_verify (lmhead_workspace_bytes, zero-filled once, left zero;
+ *            calls sharing one must not overlap). */
+lowbit_status lowbit_draft_argmax(const uint16_t* H, const void* packed_head, int M, int N, int K,
+                                  const int32_t* id_map, int32_t* ids, void* workspace,
+                                  size_t ws_bytes, void* stream);
 
 /* LM-head verify step (small-vocabulary MTP study, section 3.3: full-vocabulary verification;
  * DFlash summary, section 4.1: tau in [1, gamma + 1]; Efficient-Qwen report, section 2.2).

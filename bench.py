@@ -278,7 +278,7 @@ def build_sa(lb, torch, l2, M, name, desc):
 def build_draft_head(lb, torch, l2, M, name, desc):
     """The trimmed NVFP4 draft head: argmax over its rows, mapped to full-vocabulary ids."""
     N, K = synth.DRAFT_ROWS, synth.HEAD_K
-    w = Workload(name, desc, "tc_gemm_kernel")
+    w = Workload(name, desc, "nvfp4_stream_kernel" if M == 1 else "tc_gemm_kernel")
     codes, scales, g, ids, h = synth.nvfp4_problem(4, M, N, K)
     p = torch.empty(lb.lowbit_nvfp4_packed_bytes(N, K), dtype=torch.uint8, device="cuda")
     lb.lowbit_pack_nvfp4(dev(codes), dev(scales), g, N, K, p)

@@ -16,7 +16,8 @@ __all__ = [
     "lowbit_gemm_int4_path", "lowbit_gemm_binplane_path", "lmhead_argmax_verify_path",
     "lowbit_gemm_int4_grouped", "lowbit_gemm_desc", "lmhead_argmax_verify_noalloc",
     "lowbit_sa_packed_bytes", "lowbit_pack_sa", "lowbit_gemm_sa", "lowbit_gemm_sa_path",
-    "lowbit_nvfp4_packed_bytes", "lowbit_pack_nvfp4", "lowbit_gemm_nvfp4", "lowbit_draft_argmax",
+    "lowbit_nvfp4_packed_bytes", "lowbit_pack_nvfp4", "lowbit_gemm_nvfp4", "lowbit_gemm_nvfp4_path",
+    "lowbit_draft_argmax", "lowbit_draft_argmax_path",
 ]
 
 

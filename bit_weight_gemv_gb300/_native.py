@@ -40,7 +40,9 @@ _SIGS = {
     "lowbit_nvfp4_packed_bytes": (_sz, [_i, _i]),
     "lowbit_pack_nvfp4": (_i, [_vp, _vp, ctypes.c_float, _i, _i, _vp, _vp]),
     "lowbit_gemm_nvfp4": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp]),
+    "lowbit_gemm_nvfp4_path": (_i, [_vp, _vp, _i, _i, _i, _vp, _i, _vp]),
     "lowbit_draft_argmax": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
+    "lowbit_draft_argmax_path": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _sz, _i, _vp]),
 }
 
 
@@ -231,8 +233,14 @@ def lowbit_gemm_nvfp4(X, packed, M, N, K, Y, stream=None):
            "lowbit_gemm_nvfp4")
 
 
-def lowbit_draft_argmax(H, packed_head, M, N, K, id_map, ids, workspace, stream=None):
-    """ids int32 [M] = id_map[argmax over the N rows of an NVFP4 draft head] (id_map may be None)."""
+def lowbit_gemm_nvfp4_path(X, packed, M, N, K, Y, path, stream=None):
+    """lowbit_gemm_nvfp4 with the kernel forced (1 = streaming mat-vec, M = 1; 2 = tensor cores)."""
+    _gemm_args(X, packed, M, N, K, Y)
+    _check(lib.lowbit_gemm_nvfp4_path(_ptr(X), _ptr(packed), M, N, K, _ptr(Y), path,
+                                      _stream(stream)), "lowbit_gemm_nvfp4_path")
+
+
+def _draft_args(H, packed_head, M, N, K, id_map, ids, workspace):
     _need(H, torch.bfloat16, "H")
     _need(packed_head, torch.uint8, "packed_head")
     _need(ids, torch.int32, "ids")
@@ -243,9 +251,22 @@ def lowbit_draft_argmax(H, packed_head, M, N, K, id_map, ids, workspace, stream=
             raise ValueError("id_map too small")
     if H.numel() < M * K or ids.numel() < M:
         raise ValueError("H or ids too small")
+
+
+def lowbit_draft_argmax(H, packed_head, M, N, K, id_map, ids, workspace, stream=None):
+    """ids int32 [M] = id_map[argmax over the N rows of an NVFP4 draft head] (id_map may be None)."""
+    _draft_args(H, packed_head, M, N, K, id_map, ids, workspace)
     _check(lib.lowbit_draft_argmax(_ptr(H), _ptr(packed_head), M, N, K, _ptr(id_map), _ptr(ids),
                                    _ptr(workspace), workspace.numel(), _stream(stream)),
            "lowbit_draft_argmax")
+
+
+def lowbit_draft_argmax_path(H, packed_head, M, N, K, id_map, ids, workspace, path, stream=None):
+    """lowbit_draft_argmax with the kernel forced (1 = streaming mat-vec, M = 1; 2 = tensor cores)."""
+    _draft_args(H, packed_head, M, N, K, id_map, ids, workspace)
+    _check(lib.lowbit_draft_argmax_path(_ptr(H), _ptr(packed_head), M, N, K, _ptr(id_map),
+                                        _ptr(ids), _ptr(workspace), workspace.numel(), path,
+                                        _stream(stream)), "lowbit_draft_argmax_path")
 
 
 def _lmhead_args(H, packed_head, M, K, draft, argmax, n_accept, bonus, workspace):

@@ -276,29 +276,57 @@ lowbit_status lowbit_gemm_sa_path(const uint16_t* X, const void* packed, int P, 
 
 lowbit_status lowbit_gemm_nvfp4(const uint16_t* X, const void* packed, int M, int N, int K,
                                 uint16_t* Y, void* stream) {
-  if (!X || !packed || !Y) return LOWBIT_ERR_INVALID_ARG;
+  return lowbit_gemm_nvfp4_path(X, packed, M, N, K, Y, 0, stream);
+}
+
+lowbit_status lowbit_gemm_nvfp4_path(const uint16_t* X, const void* packed, int M, int N, int K,
+                                     uint16_t* Y, int path, void* stream) {
+  if (!X || !packed || !Y || path < 0 || path > 2) return LOWBIT_ERR_INVALID_ARG;
   const lowbit_status st = check_shape(M, N, K, 32);
   if (st != LOWBIT_OK) return st;
+  if (path == 1 && M != 1) return LOWBIT_ERR_SHAPE;
   if (!aligned16(X) || !aligned16(packed)) return LOWBIT_ERR_ALIGN;
   int* err = device_error_word();
   if (!err) return LOWBIT_ERR_CUDA;
-  return from_cuda(launch_nvfp4_tc(X, static_cast<const uint8_t*>(packed), M, N, K, Y, err,
-                                   static_cast<cudaStream_t>(stream)));
+  const uint8_t* pk = static_cast<const uint8_t*>(packed);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (path == 0) path = M == 1 ? 1 : 2;
+  if (path == 1) {
+    GemvProblem p = {X, pk, Y, N, K, 0, 1, 0, 0, 0};
+    p.early = allocation_covers(pk, kHeaderBytes + nvfp4_payload_bytes(N, K)) ? 1 : 0;
+    return from_cuda(launch_nvfp4_stream(p, nullptr, nullptr, nullptr, err, s));
+  }
+  return from_cuda(launch_nvfp4_tc(X, pk, M, N, K, Y, err, s));
 }
 
 lowbit_status lowbit_draft_argmax(const uint16_t* H, const void* packed_head, int M, int N, int K,
                                   const int32_t* id_map, int32_t* ids, void* workspace,
                                   size_t ws_bytes, void* stream) {
-  if (!H || !packed_head || !ids) return LOWBIT_ERR_INVALID_ARG;
+  return lowbit_draft_argmax_path(H, packed_head, M, N, K, id_map, ids, workspace, ws_bytes, 0,
+                                  stream);
+}
+
+lowbit_status lowbit_draft_argmax_path(const uint16_t* H, const void* packed_head, int M, int N,
+                                       int K, const int32_t* id_map, int32_t* ids,
+                                       void* workspace, size_t ws_bytes, int path, void* stream) {
+  if (!H || !packed_head || !ids || path < 0 || path > 2) return LOWBIT_ERR_INVALID_ARG;
   const lowbit_status st = check_shape(M, N, K, 32);
   if (st != LOWBIT_OK) return st;
+  if (path == 1 && M != 1) return LOWBIT_ERR_SHAPE;
   if (!workspace || ws_bytes < lmhead_workspace_bytes(2, N, K)) return LOWBIT_ERR_WORKSPACE;
   if (!aligned16(H) || !aligned16(packed_head) || !aligned16(workspace)) return LOWBIT_ERR_ALIGN;
   int* err = device_error_word();
   if (!err) return LOWBIT_ERR_CUDA;
-  return from_cuda(launch_draft_argmax_tc(H, static_cast<const uint8_t*>(packed_head), M, N, K,
-                                          id_map, ids, workspace, err,
-                                          static_cast<cudaStream_t>(stream)));
+  const uint8_t* pk = static_cast<const uint8_t*>(packed_head);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (path == 0) path = M == 1 ? 1 : 2;
+  if (path == 1) {
+    GemvProblem p = {H, pk, nullptr, N, K, 0, 1, 0, 0, 0};
+    p.early = allocation_covers(pk, kHeaderBytes + nvfp4_payload_bytes(N, K)) ? 1 : 0;
+    return from_cuda(launch_nvfp4_stream(p, static_cast<LmheadWorkspace*>(workspace), id_map, ids,
+                                         err, s));
+  }
+  return from_cuda(launch_draft_argmax_tc(H, pk, M, N, K, id_map, ids, workspace, err, s));
 }
 
 lowbit_status lmhead_argmax_verify(const uint16_t* H, const void* packed_head, int M, int N,

@@ -172,6 +172,11 @@ cudaError_t launch_pack_sa(const uint8_t* bits, const uint8_t* codes, const uint
                            int G, int N, int K, uint8_t* packed, cudaStream_t s);
 cudaError_t launch_sa_cc(const uint16_t* X, const uint8_t* packed, int P, int G, int M, int N,
                          int K, uint16_t* Y, int* err, cudaStream_t s);
+struct LmheadWorkspace;
+// NVFP4 at M = 1 (one matrix): bf16 logits into prob.Y when ws is null, else the draft head's
+// id-mapped argmax (ids[0], workspace as lmhead_argmax_verify).
+cudaError_t launch_nvfp4_stream(const GemvProblem& prob, LmheadWorkspace* ws, const int32_t* id_map,
+                                int32_t* ids, int* err, cudaStream_t s);
 cudaError_t launch_pack_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, int N, int K,
                              uint8_t* packed, cudaStream_t s);
 cudaError_t launch_nvfp4_tc(const uint16_t* X, const uint8_t* packed, int M, int N, int K,

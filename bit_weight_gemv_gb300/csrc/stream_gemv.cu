@@ -32,6 +32,7 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "verify.cuh"
 
 namespace lowbit {
 namespace {
@@ -65,6 +66,9 @@ struct StreamArgs {
   int m;        // activation rows (INT4 kernel; 1 for the plane kernels)
   int cl_begin[kMaxGemvProblems];  // copy of p[i].cluster_begin
   int* err;
+  LmheadWorkspace* ws;     // NVFP4 draft head: argmax keys and CTA counter
+  const int32_t* id_map;   // NVFP4 draft head: full-vocabulary id per row (may be null)
+  int32_t* ids;            // NVFP4 draft head: out
   GemvProblem p[kMaxGemvProblems];
 };
 
@@ -72,6 +76,19 @@ __device__ __forceinline__ void grid_wait() { asm volatile("griddepcontrol.wait;
 __device__ __forceinline__ void grid_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+
+// Stage and phase parity of block b in a ring of S stages, advanced one block at a time (a
+// runtime division per block would cost more than the rest of a block's bookkeeping).
+struct RingPos {
+  int s;
+  uint32_t ph;
+  __device__ __forceinline__ void next(int S) {
+    if (++s == S) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+};
 
 // Two-way dot product: c + a.lo16 * b.byte0 + a.hi16 * b.byte1 (lo) or with bytes 2 and 3
 // (hi); a's halves signed, b's bytes unsigned.
@@ -84,6 +101,36 @@ __device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
   int d;
   asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
+}
+
+// Activation converter shared by the INT4 and NVFP4 kernels: the 128 bf16 activations of a
+// stage (lane l holds inputs 4l..4l+3 in `raw`) to int16 with one power-of-two scale per run
+// of 64 (lanes 0..15 and 16..31); returns the four int16 values (low 16 bits) and the run's
+// 2^-sh (NaN when the run holds a non-finite value).
+struct Converted {
+  uint32_t i0, i1, i2, i3;
+  float down;
+};
+__device__ __forceinline__ Converted convert_run64(uint2 raw, int lane) {
+  const uint32_t mag = max(max(raw.x & 0x7FFFu, (raw.x >> 16) & 0x7FFFu),
+                           max(raw.y & 0x7FFFu, (raw.y >> 16) & 0x7FFFu));
+  // |x| bits order as |x|
+  const uint32_t mlo = __reduce_max_sync(0xFFFFFFFFu, lane < 16 ? mag : 0u);
+  const uint32_t mhi = __reduce_max_sync(0xFFFFFFFFu, lane < 16 ? 0u : mag);
+  const uint32_t mmax = lane < 16 ? mlo : mhi;
+  const int e = max((int)(mmax >> 7), 1);  // biased exponent of the run's max |x|
+  const int sh = min(141 - e, 126);        // max |x| * 2^sh < 2^15
+  const float up = __int_as_float((127 + sh) << 23);
+  Converted c;
+  c.down = mmax >= 0x7F80u ? __int_as_float(0x7FC00000) : __int_as_float((127 - sh) << 23);
+  // x * 2^sh is exact; adding 1.5 * 2^23 rounds it to an integer (nearest, even on ties) and
+  // leaves that integer's two's complement in the low 16 bits.
+  constexpr float kRound = 12582912.f;
+  c.i0 = __float_as_uint(fmaf(__uint_as_float(raw.x << 16), up, kRound)) & 0xFFFFu;
+  c.i1 = __float_as_uint(fmaf(__uint_as_float(raw.x & 0xFFFF0000u), up, kRound)) & 0xFFFFu;
+  c.i2 = __float_as_uint(fmaf(__uint_as_float(raw.y << 16), up, kRound)) & 0xFFFFu;
+  c.i3 = __float_as_uint(fmaf(__uint_as_float(raw.y & 0xFFFF0000u), up, kRound)) & 0xFFFFu;
+  return c;
 }
 
 // MT: activation rows the kernel is built for (1, 2 or 4); a.m <= MT rows are present.  Each
@@ -176,9 +223,10 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
       grid_wait();  // the activations may be the previous kernel's output
       for (int b = 0; b < pre; ++b) copy_x(b, b, ptx::smem_addr(&full[b]));
       int issued = pre;
-      for (int b = pre; b < nb; ++b) {
-        const int s = b % S;
-        if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), ((b / S) - 1) & 1)) {
+      RingPos rp{pre % S, (uint32_t)(pre / S) & 1u};
+      for (int b = pre; b < nb; ++b, rp.next(S)) {
+        const int s = rp.s;
+        if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), rp.ph ^ 1u)) {
           record_error(a.err, LOWBIT_ERR_TIMEOUT);
           gave_up = 1;
           break;
@@ -202,10 +250,11 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
     // at.  Owning whole stages keeps each stage's phases in order for its one converter (a
     // parity wait can never meet a phase two behind), whatever the stage count.
     if (hdr_ok) {
-      for (int b = 0; b < nb; ++b) {
-        const int s = b % S;
+      RingPos rp{0, 0u};
+      for (int b = 0; b < nb; ++b, rp.next(S)) {
+        const int s = rp.s;
         if (s % conv_warps<MT>() != warp - kConvWarp) continue;
-        const bool landed = ptx::mbar_wait(ptx::smem_addr(&full[s]), (b / S) & 1);
+        const bool landed = ptx::mbar_wait(ptx::smem_addr(&full[s]), rp.ph);
         if (!__all_sync(0xFFFFFFFFu, landed)) {
           if (lane == 0) {
             record_error(a.err, LOWBIT_ERR_TIMEOUT);
@@ -219,24 +268,10 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
         // lane l holds inputs 4l..4l+3 (code word l/2, nibbles 4(l&1)..4(l&1)+3)
         const uint2 raw =
             reinterpret_cast<const uint2*>(ring + (size_t)s * STG + kInt4Block + m * kXBytes)[lane];
-        const uint32_t mag = max(max(raw.x & 0x7FFFu, (raw.x >> 16) & 0x7FFFu),
-                                 max(raw.y & 0x7FFFu, (raw.y >> 16) & 0x7FFFu));
-        // lanes 0..15 hold inputs 0..63, lanes 16..31 inputs 64..127; |x| bits order as |x|
-        const uint32_t mlo = __reduce_max_sync(0xFFFFFFFFu, lane < 16 ? mag : 0u);
-        const uint32_t mhi = __reduce_max_sync(0xFFFFFFFFu, lane < 16 ? 0u : mag);
-        const uint32_t mmax = lane < 16 ? mlo : mhi;
-        const int e = max((int)(mmax >> 7), 1);  // biased exponent of the half group's max |x|
-        const int sh = min(141 - e, 126);        // max |x| * 2^sh < 2^15
-        const float up = __int_as_float((127 + sh) << 23);
-        const float down = mmax >= 0x7F80u ? __int_as_float(0x7FC00000)
-                                           : __int_as_float((127 - sh) << 23);
-        // x * 2^sh is exact; adding 1.5 * 2^23 rounds it to an integer (nearest, even on ties)
-        // and leaves that integer's two's complement in the low 16 bits.
-        constexpr float kRound = 12582912.f;
-        const uint32_t i0 = __float_as_uint(fmaf(__uint_as_float(raw.x << 16), up, kRound)) & 0xFFFFu;
-        const uint32_t i1 = __float_as_uint(fmaf(__uint_as_float(raw.x & 0xFFFF0000u), up, kRound)) & 0xFFFFu;
-        const uint32_t i2 = __float_as_uint(fmaf(__uint_as_float(raw.y << 16), up, kRound)) & 0xFFFFu;
-        const uint32_t i3 = __float_as_uint(fmaf(__uint_as_float(raw.y & 0xFFFF0000u), up, kRound)) & 0xFFFFu;
+        // lanes 0..15 hold inputs 0..63, lanes 16..31 inputs 64..127
+        const Converted cv = convert_run64(raw, lane);
+        const uint32_t i0 = cv.i0, i1 = cv.i1, i2 = cv.i2, i3 = cv.i3;
+        const float down = cv.down;
         const int mine = (int)(int16_t)i0 + (int)(int16_t)i1 + (int)(int16_t)i2 + (int)(int16_t)i3;
         const int sum_lo = __reduce_add_sync(0xFFFFFFFFu, lane < 16 ? mine : 0);
         const int sum_hi = __reduce_add_sync(0xFFFFFFFFu, lane < 16 ? 0 : mine);
@@ -263,9 +298,10 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
     float total[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) total[m] = 0.f;
-    for (int b = 0; b < nb; ++b) {
-      const int s = b % S;
-      const bool ready = ptx::mbar_wait(ptx::smem_addr(&xready[s]), (b / S) & 1);
+    RingPos rp{0, 0u};
+    for (int b = 0; b < nb; ++b, rp.next(S)) {
+      const int s = rp.s;
+      const bool ready = ptx::mbar_wait(ptx::smem_addr(&xready[s]), rp.ph);
       if (!__all_sync(0xFFFFFFFFu, ready)) {  // warp-uniform exit keeps the warp converged
         if (lane == 0) {
           record_error(a.err, LOWBIT_ERR_TIMEOUT);
@@ -466,9 +502,10 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
         ptx::bulk_g2s(ptx::smem_addr(stage(b) + BB), xsrc + (size_t)b * KIN, XB,
                       ptx::smem_addr(&full[b]));
       int issued = pre;
-      for (int b = pre; b < nb; ++b) {
-        const int s = b % S;
-        if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), ((b / S) - 1) & 1)) {
+      RingPos rp{pre % S, (uint32_t)(pre / S) & 1u};
+      for (int b = pre; b < nb; ++b, rp.next(S)) {
+        const int s = rp.s;
+        if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), rp.ph ^ 1u)) {
           record_error(a.err, LOWBIT_ERR_TIMEOUT);
           gave_up = 1;
           break;
@@ -489,10 +526,11 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
     // with k0 = 32w + 8n (n < 4, even inputs) or 32w + 8(n - 4) + 1 (n >= 4, odd inputs).
     // Lane l tabulates sets l, l + 32, ... (one per 128 inputs of the block).
     if (hdr_ok) {
-      for (int b = 0; b < nb; ++b) {
-        if ((b % S) % kLutWarps != warp - kLutWarp) continue;  // this warp's stages only
-        const int s = b % S;
-        const bool landed = ptx::mbar_wait(ptx::smem_addr(&full[s]), (b / S) & 1);
+      RingPos rp{0, 0u};
+      for (int b = 0; b < nb; ++b, rp.next(S)) {
+        const int s = rp.s;
+        if (s % kLutWarps != warp - kLutWarp) continue;  // this warp's stages only
+        const bool landed = ptx::mbar_wait(ptx::smem_addr(&full[s]), rp.ph);
         if (!__all_sync(0xFFFFFFFFu, landed)) {
           if (lane == 0) {
             record_error(a.err, LOWBIT_ERR_TIMEOUT);
@@ -532,9 +570,10 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
     const int q = warp & 3, h = warp >> 2;
     const int row = 32 * q + lane;
     float total = 0.f;
-    for (int b = 0; b < nb; ++b) {
-      const int s = b % S;
-      const bool ready = ptx::mbar_wait(ptx::smem_addr(&tabready[s]), (b / S) & 1);
+    RingPos rp{0, 0u};
+    for (int b = 0; b < nb; ++b, rp.next(S)) {
+      const int s = rp.s;
+      const bool ready = ptx::mbar_wait(ptx::smem_addr(&tabready[s]), rp.ph);
       if (!__all_sync(0xFFFFFFFFu, ready)) {
         if (lane == 0) {
           record_error(a.err, LOWBIT_ERR_TIMEOUT);
@@ -637,6 +676,261 @@ sa_stream_kernel(const __grid_constant__ StreamArgs a) {
   plane_stream_body<true>(a);
 }
 
+// ------------------------------------------------------------------------------ NVFP4, M = 1
+// The trimmed draft head of the small-vocabulary MTP study (section 3.3) at one token: NVFP4
+// weights (E2M1 codes, an E4M3 scale per 16 inputs, an fp32 tensor scale g) streamed as the
+// INT4 kernel streams its blocks, against the same int16 activations.
+//
+// Decoding without tables: each code is taken as u = 2 * e2m1 + 12 in 0..24, found by two byte
+// permutes per four codes.  One permute selects from the eight u of the positive codes, whose
+// bytes are all below 0x80, so a code with its sign bit set -- which prmt reads as "replicate
+// the byte's sign" -- yields 0; the other permute does the same for the negative codes with
+// the sign bits flipped; their OR is u.  The integer dot product of a run of 16 is then
+// sum x * u - 12 * sum x, exact, and the run is scaled by its E4M3 scale in fp32.
+constexpr uint32_t kNvStage = kNvfp4Block + kXBytes;
+constexpr uint32_t kUPosLo = 0x0F0E0D0Cu, kUPosHi = 0x18141210u;  // 12 + {0,1,2,3 | 4,6,8,12}
+constexpr uint32_t kUNegLo = 0x090A0B0Cu, kUNegHi = 0x00040608u;  // 12 - {0,1,2,3 | 4,6,8,12}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// E4M3 byte -> its value times 2^-120, exactly: the byte's exponent and mantissa fields placed
+// in a float's bit positions give a float with exponent e - 127 (e >= 1) or the subnormal
+// m * 2^-129 (e = 0); 0x7F / 0xFF are NaN.
+__device__ __forceinline__ float e4m3_down120(uint32_t b) {
+  const uint32_t bits = ((b << 24) & 0x80000000u) | ((b & 0x7Fu) << 20);
+  return (b & 0x7Fu) == 0x7Fu ? __uint_as_float(0x7FC00000u) : __uint_as_float(bits);
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(stream_threads<1>())
+nvfp4_stream_kernel(const __grid_constant__ StreamArgs a) {
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ __align__(8) uint64_t full[kMaxStages];
+  __shared__ __align__(8) uint64_t xready[kMaxStages];
+  __shared__ __align__(8) uint64_t empty[kMaxStages];
+  __shared__ __align__(8) uint64_t redbar;
+  __shared__ __align__(16) uint32_t xq[kMaxStages][kGroup / 2];  // int16 pairs (X[2i], X[2i+1])
+  __shared__ float xdown[kMaxStages][2];                          // 2^-sh of inputs 0..63, 64..127
+  __shared__ __align__(16) int xsum[kMaxStages][kGroup / 16];      // sum X of each run of 16
+  __shared__ float red[kCWarps][32];
+  __shared__ float part[kRowTile];
+  __shared__ int ok;
+  __shared__ int gave_up;
+  __shared__ int hdr_valid;  // the whole grid agrees on it: every CTA reads the same header
+  __shared__ float gscale;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int C = a.cluster;
+  const int cid = (int)blockIdx.x / C, crank = (int)blockIdx.x % C;
+  const GemvProblem& pr = a.p[0];  // one matrix per launch
+  const int ks = pr.ks, rank = crank % ks;
+  const int tile = (cid - pr.cluster_begin) * (C / ks) + crank / ks;
+  const int G = pr.K / kGroup;
+  const bool live = tile < row_tiles(pr.N);
+  const int g0 = (int)((long long)rank * G / ks), g1 = (int)((long long)(rank + 1) * G / ks);
+  const int nb = live ? g1 - g0 : 0;
+  const int S = a.stages;
+  const PackedHeader* hp = reinterpret_cast<const PackedHeader*>(pr.packed);
+
+  if (threadIdx.x == 0) {
+    ok = live && (pr.early || header_matches(hp, kFormatNvfp4, 0, pr.N, pr.K));
+    gave_up = 0;
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&xready[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&empty[s]), kCWarps);
+    }
+    ptx::mbar_init(ptx::smem_addr(&redbar), (uint32_t)(kRowTile * (ks > 1 ? ks - 1 : 1)));
+    ptx::fence_mbar_init();
+  }
+  if (warp < kCWarps) red[warp][lane] = 0.f;
+  __syncthreads();
+  if (C > 1) ptx::cluster_arrive();
+  if (threadIdx.x == 0) grid_launch();
+  const bool hdr_ok = ok != 0;
+  if (threadIdx.x == 0) {
+    // every CTA, live or not, checks the header: the argmax epilogue's CTA count depends on it
+    hdr_valid = header_matches(hp, kFormatNvfp4, 0, pr.N, pr.K);
+    if (!hdr_valid) ok = 0;
+    gscale = __uint_as_float(__ldg(reinterpret_cast<const uint32_t*>(hp) + 14));
+  }
+
+  if (warp == kCWarps) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0 && hdr_ok) {
+      const uint8_t* wsrc = pr.packed + kHeaderBytes + ((size_t)tile * G + g0) * kNvfp4Block;
+      const uint16_t* xsrc = pr.X + (size_t)g0 * kGroup;
+      const int pre = min(nb, S);
+      for (int b = 0; b < pre; ++b) {
+        const uint32_t bar = ptx::smem_addr(&full[b]);
+        ptx::mbar_arrive_expect_tx(bar, kNvStage);
+        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)b * kNvStage), wsrc + (size_t)b * kNvfp4Block,
+                      kNvfp4Block, bar);
+      }
+      grid_wait();  // the activations may be the previous kernel's output
+      for (int b = 0; b < pre; ++b)
+        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)b * kNvStage + kNvfp4Block), xsrc + (size_t)b * kGroup,
+                      kXBytes, ptx::smem_addr(&full[b]));
+      int issued = pre;
+      RingPos rp{pre % S, (uint32_t)(pre / S) & 1u};
+      for (int b = pre; b < nb; ++b, rp.next(S)) {
+        const int s = rp.s;
+        if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), rp.ph ^ 1u)) {
+          record_error(a.err, LOWBIT_ERR_TIMEOUT);
+          gave_up = 1;
+          break;
+        }
+        const uint32_t bar = ptx::smem_addr(&full[s]);
+        ptx::mbar_arrive_expect_tx(bar, kNvStage);
+        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)s * kNvStage), wsrc + (size_t)b * kNvfp4Block,
+                      kNvfp4Block, bar);
+        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)s * kNvStage + kNvfp4Block),
+                      xsrc + (size_t)b * kGroup, kXBytes, bar);
+        issued = b + 1;
+      }
+      for (int b = max(0, issued - S); b < issued; ++b)
+        ptx::mbar_wait(ptx::smem_addr(&full[b % S]), (b / S) & 1);
+    }
+    __syncwarp();
+  } else if (warp >= kConvWarp) {
+    // ---------------------------------------------------------------- activation converters
+    // converter c owns the stages s with s % 2 == c (each stage's phases met in order)
+    if (hdr_ok) {
+      RingPos rp{0, 0u};
+      for (int b = 0; b < nb; ++b, rp.next(S)) {
+        const int s = rp.s;
+        if (s % conv_warps<1>() != warp - kConvWarp) continue;
+        const bool landed = ptx::mbar_wait(ptx::smem_addr(&full[s]), rp.ph);
+        if (!__all_sync(0xFFFFFFFFu, landed)) {
+          if (lane == 0) {
+            record_error(a.err, LOWBIT_ERR_TIMEOUT);
+            gave_up = 1;
+          }
+          break;
+        }
+        const uint2 raw = reinterpret_cast<const uint2*>(ring + (size_t)s * kNvStage + kNvfp4Block)[lane];
+        const Converted cv = convert_run64(raw, lane);
+        reinterpret_cast<uint2*>(xq[s])[lane] = make_uint2(cv.i0 | (cv.i1 << 16), cv.i2 | (cv.i3 << 16));
+        int sum = (int)(int16_t)cv.i0 + (int)(int16_t)cv.i1 + (int)(int16_t)cv.i2 + (int)(int16_t)cv.i3;
+        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+        if ((lane & 3) == 0) xsum[s][lane >> 2] = sum;
+        if ((lane & 15) == 0) xdown[s][lane >> 4] = cv.down;
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&xready[s]));
+      }
+    }
+  } else if (warp < kCWarps && hdr_ok) {
+    // ---------------------------------------------------------------- compute
+    // Warp (q, h): rows 32q..32q+31, inputs 64h..64h+63 (chunks 2h, 2h+1; scale runs 4h..4h+3)
+    const int q = warp & 3, h = warp >> 2;
+    const int row = 32 * q + lane;
+    float total = 0.f;
+    RingPos rp{0, 0u};
+    for (int b = 0; b < nb; ++b, rp.next(S)) {
+      const int s = rp.s;
+      const bool ready = ptx::mbar_wait(ptx::smem_addr(&xready[s]), rp.ph);
+      if (!__all_sync(0xFFFFFFFFu, ready)) {
+        if (lane == 0) {
+          record_error(a.err, LOWBIT_ERR_TIMEOUT);
+          gave_up = 1;
+        }
+        break;
+      }
+      const uint8_t* st = ring + (size_t)s * kNvStage;
+      const uint4 c0 = *reinterpret_cast<const uint4*>(st + (2 * h) * (kRowTile * 16) + row * 16);
+      const uint4 c1 = *reinterpret_cast<const uint4*>(st + (2 * h + 1) * (kRowTile * 16) + row * 16);
+      const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      const uint4* xw = reinterpret_cast<const uint4*>(xq[s]) + 8 * h;  // 4 pairs per code word
+      const int4 sx = *reinterpret_cast<const int4*>(&xsum[s][4 * h]);
+      const int sxs[4] = {sx.x, sx.y, sx.z, sx.w};
+      float sub = 0.f;  // sum over the four runs of 16: e4m3 * 2^-120 * (integer dot product)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        int acc0 = -12 * sxs[j], acc1 = 0;
+#pragma unroll
+        for (int i = 2 * j; i < 2 * j + 2; ++i) {
+          const uint32_t wf = w[i] ^ 0x88888888u;
+          const uint32_t lo = prmt(kUPosLo, kUPosHi, w[i]) | prmt(kUNegLo, kUNegHi, wf);
+          const uint32_t hi = prmt(kUPosLo, kUPosHi, w[i] >> 16) | prmt(kUNegLo, kUNegHi, wf >> 16);
+          const uint4 x = xw[i];
+          acc0 = dp2a_lo(x.x, lo, acc0);
+          acc1 = dp2a_hi(x.y, lo, acc1);
+          acc0 = dp2a_lo(x.z, hi, acc0);
+          acc1 = dp2a_hi(x.w, hi, acc1);
+        }
+        sub = fmaf(e4m3_down120(st[kNvfp4ScaleOff + (4 * h + j) * kRowTile + row]), (float)(acc0 + acc1), sub);
+      }
+      const float down = xdown[s][h];
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&empty[s]));
+      total = fmaf(0.5f * down, sub * 0x1p120f, total);  // u - 12 is 2 * e2m1
+    }
+    red[warp][lane] = total;
+  }
+
+  // -------------------------------------------------------------------- reduction + output
+  __syncthreads();
+  const bool out_ok = ok != 0;
+  if (!out_ok && live && threadIdx.x == 0 && rank == 0 && tile == 0)
+    record_error(a.err, LOWBIT_ERR_INVALID_ARG);
+  if (threadIdx.x < kRowTile) {
+    const int q = threadIdx.x >> 5, l = threadIdx.x & 31;
+    part[threadIdx.x] = red[q][l] + red[q + 4][l];
+  }
+  const int n = tile * kRowTile + (int)threadIdx.x;
+  if (C > 1) ptx::cluster_wait();
+  bool have = false;  // this thread holds row n's complete sum in y
+  float y = 0.f;
+  if (ks > 1) {
+    float* slots = reinterpret_cast<float*>(ring + (size_t)S * kNvStage);  // [ks-1][128]
+    const uint32_t owner = (uint32_t)(crank - rank);
+    if (live && threadIdx.x < kRowTile) {
+      if (rank != 0) {
+        // a CTA that gave up on a wait stays out of rank 0's shared memory
+        if (!gave_up) {
+          const uint32_t la = ptx::smem_addr(&slots[(rank - 1) * kRowTile + threadIdx.x]);
+          ptx::st_dsmem_f32(ptx::map_to_rank(la, owner), part[threadIdx.x]);
+          ptx::mbar_arrive_remote(ptx::map_to_rank(ptx::smem_addr(&redbar), owner));
+        }
+      } else {
+        const bool got = ptx::mbar_wait_cluster(ptx::smem_addr(&redbar), 0);
+        if (!got) record_error(a.err, LOWBIT_ERR_TIMEOUT);
+        y = part[threadIdx.x];
+        for (int r = 1; r < ks; ++r) y += slots[(r - 1) * kRowTile + threadIdx.x];
+        have = got && out_ok && n < pr.N;
+      }
+    }
+  } else {
+    __syncthreads();
+    if (threadIdx.x < kRowTile) {
+      y = part[threadIdx.x];
+      have = out_ok && n < pr.N;
+    }
+  }
+  y *= gscale;
+  if constexpr (EPI == 0) {
+    if (have) {
+      grid_wait();
+      pr.Y[n] = float_to_bf16_bits(y);
+    }
+  } else {
+    if (hdr_valid) {
+      grid_wait();  // the previous call on this workspace has reset it
+      if (warp < kRowTile / 32) {  // warps 0..3 hold the tile's rows
+        unsigned long long key = have ? argmax_key(y, n) : 0ull;
+        key = warp_max_u64(key);
+        if (lane == 0 && key) atomicMax(&a.ws->keys[0], key);
+      }
+      draft_finish(a.ws, 1, a.id_map, a.ids);
+    }
+  }
+}
+
 int sm_count() {
   int dev = 0, nsm = 148;
   cudaGetDevice(&dev);
@@ -725,7 +1019,7 @@ constexpr int kMaxDevices = 64;
 struct OptIns {
   std::atomic<unsigned char> done[kMaxDevices];
 };
-OptIns g_int4_optins[3], g_bp_optins, g_sa_optins;  // INT4: one per row count built
+OptIns g_int4_optins[3], g_bp_optins, g_sa_optins, g_nv_optins[2];  // one per kernel built
 
 template <typename Kernel>
 cudaError_t opt_in(Kernel kern, OptIns& o, size_t budget) {
@@ -822,6 +1116,28 @@ cudaError_t launch_bp_stream(const GemvProblem* probs, int count, int* err, cuda
   a.stages = sc.maxnb < S ? sc.maxnb : S;
   const size_t smem = (size_t)a.stages * stage + slots;
   return launch_streaming(bp_stream_kernel, g_bp_optins, kSmemBudget, a, sc, smem, kBpThreads, s);
+}
+
+cudaError_t launch_nvfp4_stream(const GemvProblem& prob, LmheadWorkspace* ws, const int32_t* id_map,
+                                int32_t* ids, int* err, cudaStream_t s) {
+  StreamArgs a = {};
+  Schedule sc;
+  if (!make_schedule(&prob, 1, kGroup, kInt4TargetBlocks, kMaxSplit, a, sc)) return cudaErrorInvalidValue;
+  a.err = err;
+  a.m = 1;
+  a.ws = ws;
+  a.id_map = id_map;
+  a.ids = ids;
+  const size_t slots = (size_t)(sc.kmax - 1) * kRowTile * sizeof(float);
+  int S = slots < kInt4SmemBudget ? (int)((kInt4SmemBudget - slots) / kNvStage) : 0;
+  S = S > kMaxStages ? kMaxStages : (S < 2 ? 2 : S);
+  S -= S % conv_warps<1>();
+  a.stages = sc.maxnb < S ? sc.maxnb : S;
+  const size_t smem = (size_t)a.stages * kNvStage + slots;
+  if (ws) return launch_streaming(nvfp4_stream_kernel<1>, g_nv_optins[1], kSmemBudget, a, sc, smem,
+                                  stream_threads<1>(), s);
+  return launch_streaming(nvfp4_stream_kernel<0>, g_nv_optins[0], kSmemBudget, a, sc, smem,
+                          stream_threads<1>(), s);
 }
 
 cudaError_t launch_sa_stream(const GemvProblem* probs, int count, int* err, cudaStream_t s) {

@@ -209,10 +209,11 @@ lowbit_status lowbit_gemm_binplane(const uint16_t* X, const void* packed, int P,
 lowbit_status lowbit_gemm_sa(const uint16_t* X, const void* packed, int P, int G, int M, int N,
                              int K, uint16_t* Y, void* stream);
 
-/* Y = X * W^T for NVFP4 weights (packed by lowbit_pack_nvfp4), 1 <= M <= 32, on the tensor
- * cores: each weight written to tensor memory as the exact bf16 of e2m1 * e4m3, g applied in
- * fp32 per output, each output rounded once to bf16.  (The draft step itself needs only the
- * argmax: lowbit_draft_argmax.) */
+/* Y = X * W^T for NVFP4 weights (packed by lowbit_pack_nvfp4), 1 <= M <= 32, g applied in fp32
+ * per output, each output rounded once to bf16.  M = 1 runs the streaming mat-vec (int16
+ * activations, as the INT4 kernel); M >= 2 the tensor cores (each weight written to tensor
+ * memory as the exact bf16 of e2m1 * e4m3).  (The draft step itself needs only the argmax:
+ * lowbit_draft_argmax, which chooses its kernel the same way.) */
 lowbit_status lowbit_gemm_nvfp4(const uint16_t* X, const void* packed, int M, int N, int K,
                                 uint16_t* Y, void* stream);
 
@@ -290,6 +291,15 @@ lowbit_status lmhead_argmax_verify_path(const uint16_t* H, const void* packed_he
 /* path 1 at M >= 2: CUDA-core kernel (sign select by XOR into the activation's sign bit). */
 lowbit_status lowbit_gemm_sa_path(const uint16_t* X, const void* packed, int P, int G, int M,
                                   int N, int K, uint16_t* Y, int path, void* stream);
+/* NVFP4: path 1 = the streaming mat-vec (M = 1 only; M > 1 returns LOWBIT_ERR_SHAPE), which
+ * reads each code byte through a table of the two codes' 2 * e2m1 values and takes integer dot
+ * products with block-scaled int16 activations, each run of 16 scaled by its e4m3 scale in
+ * fp32; path 2 = the tensor-core kernel.  The library's choice is path 1 at M = 1. */
+lowbit_status lowbit_gemm_nvfp4_path(const uint16_t* X, const void* packed, int M, int N, int K,
+                                     uint16_t* Y, int path, void* stream);
+lowbit_status lowbit_draft_argmax_path(const uint16_t* H, const void* packed_head, int M, int N,
+                                       int K, const int32_t* id_map, int32_t* ids,
+                                       void* workspace, size_t ws_bytes, int path, void* stream);
 
 /* ------------------------------------------------------------------------------------------
  * Device-side error word.

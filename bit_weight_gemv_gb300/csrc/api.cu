@@ -175,7 +175,7 @@ lowbit_status lowbit_gemm_int4(const uint16_t* X, const void* packed, int M, int
 
 lowbit_status lowbit_gemm_int4_path(const uint16_t* X, const void* packed, int M, int N, int K,
                                     uint16_t* Y, int path, void* stream) {
-  if (!X || !packed || !Y || path < 0 || path > 2) return LOWBIT_ERR_INVALID_ARG;
+  if (!X || !packed || !Y || path < 0 || path > 3) return LOWBIT_ERR_INVALID_ARG;
   lowbit_status st = check_shape(M, N, K, 32);
   if (st != LOWBIT_OK) return st;
   if (!aligned16(X) || !aligned16(packed)) return LOWBIT_ERR_ALIGN;
@@ -184,6 +184,11 @@ lowbit_status lowbit_gemm_int4_path(const uint16_t* X, const void* packed, int M
   const uint8_t* pk = static_cast<const uint8_t*>(packed);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (path == 0) path = (M <= kStreamDefaultRows) ? 1 : 2;
+  if (path == 3) {
+    GemvProblem p = {X, pk, Y, N, K, 0, 1, 0, 0};
+    p.early = allocation_covers(pk, kHeaderBytes + int4_payload_bytes(N, K)) ? 1 : 0;
+    return from_cuda(launch_int4_mma(&p, 1, M, err, s));
+  }
   if (path == 1 && M <= kStreamMaxRows) {
     GemvProblem p = {X, pk, Y, N, K, 0, 1, 0, 0};
     p.early = allocation_covers(pk, kHeaderBytes + int4_payload_bytes(N, K)) ? 1 : 0;
@@ -341,7 +346,7 @@ lowbit_status lmhead_argmax_verify_path(const uint16_t* H, const void* packed_he
                                         int K, const int32_t* draft, int32_t* argmax,
                                         int32_t* n_accept, int32_t* bonus, void* workspace,
                                         size_t ws_bytes, int path, void* stream) {
-  if (!H || !packed_head || !draft || !argmax || !n_accept || !bonus || path < 0 || path > 2)
+  if (!H || !packed_head || !draft || !argmax || !n_accept || !bonus || path < 0 || path > 3)
     return LOWBIT_ERR_INVALID_ARG;
   lowbit_status st = check_shape(M, N, K, 32);
   if (st != LOWBIT_OK) return st;
@@ -355,6 +360,12 @@ lowbit_status lmhead_argmax_verify_path(const uint16_t* H, const void* packed_he
   if (path == 1)
     return from_cuda(launch_lmhead_cc(H, pk, M, N, K, draft, argmax, n_accept, bonus, workspace,
                                       err, s));
+  if (path == 3) {
+    GemvProblem p = {H, pk, nullptr, N, K, 0, 1, 0, 0};
+    p.early = allocation_covers(pk, kHeaderBytes + int4_payload_bytes(N, K)) ? 1 : 0;
+    return from_cuda(launch_lmhead_mma(p, M, static_cast<LmheadWorkspace*>(workspace), draft,
+                                       argmax, n_accept, bonus, err, s));
+  }
   return from_cuda(launch_lmhead_tc(H, pk, M, N, K, draft, argmax, n_accept, bonus, workspace,
                                     err, s));
 }

@@ -164,6 +164,13 @@ cudaError_t launch_pack_binplane(const uint8_t* bits, const uint16_t* alpha, int
 constexpr int kStreamMaxRows = 4;
 constexpr int kStreamDefaultRows = 2;
 cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int M, int* err, cudaStream_t s);
+// M = 1..32 on the warp-level tensor-core MMA (streaming skeleton): Y of every problem, or
+// the LM-head verify epilogue (one problem; workspace as lmhead_argmax_verify).
+cudaError_t launch_int4_mma(const GemvProblem* probs, int count, int M, int* err, cudaStream_t s);
+struct LmheadWorkspace;
+cudaError_t launch_lmhead_mma(const GemvProblem& prob, int M, LmheadWorkspace* ws,
+                              const int32_t* draft, int32_t* argmax, int32_t* n_accept,
+                              int32_t* bonus, int* err, cudaStream_t s);
 // Binary-plane counterpart (M = 1); every problem carries its plane count P (1..8).
 cudaError_t launch_bp_stream(const GemvProblem* probs, int count, int* err, cudaStream_t s);
 // sa-format counterpart (M = 1); every problem carries P (1..8) and G (64, 128, 256).

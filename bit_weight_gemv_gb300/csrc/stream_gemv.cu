@@ -28,6 +28,7 @@
 // integer (below 2^24 in magnitude, so exact in fp32) is scaled by s * 2^-sh in fp32, and each
 // output is rounded once to bf16.  A half group holding a non-finite activation makes its
 // rows NaN.
+#include <algorithm>
 #include <atomic>
 
 #include "common.cuh"
@@ -68,7 +69,10 @@ struct StreamArgs {
   int* err;
   LmheadWorkspace* ws;     // NVFP4 draft head: argmax keys and CTA counter
   const int32_t* id_map;   // NVFP4 draft head: full-vocabulary id per row (may be null)
-  int32_t* ids;            // NVFP4 draft head: out
+  int32_t* ids;            // draft head: mapped ids out; LM-head verify: argmax out
+  const int32_t* draft;    // LM-head verify: draft tokens (M - 1)
+  int32_t* n_accept;       // LM-head verify: accepted prefix length out
+  int32_t* bonus;          // LM-head verify: the target's token after the prefix out
   GemvProblem p[kMaxGemvProblems];
 };
 
@@ -931,6 +935,284 @@ nvfp4_stream_kernel(const __grid_constant__ StreamArgs a) {
   }
 }
 
+// ------------------------------------------------------------------------------ warp MMA, M <= 32
+// The verify block (Efficient-Qwen report, section 2.2: the target checks a block of drafts
+// in one pass; block size 16) on the warp-level tensor-core MMA: mma.sync m16n8k16, bf16
+// operands, fp32 accumulation.  At this width a 16 x 8 output tile wastes no tensor work,
+// while a 128-row tcgen05 MMA with N = 16 issues as slowly as one with N = 64, which caps a
+// weight-streaming GEMM built on it near half of the HBM bandwidth.
+//
+// Same stream and schedule as the INT4 mat-vec.  A stage holds one (tile, group) block and
+// the group's activations of every row: two TMA tile loads of 64 inputs x MT rows with the
+// 128-byte swizzle (rows M..MT-1 zero-filled), so that the eight row addresses of an
+// ldmatrix fall in distinct banks; a copy per row would cost the copy engine more than the
+// block itself.  Compute warp w owns rows 16w..16w+15 of the tile: per 16
+// inputs lane (g, t) unpacks pair t of two code words of rows 16w+g and 16w+g+8 -- exactly
+// the A fragment of the MMA -- to exact bf16 q (the nibble ORed into bf16 128.0, minus 136),
+// loads the activations' B fragments with ldmatrix and issues one MMA per 8 activation rows.
+// After a group's 128 inputs it adds s * D to fp32 totals held in registers.
+constexpr uint32_t kMmaXOff = 9216;  // the activation tile starts 1024-aligned after the block
+constexpr int kMmaWarps = 8;
+constexpr int kMmaThreads = (kMmaWarps + 1) * 32;  // compute warps, producer
+// Occupancy is what hides the dequantisation's latency: about 50 KB of shared memory per CTA
+// keeps four CTAs (MT = 16; three for MT = 32, by registers) on an SM.
+template <int MT> __host__ __device__ constexpr int mma_resident() { return MT == 16 ? 4 : 3; }
+constexpr size_t kMmaSmemBudget = 56 * 1024;
+
+// Activations of every matrix of a launch as TMA tensor maps ([M][K] bf16, boxes of 64 inputs
+// x MT rows); the maps precede the arguments shared with the other streaming kernels.
+struct MmaArgs {
+  CUtensorMap xmap[kMaxGemvProblems];
+  StreamArgs s;
+};
+constexpr int kEpiStore = 0, kEpiVerify = 1;
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ uint32_t bf16x2_sub_rn(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// Nibbles 0 and 4 of a code word (the pair k, k+1 at bits 0..3 and 16..19) -> bf16 pair (q, q+1)
+// exactly: 128 + u in bf16, minus 136.
+__device__ __forceinline__ uint32_t q_pair(uint32_t w) {
+  return bf16x2_sub_rn((w & 0x000F000Fu) | 0x43004300u, 0x43084308u);
+}
+
+template <int MT, int EPI>
+__global__ void __launch_bounds__(kMmaThreads, mma_resident<MT>())
+int4_mma_kernel(const __grid_constant__ MmaArgs A) {
+  constexpr uint32_t STG = kMmaXOff + MT * 2 * 128;  // block, then two 64-input atoms of X
+  constexpr int NT = MT / 8;  // MMA output tiles of 8 activation rows
+  const StreamArgs& a = A.s;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  // the 128-byte swizzle wants 1024-byte aligned tiles
+  uint8_t* ring = smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u);
+  __shared__ __align__(8) uint64_t full[kMaxStages];
+  __shared__ __align__(8) uint64_t empty[kMaxStages];
+  __shared__ int ok;
+  __shared__ int gave_up;
+  __shared__ int hdr_valid;  // the same in every CTA: they all read the one header
+  // Totals [MT][128], written once every stage has been consumed: they reuse the ring (at
+  // least two stages, 25 KB).  After a timed-out wait a late copy may still land there; the
+  // outputs are wrong then anyway and the error word says so.
+  float (*part)[kRowTile] = reinterpret_cast<float (*)[kRowTile]>(ring);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int C = a.cluster;
+  const int cid = (int)blockIdx.x / C, crank = (int)blockIdx.x % C;
+  int pi = 0;
+  for (int i = 1; i < a.count; ++i)
+    if (cid >= a.cl_begin[i]) pi = i;
+  const GemvProblem& pr = a.p[pi];
+  const int ks = pr.ks, rank = crank % ks;
+  const int tile = (cid - pr.cluster_begin) * (C / ks) + crank / ks;
+  const int G = pr.K / kGroup;
+  const bool live = tile < row_tiles(pr.N);
+  const int g0 = (int)((long long)rank * G / ks), g1 = (int)((long long)(rank + 1) * G / ks);
+  const int nb = live ? g1 - g0 : 0;
+  const int S = a.stages, M = a.m;
+  const PackedHeader* hp = reinterpret_cast<const PackedHeader*>(pr.packed);
+
+  if (threadIdx.x == 0) {
+    ok = live && (pr.early || header_matches(hp, kFormatInt4, 0, pr.N, pr.K));
+    gave_up = 0;
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&empty[s]), kMmaWarps);
+    }
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) grid_launch();
+  const bool hdr_ok = ok != 0;  // with `early`: only "this CTA has work"; see out_ok below
+  if (threadIdx.x == 32) {  // a compute warp checks the header; the producer does not wait on it
+    const bool hv = header_matches(hp, kFormatInt4, 0, pr.N, pr.K);
+    hdr_valid = hv;
+    if (!hv) ok = 0;
+  }
+
+  if (warp == kMmaWarps) {
+    // ---------------------------------------------------------------- producer
+    if (hdr_ok && lane == 0) {
+      const uint8_t* wsrc = pr.packed + kHeaderBytes + ((size_t)tile * G + g0) * kInt4Block;
+      const CUtensorMap* xmap = &A.xmap[pi];
+      constexpr uint32_t tx = kInt4Block + MT * 2 * 128;  // zero-filled rows count as copied
+      auto copy_x = [&](int b, int s, uint32_t bar) {
+        const uint32_t dst = ptx::smem_addr(ring + (size_t)s * STG + kMmaXOff);
+        ptx::tma_load_2d(dst, xmap, (g0 + b) * kGroup, 0, bar);
+        ptx::tma_load_2d(dst + MT * 128, xmap, (g0 + b) * kGroup + 64, 0, bar);
+      };
+      const int pre = min(nb, S);
+      for (int b = 0; b < pre; ++b) {
+        const uint32_t bar = ptx::smem_addr(&full[b]);
+        ptx::mbar_arrive_expect_tx(bar, tx);
+        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)b * STG), wsrc + (size_t)b * kInt4Block,
+                      kInt4Block, bar);
+      }
+      grid_wait();  // the activations may be the previous kernel's output
+      for (int b = 0; b < pre; ++b) copy_x(b, b, ptx::smem_addr(&full[b]));
+      int issued = pre;
+      RingPos rp{pre % S, (uint32_t)(pre / S) & 1u};
+      for (int b = pre; b < nb; ++b, rp.next(S)) {
+        const int s = rp.s;
+        if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), rp.ph ^ 1u)) {
+          record_error(a.err, LOWBIT_ERR_TIMEOUT);
+          gave_up = 1;
+          break;
+        }
+        const uint32_t bar = ptx::smem_addr(&full[s]);
+        ptx::mbar_arrive_expect_tx(bar, tx);
+        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)s * STG), wsrc + (size_t)b * kInt4Block,
+                      kInt4Block, bar);
+        copy_x(b, s, bar);
+        issued = b + 1;
+      }
+      // copies still in flight must land before the CTA may exit
+      for (int b = max(0, issued - S); b < issued; ++b)
+        ptx::mbar_wait(ptx::smem_addr(&full[b % S]), (b / S) & 1);
+    }
+    __syncwarp();
+  } else if (hdr_ok) {
+    // ---------------------------------------------------------------- compute
+    const int g = lane >> 2, t = lane & 3;
+    const int r0 = 16 * warp + g;  // rows r0 and r0 + 8 of the tile
+    // ldmatrix row of this lane: matrix lane/8 takes activation rows +8 and inputs +8.  In a
+    // swizzled atom, 16-byte chunk c of row n sits at chunk c ^ (n % 8); the chunks a step
+    // reads are 2 * (step % 4) + (inputs +8), so xsw[i] is the lane's address for step i % 4.
+    const int xn = (lane & 7) + ((lane >> 4) << 3), xu = ((lane >> 3) & 1) ^ (lane & 7);
+    uint32_t xsw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) xsw[i] = (uint32_t)(xn * 128 + (((2 * i) ^ xu) << 4));
+    float acc[NT][4];
+#pragma unroll
+    for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    RingPos rp{0, 0u};
+    for (int b = 0; b < nb; ++b, rp.next(S)) {
+      const int s = rp.s;
+      const bool landed = ptx::mbar_wait(ptx::smem_addr(&full[s]), rp.ph);
+      if (!__all_sync(0xFFFFFFFFu, landed)) {
+        if (lane == 0) {
+          record_error(a.err, LOWBIT_ERR_TIMEOUT);
+          gave_up = 1;
+        }
+        break;
+      }
+      const uint8_t* st = ring + (size_t)s * STG;
+      const uint32_t xs = ptx::smem_addr(st + kMmaXOff);
+      float d[NT][4];
+#pragma unroll
+      for (int i = 0; i < NT; ++i) d[i][0] = d[i][1] = d[i][2] = d[i][3] = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {  // 32-input chunks
+        const uint4 w0 = *reinterpret_cast<const uint4*>(st + c * (kRowTile * 16) + r0 * 16);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(st + c * (kRowTile * 16) + (r0 + 8) * 16);
+        // word i holds inputs 8i..8i+7 of the chunk; pair t of it (inputs 8i+2t, 8i+2t+1) is
+        // this lane's share, shifted down to nibble 0
+        const uint32_t u0[4] = {w0.x >> (4 * t), w0.y >> (4 * t), w0.z >> (4 * t), w0.w >> (4 * t)};
+        const uint32_t u1[4] = {w1.x >> (4 * t), w1.y >> (4 * t), w1.z >> (4 * t), w1.w >> (4 * t)};
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {  // 16-input steps
+          const uint32_t a0 = q_pair(u0[2 * j]), a1 = q_pair(u1[2 * j]);
+          const uint32_t a2 = q_pair(u0[2 * j + 1]), a3 = q_pair(u1[2 * j + 1]);
+#pragma unroll
+          for (int hh = 0; hh < MT / 16; ++hh) {
+            uint32_t b0, b1, b2, b3;
+            // step 2c + j: atom c / 2, chunks 4 (c % 2) + 2j (+1)
+            ldsm_x4(xs + xsw[(2 * c + j) & 3] + (c >> 1) * (MT * 128) + hh * 16 * 128, b0, b1, b2, b3);
+            mma_16816(d[2 * hh], a0, a1, a2, a3, b0, b1);
+            mma_16816(d[2 * hh + 1], a0, a1, a2, a3, b2, b3);
+          }
+        }
+      }
+      const float s0 = half_bits_to_float(*reinterpret_cast<const uint16_t*>(st + kInt4ScaleOff + r0 * 2));
+      const float s1 = half_bits_to_float(*reinterpret_cast<const uint16_t*>(st + kInt4ScaleOff + (r0 + 8) * 2));
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&empty[s]));
+#pragma unroll
+      for (int i = 0; i < NT; ++i) {
+        acc[i][0] = fmaf(s0, d[i][0], acc[i][0]);
+        acc[i][1] = fmaf(s0, d[i][1], acc[i][1]);
+        acc[i][2] = fmaf(s1, d[i][2], acc[i][2]);
+        acc[i][3] = fmaf(s1, d[i][3], acc[i][3]);
+      }
+    }
+    // every warp has read its last stage before any total lands on the ring
+    ptx::named_barrier(1, kMmaWarps * 32);
+    // D element (row g | g + 8, column 2t | 2t + 1) of tile i: weight row r0 | r0 + 8,
+    // activation row 8i + 2t | 8i + 2t + 1
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+      part[8 * i + 2 * t][r0] = acc[i][0];
+      part[8 * i + 2 * t + 1][r0] = acc[i][1];
+      part[8 * i + 2 * t][r0 + 8] = acc[i][2];
+      part[8 * i + 2 * t + 1][r0 + 8] = acc[i][3];
+    }
+  }
+
+  // -------------------------------------------------------------------- reduction + output
+  // The ks CTAs of a split tile reduce through distributed shared memory: rank r reads rows
+  // r*128/ks .. (r+1)*128/ks - 1 of every peer's totals and finishes them.  Both cluster
+  // barriers are reached by every CTA (its own waits are bounded), the second one keeping
+  // each CTA's totals alive until its peers have read them.
+  __syncthreads();
+  const bool out_ok = ok != 0;
+  if (!out_ok && live && threadIdx.x == 0 && rank == 0 && tile == 0)
+    record_error(a.err, LOWBIT_ERR_INVALID_ARG);
+  const bool owner_thread = threadIdx.x < kMmaWarps * 32;
+  if (C > 1) ptx::cluster_sync();
+  const bool verify = EPI == kEpiVerify && hdr_valid;
+  if (live && out_ok && owner_thread) {
+    grid_wait();  // outputs and the verify workspace belong to the previous kernel until now
+    const int rows = kRowTile / ks, rbase = rank * rows;
+    const uint32_t base = (uint32_t)(crank - rank);  // rank 0 of this tile
+    for (int i0 = 0; i0 < rows * MT; i0 += kMmaWarps * 32) {  // the same trip count in every lane
+      const int idx = i0 + (int)threadIdx.x;
+      const int m = idx / rows, row = rbase + idx % rows;
+      const int n = tile * kRowTile + row;
+      const bool in = idx < rows * MT && m < M && n < pr.N;
+      float y = 0.f;
+      if (in) {
+        if (ks == 1) {
+          y = part[m][row];
+        } else {
+          const uint32_t la = ptx::smem_addr(&part[m][row]);
+          for (int q = 0; q < ks; ++q) y += ptx::ld_dsmem_f32(la, base + (uint32_t)q);
+        }
+      }
+      if constexpr (EPI == kEpiStore) {
+        if (in) pr.Y[(size_t)m * pr.N + n] = float_to_bf16_bits(y);
+      } else {
+        unsigned long long key = in ? argmax_key(y, n) : 0ull;
+        if (rows >= 32) {  // a warp's 32 values share one activation row
+          key = warp_max_u64(key);
+          if (lane == 0 && key) atomicMax(&a.ws->keys[min(m, 31)], key);
+        } else if (key) {
+          atomicMax(&a.ws->keys[m], key);
+        }
+      }
+    }
+  }
+  if (C > 1) ptx::cluster_sync();
+  if (verify) {
+    grid_wait();
+    lmhead_finish(a.ws, M, a.draft, a.ids, a.n_accept, a.bonus);
+  }
+}
+
 int sm_count() {
   int dev = 0, nsm = 148;
   cudaGetDevice(&dev);
@@ -950,7 +1232,7 @@ struct Schedule {
 };
 
 bool make_schedule(const GemvProblem* probs, int count, int kin, int target, int max_split,
-                   StreamArgs& a, Schedule& out) {
+                   StreamArgs& a, Schedule& out, int resident_per_sm = kResidentPerSm) {
   const int nsm = sm_count();
   int ks[kMaxGemvProblems];
   long long ctas = 0;
@@ -963,7 +1245,7 @@ bool make_schedule(const GemvProblem* probs, int count, int kin, int target, int
   }
   // Double every split while the doubled grid still fits the SMs' resident capacity: more
   // concurrent streams, each with fewer blocks.
-  const long long resident = (long long)kResidentPerSm * nsm;
+  const long long resident = (long long)resident_per_sm * nsm;
   for (bool grew = true; grew;) {
     grew = false;
     long long next = 0;
@@ -1019,7 +1301,7 @@ constexpr int kMaxDevices = 64;
 struct OptIns {
   std::atomic<unsigned char> done[kMaxDevices];
 };
-OptIns g_int4_optins[3], g_bp_optins, g_sa_optins, g_nv_optins[2];  // one per kernel built
+OptIns g_int4_optins[3], g_bp_optins, g_sa_optins, g_nv_optins[2], g_mma_optins[4];  // one per kernel built
 
 template <typename Kernel>
 cudaError_t opt_in(Kernel kern, OptIns& o, size_t budget) {
@@ -1033,8 +1315,8 @@ cudaError_t opt_in(Kernel kern, OptIns& o, size_t budget) {
   return e;
 }
 
-template <typename Kernel>
-cudaError_t launch_streaming(Kernel kern, OptIns& o, size_t budget, const StreamArgs& a,
+template <typename Kernel, typename Args>
+cudaError_t launch_streaming(Kernel kern, OptIns& o, size_t budget, const Args& a,
                              const Schedule& sc, size_t smem, int threads, cudaStream_t s) {
   if (smem > budget) return cudaErrorInvalidValue;
   cudaError_t e = opt_in(kern, o, budget);
@@ -1091,6 +1373,81 @@ cudaError_t launch_int4_stream_mt(const GemvProblem* probs, int count, int M, in
 }
 
 }  // namespace
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 x_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+template <int MT, int EPI>
+cudaError_t launch_int4_mma_mt(const GemvProblem* probs, int count, int M, LmheadWorkspace* ws,
+                               const int32_t* draft, int32_t* argmax, int32_t* n_accept,
+                               int32_t* bonus, int* err, cudaStream_t s) {
+  constexpr uint32_t stage = kMmaXOff + MT * 2 * 128;
+  auto encode = x_map_encoder();
+  if (!encode) return cudaErrorNotSupported;
+  MmaArgs A = {};
+  StreamArgs& a = A.s;
+  Schedule sc;
+  if (!make_schedule(probs, count, kGroup, kInt4TargetBlocks, kMaxSplit, a, sc, mma_resident<MT>()))
+    return cudaErrorInvalidValue;
+  a.err = err;
+  a.m = M;
+  a.ws = ws;
+  a.draft = draft;
+  a.ids = argmax;
+  a.n_accept = n_accept;
+  a.bonus = bonus;
+  for (int i = 0; i < a.count; ++i) {
+    // X [M][K] bf16 as matrix i's activations (in schedule order); rows >= M read as zero
+    cuuint64_t dims[2] = {(cuuint64_t)a.p[i].K, (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)a.p[i].K * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)MT};
+    cuuint32_t estr[2] = {1, 1};
+    if (encode(&A.xmap[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(a.p[i].X),
+               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  int S = (int)((kMmaSmemBudget - 1024) / stage);
+  S = S > kMaxStages ? kMaxStages : (S < 2 ? 2 : S);
+  a.stages = sc.maxnb < S ? sc.maxnb : S;
+  // the totals [MT][128] reuse the ring; 1 KB of slack aligns the ring
+  const size_t smem = std::max((size_t)a.stages * stage, (size_t)MT * kRowTile * sizeof(float)) + 1024;
+  constexpr int slot_i = (MT == 16 ? 0 : 1) + 2 * EPI;
+  return launch_streaming(int4_mma_kernel<MT, EPI>, g_mma_optins[slot_i], kMmaSmemBudget, A, sc,
+                          smem, kMmaThreads, s);
+}
+
+}  // namespace
+
+cudaError_t launch_int4_mma(const GemvProblem* probs, int count, int M, int* err, cudaStream_t s) {
+  if (count < 1 || count > kMaxGemvProblems || M < 1 || M > 32) return cudaErrorInvalidValue;
+  if (M <= 16)
+    return launch_int4_mma_mt<16, kEpiStore>(probs, count, M, nullptr, nullptr, nullptr, nullptr,
+                                             nullptr, err, s);
+  return launch_int4_mma_mt<32, kEpiStore>(probs, count, M, nullptr, nullptr, nullptr, nullptr,
+                                           nullptr, err, s);
+}
+
+cudaError_t launch_lmhead_mma(const GemvProblem& prob, int M, LmheadWorkspace* ws,
+                              const int32_t* draft, int32_t* argmax, int32_t* n_accept,
+                              int32_t* bonus, int* err, cudaStream_t s) {
+  if (M < 1 || M > 32) return cudaErrorInvalidValue;
+  if (M <= 16)
+    return launch_int4_mma_mt<16, kEpiVerify>(&prob, 1, M, ws, draft, argmax, n_accept, bonus, err, s);
+  return launch_int4_mma_mt<32, kEpiVerify>(&prob, 1, M, ws, draft, argmax, n_accept, bonus, err, s);
+}
 
 cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int M, int* err, cudaStream_t s) {
   if (count < 1 || count > kMaxGemvProblems || M < 1 || M > kStreamMaxRows) return cudaErrorInvalidValue;

@@ -54,7 +54,8 @@ def gemm_bp_gpu(lb, x, packed, P, M, N, K, path=0):
     return host_bits(Y)
 
 
-PATHS = (1, 2)   # 1 = CUDA-core kernels, 2 = tensor-core kernels
+PATHS = (1, 2)   # 1 = CUDA-core kernels, 2 = tensor-core kernels (tcgen05)
+INT4_PATHS = (1, 2, 3)   # INT4 and the LM head also: 3 = warp-level MMA kernels
 
 
 # ------------------------------------------------------------------------- packing
@@ -85,7 +86,7 @@ def test_pack_binplane_bit_exact(lb, P, N, K):
 
 # ------------------------------------------------------------------------- INT4 GEMV / GEMM
 
-@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("path", INT4_PATHS)
 @pytest.mark.parametrize("M,N,K", [(1, 256, 512), (1, 257, 384), (1, 1, 128), (1, 8, 1024),
                                    (1, 100, 12288), (2, 96, 256), (3, 65, 640), (16, 300, 1280),
                                    (32, 33, 384), (5, 1, 128), (17, 129, 2048), (16, 2000, 256)])
@@ -99,7 +100,7 @@ def test_int4_small_and_ragged(lb, M, N, K, path):
 ACT_SCALE = {"tiny": 2.0 ** 90, "huge": 2.0 ** -90}
 
 
-@pytest.mark.parametrize("M,path", [(1, 1), (16, 1), (16, 2)])
+@pytest.mark.parametrize("M,path", [(1, 1), (16, 1), (16, 2), (16, 3), (32, 3)])
 @pytest.mark.parametrize("kind", synth.ACTIVATION_KINDS)
 def test_int4_activation_structures(lb, kind, M, path):
     """Outlier channels, per-run magnitude swings, extreme exponents, zeros and sparsity: the
@@ -114,7 +115,7 @@ def test_int4_activation_structures(lb, kind, M, path):
                scale=ACT_SCALE.get(kind, 1.0))
 
 
-@pytest.mark.parametrize("M,path", [(1, 1), (16, 1), (16, 2)])
+@pytest.mark.parametrize("M,path", [(1, 1), (16, 1), (16, 2), (16, 3), (32, 3)])
 def test_int4_nan_activation(lb, M, path):
     """A NaN activation in token 0 makes token 0's outputs NaN and leaves the others exact."""
     N, K = 300, 640
@@ -165,7 +166,7 @@ def test_int4_config0_tiny_gemv(lb):
     check_gemm(y, oint4.gemm(x, codes, scales), "config 0")
 
 
-@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("path", INT4_PATHS)
 @pytest.mark.parametrize("proj", range(7))
 def test_int4_config1_decode_layer(lb, proj, path):
     cfg = synth.CONFIGS[1]
@@ -175,7 +176,7 @@ def test_int4_config1_decode_layer(lb, proj, path):
     check_gemm(y, oint4.gemm(x, codes, scales), f"config 1 proj {proj} path={path}")
 
 
-@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("path", INT4_PATHS)
 @pytest.mark.parametrize("M", synth.M_SWEEP)
 @pytest.mark.parametrize("proj", [0, 1, 6])
 def test_int4_config2_verify_sweep(lb, proj, M, path):
@@ -244,7 +245,7 @@ def check_lmhead(a, n, b, logits, drafts, j, what):
         assert n == j, what
 
 
-@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("path", INT4_PATHS)
 @pytest.mark.parametrize("rows", synth.HEAD_ROWS)
 def test_lmhead_config4(lb, rows, path):
     cfg = synth.CONFIGS[4]
@@ -262,7 +263,7 @@ def test_lmhead_config4(lb, rows, path):
     assert int(ws.sum().item()) == 0
 
 
-@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("path", INT4_PATHS)
 @pytest.mark.parametrize("M,N,K", [(2, 40, 128), (16, 1000, 512), (32, 257, 256), (7, 5, 128),
                                    (16, 300, 2048)])
 def test_lmhead_small_and_planted(lb, M, N, K, path):
@@ -283,7 +284,7 @@ def test_lmhead_small_and_planted(lb, M, N, K, path):
 
 # ------------------------------------------------------------------------- error paths
 
-@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("path", INT4_PATHS)
 def test_header_mismatch_is_recorded_and_nothing_written(lb, path):
     codes, scales, x = synth.int4_problem(1, 1, 64, 256)
     packed = pack_int4_gpu(lb, codes, scales)
@@ -295,7 +296,7 @@ def test_header_mismatch_is_recorded_and_nothing_written(lb, path):
     assert lb.lowbit_device_error() == 0                        # cleared by the read
 
 
-@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("path", INT4_PATHS)
 def test_header_mismatch_beyond_the_allocation(lb, path):
     """A claimed shape whose payload cannot lie inside the buffer's allocation: the kernels
     check the header before reading any weight, record the mismatch and write nothing."""

@@ -206,7 +206,7 @@ LAYER_GROUPS = {"deps": ((0, 1, 2), (3,), (4, 5), (6,)), "all": ((0, 1, 2, 3, 4,
 
 def build_int4_layer(lb, torch, l2, M, path, seed, name, desc, grouping=None):
     w = Workload(name, desc, "int4_stream_kernel" if ((M <= 2 and path == 0) or (M <= 4 and path == 1))
-                 else ("int4_gemm_cc_kernel" if path == 1 else "tc_gemm_kernel"))
+                 else {1: "int4_gemm_cc_kernel", 2: "tc_gemm_kernel"}.get(path, "int4_mma_kernel"))
     shapes = [(k, n) for _, k, n in synth.LAYER_4B]
     w.bytes = sum(algorithmic_int4_bytes(N, K) for K, N in shapes)
     C = copies_for(w.bytes, l2)
@@ -226,8 +226,9 @@ def build_int4_layer(lb, torch, l2, M, path, seed, name, desc, grouping=None):
     else:
         groups = LAYER_GROUPS[grouping]
         for c in range(C):
-            w.calls.append([(lambda grp=grp, c=c: lb.lowbit_gemm_int4_grouped(
-                [(X[j], packs[j][c], shapes[j][1], shapes[j][0], Y[j]) for j in grp], M))
+            w.calls.append([(lambda grp=grp, c=c: lb.lowbit_gemm_int4_grouped_path(
+                [(X[j], packs[j][c], shapes[j][1], shapes[j][0], Y[j]) for j in grp], M,
+                path if (path != 1 or M <= 4) else 0))
                 for grp in groups])
         w.launches = len(groups)
     w.M, w.tokens = M, M
@@ -295,7 +296,7 @@ def build_draft_head(lb, torch, l2, M, name, desc):
 
 def build_lmhead(lb, torch, l2, N, path, name, desc):
     M, K = synth.VERIFY_BLOCK, synth.HEAD_K
-    w = Workload(name, desc, "tc_gemm_kernel" if path != 1 else "int4_gemm_cc_kernel")
+    w = Workload(name, desc, {1: "int4_gemm_cc_kernel", 2: "tc_gemm_kernel"}.get(path, "int4_mma_kernel"))
     codes, scales, h = synth.int4_problem(4, M, N, K)
     p = torch.empty(lb.lowbit_int4_packed_bytes(N, K), dtype=torch.uint8, device="cuda")
     lb.lowbit_pack_int4(dev(codes), f16_dev(scales), N, K, p)
@@ -575,7 +576,8 @@ def run_ours(args):
     rows = {}
     if not args.no_rows and rank == 0:
         names = [(n, 0) for n in WORKLOADS if n not in (args.workload, "tiny")]
-        names += [("decode", 2), ("binplane_m1", 1), ("binplane_m1", 2)]
+        names += [("decode", 2), ("binplane_m1", 1), ("binplane_m1", 2), ("verify_all", 2),
+                  ("lmhead_full", 2)]
         names = [nm for nm in names if nm != (args.workload, args.path)]
         rows = measure_rows(lb, torch, peak, l2, names)
 
@@ -681,8 +683,9 @@ def main():
     ap.add_argument("--no-rows", action="store_true", help="skip the secondary rows")
     ap.add_argument("--workload", choices=WORKLOADS, default="decode_deps",
                     help="timed step (default: decode through one 4B-class layer, M=1)")
-    ap.add_argument("--path", type=int, choices=(0, 1, 2), default=0,
-                    help="kernel family: 0 library choice, 1 CUDA cores, 2 tensor cores")
+    ap.add_argument("--path", type=int, choices=(0, 1, 2, 3), default=0,
+                    help="kernel family: 0 library choice, 1 CUDA cores, 2 tcgen05, 3 warp MMA "
+                         "(INT4 and the LM head)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing")
     args = ap.parse_args()
     if args.warmup < 3:

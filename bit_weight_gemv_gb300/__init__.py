@@ -14,7 +14,7 @@ __all__ = [
     "lowbit_gemm_int4", "lowbit_int4_packed_bytes", "lowbit_pack_binplane", "lowbit_pack_int4",
     "lowbit_status_string", "lowbit_validate_packed", "lowbit_version",
     "lowbit_gemm_int4_path", "lowbit_gemm_binplane_path", "lmhead_argmax_verify_path",
-    "lowbit_gemm_int4_grouped", "lowbit_gemm_desc", "lmhead_argmax_verify_noalloc",
+    "lowbit_gemm_int4_grouped", "lowbit_gemm_int4_grouped_path", "lowbit_gemm_desc", "lmhead_argmax_verify_noalloc",
     "lowbit_sa_packed_bytes", "lowbit_pack_sa", "lowbit_gemm_sa", "lowbit_gemm_sa_path",
     "lowbit_nvfp4_packed_bytes", "lowbit_pack_nvfp4", "lowbit_gemm_nvfp4", "lowbit_gemm_nvfp4_path",
     "lowbit_draft_argmax", "lowbit_draft_argmax_path",

@@ -41,6 +41,7 @@ _SIGS = {
     "lowbit_pack_nvfp4": (_i, [_vp, _vp, ctypes.c_float, _i, _i, _vp, _vp]),
     "lowbit_gemm_nvfp4": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp]),
     "lowbit_gemm_nvfp4_path": (_i, [_vp, _vp, _i, _i, _i, _vp, _i, _vp]),
+    "lowbit_gemm_int4_grouped_path": (_i, [_vp, _i, _i, _i, _vp]),
     "lowbit_draft_argmax": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
     "lowbit_draft_argmax_path": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _sz, _i, _vp]),
 }
@@ -149,22 +150,35 @@ def lowbit_gemm_int4(X, packed, M, N, K, Y, stream=None):
 
 
 def lowbit_gemm_int4_path(X, packed, M, N, K, Y, path, stream=None):
-    """lowbit_gemm_int4 with the kernel family forced (1 = CUDA cores, 2 = tensor cores)."""
+    """lowbit_gemm_int4 with the kernel family forced (1 = CUDA cores, 2 = tcgen05, 3 = warp MMA)."""
     _gemm_args(X, packed, M, N, K, Y)
     _check(lib.lowbit_gemm_int4_path(_ptr(X), _ptr(packed), M, N, K, _ptr(Y), path,
                                      _stream(stream)), "lowbit_gemm_int4_path")
+
+
+def _descs(problems, M):
+    n = len(problems)
+    arr = (lowbit_gemm_desc * max(1, n))()
+    for i, (X, packed, N, K, Y) in enumerate(problems):
+        _gemm_args(X, packed, M, N, K, Y)
+        arr[i] = lowbit_gemm_desc(X.data_ptr(), packed.data_ptr(), Y.data_ptr(), N, K)
+    return arr, n
 
 
 def lowbit_gemm_int4_grouped(problems, M, stream=None):
     """Several independent INT4 multiplies with a common M in one call.
 
     problems: sequence of (X, packed, N, K, Y) tuples, 1 to 8 of them."""
-    n = len(problems)
-    arr = (lowbit_gemm_desc * max(1, n))()
-    for i, (X, packed, N, K, Y) in enumerate(problems):
-        _gemm_args(X, packed, M, N, K, Y)
-        arr[i] = lowbit_gemm_desc(X.data_ptr(), packed.data_ptr(), Y.data_ptr(), N, K)
+    arr, n = _descs(problems, M)
     _check(lib.lowbit_gemm_int4_grouped(arr, n, M, _stream(stream)), "lowbit_gemm_int4_grouped")
+
+
+def lowbit_gemm_int4_grouped_path(problems, M, path, stream=None):
+    """lowbit_gemm_int4_grouped with the kernel family forced (1 = streaming, M <= 4;
+    2 = tcgen05; 3 = warp-level MMA)."""
+    arr, n = _descs(problems, M)
+    _check(lib.lowbit_gemm_int4_grouped_path(arr, n, M, path, _stream(stream)),
+           "lowbit_gemm_int4_grouped_path")
 
 
 def lowbit_gemm_binplane(X, packed, P, M, N, K, Y, stream=None):
@@ -290,7 +304,7 @@ def lmhead_argmax_verify(H, packed_head, M, N, K, draft, argmax, n_accept, bonus
 
 def lmhead_argmax_verify_path(H, packed_head, M, N, K, draft, argmax, n_accept, bonus, workspace,
                               path, stream=None):
-    """lmhead_argmax_verify with the kernel family forced (1 = CUDA cores, 2 = tensor cores)."""
+    """lmhead_argmax_verify with the kernel family forced (1 = CUDA cores, 2 = tcgen05, 3 = warp MMA)."""
     _lmhead_args(H, packed_head, M, K, draft, argmax, n_accept, bonus, workspace)
     _check(lib.lmhead_argmax_verify_path(_ptr(H), _ptr(packed_head), M, N, K, _ptr(draft),
                                          _ptr(argmax), _ptr(n_accept), _ptr(bonus),

@@ -183,7 +183,7 @@ lowbit_status lowbit_gemm_int4_path(const uint16_t* X, const void* packed, int M
   if (!err) return LOWBIT_ERR_CUDA;
   const uint8_t* pk = static_cast<const uint8_t*>(packed);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (path == 0) path = (M <= kStreamDefaultRows) ? 1 : 2;
+  if (path == 0) path = (M <= kStreamDefaultRows) ? 1 : 3;
   if (path == 3) {
     GemvProblem p = {X, pk, Y, N, K, 0, 1, 0, 0};
     p.early = allocation_covers(pk, kHeaderBytes + int4_payload_bytes(N, K)) ? 1 : 0;
@@ -200,7 +200,13 @@ lowbit_status lowbit_gemm_int4_path(const uint16_t* X, const void* packed, int M
 
 lowbit_status lowbit_gemm_int4_grouped(const lowbit_gemm_desc* descs, int count, int M,
                                        void* stream) {
-  if (!descs || count < 1 || count > kMaxGemvProblems) return LOWBIT_ERR_INVALID_ARG;
+  return lowbit_gemm_int4_grouped_path(descs, count, M, 0, stream);
+}
+
+lowbit_status lowbit_gemm_int4_grouped_path(const lowbit_gemm_desc* descs, int count, int M,
+                                            int path, void* stream) {
+  if (!descs || count < 1 || count > kMaxGemvProblems || path < 0 || path > 3)
+    return LOWBIT_ERR_INVALID_ARG;
   for (int i = 0; i < count; ++i) {
     const lowbit_gemm_desc& d = descs[i];
     if (!d.X || !d.packed || !d.Y) return LOWBIT_ERR_INVALID_ARG;
@@ -208,23 +214,21 @@ lowbit_status lowbit_gemm_int4_grouped(const lowbit_gemm_desc* descs, int count,
     if (st != LOWBIT_OK) return st;
     if (!aligned16(d.X) || !aligned16(d.packed)) return LOWBIT_ERR_ALIGN;
   }
+  if (path == 1 && M > kStreamMaxRows) return LOWBIT_ERR_SHAPE;
   int* err = device_error_word();
   if (!err) return LOWBIT_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (M <= kStreamDefaultRows) {
-    GemvProblem p[kMaxGemvProblems];
-    for (int i = 0; i < count; ++i) {
-      p[i] = GemvProblem{descs[i].X, static_cast<const uint8_t*>(descs[i].packed), descs[i].Y,
-                         descs[i].N, descs[i].K, 0, 1, 0, 0};
-      p[i].early = allocation_covers(descs[i].packed,
-                                     kHeaderBytes + int4_payload_bytes(descs[i].N, descs[i].K)) ? 1 : 0;
-    }
-    return from_cuda(launch_int4_stream(p, count, M, err, s));
-  }
+  if (path == 0) path = M <= kStreamDefaultRows ? 1 : 3;
   GemvProblem p[kMaxGemvProblems];
-  for (int i = 0; i < count; ++i)
+  for (int i = 0; i < count; ++i) {
     p[i] = GemvProblem{descs[i].X, static_cast<const uint8_t*>(descs[i].packed), descs[i].Y,
                        descs[i].N, descs[i].K, 0, 1, 0, 0};
+    p[i].early = allocation_covers(descs[i].packed,
+                                   kHeaderBytes + int4_payload_bytes(descs[i].N, descs[i].K)) ? 1 : 0;
+  }
+  if (path == 1) return from_cuda(launch_int4_stream(p, count, M, err, s));
+  if (path == 3) return from_cuda(launch_int4_mma(p, count, M, err, s));
+  for (int i = 0; i < count; ++i) p[i].early = 0;
   return from_cuda(launch_int4_tc_grouped(p, count, M, err, s));
 }
 
@@ -357,6 +361,7 @@ lowbit_status lmhead_argmax_verify_path(const uint16_t* H, const void* packed_he
   if (!err) return LOWBIT_ERR_CUDA;
   const uint8_t* pk = static_cast<const uint8_t*>(packed_head);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (path == 0) path = 3;
   if (path == 1)
     return from_cuda(launch_lmhead_cc(H, pk, M, N, K, draft, argmax, n_accept, bonus, workspace,
                                       err, s));

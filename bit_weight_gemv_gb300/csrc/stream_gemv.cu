@@ -1006,6 +1006,7 @@ int4_mma_kernel(const __grid_constant__ MmaArgs A) {
   __shared__ int ok;
   __shared__ int gave_up;
   __shared__ int hdr_valid;  // the same in every CTA: they all read the one header
+  __shared__ unsigned long long kmax[MT];  // verify: this CTA's best key per activation row
   // Totals [MT][128], written once every stage has been consumed: they reuse the ring (at
   // least two stages, 25 KB).  After a timed-out wait a late copy may still land there; the
   // outputs are wrong then anyway and the error word says so.
@@ -1027,6 +1028,7 @@ int4_mma_kernel(const __grid_constant__ MmaArgs A) {
   const int S = a.stages, M = a.m;
   const PackedHeader* hp = reinterpret_cast<const PackedHeader*>(pr.packed);
 
+  if (threadIdx.x < MT) kmax[threadIdx.x] = 0ull;
   if (threadIdx.x == 0) {
     ok = live && (pr.early || header_matches(hp, kFormatInt4, 0, pr.N, pr.K));
     gave_up = 0;
@@ -1199,16 +1201,19 @@ int4_mma_kernel(const __grid_constant__ MmaArgs A) {
         unsigned long long key = in ? argmax_key(y, n) : 0ull;
         if (rows >= 32) {  // a warp's 32 values share one activation row
           key = warp_max_u64(key);
-          if (lane == 0 && key) atomicMax(&a.ws->keys[min(m, 31)], key);
+          if (lane == 0 && key) atomicMax(&kmax[min(m, MT - 1)], key);
         } else if (key) {
-          atomicMax(&a.ws->keys[m], key);
+          atomicMax(&kmax[m], key);
         }
       }
     }
   }
   if (C > 1) ptx::cluster_sync();
   if (verify) {
+    // one global atomic per activation row and CTA
+    __syncthreads();
     grid_wait();
+    if (threadIdx.x < M && kmax[threadIdx.x]) atomicMax(&a.ws->keys[threadIdx.x], kmax[threadIdx.x]);
     lmhead_finish(a.ws, M, a.draft, a.ids, a.n_accept, a.bonus);
   }
 }

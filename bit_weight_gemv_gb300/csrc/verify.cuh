@@ -49,6 +49,7 @@ __device__ __forceinline__ void lmhead_finish(LmheadWorkspace* ws, int M,
                                               int32_t* __restrict__ n_accept,
                                               int32_t* __restrict__ bonus) {
   __shared__ int is_last;
+  __shared__ int win[32];
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -58,17 +59,17 @@ __device__ __forceinline__ void lmhead_finish(LmheadWorkspace* ws, int M,
   __syncthreads();
   if (!is_last) return;
   __threadfence();
+  if (threadIdx.x < M) {
+    const int a = argmax_key_row(atomicExch(&ws->keys[threadIdx.x], 0ull));
+    win[threadIdx.x] = a;
+    argmax[threadIdx.x] = a;
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
-    int a[32];
-    for (int t = 0; t < M; ++t) {
-      const unsigned long long k = atomicExch(&ws->keys[t], 0ull);
-      a[t] = argmax_key_row(k);
-      argmax[t] = a[t];
-    }
     int n = 0;
-    while (n < M - 1 && draft[n] == a[n]) ++n;
+    while (n < M - 1 && draft[n] == win[n]) ++n;
     *n_accept = n;
-    *bonus = a[n];
+    *bonus = win[n];
     atomicExch(&ws->counter, 0u);
   }
 }

@@ -168,7 +168,8 @@ lowbit_status lowbit_validate_packed(const void* packed, int format, int P, int 
  * of the run's largest, otherwise rounded to a multiple of 2^-15 of that largest) and the
  * products within a run are summed exactly in integers; a non-finite activation makes every
  * output of its row NaN.
- * M >= 3 runs the tensor-core skinny GEMM (exact bf16 products, fp32 sums per group). */
+ * M >= 3 runs the skinny GEMM on the warp-level tensor-core MMA (exact bf16 q times the bf16
+ * activations, fp32 accumulation within a group, then s times the group's sum added in fp32). */
 lowbit_status lowbit_gemm_int4(const uint16_t* X, const void* packed, int M, int N, int K,
                                uint16_t* Y, void* stream);
 
@@ -183,7 +184,7 @@ typedef struct lowbit_gemm_desc {
 
 /* Several independent INT4 multiplies with a common M (for example the q, k and v projections
  * of a decoder layer, which read the same activations), each with the contract and rounding
- * of lowbit_gemm_int4.  They share ONE launch (the streaming kernel at M <= 2, the tensor-core
+ * of lowbit_gemm_int4.  They share ONE launch (the streaming kernel at M <= 2, the warp-MMA
  * GEMM above), so the launch, pipeline fill and drain are paid once for the group instead of
  * once per matrix.
  *   descs : HOST array of `count` descriptors, 1 <= count <= 8; read during the call only.
@@ -191,6 +192,10 @@ typedef struct lowbit_gemm_desc {
  *   the group.  Every descriptor is validated before anything is enqueued. */
 lowbit_status lowbit_gemm_int4_grouped(const lowbit_gemm_desc* descs, int count, int M,
                                        void* stream);
+/* The same with the kernel family forced: `path` as lowbit_gemm_int4_path (1: the streaming
+ * kernel, M <= 4, else LOWBIT_ERR_SHAPE). */
+lowbit_status lowbit_gemm_int4_grouped_path(const lowbit_gemm_desc* descs, int count, int M,
+                                            int path, void* stream);
 
 /* Y = X * W^T for binary-plane weights (ShiftAddQwen README, "Method" and "Format"):
  *   y[m][n] = sum_p sum_g alpha[p][n][g] * sum_{k in g} b[p][n][k] * x[m][k].
@@ -276,9 +281,12 @@ lowbit_status lmhead_argmax_verify_noalloc(const uint16_t* H, const void* packed
  * plus `path`: 0 = the library's choice; 1 = the CUDA-core kernels (INT4: the streaming
  * kernel up to M = 4, integer dot products on block-scaled int16 activations, and a
  * row-per-lane bf16 kernel above; planes: the table-driven streaming kernel at M = 1 and a
- * sign-XOR kernel above; LM head: the row-per-lane kernel); 2 = the tensor-core kernels
- * (dequantisation into tensor memory, tcgen05 MMA with fp32 accumulation).  Other values:
- * INVALID_ARG.
+ * sign-XOR kernel above; LM head: the row-per-lane kernel); 2 = the tcgen05 kernels
+ * (dequantisation into tensor memory, tcgen05 MMA with fp32 accumulation); 3 (INT4 and the
+ * LM head only, any M) = the warp-level MMA kernels (mma.sync m16n8k16 on bf16 fragments
+ * unpacked in registers).  The library's choice for M >= 3 INT4 and for the LM head is 3:
+ * with 16 activation rows a 128-row tcgen05 MMA issues as slowly as with 64, and the
+ * weight stream then outruns it.  Other values: INVALID_ARG.
  */
 lowbit_status lowbit_gemm_int4_path(const uint16_t* X, const void* packed, int M, int N, int K,
                                     uint16_t* Y, int path, void* stream);

@@ -336,14 +336,17 @@ def test_shape_errors_raise(lb):
 
 # ------------------------------------------------------------------------- grouped multiplies
 
-def _grouped(lb, M, shapes, seed):
+def _grouped(lb, M, shapes, seed, path=0):
     probs, refs = [], []
     for j, (K, N) in enumerate(shapes):
         codes, scales, x = synth.int4_problem(seed, M, N, K, j)
         Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
         probs.append((bf16_dev(x), pack_int4_gpu(lb, codes, scales), N, K, Y))
         refs.append(oint4.gemm(x, codes, scales))
-    lb.lowbit_gemm_int4_grouped(probs, M)
+    if path:
+        lb.lowbit_gemm_int4_grouped_path(probs, M, path)
+    else:
+        lb.lowbit_gemm_int4_grouped(probs, M)
     torch.cuda.synchronize()
     return [host_bits(p[4]) for p in probs], refs
 
@@ -364,11 +367,12 @@ def test_grouped_config1_layer_in_one_call(lb, M):
     ((2560, 9728), (2560, 9728)),                        # gate, up
     ((12288, 100), (128, 8), (256, 129), (640, 65), (128, 2), (1024, 33), (384, 1000), (896, 7)),
 ])
-@pytest.mark.parametrize("M", [1, 2, 16, 32])
-def test_grouped_ragged_mixes(lb, shapes, M):
-    ys, refs = _grouped(lb, M, shapes, 11)
+@pytest.mark.parametrize("M,path", [(1, 0), (2, 0), (16, 0), (32, 0), (16, 2), (32, 2), (4, 1),
+                                    (3, 3)])
+def test_grouped_ragged_mixes(lb, shapes, M, path):
+    ys, refs = _grouped(lb, M, shapes, 11, path)
     for j, (y, r) in enumerate(zip(ys, refs)):
-        check_gemm(y, r, f"grouped M={M} mix {shapes} item {j}")
+        check_gemm(y, r, f"grouped M={M} path={path} mix {shapes} item {j}")
 
 
 def test_grouped_matches_single_calls_bit_for_bit(lb):

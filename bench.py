@@ -237,7 +237,9 @@ def build_int4_layer(lb, torch, l2, M, path, seed, name, desc, grouping=None):
 
 
 def build_binplane(lb, torch, l2, M, path, name, desc):
-    w = Workload(name, desc, "bp_stream_kernel" if (M == 1 and path != 2) else "tc_gemm_kernel")
+    w = Workload(name, desc, "bp_stream_kernel" if (M == 1 and path in (0, 1))
+                 else ("tc_gemm_kernel" if path == 2 else
+                       ("binplane_cc_kernel" if path == 1 else "bp_mma_kernel")))
     mats = []
     for si, (K, N) in enumerate(synth.BINPLANE_SHAPES):
         for P in synth.BINPLANE_PLANES:
@@ -577,7 +579,7 @@ def run_ours(args):
     if not args.no_rows and rank == 0:
         names = [(n, 0) for n in WORKLOADS if n not in (args.workload, "tiny")]
         names += [("decode", 2), ("binplane_m1", 1), ("binplane_m1", 2), ("verify_all", 2),
-                  ("lmhead_full", 2)]
+                  ("lmhead_full", 2), ("binplane_m16", 2)]
         names = [nm for nm in names if nm != (args.workload, args.path)]
         rows = measure_rows(lb, torch, peak, l2, names)
 

@@ -239,7 +239,7 @@ lowbit_status lowbit_gemm_binplane(const uint16_t* X, const void* packed, int P,
 
 lowbit_status lowbit_gemm_binplane_path(const uint16_t* X, const void* packed, int P, int M,
                                         int N, int K, uint16_t* Y, int path, void* stream) {
-  if (!X || !packed || !Y || path < 0 || path > 2) return LOWBIT_ERR_INVALID_ARG;
+  if (!X || !packed || !Y || path < 0 || path > 3) return LOWBIT_ERR_INVALID_ARG;
   lowbit_status st = check_shape(M, N, K, 32);
   if (st != LOWBIT_OK) return st;
   if (P < 1 || P > 8) return LOWBIT_ERR_SHAPE;
@@ -248,11 +248,16 @@ lowbit_status lowbit_gemm_binplane_path(const uint16_t* X, const void* packed, i
   if (!err) return LOWBIT_ERR_CUDA;
   const uint8_t* pk = static_cast<const uint8_t*>(packed);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (path == 0) path = (M == 1) ? 1 : 2;
+  if (path == 0) path = (M == 1) ? 1 : 3;
   if (path == 1 && M == 1) {
     GemvProblem p = {X, pk, Y, N, K, 0, 1, 0, P};
     p.early = allocation_covers(pk, kHeaderBytes + binplane_payload_bytes(P, N, K)) ? 1 : 0;
     return from_cuda(launch_bp_stream(&p, 1, err, s));
+  }
+  if (path == 3) {
+    GemvProblem p = {X, pk, Y, N, K, 0, 1, 0, P};
+    p.early = allocation_covers(pk, kHeaderBytes + binplane_payload_bytes(P, N, K)) ? 1 : 0;
+    return from_cuda(launch_bp_mma(p, M, err, s));
   }
   if (path == 1) return from_cuda(launch_binplane_cc(X, pk, P, M, N, K, Y, err, s));
   return from_cuda(launch_binplane_tc(X, pk, P, M, N, K, Y, err, s));

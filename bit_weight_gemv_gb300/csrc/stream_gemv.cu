@@ -951,7 +951,22 @@ nvfp4_stream_kernel(const __grid_constant__ StreamArgs a) {
 // the A fragment of the MMA -- to exact bf16 q (the nibble ORed into bf16 128.0, minus 136),
 // loads the activations' B fragments with ldmatrix and issues one MMA per 8 activation rows.
 // After a group's 128 inputs it adds s * D to fp32 totals held in registers.
-constexpr uint32_t kMmaXOff = 9216;  // the activation tile starts 1024-aligned after the block
+constexpr int kMmaInt4 = 0, kMmaPlanes = 1;  // weight formats of the warp-MMA kernels
+// Stage layout: the block, then the activation tile at the next 1024-byte boundary.
+__host__ __device__ constexpr uint32_t mma_block_bytes(int fmt, int P) {
+  return fmt == kMmaInt4 ? kInt4Block : (uint32_t)P * (kRowTile * 16 + kRowTile * 2);
+}
+__host__ __device__ constexpr uint32_t mma_x_off(int fmt, int P) {
+  return (mma_block_bytes(fmt, P) + 1023u) / 1024u * 1024u;
+}
+__host__ __device__ constexpr uint32_t mma_stage_bytes(int fmt, int P, int MT) {
+  return mma_x_off(fmt, P) + (uint32_t)MT * 2 * 128;
+}
+// A pair of binary-plane signs -> the bf16 pair (+-1, +-1): bits `sh` below 15 and 31 of w
+// (set = +1) moved to the sign bits of bf16 -1.0.
+__device__ __forceinline__ uint32_t pm1_pair(uint32_t w, int sh) {
+  return ((w << sh) & 0x80008000u) ^ 0xBF80BF80u;
+}
 constexpr int kMmaWarps = 8;
 constexpr int kMmaThreads = (kMmaWarps + 1) * 32;  // compute warps, producer
 // Occupancy is what hides the dequantisation's latency: about 50 KB of shared memory per CTA
@@ -992,10 +1007,8 @@ __device__ __forceinline__ uint32_t q_pair(uint32_t w) {
   return bf16x2_sub_rn((w & 0x000F000Fu) | 0x43004300u, 0x43084308u);
 }
 
-template <int MT, int EPI>
-__global__ void __launch_bounds__(kMmaThreads, mma_resident<MT>())
-int4_mma_kernel(const __grid_constant__ MmaArgs A) {
-  constexpr uint32_t STG = kMmaXOff + MT * 2 * 128;  // block, then two 64-input atoms of X
+template <int FMT, int MT, int EPI>
+__device__ __forceinline__ void mma_body(const MmaArgs& A) {
   constexpr int NT = MT / 8;  // MMA output tiles of 8 activation rows
   const StreamArgs& a = A.s;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -1027,10 +1040,14 @@ int4_mma_kernel(const __grid_constant__ MmaArgs A) {
   const int nb = live ? g1 - g0 : 0;
   const int S = a.stages, M = a.m;
   const PackedHeader* hp = reinterpret_cast<const PackedHeader*>(pr.packed);
+  const int P = FMT == kMmaInt4 ? 0 : pr.P;
+  const uint32_t BB = mma_block_bytes(FMT, P), XOFF = mma_x_off(FMT, P);
+  const uint32_t STG = mma_stage_bytes(FMT, P, MT);  // block, then two 64-input atoms of X
+  const uint32_t fmt_id = FMT == kMmaInt4 ? kFormatInt4 : kFormatBinplane;
 
   if (threadIdx.x < MT) kmax[threadIdx.x] = 0ull;
   if (threadIdx.x == 0) {
-    ok = live && (pr.early || header_matches(hp, kFormatInt4, 0, pr.N, pr.K));
+    ok = live && (pr.early || header_matches(hp, fmt_id, P, pr.N, pr.K));
     gave_up = 0;
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
@@ -1042,7 +1059,7 @@ int4_mma_kernel(const __grid_constant__ MmaArgs A) {
   if (threadIdx.x == 0) grid_launch();
   const bool hdr_ok = ok != 0;  // with `early`: only "this CTA has work"; see out_ok below
   if (threadIdx.x == 32) {  // a compute warp checks the header; the producer does not wait on it
-    const bool hv = header_matches(hp, kFormatInt4, 0, pr.N, pr.K);
+    const bool hv = header_matches(hp, fmt_id, P, pr.N, pr.K);
     hdr_valid = hv;
     if (!hv) ok = 0;
   }
@@ -1050,11 +1067,11 @@ int4_mma_kernel(const __grid_constant__ MmaArgs A) {
   if (warp == kMmaWarps) {
     // ---------------------------------------------------------------- producer
     if (hdr_ok && lane == 0) {
-      const uint8_t* wsrc = pr.packed + kHeaderBytes + ((size_t)tile * G + g0) * kInt4Block;
+      const uint8_t* wsrc = pr.packed + kHeaderBytes + ((size_t)tile * G + g0) * BB;
       const CUtensorMap* xmap = &A.xmap[pi];
-      constexpr uint32_t tx = kInt4Block + MT * 2 * 128;  // zero-filled rows count as copied
+      const uint32_t tx = BB + MT * 2 * 128;  // zero-filled rows count as copied
       auto copy_x = [&](int b, int s, uint32_t bar) {
-        const uint32_t dst = ptx::smem_addr(ring + (size_t)s * STG + kMmaXOff);
+        const uint32_t dst = ptx::smem_addr(ring + (size_t)s * STG + XOFF);
         ptx::tma_load_2d(dst, xmap, (g0 + b) * kGroup, 0, bar);
         ptx::tma_load_2d(dst + MT * 128, xmap, (g0 + b) * kGroup + 64, 0, bar);
       };
@@ -1062,8 +1079,7 @@ int4_mma_kernel(const __grid_constant__ MmaArgs A) {
       for (int b = 0; b < pre; ++b) {
         const uint32_t bar = ptx::smem_addr(&full[b]);
         ptx::mbar_arrive_expect_tx(bar, tx);
-        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)b * STG), wsrc + (size_t)b * kInt4Block,
-                      kInt4Block, bar);
+        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)b * STG), wsrc + (size_t)b * BB, BB, bar);
       }
       grid_wait();  // the activations may be the previous kernel's output
       for (int b = 0; b < pre; ++b) copy_x(b, b, ptx::smem_addr(&full[b]));
@@ -1078,8 +1094,7 @@ int4_mma_kernel(const __grid_constant__ MmaArgs A) {
         }
         const uint32_t bar = ptx::smem_addr(&full[s]);
         ptx::mbar_arrive_expect_tx(bar, tx);
-        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)s * STG), wsrc + (size_t)b * kInt4Block,
-                      kInt4Block, bar);
+        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)s * STG), wsrc + (size_t)b * BB, BB, bar);
         copy_x(b, s, bar);
         issued = b + 1;
       }
@@ -1114,42 +1129,81 @@ int4_mma_kernel(const __grid_constant__ MmaArgs A) {
         break;
       }
       const uint8_t* st = ring + (size_t)s * STG;
-      const uint32_t xs = ptx::smem_addr(st + kMmaXOff);
-      float d[NT][4];
+      const uint32_t xs = ptx::smem_addr(st + XOFF);
+      if constexpr (FMT == kMmaInt4) {
+        float d[NT][4];
 #pragma unroll
-      for (int i = 0; i < NT; ++i) d[i][0] = d[i][1] = d[i][2] = d[i][3] = 0.f;
+        for (int i = 0; i < NT; ++i) d[i][0] = d[i][1] = d[i][2] = d[i][3] = 0.f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {  // 32-input chunks
-        const uint4 w0 = *reinterpret_cast<const uint4*>(st + c * (kRowTile * 16) + r0 * 16);
-        const uint4 w1 = *reinterpret_cast<const uint4*>(st + c * (kRowTile * 16) + (r0 + 8) * 16);
-        // word i holds inputs 8i..8i+7 of the chunk; pair t of it (inputs 8i+2t, 8i+2t+1) is
-        // this lane's share, shifted down to nibble 0
-        const uint32_t u0[4] = {w0.x >> (4 * t), w0.y >> (4 * t), w0.z >> (4 * t), w0.w >> (4 * t)};
-        const uint32_t u1[4] = {w1.x >> (4 * t), w1.y >> (4 * t), w1.z >> (4 * t), w1.w >> (4 * t)};
+        for (int c = 0; c < 4; ++c) {  // 32-input chunks
+          const uint4 w0 = *reinterpret_cast<const uint4*>(st + c * (kRowTile * 16) + r0 * 16);
+          const uint4 w1 = *reinterpret_cast<const uint4*>(st + c * (kRowTile * 16) + (r0 + 8) * 16);
+          // word i holds inputs 8i..8i+7 of the chunk; pair t of it (inputs 8i+2t, 8i+2t+1) is
+          // this lane's share, shifted down to nibble 0
+          const uint32_t u0[4] = {w0.x >> (4 * t), w0.y >> (4 * t), w0.z >> (4 * t), w0.w >> (4 * t)};
+          const uint32_t u1[4] = {w1.x >> (4 * t), w1.y >> (4 * t), w1.z >> (4 * t), w1.w >> (4 * t)};
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {  // 16-input steps
-          const uint32_t a0 = q_pair(u0[2 * j]), a1 = q_pair(u1[2 * j]);
-          const uint32_t a2 = q_pair(u0[2 * j + 1]), a3 = q_pair(u1[2 * j + 1]);
+          for (int j = 0; j < 2; ++j) {  // 16-input steps
+            const uint32_t a0 = q_pair(u0[2 * j]), a1 = q_pair(u1[2 * j]);
+            const uint32_t a2 = q_pair(u0[2 * j + 1]), a3 = q_pair(u1[2 * j + 1]);
 #pragma unroll
-          for (int hh = 0; hh < MT / 16; ++hh) {
-            uint32_t b0, b1, b2, b3;
-            // step 2c + j: atom c / 2, chunks 4 (c % 2) + 2j (+1)
-            ldsm_x4(xs + xsw[(2 * c + j) & 3] + (c >> 1) * (MT * 128) + hh * 16 * 128, b0, b1, b2, b3);
-            mma_16816(d[2 * hh], a0, a1, a2, a3, b0, b1);
-            mma_16816(d[2 * hh + 1], a0, a1, a2, a3, b2, b3);
+            for (int hh = 0; hh < MT / 16; ++hh) {
+              uint32_t b0, b1, b2, b3;
+              // step 2c + j: atom c / 2, chunks 4 (c % 2) + 2j (+1)
+              ldsm_x4(xs + xsw[(2 * c + j) & 3] + (c >> 1) * (MT * 128) + hh * 16 * 128, b0, b1, b2, b3);
+              mma_16816(d[2 * hh], a0, a1, a2, a3, b0, b1);
+              mma_16816(d[2 * hh + 1], a0, a1, a2, a3, b2, b3);
+            }
           }
         }
-      }
-      const float s0 = half_bits_to_float(*reinterpret_cast<const uint16_t*>(st + kInt4ScaleOff + r0 * 2));
-      const float s1 = half_bits_to_float(*reinterpret_cast<const uint16_t*>(st + kInt4ScaleOff + (r0 + 8) * 2));
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&empty[s]));
+        const float s0 = half_bits_to_float(*reinterpret_cast<const uint16_t*>(st + kInt4ScaleOff + r0 * 2));
+        const float s1 = half_bits_to_float(*reinterpret_cast<const uint16_t*>(st + kInt4ScaleOff + (r0 + 8) * 2));
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&empty[s]));
 #pragma unroll
-      for (int i = 0; i < NT; ++i) {
-        acc[i][0] = fmaf(s0, d[i][0], acc[i][0]);
-        acc[i][1] = fmaf(s0, d[i][1], acc[i][1]);
-        acc[i][2] = fmaf(s1, d[i][2], acc[i][2]);
-        acc[i][3] = fmaf(s1, d[i][3], acc[i][3]);
+        for (int i = 0; i < NT; ++i) {
+          acc[i][0] = fmaf(s0, d[i][0], acc[i][0]);
+          acc[i][1] = fmaf(s0, d[i][1], acc[i][1]);
+          acc[i][2] = fmaf(s1, d[i][2], acc[i][2]);
+          acc[i][3] = fmaf(s1, d[i][3], acc[i][3]);
+        }
+      } else {
+        // Binary planes: word w of a plane row covers inputs 32w..32w+31, bit i the sign of
+        // 32w + 2i and bit 16 + i that of 32w + 2i + 1.  Step s's A fragment takes pairs
+        // i = 8 (s % 2) + t and i + 4 of word s / 2.
+        for (int p = 0; p < P; ++p) {
+          const uint4 w0 = *reinterpret_cast<const uint4*>(st + p * (kRowTile * 16) + r0 * 16);
+          const uint4 w1 = *reinterpret_cast<const uint4*>(st + p * (kRowTile * 16) + (r0 + 8) * 16);
+          const uint32_t W0[4] = {w0.x, w0.y, w0.z, w0.w}, W1[4] = {w1.x, w1.y, w1.z, w1.w};
+          float d[NT][4];
+#pragma unroll
+          for (int i = 0; i < NT; ++i) d[i][0] = d[i][1] = d[i][2] = d[i][3] = 0.f;
+#pragma unroll
+          for (int ss = 0; ss < 8; ++ss) {
+            const int sh = 15 - 8 * (ss & 1) - t;  // bit i to bit 15
+            const uint32_t a0 = pm1_pair(W0[ss >> 1], sh), a1 = pm1_pair(W1[ss >> 1], sh);
+            const uint32_t a2 = pm1_pair(W0[ss >> 1], sh - 4), a3 = pm1_pair(W1[ss >> 1], sh - 4);
+#pragma unroll
+            for (int hh = 0; hh < MT / 16; ++hh) {
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4(xs + xsw[ss & 3] + (ss >> 2) * (MT * 128) + hh * 16 * 128, b0, b1, b2, b3);
+              mma_16816(d[2 * hh], a0, a1, a2, a3, b0, b1);
+              mma_16816(d[2 * hh + 1], a0, a1, a2, a3, b2, b3);
+            }
+          }
+          const uint8_t* al = st + binplane_alpha_off(P) + p * (kRowTile * 2);
+          const float s0 = half_bits_to_float(*reinterpret_cast<const uint16_t*>(al + r0 * 2));
+          const float s1 = half_bits_to_float(*reinterpret_cast<const uint16_t*>(al + (r0 + 8) * 2));
+#pragma unroll
+          for (int i = 0; i < NT; ++i) {
+            acc[i][0] = fmaf(s0, d[i][0], acc[i][0]);
+            acc[i][1] = fmaf(s0, d[i][1], acc[i][1]);
+            acc[i][2] = fmaf(s1, d[i][2], acc[i][2]);
+            acc[i][3] = fmaf(s1, d[i][3], acc[i][3]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&empty[s]));
       }
     }
     // every warp has read its last stage before any total lands on the ring
@@ -1216,6 +1270,20 @@ int4_mma_kernel(const __grid_constant__ MmaArgs A) {
     if (threadIdx.x < M && kmax[threadIdx.x]) atomicMax(&a.ws->keys[threadIdx.x], kmax[threadIdx.x]);
     lmhead_finish(a.ws, M, a.draft, a.ids, a.n_accept, a.bonus);
   }
+}
+
+template <int MT, int EPI>
+__global__ void __launch_bounds__(kMmaThreads, mma_resident<MT>())
+int4_mma_kernel(const __grid_constant__ MmaArgs A) {
+  mma_body<kMmaInt4, MT, EPI>(A);
+}
+
+// The same for binary planes (ShiftAddQwen README, "Method"): one MMA set per plane on exact
+// +-1 fragments, alpha per (plane, row, group) applied in fp32.
+template <int MT>
+__global__ void __launch_bounds__(kMmaThreads, mma_resident<MT>())
+bp_mma_kernel(const __grid_constant__ MmaArgs A) {
+  mma_body<kMmaPlanes, MT, kEpiStore>(A);
 }
 
 int sm_count() {
@@ -1306,7 +1374,7 @@ constexpr int kMaxDevices = 64;
 struct OptIns {
   std::atomic<unsigned char> done[kMaxDevices];
 };
-OptIns g_int4_optins[3], g_bp_optins, g_sa_optins, g_nv_optins[2], g_mma_optins[4];  // one per kernel built
+OptIns g_int4_optins[3], g_bp_optins, g_sa_optins, g_nv_optins[2], g_mma_optins[6];  // one per kernel built
 
 template <typename Kernel>
 cudaError_t opt_in(Kernel kern, OptIns& o, size_t budget) {
@@ -1394,11 +1462,14 @@ PFN_cuTensorMapEncodeTiled_v12000 x_map_encoder() {
   return fn;
 }
 
-template <int MT, int EPI>
-cudaError_t launch_int4_mma_mt(const GemvProblem* probs, int count, int M, LmheadWorkspace* ws,
-                               const int32_t* draft, int32_t* argmax, int32_t* n_accept,
-                               int32_t* bonus, int* err, cudaStream_t s) {
-  constexpr uint32_t stage = kMmaXOff + MT * 2 * 128;
+template <int FMT, int MT, int EPI>
+cudaError_t launch_mma_mt(const GemvProblem* probs, int count, int M, LmheadWorkspace* ws,
+                          const int32_t* draft, int32_t* argmax, int32_t* n_accept,
+                          int32_t* bonus, int* err, cudaStream_t s) {
+  const int P = FMT == kMmaInt4 ? 0 : probs[0].P;
+  for (int i = 1; i < count; ++i)
+    if (FMT != kMmaInt4 && probs[i].P != P) return cudaErrorInvalidValue;  // one stage size
+  const uint32_t stage = mma_stage_bytes(FMT, P, MT);
   auto encode = x_map_encoder();
   if (!encode) return cudaErrorNotSupported;
   MmaArgs A = {};
@@ -1425,13 +1496,19 @@ cudaError_t launch_int4_mma_mt(const GemvProblem* probs, int count, int M, Lmhea
       return cudaErrorInvalidValue;
   }
   int S = (int)((kMmaSmemBudget - 1024) / stage);
-  S = S > kMaxStages ? kMaxStages : (S < 2 ? 2 : S);
+  S = S > kMaxStages ? kMaxStages : S;
+  if (S < 2) return cudaErrorInvalidValue;
   a.stages = sc.maxnb < S ? sc.maxnb : S;
   // the totals [MT][128] reuse the ring; 1 KB of slack aligns the ring
   const size_t smem = std::max((size_t)a.stages * stage, (size_t)MT * kRowTile * sizeof(float)) + 1024;
-  constexpr int slot_i = (MT == 16 ? 0 : 1) + 2 * EPI;
-  return launch_streaming(int4_mma_kernel<MT, EPI>, g_mma_optins[slot_i], kMmaSmemBudget, A, sc,
-                          smem, kMmaThreads, s);
+  if constexpr (FMT == kMmaInt4) {
+    constexpr int slot_i = (MT == 16 ? 0 : 1) + 2 * EPI;
+    return launch_streaming(int4_mma_kernel<MT, EPI>, g_mma_optins[slot_i], kMmaSmemBudget, A, sc,
+                            smem, kMmaThreads, s);
+  } else {
+    return launch_streaming(bp_mma_kernel<MT>, g_mma_optins[MT == 16 ? 4 : 5], kMmaSmemBudget, A,
+                            sc, smem, kMmaThreads, s);
+  }
 }
 
 }  // namespace
@@ -1439,10 +1516,19 @@ cudaError_t launch_int4_mma_mt(const GemvProblem* probs, int count, int M, Lmhea
 cudaError_t launch_int4_mma(const GemvProblem* probs, int count, int M, int* err, cudaStream_t s) {
   if (count < 1 || count > kMaxGemvProblems || M < 1 || M > 32) return cudaErrorInvalidValue;
   if (M <= 16)
-    return launch_int4_mma_mt<16, kEpiStore>(probs, count, M, nullptr, nullptr, nullptr, nullptr,
-                                             nullptr, err, s);
-  return launch_int4_mma_mt<32, kEpiStore>(probs, count, M, nullptr, nullptr, nullptr, nullptr,
-                                           nullptr, err, s);
+    return launch_mma_mt<kMmaInt4, 16, kEpiStore>(probs, count, M, nullptr, nullptr, nullptr,
+                                                  nullptr, nullptr, err, s);
+  return launch_mma_mt<kMmaInt4, 32, kEpiStore>(probs, count, M, nullptr, nullptr, nullptr,
+                                                nullptr, nullptr, err, s);
+}
+
+cudaError_t launch_bp_mma(const GemvProblem& prob, int M, int* err, cudaStream_t s) {
+  if (M < 1 || M > 32 || prob.P < 1 || prob.P > 8) return cudaErrorInvalidValue;
+  if (M <= 16)
+    return launch_mma_mt<kMmaPlanes, 16, kEpiStore>(&prob, 1, M, nullptr, nullptr, nullptr, nullptr,
+                                                    nullptr, err, s);
+  return launch_mma_mt<kMmaPlanes, 32, kEpiStore>(&prob, 1, M, nullptr, nullptr, nullptr, nullptr,
+                                                  nullptr, err, s);
 }
 
 cudaError_t launch_lmhead_mma(const GemvProblem& prob, int M, LmheadWorkspace* ws,
@@ -1450,8 +1536,10 @@ cudaError_t launch_lmhead_mma(const GemvProblem& prob, int M, LmheadWorkspace* w
                               int32_t* bonus, int* err, cudaStream_t s) {
   if (M < 1 || M > 32) return cudaErrorInvalidValue;
   if (M <= 16)
-    return launch_int4_mma_mt<16, kEpiVerify>(&prob, 1, M, ws, draft, argmax, n_accept, bonus, err, s);
-  return launch_int4_mma_mt<32, kEpiVerify>(&prob, 1, M, ws, draft, argmax, n_accept, bonus, err, s);
+    return launch_mma_mt<kMmaInt4, 16, kEpiVerify>(&prob, 1, M, ws, draft, argmax, n_accept, bonus,
+                                                   err, s);
+  return launch_mma_mt<kMmaInt4, 32, kEpiVerify>(&prob, 1, M, ws, draft, argmax, n_accept, bonus,
+                                                 err, s);
 }
 
 cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int M, int* err, cudaStream_t s) {

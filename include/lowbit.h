@@ -199,7 +199,9 @@ lowbit_status lowbit_gemm_int4_grouped_path(const lowbit_gemm_desc* descs, int c
 
 /* Y = X * W^T for binary-plane weights (ShiftAddQwen README, "Method" and "Format"):
  *   y[m][n] = sum_p sum_g alpha[p][n][g] * sum_{k in g} b[p][n][k] * x[m][k].
- *   Shapes and rounding as lowbit_gemm_int4; packed from lowbit_pack_binplane(P, N, K). */
+ *   Shapes and rounding as lowbit_gemm_int4; packed from lowbit_pack_binplane(P, N, K).
+ *   M = 1 runs the table-driven streaming kernel; M >= 2 the warp-level MMA on exact +-1
+ *   bf16 fragments, one MMA set per plane, alpha applied per (plane, group) in fp32. */
 lowbit_status lowbit_gemm_binplane(const uint16_t* X, const void* packed, int P, int M, int N,
                                    int K, uint16_t* Y, void* stream);
 
@@ -282,9 +284,10 @@ lowbit_status lmhead_argmax_verify_noalloc(const uint16_t* H, const void* packed
  * kernel up to M = 4, integer dot products on block-scaled int16 activations, and a
  * row-per-lane bf16 kernel above; planes: the table-driven streaming kernel at M = 1 and a
  * sign-XOR kernel above; LM head: the row-per-lane kernel); 2 = the tcgen05 kernels
- * (dequantisation into tensor memory, tcgen05 MMA with fp32 accumulation); 3 (INT4 and the
- * LM head only, any M) = the warp-level MMA kernels (mma.sync m16n8k16 on bf16 fragments
- * unpacked in registers).  The library's choice for M >= 3 INT4 and for the LM head is 3:
+ * (dequantisation into tensor memory, tcgen05 MMA with fp32 accumulation); 3 (INT4, binary planes
+ * and the LM head, any M) = the warp-level MMA kernels (mma.sync m16n8k16 on bf16 fragments
+ * unpacked in registers; binary planes too).  The library's choice for M >= 3 INT4, for binary
+ * planes at M >= 2 and for the LM head is 3:
  * with 16 activation rows a 128-row tcgen05 MMA issues as slowly as with 64, and the
  * weight stream then outruns it.  Other values: INVALID_ARG.
  */

@@ -55,7 +55,7 @@ def gemm_bp_gpu(lb, x, packed, P, M, N, K, path=0):
 
 
 PATHS = (1, 2)   # 1 = CUDA-core kernels, 2 = tensor-core kernels (tcgen05)
-INT4_PATHS = (1, 2, 3)   # INT4 and the LM head also: 3 = warp-level MMA kernels
+INT4_PATHS = (1, 2, 3)   # INT4, binary planes and the LM head also: 3 = warp-level MMA kernels
 
 
 # ------------------------------------------------------------------------- packing
@@ -129,7 +129,7 @@ def test_int4_nan_activation(lb, M, path):
         check_gemm(y[1:], oint4.gemm(x[1:], codes, scales), f"int4 NaN rows 1.. path={path}")
 
 
-@pytest.mark.parametrize("M,path", [(1, 1), (16, 2)])
+@pytest.mark.parametrize("M,path", [(1, 1), (16, 2), (16, 3)])
 @pytest.mark.parametrize("kind", ("outlier", "mixed_scale", "tiny", "sparse"))
 def test_binplane_activation_structures(lb, kind, M, path):
     P, N, K = 3, 260, 1024
@@ -198,7 +198,7 @@ def test_int4_config2_remaining_projections(lb, proj):
 
 # ------------------------------------------------------------------------- binary planes
 
-@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("path", INT4_PATHS)
 @pytest.mark.parametrize("P,M,N,K", [(3, 1, 64, 256), (4, 2, 33, 128), (1, 16, 300, 512),
                                      (2, 5, 8, 1024), (3, 32, 40, 384), (8, 20, 130, 640)])
 def test_binplane_small_and_ragged(lb, P, M, N, K, path):
@@ -208,7 +208,7 @@ def test_binplane_small_and_ragged(lb, P, M, N, K, path):
     check_gemm(y, obp.gemm(x, bits, alpha), f"binplane P={P} M={M} N={N} K={K} path={path}")
 
 
-@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("path", INT4_PATHS)
 @pytest.mark.parametrize("shape", [0, 1])
 @pytest.mark.parametrize("P", synth.BINPLANE_PLANES)
 @pytest.mark.parametrize("M", (1, 16))

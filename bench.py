@@ -258,8 +258,9 @@ def build_binplane(lb, torch, l2, M, path, name, desc):
     return w
 
 
-def build_sa(lb, torch, l2, M, name, desc):
-    w = Workload(name, desc, "sa_stream_kernel" if M == 1 else "tc_gemm_kernel")
+def build_sa(lb, torch, l2, M, name, desc, path=0):
+    w = Workload(name, desc, "sa_stream_kernel" if M == 1 else
+                 {1: "binplane_cc_kernel", 2: "tc_gemm_kernel"}.get(path, "sa_mma_kernel"))
     mats = []
     for si, (K, N) in enumerate(synth.SA_SHAPES):
         for P, G in synth.SA_TYPES:
@@ -271,9 +272,9 @@ def build_sa(lb, torch, l2, M, name, desc):
     C = copies_for(w.bytes, l2)
     copies = [_copies(m[4], C, torch) for m in mats]
     for c in range(C):
-        w.calls.append([(lambda i=i, c=c: lb.lowbit_gemm_sa(
-            mats[i][5], copies[i][c], mats[i][0], mats[i][1], M, mats[i][3], mats[i][2], mats[i][6]))
-            for i in range(len(mats))])
+        w.calls.append([(lambda i=i, c=c: lb.lowbit_gemm_sa_path(
+            mats[i][5], copies[i][c], mats[i][0], mats[i][1], M, mats[i][3], mats[i][2], mats[i][6],
+            path)) for i in range(len(mats))])
     w.M, w.tokens, w.launches = M, M, len(mats)
     return w
 
@@ -379,7 +380,7 @@ def build_workload(lb, torch, l2, name, path):
         types = ", ".join(f"sa{P}{'' if G == 64 else '_' + str(G)}" for P, G in synth.SA_TYPES)
         return build_sa(lb, torch, l2, M, name,
                         f"deployed ShiftAdd format ({types}: u8 scale codes, fp16 d per 256 inputs): "
-                        f"(K,N) in {{(4096,12288),(12288,4096)}}, M={M}")
+                        f"(K,N) in {{(4096,12288),(12288,4096)}}, M={M}", path)
     if name in ("draft_m1", "draft_m16"):
         M = 1 if name == "draft_m1" else 16
         return build_draft_head(lb, torch, l2, M, name,
@@ -579,7 +580,7 @@ def run_ours(args):
     if not args.no_rows and rank == 0:
         names = [(n, 0) for n in WORKLOADS if n not in (args.workload, "tiny")]
         names += [("decode", 2), ("binplane_m1", 1), ("binplane_m1", 2), ("verify_all", 2),
-                  ("lmhead_full", 2), ("binplane_m16", 2)]
+                  ("lmhead_full", 2), ("binplane_m16", 2), ("sa_m16", 2)]
         names = [nm for nm in names if nm != (args.workload, args.path)]
         rows = measure_rows(lb, torch, peak, l2, names)
 

@@ -219,7 +219,7 @@ def lowbit_gemm_sa(X, packed, P, G, M, N, K, Y, stream=None):
 
 
 def lowbit_gemm_sa_path(X, packed, P, G, M, N, K, Y, path, stream=None):
-    """lowbit_gemm_sa with the kernel family forced (1 = CUDA cores, 2 = tensor cores)."""
+    """lowbit_gemm_sa with the kernel family forced (1 = CUDA cores, 2 = tcgen05, 3 = warp MMA)."""
     _gemm_args(X, packed, M, N, K, Y)
     _check(lib.lowbit_gemm_sa_path(_ptr(X), _ptr(packed), P, G, M, N, K, _ptr(Y), path,
                                    _stream(stream)), "lowbit_gemm_sa_path")

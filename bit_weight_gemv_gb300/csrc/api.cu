@@ -270,7 +270,7 @@ lowbit_status lowbit_gemm_sa(const uint16_t* X, const void* packed, int P, int G
 
 lowbit_status lowbit_gemm_sa_path(const uint16_t* X, const void* packed, int P, int G, int M,
                                   int N, int K, uint16_t* Y, int path, void* stream) {
-  if (!X || !packed || !Y || path < 0 || path > 2) return LOWBIT_ERR_INVALID_ARG;
+  if (!X || !packed || !Y || path < 0 || path > 3) return LOWBIT_ERR_INVALID_ARG;
   const lowbit_status st = check_sa(P, G, M, N, K);
   if (st != LOWBIT_OK) return st;
   if (!aligned16(X) || !aligned16(packed)) return LOWBIT_ERR_ALIGN;
@@ -278,11 +278,16 @@ lowbit_status lowbit_gemm_sa_path(const uint16_t* X, const void* packed, int P, 
   if (!err) return LOWBIT_ERR_CUDA;
   const uint8_t* pk = static_cast<const uint8_t*>(packed);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (path == 0) path = (M == 1) ? 1 : 2;
+  if (path == 0) path = (M == 1) ? 1 : 3;
   if (path == 1 && M == 1) {
     GemvProblem p = {X, pk, Y, N, K, 0, 1, 0, P, G};
     p.early = allocation_covers(pk, kHeaderBytes + sa_payload_bytes(P, G, N, K)) ? 1 : 0;
     return from_cuda(launch_sa_stream(&p, 1, err, s));
+  }
+  if (path == 3) {
+    GemvProblem p = {X, pk, Y, N, K, 0, 1, 0, P, G};
+    p.early = allocation_covers(pk, kHeaderBytes + sa_payload_bytes(P, G, N, K)) ? 1 : 0;
+    return from_cuda(launch_sa_mma(p, M, err, s));
   }
   if (path == 1) return from_cuda(launch_sa_cc(X, pk, P, G, M, N, K, Y, err, s));
   return from_cuda(launch_sa_tc(X, pk, P, G, M, N, K, Y, err, s));

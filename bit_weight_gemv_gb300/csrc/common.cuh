@@ -169,6 +169,8 @@ cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int M, int* 
 cudaError_t launch_int4_mma(const GemvProblem* probs, int count, int M, int* err, cudaStream_t s);
 // Binary planes (one matrix, P planes) on the same warp-level MMA kernel, 1 <= M <= 32.
 cudaError_t launch_bp_mma(const GemvProblem& prob, int M, int* err, cudaStream_t s);
+// The sa format (one matrix: P planes, code group G) on the same kernel, 1 <= M <= 32.
+cudaError_t launch_sa_mma(const GemvProblem& prob, int M, int* err, cudaStream_t s);
 struct LmheadWorkspace;
 cudaError_t launch_lmhead_mma(const GemvProblem& prob, int M, LmheadWorkspace* ws,
                               const int32_t* draft, int32_t* argmax, int32_t* n_accept,

@@ -951,16 +951,21 @@ nvfp4_stream_kernel(const __grid_constant__ StreamArgs a) {
 // the A fragment of the MMA -- to exact bf16 q (the nibble ORed into bf16 128.0, minus 136),
 // loads the activations' B fragments with ldmatrix and issues one MMA per 8 activation rows.
 // After a group's 128 inputs it adds s * D to fp32 totals held in registers.
-constexpr int kMmaInt4 = 0, kMmaPlanes = 1;  // weight formats of the warp-MMA kernels
-// Stage layout: the block, then the activation tile at the next 1024-byte boundary.
-__host__ __device__ constexpr uint32_t mma_block_bytes(int fmt, int P) {
-  return fmt == kMmaInt4 ? kInt4Block : (uint32_t)P * (kRowTile * 16 + kRowTile * 2);
+constexpr int kMmaInt4 = 0, kMmaPlanes = 1, kMmaSa = 2;  // weight formats of the warp-MMA kernels
+// Inputs per block: a group of 128 (INT4, binary planes) or an sa super-block of 256.
+__host__ __device__ constexpr int mma_kin(int fmt) { return fmt == kMmaSa ? kSuper : kGroup; }
+// Stage layout: the block, then the activation tile (kin inputs x MT rows, 64-input swizzle
+// atoms) at the next 1024-byte boundary.
+__host__ __device__ constexpr uint32_t mma_block_bytes(int fmt, int P, int GS) {
+  return fmt == kMmaInt4 ? kInt4Block
+       : fmt == kMmaPlanes ? (uint32_t)P * (kRowTile * 16 + kRowTile * 2)
+       : (uint32_t)P * 2 * kRowTile * 16 + (uint32_t)P * (kSuper / GS) * kRowTile + kRowTile * 2;
 }
-__host__ __device__ constexpr uint32_t mma_x_off(int fmt, int P) {
-  return (mma_block_bytes(fmt, P) + 1023u) / 1024u * 1024u;
+__host__ __device__ constexpr uint32_t mma_x_off(int fmt, int P, int GS) {
+  return (mma_block_bytes(fmt, P, GS) + 1023u) / 1024u * 1024u;
 }
-__host__ __device__ constexpr uint32_t mma_stage_bytes(int fmt, int P, int MT) {
-  return mma_x_off(fmt, P) + (uint32_t)MT * 2 * 128;
+__host__ __device__ constexpr uint32_t mma_stage_bytes(int fmt, int P, int GS, int MT) {
+  return mma_x_off(fmt, P, GS) + (uint32_t)MT * 2 * mma_kin(fmt);
 }
 // A pair of binary-plane signs -> the bf16 pair (+-1, +-1): bits `sh` below 15 and 31 of w
 // (set = +1) moved to the sign bits of bf16 -1.0.
@@ -973,6 +978,8 @@ constexpr int kMmaThreads = (kMmaWarps + 1) * 32;  // compute warps, producer
 // keeps four CTAs (MT = 16; three for MT = 32, by registers) on an SM.
 template <int MT> __host__ __device__ constexpr int mma_resident() { return MT == 16 ? 4 : 3; }
 constexpr size_t kMmaSmemBudget = 56 * 1024;
+// sa super-blocks with many planes need larger stages: two of them, fewer CTAs per SM
+constexpr size_t kMmaSmemBudgetMax = 110 * 1024;
 
 // Activations of every matrix of a launch as TMA tensor maps ([M][K] bf16, boxes of 64 inputs
 // x MT rows); the maps precede the arguments shared with the other streaming kernels.
@@ -1034,20 +1041,25 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
   const GemvProblem& pr = a.p[pi];
   const int ks = pr.ks, rank = crank % ks;
   const int tile = (cid - pr.cluster_begin) * (C / ks) + crank / ks;
-  const int G = pr.K / kGroup;
+  constexpr int KIN = mma_kin(FMT), NATOM = KIN / 64;
+  const int G = pr.K / KIN;  // blocks along K
   const bool live = tile < row_tiles(pr.N);
   const int g0 = (int)((long long)rank * G / ks), g1 = (int)((long long)(rank + 1) * G / ks);
   const int nb = live ? g1 - g0 : 0;
   const int S = a.stages, M = a.m;
   const PackedHeader* hp = reinterpret_cast<const PackedHeader*>(pr.packed);
-  const int P = FMT == kMmaInt4 ? 0 : pr.P;
-  const uint32_t BB = mma_block_bytes(FMT, P), XOFF = mma_x_off(FMT, P);
-  const uint32_t STG = mma_stage_bytes(FMT, P, MT);  // block, then two 64-input atoms of X
-  const uint32_t fmt_id = FMT == kMmaInt4 ? kFormatInt4 : kFormatBinplane;
+  const int P = FMT == kMmaInt4 ? 0 : pr.P, GS = FMT == kMmaSa ? pr.G : 0;
+  const uint32_t BB = mma_block_bytes(FMT, P, GS), XOFF = mma_x_off(FMT, P, GS);
+  const uint32_t STG = mma_stage_bytes(FMT, P, GS, MT);  // block, then the activation atoms
+  auto header_ok = [&]() {
+    return FMT == kMmaSa ? header_matches_sa(hp, P, GS, pr.N, pr.K)
+                         : header_matches(hp, FMT == kMmaInt4 ? kFormatInt4 : kFormatBinplane, P,
+                                          pr.N, pr.K);
+  };
 
   if (threadIdx.x < MT) kmax[threadIdx.x] = 0ull;
   if (threadIdx.x == 0) {
-    ok = live && (pr.early || header_matches(hp, fmt_id, P, pr.N, pr.K));
+    ok = live && (pr.early || header_ok());
     gave_up = 0;
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
@@ -1059,7 +1071,7 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
   if (threadIdx.x == 0) grid_launch();
   const bool hdr_ok = ok != 0;  // with `early`: only "this CTA has work"; see out_ok below
   if (threadIdx.x == 32) {  // a compute warp checks the header; the producer does not wait on it
-    const bool hv = header_matches(hp, fmt_id, P, pr.N, pr.K);
+    const bool hv = header_ok();
     hdr_valid = hv;
     if (!hv) ok = 0;
   }
@@ -1069,11 +1081,12 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
     if (hdr_ok && lane == 0) {
       const uint8_t* wsrc = pr.packed + kHeaderBytes + ((size_t)tile * G + g0) * BB;
       const CUtensorMap* xmap = &A.xmap[pi];
-      const uint32_t tx = BB + MT * 2 * 128;  // zero-filled rows count as copied
+      const uint32_t tx = BB + MT * 2 * KIN;  // zero-filled rows count as copied
       auto copy_x = [&](int b, int s, uint32_t bar) {
         const uint32_t dst = ptx::smem_addr(ring + (size_t)s * STG + XOFF);
-        ptx::tma_load_2d(dst, xmap, (g0 + b) * kGroup, 0, bar);
-        ptx::tma_load_2d(dst + MT * 128, xmap, (g0 + b) * kGroup + 64, 0, bar);
+#pragma unroll
+        for (int at = 0; at < NATOM; ++at)
+          ptx::tma_load_2d(dst + at * MT * 128, xmap, (g0 + b) * KIN + 64 * at, 0, bar);
       };
       const int pre = min(nb, S);
       for (int b = 0; b < pre; ++b) {
@@ -1167,7 +1180,7 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
           acc[i][2] = fmaf(s1, d[i][2], acc[i][2]);
           acc[i][3] = fmaf(s1, d[i][3], acc[i][3]);
         }
-      } else {
+      } else if constexpr (FMT == kMmaPlanes) {
         // Binary planes: word w of a plane row covers inputs 32w..32w+31, bit i the sign of
         // 32w + 2i and bit 16 + i that of 32w + 2i + 1.  Step s's A fragment takes pairs
         // i = 8 (s % 2) + t and i + 4 of word s / 2.
@@ -1200,6 +1213,53 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
             acc[i][1] = fmaf(s0, d[i][1], acc[i][1]);
             acc[i][2] = fmaf(s1, d[i][2], acc[i][2]);
             acc[i][3] = fmaf(s1, d[i][3], acc[i][3]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&empty[s]));
+      } else {
+        // sa format (ShiftAddQwen README, "Format"): a super-block of 256 inputs, per plane two
+        // halves of 128 laid out as a binary plane; alpha = d * a with one u8 code a per plane
+        // and group of GS inputs, so the MMA sums of every GS / 16 steps are folded with
+        // d * a (exact in fp32: 8 x 11 significant bits).
+        const int fk = GS / 16;  // steps per code group: 4, 8 or 16
+        const float d0 = half_bits_to_float(*reinterpret_cast<const uint16_t*>(st + sa_d_off(P, GS) + r0 * 2));
+        const float d1 = half_bits_to_float(*reinterpret_cast<const uint16_t*>(st + sa_d_off(P, GS) + (r0 + 8) * 2));
+        for (int p = 0; p < P; ++p) {
+          float d[NT][4];
+#pragma unroll
+          for (int i = 0; i < NT; ++i) d[i][0] = d[i][1] = d[i][2] = d[i][3] = 0.f;
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            const uint4 w0 = *reinterpret_cast<const uint4*>(st + (p * 2 + hb) * (kRowTile * 16) + r0 * 16);
+            const uint4 w1 = *reinterpret_cast<const uint4*>(st + (p * 2 + hb) * (kRowTile * 16) + (r0 + 8) * 16);
+            const uint32_t W0[4] = {w0.x, w0.y, w0.z, w0.w}, W1[4] = {w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+            for (int ss = 0; ss < 8; ++ss) {
+              const int kk = 8 * hb + ss;  // step within the super-block
+              const int sh = 15 - 8 * (ss & 1) - t;
+              const uint32_t a0 = pm1_pair(W0[ss >> 1], sh), a1 = pm1_pair(W1[ss >> 1], sh);
+              const uint32_t a2 = pm1_pair(W0[ss >> 1], sh - 4), a3 = pm1_pair(W1[ss >> 1], sh - 4);
+#pragma unroll
+              for (int hh = 0; hh < MT / 16; ++hh) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(xs + xsw[kk & 3] + (kk >> 2) * (MT * 128) + hh * 16 * 128, b0, b1, b2, b3);
+                mma_16816(d[2 * hh], a0, a1, a2, a3, b0, b1);
+                mma_16816(d[2 * hh + 1], a0, a1, a2, a3, b2, b3);
+              }
+              if ((kk & (fk - 1)) == fk - 1) {  // the code group's last step
+                const uint8_t* cd = st + sa_code_off(P) + (p * (kSuper / GS) + kk / fk) * kRowTile;
+                const float s0 = d0 * (float)cd[r0], s1 = d1 * (float)cd[r0 + 8];
+#pragma unroll
+                for (int i = 0; i < NT; ++i) {
+                  acc[i][0] = fmaf(s0, d[i][0], acc[i][0]);
+                  acc[i][1] = fmaf(s0, d[i][1], acc[i][1]);
+                  acc[i][2] = fmaf(s1, d[i][2], acc[i][2]);
+                  acc[i][3] = fmaf(s1, d[i][3], acc[i][3]);
+                  d[i][0] = d[i][1] = d[i][2] = d[i][3] = 0.f;
+                }
+              }
+            }
           }
         }
         __syncwarp();
@@ -1284,6 +1344,13 @@ template <int MT>
 __global__ void __launch_bounds__(kMmaThreads, mma_resident<MT>())
 bp_mma_kernel(const __grid_constant__ MmaArgs A) {
   mma_body<kMmaPlanes, MT, kEpiStore>(A);
+}
+
+// And for the deployed sa format: super-blocks of 256 inputs, alpha = d * a per code group.
+template <int MT>
+__global__ void __launch_bounds__(kMmaThreads, mma_resident<MT>())
+sa_mma_kernel(const __grid_constant__ MmaArgs A) {
+  mma_body<kMmaSa, MT, kEpiStore>(A);
 }
 
 int sm_count() {
@@ -1374,7 +1441,7 @@ constexpr int kMaxDevices = 64;
 struct OptIns {
   std::atomic<unsigned char> done[kMaxDevices];
 };
-OptIns g_int4_optins[3], g_bp_optins, g_sa_optins, g_nv_optins[2], g_mma_optins[6];  // one per kernel built
+OptIns g_int4_optins[3], g_bp_optins, g_sa_optins, g_nv_optins[2], g_mma_optins[8];  // one per kernel built
 
 template <typename Kernel>
 cudaError_t opt_in(Kernel kern, OptIns& o, size_t budget) {
@@ -1466,16 +1533,17 @@ template <int FMT, int MT, int EPI>
 cudaError_t launch_mma_mt(const GemvProblem* probs, int count, int M, LmheadWorkspace* ws,
                           const int32_t* draft, int32_t* argmax, int32_t* n_accept,
                           int32_t* bonus, int* err, cudaStream_t s) {
-  const int P = FMT == kMmaInt4 ? 0 : probs[0].P;
-  for (int i = 1; i < count; ++i)
-    if (FMT != kMmaInt4 && probs[i].P != P) return cudaErrorInvalidValue;  // one stage size
-  const uint32_t stage = mma_stage_bytes(FMT, P, MT);
+  const int P = FMT == kMmaInt4 ? 0 : probs[0].P, GS = FMT == kMmaSa ? probs[0].G : 0;
+  for (int i = 1; i < count; ++i)  // one stage size per launch
+    if (FMT != kMmaInt4 && (probs[i].P != P || probs[i].G != probs[0].G)) return cudaErrorInvalidValue;
+  const uint32_t stage = mma_stage_bytes(FMT, P, GS, MT);
   auto encode = x_map_encoder();
   if (!encode) return cudaErrorNotSupported;
   MmaArgs A = {};
   StreamArgs& a = A.s;
   Schedule sc;
-  if (!make_schedule(probs, count, kGroup, kInt4TargetBlocks, kMaxSplit, a, sc, mma_resident<MT>()))
+  if (!make_schedule(probs, count, mma_kin(FMT), FMT == kMmaSa ? kInt4TargetBlocks / 2 : kInt4TargetBlocks,
+                     kMaxSplit, a, sc, mma_resident<MT>()))
     return cudaErrorInvalidValue;
   a.err = err;
   a.m = M;
@@ -1495,19 +1563,23 @@ cudaError_t launch_mma_mt(const GemvProblem* probs, int count, int M, LmheadWork
                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  int S = (int)((kMmaSmemBudget - 1024) / stage);
-  S = S > kMaxStages ? kMaxStages : S;
-  if (S < 2) return cudaErrorInvalidValue;
+  const size_t budget = FMT == kMmaSa ? kMmaSmemBudgetMax : kMmaSmemBudget;
+  int S = (int)((kMmaSmemBudget - 1024) / stage);  // aims at four CTAs per SM
+  S = S > kMaxStages ? kMaxStages : (S < 2 ? 2 : S);
   a.stages = sc.maxnb < S ? sc.maxnb : S;
   // the totals [MT][128] reuse the ring; 1 KB of slack aligns the ring
   const size_t smem = std::max((size_t)a.stages * stage, (size_t)MT * kRowTile * sizeof(float)) + 1024;
+  if (smem > budget) return cudaErrorInvalidValue;
   if constexpr (FMT == kMmaInt4) {
     constexpr int slot_i = (MT == 16 ? 0 : 1) + 2 * EPI;
-    return launch_streaming(int4_mma_kernel<MT, EPI>, g_mma_optins[slot_i], kMmaSmemBudget, A, sc,
+    return launch_streaming(int4_mma_kernel<MT, EPI>, g_mma_optins[slot_i], budget, A, sc, smem,
+                            kMmaThreads, s);
+  } else if constexpr (FMT == kMmaPlanes) {
+    return launch_streaming(bp_mma_kernel<MT>, g_mma_optins[MT == 16 ? 4 : 5], budget, A, sc,
                             smem, kMmaThreads, s);
   } else {
-    return launch_streaming(bp_mma_kernel<MT>, g_mma_optins[MT == 16 ? 4 : 5], kMmaSmemBudget, A,
-                            sc, smem, kMmaThreads, s);
+    return launch_streaming(sa_mma_kernel<MT>, g_mma_optins[MT == 16 ? 6 : 7], budget, A, sc,
+                            smem, kMmaThreads, s);
   }
 }
 
@@ -1520,6 +1592,16 @@ cudaError_t launch_int4_mma(const GemvProblem* probs, int count, int M, int* err
                                                   nullptr, nullptr, err, s);
   return launch_mma_mt<kMmaInt4, 32, kEpiStore>(probs, count, M, nullptr, nullptr, nullptr,
                                                 nullptr, nullptr, err, s);
+}
+
+cudaError_t launch_sa_mma(const GemvProblem& prob, int M, int* err, cudaStream_t s) {
+  if (M < 1 || M > 32 || prob.P < 1 || prob.P > 8) return cudaErrorInvalidValue;
+  if (prob.G != 64 && prob.G != 128 && prob.G != 256) return cudaErrorInvalidValue;
+  if (M <= 16)
+    return launch_mma_mt<kMmaSa, 16, kEpiStore>(&prob, 1, M, nullptr, nullptr, nullptr, nullptr,
+                                                nullptr, err, s);
+  return launch_mma_mt<kMmaSa, 32, kEpiStore>(&prob, 1, M, nullptr, nullptr, nullptr, nullptr,
+                                              nullptr, err, s);
 }
 
 cudaError_t launch_bp_mma(const GemvProblem& prob, int M, int* err, cudaStream_t s) {

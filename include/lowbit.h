@@ -210,8 +210,8 @@ lowbit_status lowbit_gemm_binplane(const uint16_t* X, const void* packed, int P,
  *   fp32 accumulation, each output rounded once to bf16.  X, Y as lowbit_gemm_int4,
  *   1 <= M <= 32; packed from lowbit_pack_sa(P, G, N, K); K % 256 == 0.  M = 1 runs the
  *   streaming mat-vec (per plane a table-driven sign-select-and-add, one scale per group);
- *   M >= 2 runs the tensor-core GEMM (weights written as +-a in bf16, d applied per 256
- *   inputs in fp32).
+ *   M >= 2 runs the warp-level MMA on exact +-1 fragments, each code group's sums scaled by
+ *   d * a in fp32 (path 2: the tcgen05 GEMM, weights written as +-a in bf16).
  *   The header (format 3, P, N, K, G) is checked on the device as for the other formats. */
 lowbit_status lowbit_gemm_sa(const uint16_t* X, const void* packed, int P, int G, int M, int N,
                              int K, uint16_t* Y, void* stream);
@@ -284,10 +284,10 @@ lowbit_status lmhead_argmax_verify_noalloc(const uint16_t* H, const void* packed
  * kernel up to M = 4, integer dot products on block-scaled int16 activations, and a
  * row-per-lane bf16 kernel above; planes: the table-driven streaming kernel at M = 1 and a
  * sign-XOR kernel above; LM head: the row-per-lane kernel); 2 = the tcgen05 kernels
- * (dequantisation into tensor memory, tcgen05 MMA with fp32 accumulation); 3 (INT4, binary planes
- * and the LM head, any M) = the warp-level MMA kernels (mma.sync m16n8k16 on bf16 fragments
+ * (dequantisation into tensor memory, tcgen05 MMA with fp32 accumulation); 3 (INT4, binary planes,
+ * the sa format and the LM head, any M) = the warp-level MMA kernels (mma.sync m16n8k16 on bf16 fragments
  * unpacked in registers; binary planes too).  The library's choice for M >= 3 INT4, for binary
- * planes at M >= 2 and for the LM head is 3:
+ * planes and the sa format at M >= 2 and for the LM head is 3:
  * with 16 activation rows a 128-row tcgen05 MMA issues as slowly as with 64, and the
  * weight stream then outruns it.  Other values: INVALID_ARG.
  */

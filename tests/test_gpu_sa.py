@@ -49,7 +49,7 @@ def test_pack_sa_bit_exact(lb, P, G, N, K):
     assert g2 == G and np.array_equal(b2, bits) and np.array_equal(c2, codes) and np.array_equal(d2, d)
 
 
-@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("path", [1, 2, 3])
 @pytest.mark.parametrize("M", [1, 2, 3, 16, 32])
 @pytest.mark.parametrize("P,G,N,K", [(1, 64, 1, 256), (2, 64, 65, 512), (3, 128, 257, 1280),
                                      (4, 256, 300, 768), (6, 64, 130, 256), (8, 128, 100, 512),
@@ -60,7 +60,7 @@ def test_sa_small_and_ragged(lb, P, G, N, K, M, path):
     check_gemm(y, osa.gemm(x, bits, codes, d, G), f"sa P={P} G={G} M={M} N={N} K={K} path={path}")
 
 
-@pytest.mark.parametrize("M,path", [(1, 0), (16, 0), (16, 1)])
+@pytest.mark.parametrize("M,path", [(1, 0), (16, 0), (16, 1), (16, 2)])
 @pytest.mark.parametrize("P,G", synth.SA_TYPES)
 @pytest.mark.parametrize("shape", range(len(synth.SA_SHAPES)))
 def test_sa_config3_shapes(lb, shape, P, G, M, path):
@@ -88,7 +88,7 @@ def test_sa_m1_activation_structures(lb, kind):
                scale=2.0 ** 90 if kind == "tiny" else 1.0)
 
 
-@pytest.mark.parametrize("M,path", [(1, 0), (4, 1), (4, 2)])
+@pytest.mark.parametrize("M,path", [(1, 0), (4, 1), (4, 2), (4, 3)])
 @pytest.mark.parametrize("wrong", ["G", "P", "N"])
 def test_sa_header_mismatch_leaves_outputs(lb, wrong, M, path):
     """A buffer packed for other (P, G, N) is rejected on the device: the error word is set and
@@ -121,5 +121,5 @@ def test_sa_validation(lb):
             lb.lowbit_gemm_sa(X, packed, P2, G2, M2, N, K2, Y)
         assert e.value.status == 2, (P2, G2, M2, K2)
     with pytest.raises(lb.LowbitError) as e:
-        lb.lowbit_gemm_sa_path(X, packed, P, G, 1, N, K, Y, 3)
+        lb.lowbit_gemm_sa_path(X, packed, P, G, 1, N, K, Y, 4)
     assert e.value.status == 1

@@ -77,14 +77,15 @@ def test_sa_config3_shapes(lb, shape, P, G, M, path):
                    f"sa config 3 shape {shape} M=16 sampled")
 
 
+@pytest.mark.parametrize("M,path", [(1, 0), (16, 2), (16, 3)])
 @pytest.mark.parametrize("kind", ("outlier", "mixed_scale", "tiny", "sparse"))
-def test_sa_m1_activation_structures(lb, kind):
+def test_sa_activation_structures(lb, kind, M, path):
     P, G, N, K = 3, 64, 260, 1024
     g = synth.generator(23, synth.ACTIVATION_KINDS.index(kind))
     bits, codes, d = synth.sa_weights(g, P, N, K, G)
-    x = synth.activation_variant(g, 1, K, kind)
-    y = gemm_sa_gpu(lb, x, pack_sa_gpu(lb, bits, codes, d, G), P, G, 1, N, K)
-    check_gemm(y, osa.gemm(x, bits, codes, d, G), f"sa {kind}",
+    x = synth.activation_variant(g, M, K, kind)
+    y = gemm_sa_gpu(lb, x, pack_sa_gpu(lb, bits, codes, d, G), P, G, M, N, K, path)
+    check_gemm(y, osa.gemm(x, bits, codes, d, G), f"sa {kind} M={M} path={path}",
                scale=2.0 ** 90 if kind == "tiny" else 1.0)
 
 

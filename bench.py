@@ -75,6 +75,39 @@ def read_peaks():
     return 6800.0, "fallback"
 
 
+def read_tensor_peak():
+    """bf16 dense tensor peak in TFLOP/s for a kernel timed alone (burst), and its source."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
+def step_stats(torch, rep, steps, repeats=20):
+    """Per-step device time over `repeats` separately timed runs of steps // repeats steps
+    each (after the main measurement): median, p10 and p90 in microseconds."""
+    each = max(1, steps // repeats)
+    ts = []
+    for r in range(repeats):
+        ts.append(time_graphs(torch, rep, each, 0) / each * 1e6)
+    ts.sort()
+    q = lambda f: ts[min(len(ts) - 1, int(round(f * (len(ts) - 1))))]
+    return {"median_us": round(q(0.5), 3), "p10_us": round(q(0.1), 3), "p90_us": round(q(0.9), 3),
+            "repeats": repeats, "steps_each": each}
+
+
+def cold_step_us(torch, rep, l2_bytes):
+    """One step right after L2 has been overwritten (a buffer twice its size), timed alone."""
+    flush = torch.empty(2 * l2_bytes, dtype=torch.uint8, device="cuda")
+    flush.fill_(1)
+    torch.cuda.synchronize()
+    us = time_graphs(torch, rep, 1, 0) * 1e6
+    del flush
+    return round(us, 3)
+
 def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), \
         int(os.environ.get("LOCAL_RANK", 0))
@@ -184,6 +217,7 @@ class Workload:
         self.tokens = 0
         self.launches = 0
         self.M = 0
+        self.weights = 0         # weight elements per step (N*K summed), for tensor flops
         self.host_io = None      # (inputs on device, outputs on device) for the e2e leg
 
     def step(self, c):
@@ -209,6 +243,7 @@ def build_int4_layer(lb, torch, l2, M, path, seed, name, desc, grouping=None):
                  else {1: "int4_gemm_cc_kernel", 2: "tc_gemm_kernel"}.get(path, "int4_mma_kernel"))
     shapes = [(k, n) for _, k, n in synth.LAYER_4B]
     w.bytes = sum(algorithmic_int4_bytes(N, K) for K, N in shapes)
+    w.weights = sum(N * K for K, N in shapes)
     C = copies_for(w.bytes, l2)
     packs, X, Y = [], [], []
     for j, (K, N) in enumerate(shapes):
@@ -248,6 +283,7 @@ def build_binplane(lb, torch, l2, M, path, name, desc):
             lb.lowbit_pack_binplane(dev(bits), f16_dev(alpha), P, N, K, p)
             mats.append((P, K, N, p, bf16_dev(x), torch.empty((M, N), dtype=torch.bfloat16, device="cuda")))
             w.bytes += algorithmic_binplane_bytes(P, N, K)
+            w.weights += N * K
     C = copies_for(w.bytes, l2)
     copies = [_copies(m[3], C, torch) for m in mats]
     for c in range(C):
@@ -269,6 +305,7 @@ def build_sa(lb, torch, l2, M, name, desc, path=0):
             lb.lowbit_pack_sa(dev(bits), dev(codes), f16_dev(d), P, G, N, K, p)
             mats.append((P, G, K, N, p, bf16_dev(x), torch.empty((M, N), dtype=torch.bfloat16, device="cuda")))
             w.bytes += algorithmic_sa_bytes(P, G, N, K)
+            w.weights += N * K
     C = copies_for(w.bytes, l2)
     copies = [_copies(m[4], C, torch) for m in mats]
     for c in range(C):
@@ -287,6 +324,7 @@ def build_draft_head(lb, torch, l2, M, name, desc):
     p = torch.empty(lb.lowbit_nvfp4_packed_bytes(N, K), dtype=torch.uint8, device="cuda")
     lb.lowbit_pack_nvfp4(dev(codes), dev(scales), g, N, K, p)
     w.bytes = algorithmic_nvfp4_bytes(N, K)
+    w.weights = N * K
     packs = _copies(p, copies_for(w.bytes, l2), torch)
     H, idm = bf16_dev(h), dev(ids)
     out = torch.empty(M, dtype=torch.int32, device="cuda")
@@ -305,6 +343,7 @@ def build_lmhead(lb, torch, l2, N, path, name, desc):
     lb.lowbit_pack_int4(dev(codes), f16_dev(scales), N, K, p)
     del codes
     w.bytes = algorithmic_int4_bytes(N, K)
+    w.weights = N * K
     C = copies_for(w.bytes, l2, 2)
     packs = _copies(p, C, torch)
     H = bf16_dev(h)
@@ -329,6 +368,7 @@ def build_head_gemv(lb, torch, l2, path, name, desc):
     lb.lowbit_pack_int4(dev(codes), f16_dev(scales), N, K, p)
     del codes
     w.bytes = algorithmic_int4_bytes(N, K)
+    w.weights = N * K
     packs = _copies(p, copies_for(w.bytes, l2, 2), torch)
     X, Y = bf16_dev(x), torch.empty((1, N), dtype=torch.bfloat16, device="cuda")
     for c in range(len(packs)):
@@ -471,8 +511,11 @@ def copies_for(bytes_per_copy, l2_bytes, factor=4):
 
 
 def measure_rows(lb, torch, peak, l2, names, budget_s=0.5):
-    """Secondary rows: every other workload, timed the same way (CUDA graphs, rotation)."""
+    """Secondary rows: every other workload, timed the same way (CUDA graphs, rotation), with
+    the spread of 10 separately timed repeats and, at M >= 16, the fraction of the bf16 tensor
+    peak (dense-equivalent 2*M*N*K flops)."""
     rows = {}
+    tpeak, _ = read_tensor_peak()
     for name, path in names:
         w = build_workload(lb, torch, l2, name, path)
         graphs = capture(torch, w, len(w.calls))
@@ -485,7 +528,12 @@ def measure_rows(lb, torch, peak, l2, names, budget_s=0.5):
         rows[key] = {"us_per_step": round(per * 1e6, 3), "GB_s": round(gbs, 1),
                      "frac_of_hbm_peak": round(gbs / peak, 4), "tok_s": round(w.tokens / per, 1),
                      "kernel": w.kernel, "launches_per_step": w.launches, "steps": steps,
-                     "weight_bytes_per_step": w.bytes}
+                     "weight_bytes_per_step": w.bytes,
+                     "spread": step_stats(torch, graphs, max(10, steps // 2), repeats=10)}
+        if w.M >= 16 and w.weights:
+            tf = 2.0 * w.M * w.weights / per / 1e12
+            rows[key]["tensor_tflops"] = round(tf, 2)
+            rows[key]["frac_of_tensor_peak"] = round(tf / tpeak, 4)
         del graphs, w
         torch.cuda.empty_cache()
     return rows
@@ -534,6 +582,9 @@ def run_ours(args):
     units = w.bytes * args.steps
     rate, slowest = whole_job_rate(units, secs, world)
     per_rank_gbs = units / secs / 1e9
+    # outside the timed region: the spread of separately timed repeats, and one cold step
+    spread = step_stats(torch, graphs, args.steps)
+    cold = cold_step_us(torch, graphs, l2)
     del graphs
 
     # e2e through the public API with host buffers: every step copies the step's activations
@@ -613,8 +664,16 @@ def run_ours(args):
             "e2e": e2e,
             "gpu_launches": w.launches * args.steps,
             "clocks": clocks,
+            "step_time_spread": spread,
+            "cold_step_us": cold,
             "rows": rows,
         }
+        if w.M >= 16 and w.weights:
+            tpeak, tkind = read_tensor_peak()
+            tf = 2.0 * w.M * w.weights * args.steps / secs / 1e12
+            out["tensor"] = {"tflops": round(tf, 2), "peak": tpeak, "peak_source": tkind,
+                             "frac": round(tf / tpeak, 4),
+                             "flops": "dense-equivalent 2*M*N*K per matrix"}
         print(json.dumps(out))
     if world > 1:
         import torch.distributed as dist

@@ -78,3 +78,38 @@ def test_host_validation_rejects_before_any_launch(lib):
                   ctypes.c_size_t, vp]
     assert g(fake, fake, 16, 64, 128, fake, fake, fake, fake, fake, 100, None) == 4  # workspace
     assert g(fake, fake, 1, 64, 128, fake, fake, fake, fake, fake, 512, None) == 2   # M < 2
+
+
+def test_kernel_family_selection_is_validated_on_the_host(lib):
+    """The `_path` calls reject unknown families and shapes a family cannot take before
+    touching the device (status 1 = invalid argument, 2 = shape)."""
+    vp, ci = ctypes.c_void_p, ctypes.c_int
+    fake = vp(0x1000)
+    f = lib.lowbit_gemm_int4_path
+    f.argtypes = [vp, vp, ci, ci, ci, vp, ci, vp]
+    assert f(fake, fake, 16, 64, 128, fake, 4, None) == 1
+    assert f(fake, fake, 16, 64, 128, fake, -1, None) == 1
+    b = lib.lowbit_gemm_binplane_path
+    b.argtypes = [vp, vp, ci, ci, ci, ci, vp, ci, vp]
+    assert b(fake, fake, 3, 16, 64, 128, fake, 4, None) == 1
+    sa = lib.lowbit_gemm_sa_path
+    sa.argtypes = [vp, vp, ci, ci, ci, ci, ci, vp, ci, vp]
+    assert sa(fake, fake, 3, 64, 16, 64, 256, fake, 4, None) == 1
+    nv = lib.lowbit_gemm_nvfp4_path
+    nv.argtypes = [vp, vp, ci, ci, ci, vp, ci, vp]
+    assert nv(fake, fake, 2, 64, 128, fake, 1, None) == 2         # the streaming kernel is M = 1
+    assert nv(fake, fake, 1, 64, 128, fake, 3, None) == 1
+    d = lib.lowbit_draft_argmax_path
+    d.argtypes = [vp, vp, ci, ci, ci, vp, vp, vp, ctypes.c_size_t, ci, vp]
+    assert d(fake, fake, 2, 64, 128, None, fake, fake, 512, 1, None) == 2
+    assert d(fake, fake, 1, 64, 128, None, fake, fake, 512, 7, None) == 1
+
+    class Desc(ctypes.Structure):
+        _fields_ = [("X", vp), ("packed", vp), ("Y", vp), ("N", ci), ("K", ci)]
+
+    arr = (Desc * 2)(Desc(fake, fake, fake, 64, 128), Desc(fake, fake, fake, 32, 256))
+    g = lib.lowbit_gemm_int4_grouped_path
+    g.argtypes = [vp, ci, ci, ci, vp]
+    assert g(ctypes.cast(arr, vp), 2, 16, 4, None) == 1
+    assert g(ctypes.cast(arr, vp), 2, 5, 1, None) == 2           # the streaming kernel takes M <= 4
+    assert g(ctypes.cast(arr, vp), 9, 16, 0, None) == 1           # at most 8 problems

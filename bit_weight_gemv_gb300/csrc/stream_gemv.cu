@@ -967,15 +967,15 @@ __host__ __device__ constexpr uint32_t mma_x_off(int fmt, int P, int GS) {
 __host__ __device__ constexpr uint32_t mma_stage_bytes(int fmt, int P, int GS, int MT) {
   return mma_x_off(fmt, P, GS) + (uint32_t)MT * 2 * mma_kin(fmt);
 }
-// A pair of binary-plane signs -> the bf16 pair (+-1, +-1): bits `sh` below 15 and 31 of w
-// (set = +1) moved to the sign bits of bf16 -1.0.
+// A pair of binary-plane signs -> the bf16 pair (+-1, +-1): bits 15 - sh and 31 - sh of w
+// (set = +1) shifted onto the sign bits and XORed into bf16 (-1.0, -1.0).
 __device__ __forceinline__ uint32_t pm1_pair(uint32_t w, int sh) {
   return ((w << sh) & 0x80008000u) ^ 0xBF80BF80u;
 }
 constexpr int kMmaWarps = 8;
 constexpr int kMmaThreads = (kMmaWarps + 1) * 32;  // compute warps, producer
-// Occupancy is what hides the dequantisation's latency: about 50 KB of shared memory per CTA
-// keeps four CTAs (MT = 16; three for MT = 32, by registers) on an SM.
+// Occupancy is what hides the fragment unpacking's latency: about 55 KB of shared memory per
+// CTA keeps four CTAs (MT = 16; three for MT = 32, by registers) on an SM.
 template <int MT> __host__ __device__ constexpr int mma_resident() { return MT == 16 ? 4 : 3; }
 constexpr size_t kMmaSmemBudget = 56 * 1024;
 // sa super-blocks with many planes need larger stages: two of them, fewer CTAs per SM
@@ -1008,8 +1008,8 @@ __device__ __forceinline__ uint32_t bf16x2_sub_rn(uint32_t a, uint32_t b) {
   asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
-// Nibbles 0 and 4 of a code word (the pair k, k+1 at bits 0..3 and 16..19) -> bf16 pair (q, q+1)
-// exactly: 128 + u in bf16, minus 136.
+// The nibbles at bits 0..3 and 16..19 of a code word (inputs k and k+1) -> the bf16 pair
+// (q[k], q[k+1]) exactly: 128 + u in bf16, minus 136.
 __device__ __forceinline__ uint32_t q_pair(uint32_t w) {
   return bf16x2_sub_rn((w & 0x000F000Fu) | 0x43004300u, 0x43084308u);
 }
@@ -1027,9 +1027,9 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
   __shared__ int gave_up;
   __shared__ int hdr_valid;  // the same in every CTA: they all read the one header
   __shared__ unsigned long long kmax[MT];  // verify: this CTA's best key per activation row
-  // Totals [MT][128], written once every stage has been consumed: they reuse the ring (at
-  // least two stages, 25 KB).  After a timed-out wait a late copy may still land there; the
-  // outputs are wrong then anyway and the error word says so.
+  // Totals [MT][128], written once every stage has been consumed: they reuse the ring (the
+  // launcher allocates at least MT * 512 bytes).  After a timed-out wait a late copy may still
+  // land there; the outputs are wrong then anyway and the error word says so.
   float (*part)[kRowTile] = reinterpret_cast<float (*)[kRowTile]>(ring);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

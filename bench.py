@@ -239,6 +239,8 @@ LAYER_GROUPS = {"deps": ((0, 1, 2), (3,), (4, 5), (6,)), "all": ((0, 1, 2, 3, 4,
 
 
 def build_int4_layer(lb, torch, l2, M, path, seed, name, desc, grouping=None):
+    if grouping is not None and path == 1 and M > 4:
+        path = 0  # grouped calls have no CUDA-core kernel above the streaming kernel's 4 rows
     w = Workload(name, desc, "int4_stream_kernel" if ((M <= 2 and path == 0) or (M <= 4 and path == 1))
                  else {1: "int4_gemm_cc_kernel", 2: "tc_gemm_kernel"}.get(path, "int4_mma_kernel"))
     shapes = [(k, n) for _, k, n in synth.LAYER_4B]
@@ -262,8 +264,7 @@ def build_int4_layer(lb, torch, l2, M, path, seed, name, desc, grouping=None):
         groups = LAYER_GROUPS[grouping]
         for c in range(C):
             w.calls.append([(lambda grp=grp, c=c: lb.lowbit_gemm_int4_grouped_path(
-                [(X[j], packs[j][c], shapes[j][1], shapes[j][0], Y[j]) for j in grp], M,
-                path if (path != 1 or M <= 4) else 0))
+                [(X[j], packs[j][c], shapes[j][1], shapes[j][0], Y[j]) for j in grp], M, path))
                 for grp in groups])
         w.launches = len(groups)
     w.M, w.tokens = M, M

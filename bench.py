@@ -91,8 +91,8 @@ def step_stats(torch, rep, steps, repeats=20):
     each (after the main measurement): median, p10 and p90 in microseconds."""
     each = max(1, steps // repeats)
     ts = []
-    for r in range(repeats):
-        ts.append(time_graphs(torch, rep, each, 0) / each * 1e6)
+    for r in range(repeats):  # the rotation continues, so no repeat re-reads an L2-resident copy
+        ts.append(time_graphs(torch, rep, each, 0, start=r * each) / each * 1e6)
     ts.sort()
     q = lambda f: ts[min(len(ts) - 1, int(round(f * (len(ts) - 1))))]
     return {"median_us": round(q(0.5), 3), "p10_us": round(q(0.1), 3), "p90_us": round(q(0.9), 3),
@@ -247,14 +247,21 @@ def build_int4_layer(lb, torch, l2, M, path, seed, name, desc, grouping=None):
     w.bytes = sum(algorithmic_int4_bytes(N, K) for K, N in shapes)
     w.weights = sum(N * K for K, N in shapes)
     C = copies_for(w.bytes, l2)
+    # one device buffer for all activations and one for all outputs (16-byte aligned views),
+    # so an end-to-end step moves them with one copy each way
+    xoff = np.cumsum([0] + [M * K for K, _ in shapes])
+    yoff = np.cumsum([0] + [M * N for _, N in shapes])
+    Xflat = torch.empty(int(xoff[-1]), dtype=torch.bfloat16, device="cuda")
+    Yflat = torch.empty(int(yoff[-1]), dtype=torch.bfloat16, device="cuda")
     packs, X, Y = [], [], []
     for j, (K, N) in enumerate(shapes):
         codes, scales, x = synth.int4_problem(seed, M, N, K, j)
         p = torch.empty(lb.lowbit_int4_packed_bytes(N, K), dtype=torch.uint8, device="cuda")
         lb.lowbit_pack_int4(dev(codes), f16_dev(scales), N, K, p)
         packs.append(_copies(p, C, torch))
-        X.append(bf16_dev(x))
-        Y.append(torch.empty((M, N), dtype=torch.bfloat16, device="cuda"))
+        X.append(Xflat[int(xoff[j]):int(xoff[j + 1])].view(M, K))
+        X[-1].copy_(bf16_dev(x))
+        Y.append(Yflat[int(yoff[j]):int(yoff[j + 1])].view(M, N))
     if grouping is None:
         for c in range(C):
             w.calls.append([(lambda j=j, K=K, N=N, c=c: lb.lowbit_gemm_int4_path(
@@ -268,7 +275,7 @@ def build_int4_layer(lb, torch, l2, M, path, seed, name, desc, grouping=None):
                 for grp in groups])
         w.launches = len(groups)
     w.M, w.tokens = M, M
-    w.host_io = (X, Y)
+    w.host_io = (Xflat, Yflat)
     return w
 
 
@@ -444,53 +451,79 @@ WORKLOADS = ("decode", "decode_deps", "decode_all", "verify", "verify_deps", "ve
 
 
 class Replay:
-    """CUDA graphs for a workload: `full` replays one whole rotation (n steps, one per weight
-    copy) so the host pays one graph launch per n steps; `single[i]` replays step i alone and
-    tops a timed run up to an exact step count."""
+    """CUDA graphs for a workload, captured ahead of any timed region.
 
-    def __init__(self, full, single, n):
-        self.full, self.single, self.n = full, single, n
+    A run of `steps` steps starting at weight copy `start` is replayed from graphs covering
+    exactly those steps: one graph when the run is short (up to `short` steps), otherwise a
+    graph up to the next rotation boundary, whole-rotation graphs (n steps, one per weight
+    copy) and a graph for the remainder.  Graphs are captured on first use and cached, so the
+    host pays a handful of graph launches per timed run and the GPU sees the steps back to back."""
+
+    def __init__(self, torch, step, n, short=512):
+        self.torch, self.step, self.n, self.short = torch, step, n, short
+        self.cache = {}
+
+    def _graph(self, start, length):
+        key = (start % self.n, length)
+        g = self.cache.get(key)
+        if g is None:
+            torch = self.torch
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, capture_error_mode="thread_local"):
+                for i in range(start, start + length):
+                    self.step(i)
+            torch.cuda.synchronize()
+            self.cache[key] = g
+        return g
+
+    def plan(self, steps, start=0):
+        """The graphs that replay steps start .. start + steps - 1 (captured now if needed)."""
+        if steps <= 0:
+            return []
+        if steps <= self.short:
+            return [self._graph(start, steps)]
+        out, i = [], start
+        head = (-i) % self.n
+        if head:
+            out.append(self._graph(i, head))
+            i += head
+        full = (start + steps - i) // self.n
+        out += [self._graph(0, self.n)] * full
+        i += full * self.n
+        if start + steps > i:
+            out.append(self._graph(i, start + steps - i))
+        return out
 
     def run(self, steps, start=0):
-        i = start
-        while steps > 0:
-            if i % self.n == 0 and steps >= self.n:
-                self.full.replay()
-                steps -= self.n
-                i += self.n
-            else:
-                self.single[i % self.n].replay()
-                steps -= 1
-                i += 1
-        return i
+        for g in self.plan(steps, start):
+            g.replay()
+        return start + steps
 
 
 def capture(torch, w, n):
+    """Eager warm-up of every weight copy (outside any capture), then a graph replayer."""
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
         for i in range(n):
-            w.step(i)                  # eager warm-up outside capture
+            w.step(i)
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
-    single = []
-    for i in range(n):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, capture_error_mode="thread_local"):
-            w.step(i)
-        single.append(g)
-    full = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(full, capture_error_mode="thread_local"):
-        for i in range(n):
-            w.step(i)
-    torch.cuda.synchronize()
-    return Replay(full, single, n)
+    return Replay(torch, w.step, n)
 
 
-def time_graphs(torch, rep, steps, warmup, world=1):
+def time_graphs(torch, rep, steps, warmup, world=1, start=0):
     """Device time of exactly `steps` steps after `warmup` untimed ones (CUDA events on the
-    launching stream, barrier + synchronize on both sides)."""
-    rep.run(warmup)
+    launching stream, barrier + synchronize on both sides).  Every graph either run replays is
+    captured before the timed region starts."""
+    warm = rep.plan(warmup, start)
+    timed = rep.plan(steps, start + warmup)
+    # a graph's first launch also uploads it to the device: launch every graph of the timed
+    # run once beforehand (untimed), then the W warm-up steps
+    for g in {id(g): g for g in timed}.values():
+        g.replay()
+    for g in warm:
+        g.replay()
     torch.cuda.synchronize()
     if world > 1:
         import torch.distributed as dist
@@ -498,7 +531,8 @@ def time_graphs(torch, rep, steps, warmup, world=1):
     st = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(st)
-    rep.run(steps)
+    for g in timed:
+        g.replay()
     e1.record(st)
     torch.cuda.synchronize()
     if world > 1:
@@ -561,6 +595,54 @@ def cpu_baseline_oracle(budget_s=10.0, rows_fraction=1.0):
     return nbytes * reps / secs / 1e9, reps, nbytes, secs
 
 
+THREAD_ENV = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+
+
+def os_threads():
+    """Threads of this process right now (Linux), or None."""
+    try:
+        return len(os.listdir("/proc/self/task"))
+    except OSError:
+        return None
+
+
+def cpu_baseline_child(threads, budget_s):
+    """Time the oracle in a fresh interpreter whose BLAS and OpenMP pools are limited to
+    `threads` (the limit is read when numpy loads, so it needs its own process)."""
+    env = dict(os.environ)
+    for k in THREAD_ENV:
+        env[k] = str(threads)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-child",
+                        "--cpu-budget", str(budget_s)], env=env, capture_output=True, text=True,
+                       timeout=budget_s * 6 + 120)
+    if r.returncode != 0:
+        return None
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    d["threads_requested"] = threads
+    return d
+
+
+def cpu_baseline_two_modes(budget_s):
+    """SURVEY-style CPU baseline: the oracle with one thread and with every host core."""
+    cores = os.cpu_count() or 1
+    one = cpu_baseline_child(1, budget_s / 2)
+    allc = cpu_baseline_child(cores, budget_s / 2)
+    if allc is None:
+        return None
+    sample = (f"{allc['reps']} passes of the oracle (numpy fp64 dequant + multiply) over "
+              f"{allc['row_fraction']:.2%} of the rows of each of the seven M=1 projections of one "
+              f"layer ({allc['nbytes']} algorithmic bytes per pass), {allc['secs']:.1f} s")
+    out = {"value": round(allc["gbs"], 4), "unit": "GB/s", "cores": allc["threads_requested"],
+           "threads_seen": allc["threads_seen"], "kind": "oracle", "sample": sample,
+           "thread_env": ",".join(THREAD_ENV)}
+    if one is not None:
+        out["one_thread"] = {"value": round(one["gbs"], 4), "unit": "GB/s", "cores": 1,
+                             "threads_seen": one["threads_seen"],
+                             "sample": f"{one['reps']} passes over {one['row_fraction']:.2%} of "
+                                       f"the rows ({one['nbytes']} bytes per pass), {one['secs']:.1f} s"}
+    return out
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_env()
@@ -589,23 +671,36 @@ def run_ours(args):
     del graphs
 
     # e2e through the public API with host buffers: every step copies the step's activations
-    # in from pinned host memory, runs the step's calls, and copies the outputs back.
+    # in from pinned host memory (one copy), makes the step's library calls, and copies all
+    # outputs back (one copy).  Timed on the host clock around graph replays of those steps,
+    # the way a serving loop issues a decode step; the same steps issued eagerly from Python
+    # are reported beside it as the host's issue rate.
     e2e = None
     if w.host_io is not None:
         Xd, Yd = w.host_io
-        Xh = [x.cpu().pin_memory() for x in Xd]
-        Yh = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in Yd]
-        h2d = sum(x.numel() * 2 for x in Xh)
-        d2h = sum(y.numel() * 2 for y in Yh)
-        e2e_steps = max(20, min(args.steps, 2000))
+        Xh = Xd.cpu().pin_memory()
+        Yh = torch.empty(Yd.shape, dtype=Yd.dtype).pin_memory()
+        h2d, d2h = Xh.numel() * Xh.element_size(), Yh.numel() * Yh.element_size()
 
         def e2e_step(i):
-            for j in range(len(Xd)):
-                Xd[j].copy_(Xh[j], non_blocking=True)
+            Xd.copy_(Xh, non_blocking=True)
             w.step(i)
-            for j in range(len(Yd)):
-                Yh[j].copy_(Yd[j], non_blocking=True)
+            Yh.copy_(Yd, non_blocking=True)
 
+        e2e_rep = Replay(torch, e2e_step, C)
+        e2e_steps = max(20, min(args.steps, 2000))
+        timed = e2e_rep.plan(e2e_steps, 5)
+        e2e_rep.run(5)
+        torch.cuda.synchronize()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        t0 = time.perf_counter()
+        for g in timed:
+            g.replay()
+        torch.cuda.synchronize()
+        e2e_secs = time.perf_counter() - t0
+        e2e_rate, _ = whole_job_rate(w.bytes * e2e_steps, e2e_secs, world)
         for i in range(5):
             e2e_step(i)
         torch.cuda.synchronize()
@@ -613,11 +708,14 @@ def run_ours(args):
         for i in range(e2e_steps):
             e2e_step(i)
         torch.cuda.synchronize()
-        e2e_secs = time.perf_counter() - t0
-        e2e_rate, _ = whole_job_rate(w.bytes * e2e_steps, e2e_secs, world)
+        eager_rate, _ = whole_job_rate(w.bytes * e2e_steps, time.perf_counter() - t0, world)
+        del e2e_rep
         e2e = {"value": round(e2e_rate / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h,
-               "note": "eager API calls per step with pinned host activations/outputs"}
+               "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "note": "host clock around graph replays of steps that copy the activations in "
+                       "from pinned host memory, call the library, and copy the outputs out",
+               "eager_value": round(eager_rate / 1e9, 2),
+               "eager_note": "the same steps as eager Python calls (host issue rate)"}
 
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
@@ -638,11 +736,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and args.cpu_budget > 0:
-        gbs, reps, nbytes, csecs = cpu_baseline_oracle(args.cpu_budget)
-        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
-               "sample": f"{reps} passes of the oracle (numpy fp64 dequant + multiply) over the "
-                         f"seven M=1 projections of one layer ({nbytes} algorithmic bytes each), "
-                         f"{csecs:.1f} s"}
+        cpu = cpu_baseline_two_modes(args.cpu_budget)
 
     if rank == 0:
         out = {
@@ -654,7 +748,9 @@ def run_ours(args):
                        "weight_bytes_per_step": w.bytes, "rotating_copies": C,
                        "l2_policy": f"inputs larger than L2: {C} rotating weight copies, "
                                     f"{C * w.bytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB",
-                       "replay": "one CUDA graph per rotation of the weight copies", "kernel_path": args.path},
+                       "replay": "CUDA graphs covering exactly the timed steps, captured and "
+                                 "launched once (untimed) before the warm-up steps",
+                       "kernel_path": args.path, "arith": arith_note(w)},
             "tok_s": round(w.tokens * args.steps * world / slowest, 1),
             "roofline": {"bound": "hbm", "achieved": round(per_rank_gbs, 2), "peak": peak,
                          "unit": "GB/s", "frac": round(per_rank_gbs / peak, 4),
@@ -679,6 +775,17 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def arith_note(w):
+    """What the timed kernels compute in: the JSON line's dtype names the data type in and out."""
+    if w.kernel in ("int4_stream_kernel", "nvfp4_stream_kernel"):
+        return ("bf16 activations in, bf16 out; inside the kernel each run of 64 activations is "
+                "held as int16 under one power of two (exact within 2^7 of the run's largest), "
+                "integer dot products with the 4-bit codes, fp32 scaling and accumulation")
+    if w.kernel in ("bp_stream_kernel", "sa_stream_kernel"):
+        return "bf16 in/out; fp32 tables of signed activation sums, fp32 accumulation"
+    return "bf16 in/out; bf16 tensor-core operands, fp32 accumulation"
 
 
 def _src_sha(sources=()):
@@ -731,7 +838,7 @@ def run_reference(args):
            "config": {"workload": DEFAULT_WORKLOAD_DESC, "name": "decode_deps", "M": 1,
                       "weight_bytes_per_step": LAYER_BYTES},
            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": os.cpu_count(),
-                            "kind": "oracle", "sample": sample},
+                            "threads_seen": os_threads(), "kind": "oracle", "sample": sample},
            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out))
@@ -750,7 +857,17 @@ def main():
                     help="kernel family: 0 library choice, 1 CUDA cores, 2 tcgen05, 3 warp MMA "
                          "(INT4 and the LM head)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing")
+    ap.add_argument("--cpu-child", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.cpu_child:  # one CPU-baseline measurement in this process (see cpu_baseline_child)
+        # a bounded sample: a pass over 1/64 of every projection's rows sizes the fraction
+        # that lets a few passes fit the budget
+        _, _, _, t64 = cpu_baseline_oracle(0.0, 1 / 64)
+        frac = min(1.0, max(1 / 64, args.cpu_budget / 3 / max(64 * t64, 1e-9)))
+        gbs, reps, nbytes, secs = cpu_baseline_oracle(args.cpu_budget, frac)
+        print(json.dumps({"gbs": gbs, "reps": reps, "nbytes": nbytes, "secs": secs,
+                          "row_fraction": frac, "threads_seen": os_threads()}))
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

@@ -18,6 +18,8 @@ __all__ = [
     "lowbit_sa_packed_bytes", "lowbit_pack_sa", "lowbit_gemm_sa", "lowbit_gemm_sa_path",
     "lowbit_nvfp4_packed_bytes", "lowbit_pack_nvfp4", "lowbit_gemm_nvfp4", "lowbit_gemm_nvfp4_path",
     "lowbit_draft_argmax", "lowbit_draft_argmax_path",
+    "lowbit_debug_inject_stall",
+    "lmhead_argmax_partial", "lmhead_accept_keys",
 ]
 
 

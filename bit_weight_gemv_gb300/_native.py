@@ -33,6 +33,9 @@ _SIGS = {
     "lowbit_gemm_binplane_path": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _i, _vp]),
     "lmhead_argmax_verify_path": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _sz, _i, _vp]),
     "lowbit_device_error": (_i, [_vp, ctypes.POINTER(_i)]),
+    "lowbit_debug_inject_stall": (_i, [_i]),
+    "lmhead_argmax_partial": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
+    "lmhead_accept_keys": (_i, [_vp, _i, _i, _vp, _vp, _vp, _vp, _vp]),
     "lowbit_sa_packed_bytes": (_sz, [_i, _i, _i, _i]),
     "lowbit_pack_sa": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp]),
     "lowbit_gemm_sa": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
@@ -332,3 +335,33 @@ def lowbit_device_error(stream=None) -> int:
     out = ctypes.c_int(0)
     _check(lib.lowbit_device_error(_stream(stream), ctypes.byref(out)), "lowbit_device_error")
     return out.value
+
+
+def lowbit_debug_inject_stall(on: bool) -> None:
+    """Testing only: make later streaming / warp-MMA launches give up on their data waits."""
+    _check(lib.lowbit_debug_inject_stall(1 if on else 0), "lowbit_debug_inject_stall")
+
+
+def lmhead_argmax_partial(H, packed_shard, M, N, K, row_offset, keys_out, workspace, stream=None):
+    """One shard of a row-sharded LM head: keys_out int64 [M] = the slice's best
+    (logit, global row) key per token (see include/lowbit.h)."""
+    _need(H, torch.bfloat16, "H")
+    _need(packed_shard, torch.uint8, "packed_shard")
+    _need(keys_out, torch.int64, "keys_out")
+    _need(workspace, torch.uint8, "workspace")
+    if H.numel() < M * K or keys_out.numel() < M:
+        raise ValueError("H or keys_out too small")
+    _check(lib.lmhead_argmax_partial(_ptr(H), _ptr(packed_shard), M, N, K, row_offset,
+                                     _ptr(keys_out), _ptr(workspace), workspace.numel(),
+                                     _stream(stream)), "lmhead_argmax_partial")
+
+
+def lmhead_accept_keys(keys, W, M, draft, argmax, n_accept, bonus, stream=None):
+    """Merge W shards' keys (int64 [W][M]) into the full head's argmax, then greedy acceptance."""
+    _need(keys, torch.int64, "keys")
+    for t, nm in ((draft, "draft"), (argmax, "argmax"), (n_accept, "n_accept"), (bonus, "bonus")):
+        _need(t, torch.int32, nm)
+    if keys.numel() < W * M or draft.numel() < M - 1 or argmax.numel() < M:
+        raise ValueError("keys, draft or argmax too small")
+    _check(lib.lmhead_accept_keys(_ptr(keys), W, M, _ptr(draft), _ptr(argmax), _ptr(n_accept),
+                                  _ptr(bonus), _stream(stream)), "lmhead_accept_keys")

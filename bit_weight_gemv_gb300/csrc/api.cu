@@ -3,6 +3,8 @@
 #include <cudaTypedefs.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace lowbit {
@@ -13,6 +15,7 @@ constexpr int kMaxK = 65536;
 
 // One error word per device (see lowbit_device_error).
 __device__ int g_device_error;
+std::atomic<int> g_debug_stall{0};
 int* g_err_ptr[kMaxDevices] = {nullptr};
 
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
@@ -35,6 +38,8 @@ inline lowbit_status check_sa(int P, int G, int M, int N, int K) {
 inline lowbit_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LOWBIT_OK : LOWBIT_ERR_CUDA; }
 
 }  // namespace
+
+int debug_stall() { return g_debug_stall.load(std::memory_order_relaxed); }
 
 int* device_error_word() {
   int dev = 0;
@@ -66,6 +71,18 @@ bool allocation_covers(const void* p, size_t bytes) {
   if (get_attr(&start, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, dp) != CUDA_SUCCESS) return false;
   if (get_attr(&size, CU_POINTER_ATTRIBUTE_RANGE_SIZE, dp) != CUDA_SUCCESS) return false;
   return dp >= start && bytes <= size && dp - start <= size - bytes;
+}
+
+lowbit_status check_lmhead_args(const uint16_t* H, const void* packed_head, int M, int N, int K,
+                                const int32_t* draft, const int32_t* argmax, const int32_t* n_accept,
+                                const int32_t* bonus, const void* workspace, size_t ws_bytes) {
+  if (!H || !packed_head || !draft || !argmax || !n_accept || !bonus) return LOWBIT_ERR_INVALID_ARG;
+  const lowbit_status st = check_shape(M, N, K, 32);
+  if (st != LOWBIT_OK) return st;
+  if (M < 2) return LOWBIT_ERR_SHAPE;
+  if (!workspace || ws_bytes < lmhead_workspace_bytes(M, N, K)) return LOWBIT_ERR_WORKSPACE;
+  if (!aligned16(H) || !aligned16(packed_head) || !aligned16(workspace)) return LOWBIT_ERR_ALIGN;
+  return LOWBIT_OK;
 }
 
 }  // namespace lowbit
@@ -232,6 +249,7 @@ lowbit_status lowbit_gemm_int4_grouped_path(const lowbit_gemm_desc* descs, int c
   return from_cuda(launch_int4_tc_grouped(p, count, M, err, s));
 }
 
+
 lowbit_status lowbit_gemm_binplane(const uint16_t* X, const void* packed, int P, int M, int N,
                                    int K, uint16_t* Y, void* stream) {
   return lowbit_gemm_binplane_path(X, packed, P, M, N, K, Y, 0, stream);
@@ -360,13 +378,10 @@ lowbit_status lmhead_argmax_verify_path(const uint16_t* H, const void* packed_he
                                         int K, const int32_t* draft, int32_t* argmax,
                                         int32_t* n_accept, int32_t* bonus, void* workspace,
                                         size_t ws_bytes, int path, void* stream) {
-  if (!H || !packed_head || !draft || !argmax || !n_accept || !bonus || path < 0 || path > 3)
-    return LOWBIT_ERR_INVALID_ARG;
-  lowbit_status st = check_shape(M, N, K, 32);
+  if (path < 0 || path > 3) return LOWBIT_ERR_INVALID_ARG;
+  const lowbit_status st = check_lmhead_args(H, packed_head, M, N, K, draft, argmax, n_accept,
+                                             bonus, workspace, ws_bytes);
   if (st != LOWBIT_OK) return st;
-  if (M < 2) return LOWBIT_ERR_SHAPE;
-  if (!workspace || ws_bytes < lmhead_workspace_bytes(M, N, K)) return LOWBIT_ERR_WORKSPACE;
-  if (!aligned16(H) || !aligned16(packed_head) || !aligned16(workspace)) return LOWBIT_ERR_ALIGN;
   int* err = device_error_word();
   if (!err) return LOWBIT_ERR_CUDA;
   const uint8_t* pk = static_cast<const uint8_t*>(packed_head);
@@ -383,6 +398,11 @@ lowbit_status lmhead_argmax_verify_path(const uint16_t* H, const void* packed_he
   }
   return from_cuda(launch_lmhead_tc(H, pk, M, N, K, draft, argmax, n_accept, bonus, workspace,
                                     err, s));
+}
+
+lowbit_status lowbit_debug_inject_stall(int on) {
+  g_debug_stall.store(on ? 1 : 0, std::memory_order_relaxed);
+  return LOWBIT_OK;
 }
 
 lowbit_status lowbit_device_error(void* stream, int* status_out) {

@@ -132,7 +132,17 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
 
 // ------------------------------------------------------------------ launchers (host side)
 
+// Host-side validation shared by the LM-head verify entry points (lmhead_argmax_verify and its
+// variants): LOWBIT_OK or the status the call returns without enqueueing anything.
+lowbit_status check_lmhead_args(const uint16_t* H, const void* packed_head, int M, int N, int K,
+                                const int32_t* draft, const int32_t* argmax, const int32_t* n_accept,
+                                const int32_t* bonus, const void* workspace, size_t ws_bytes);
+
 int* device_error_word();  // address of the current device's error word (nullptr on failure)
+
+// The test-only stall setting (lowbit_debug_inject_stall): nonzero makes the streaming and
+// warp-MMA launches that follow give up on their data waits.
+int debug_stall();
 
 // True when [p, p + bytes) lies inside one device allocation (driver range query); false when
 // it does not or when the query is unavailable.
@@ -175,6 +185,10 @@ struct LmheadWorkspace;
 cudaError_t launch_lmhead_mma(const GemvProblem& prob, int M, LmheadWorkspace* ws,
                               const int32_t* draft, int32_t* argmax, int32_t* n_accept,
                               int32_t* bonus, int* err, cudaStream_t s);
+// One shard of a row-sharded INT4 LM head (rows row_offset .. row_offset + N - 1 of the full
+// vocabulary): keys_out[m] = the shard's best (logit, global row) key of token m.
+cudaError_t launch_lmhead_keys_mma(const GemvProblem& prob, int M, LmheadWorkspace* ws, int row_offset,
+                                   unsigned long long* keys_out, int* err, cudaStream_t s);
 // Binary-plane counterpart (M = 1); every problem carries its plane count P (1..8).
 cudaError_t launch_bp_stream(const GemvProblem* probs, int count, int* err, cudaStream_t s);
 // sa-format counterpart (M = 1); every problem carries P (1..8) and G (64, 128, 256).

@@ -65,6 +65,8 @@ struct StreamArgs {
   int stages;
   int cluster;  // C
   int m;        // activation rows (INT4 kernel; 1 for the plane kernels)
+  int stall;    // test-only stall setting (lowbit_debug_inject_stall); 0 in normal use
+  int row_offset;  // sharded LM head: global vocabulary row of this shard's row 0
   int cl_begin[kMaxGemvProblems];  // copy of p[i].cluster_begin
   int* err;
   LmheadWorkspace* ws;     // NVFP4 draft head: argmax keys and CTA counter
@@ -73,8 +75,30 @@ struct StreamArgs {
   const int32_t* draft;    // LM-head verify: draft tokens (M - 1)
   int32_t* n_accept;       // LM-head verify: accepted prefix length out
   int32_t* bonus;          // LM-head verify: the target's token after the prefix out
+  unsigned long long* keys_out;  // sharded LM head: the shard's best key per token out
   GemvProblem p[kMaxGemvProblems];
 };
+
+// Wait limits in SM clock cycles.  Every wait gives up after kWaitLimit (about a second at the
+// boost clock).  Under the test-only stall setting a launch's compute warps first wait on an
+// mbarrier that nothing arrives on, give up after kStallLimit (about a millisecond) and skip
+// their blocks; the producer then issues only its first ring of copies (and still waits for
+// them before it exits) and the warps that prepare stages handle only those, so no other wait
+// can run out.  The loops themselves are those of normal operation.
+constexpr long long kWaitLimit = 2000000000LL;
+constexpr long long kStallLimit = 2000000LL;
+
+// The compute warps' check under the stall setting: true when the warp must skip its blocks.
+__device__ __forceinline__ bool stalled_out(const StreamArgs& a, uint32_t never_bar, int* err,
+                                            int& gave_up, int lane) {
+  if (!a.stall) return false;
+  const bool ok = ptx::mbar_wait(never_bar, 0u, kStallLimit);  // nothing arrives: times out
+  if (!__all_sync(0xFFFFFFFFu, ok) && lane == 0) {
+    record_error(err, LOWBIT_ERR_TIMEOUT);
+    gave_up = 1;
+  }
+  return true;
+}
 
 __device__ __forceinline__ void grid_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_launch() {
@@ -148,6 +172,7 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
   __shared__ __align__(8) uint64_t xready[kMaxStages];  // the stage's int16 activations are set
   __shared__ __align__(8) uint64_t empty[kMaxStages];
   __shared__ __align__(8) uint64_t redbar;  // rank 0 of a split tile: partials have arrived
+  __shared__ __align__(8) uint64_t never;   // nothing arrives on it (test-only stall setting)
   // Per stage: the int16 activations, one uint4 per code word j holding the 16-bit pairs
   // (X[8j], X[8j+4]), (X[8j+1], X[8j+5]), (X[8j+2], X[8j+6]), (X[8j+3], X[8j+7]) -- the
   // order in which the two byte words of code word j meet them -- and, for inputs 0..63 and
@@ -187,6 +212,7 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
     }
     // rank 0 of a split tile receives one arrival per row from each other rank
     ptx::mbar_init(ptx::smem_addr(&redbar), (uint32_t)(kRowTile * (ks > 1 ? ks - 1 : 1)));
+    ptx::mbar_init(ptx::smem_addr(&never), 1);
     ptx::fence_mbar_init();
   }
   if (warp < kCWarps) {
@@ -228,7 +254,7 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
       for (int b = 0; b < pre; ++b) copy_x(b, b, ptx::smem_addr(&full[b]));
       int issued = pre;
       RingPos rp{pre % S, (uint32_t)(pre / S) & 1u};
-      for (int b = pre; b < nb; ++b, rp.next(S)) {
+      for (int b = pre; b < (a.stall ? pre : nb); ++b, rp.next(S)) {
         const int s = rp.s;
         if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), rp.ph ^ 1u)) {
           record_error(a.err, LOWBIT_ERR_TIMEOUT);
@@ -255,7 +281,7 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
     // parity wait can never meet a phase two behind), whatever the stage count.
     if (hdr_ok) {
       RingPos rp{0, 0u};
-      for (int b = 0; b < nb; ++b, rp.next(S)) {
+      for (int b = 0; b < (a.stall ? min(nb, S) : nb); ++b, rp.next(S)) {
         const int s = rp.s;
         if (s % conv_warps<MT>() != warp - kConvWarp) continue;
         const bool landed = ptx::mbar_wait(ptx::smem_addr(&full[s]), rp.ph);
@@ -303,7 +329,8 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
 #pragma unroll
     for (int m = 0; m < MT; ++m) total[m] = 0.f;
     RingPos rp{0, 0u};
-    for (int b = 0; b < nb; ++b, rp.next(S)) {
+    const int nbc = stalled_out(a, ptx::smem_addr(&never), a.err, gave_up, lane) ? 0 : nb;
+    for (int b = 0; b < nbc; ++b, rp.next(S)) {
       const int s = rp.s;
       const bool ready = ptx::mbar_wait(ptx::smem_addr(&xready[s]), rp.ph);
       if (!__all_sync(0xFFFFFFFFu, ready)) {  // warp-uniform exit keeps the warp converged
@@ -358,7 +385,8 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
 
   // -------------------------------------------------------------------- reduction + store
   __syncthreads();
-  const bool out_ok = ok != 0;  // header verified (before or alongside the copies)
+  // header verified (before or alongside the copies) and every wait of this CTA completed
+  const bool out_ok = ok != 0 && !gave_up;
   if (!out_ok && live && threadIdx.x == 0 && rank == 0 && tile == 0)
     record_error(a.err, LOWBIT_ERR_INVALID_ARG);
   if (threadIdx.x < kRowTile) {
@@ -385,7 +413,9 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
         }
         ptx::mbar_arrive_remote(ptx::map_to_rank(ptx::smem_addr(&redbar), owner));
       } else {
-        const bool got = ptx::mbar_wait_cluster(ptx::smem_addr(&redbar), 0);
+        // Under the stall setting every live CTA gives up and pushes nothing, so the short
+        // limit cannot end this wait before a push that is still coming.
+        const bool got = ptx::mbar_wait_cluster(ptx::smem_addr(&redbar), 0, a.stall ? kStallLimit : kWaitLimit);
         if (!got) record_error(a.err, LOWBIT_ERR_TIMEOUT);
         grid_wait();
         for (int m = 0; m < M; ++m) {
@@ -443,6 +473,7 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
   __shared__ __align__(8) uint64_t tabready[kMaxStages];
   __shared__ __align__(8) uint64_t empty[kMaxStages];
   __shared__ __align__(8) uint64_t redbar;
+  __shared__ __align__(8) uint64_t never;  // nothing arrives on it (test-only stall setting)
   __shared__ float red[kCWarps][32];
   __shared__ float part[kRowTile];
   __shared__ int ok;
@@ -479,6 +510,7 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
       ptx::mbar_init(ptx::smem_addr(&empty[s]), kCWarps);
     }
     ptx::mbar_init(ptx::smem_addr(&redbar), (uint32_t)(kRowTile * (ks > 1 ? ks - 1 : 1)));
+    ptx::mbar_init(ptx::smem_addr(&never), 1);
     ptx::fence_mbar_init();
   }
   if (warp < kCWarps) red[warp][lane] = 0.f;
@@ -507,7 +539,7 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
                       ptx::smem_addr(&full[b]));
       int issued = pre;
       RingPos rp{pre % S, (uint32_t)(pre / S) & 1u};
-      for (int b = pre; b < nb; ++b, rp.next(S)) {
+      for (int b = pre; b < (a.stall ? pre : nb); ++b, rp.next(S)) {
         const int s = rp.s;
         if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), rp.ph ^ 1u)) {
           record_error(a.err, LOWBIT_ERR_TIMEOUT);
@@ -531,7 +563,7 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
     // Lane l tabulates sets l, l + 32, ... (one per 128 inputs of the block).
     if (hdr_ok) {
       RingPos rp{0, 0u};
-      for (int b = 0; b < nb; ++b, rp.next(S)) {
+      for (int b = 0; b < (a.stall ? min(nb, S) : nb); ++b, rp.next(S)) {
         const int s = rp.s;
         if (s % kLutWarps != warp - kLutWarp) continue;  // this warp's stages only
         const bool landed = ptx::mbar_wait(ptx::smem_addr(&full[s]), rp.ph);
@@ -575,7 +607,8 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
     const int row = 32 * q + lane;
     float total = 0.f;
     RingPos rp{0, 0u};
-    for (int b = 0; b < nb; ++b, rp.next(S)) {
+    const int nbc = stalled_out(a, ptx::smem_addr(&never), a.err, gave_up, lane) ? 0 : nb;
+    for (int b = 0; b < nbc; ++b, rp.next(S)) {
       const int s = rp.s;
       const bool ready = ptx::mbar_wait(ptx::smem_addr(&tabready[s]), rp.ph);
       if (!__all_sync(0xFFFFFFFFu, ready)) {
@@ -631,7 +664,7 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
 
   // -------------------------------------------------------------------- reduction + store
   __syncthreads();
-  const bool out_ok = ok != 0;
+  const bool out_ok = ok != 0 && !gave_up;  // header verified, every wait completed
   if (!out_ok && live && threadIdx.x == 0 && rank == 0 && tile == 0)
     record_error(a.err, LOWBIT_ERR_INVALID_ARG);
   if (threadIdx.x < kRowTile) {
@@ -652,7 +685,8 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
         ptx::st_dsmem_f32(ptx::map_to_rank(la, owner), part[threadIdx.x]);
         ptx::mbar_arrive_remote(ptx::map_to_rank(ptx::smem_addr(&redbar), owner));
       } else {
-        const bool got = ptx::mbar_wait_cluster(ptx::smem_addr(&redbar), 0);
+        // under the stall setting no push can still be coming (see the INT4 kernel)
+        const bool got = ptx::mbar_wait_cluster(ptx::smem_addr(&redbar), 0, a.stall ? kStallLimit : kWaitLimit);
         if (!got) record_error(a.err, LOWBIT_ERR_TIMEOUT);
         float y = part[threadIdx.x];
         for (int r = 1; r < ks; ++r) y += slots[(r - 1) * kRowTile + threadIdx.x];
@@ -717,6 +751,7 @@ nvfp4_stream_kernel(const __grid_constant__ StreamArgs a) {
   __shared__ __align__(8) uint64_t xready[kMaxStages];
   __shared__ __align__(8) uint64_t empty[kMaxStages];
   __shared__ __align__(8) uint64_t redbar;
+  __shared__ __align__(8) uint64_t never;  // nothing arrives on it (test-only stall setting)
   __shared__ __align__(16) uint32_t xq[kMaxStages][kGroup / 2];  // int16 pairs (X[2i], X[2i+1])
   __shared__ float xdown[kMaxStages][2];                          // 2^-sh of inputs 0..63, 64..127
   __shared__ __align__(16) int xsum[kMaxStages][kGroup / 16];      // sum X of each run of 16
@@ -724,6 +759,7 @@ nvfp4_stream_kernel(const __grid_constant__ StreamArgs a) {
   __shared__ float part[kRowTile];
   __shared__ int ok;
   __shared__ int gave_up;
+  __shared__ int tile_got;   // rank 0 of a split tile: every peer's partial sums arrived
   __shared__ int hdr_valid;  // the whole grid agrees on it: every CTA reads the same header
   __shared__ float gscale;
 
@@ -743,12 +779,14 @@ nvfp4_stream_kernel(const __grid_constant__ StreamArgs a) {
   if (threadIdx.x == 0) {
     ok = live && (pr.early || header_matches(hp, kFormatNvfp4, 0, pr.N, pr.K));
     gave_up = 0;
+    tile_got = 1;
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
       ptx::mbar_init(ptx::smem_addr(&xready[s]), 1);
       ptx::mbar_init(ptx::smem_addr(&empty[s]), kCWarps);
     }
     ptx::mbar_init(ptx::smem_addr(&redbar), (uint32_t)(kRowTile * (ks > 1 ? ks - 1 : 1)));
+    ptx::mbar_init(ptx::smem_addr(&never), 1);
     ptx::fence_mbar_init();
   }
   if (warp < kCWarps) red[warp][lane] = 0.f;
@@ -781,7 +819,7 @@ nvfp4_stream_kernel(const __grid_constant__ StreamArgs a) {
                       kXBytes, ptx::smem_addr(&full[b]));
       int issued = pre;
       RingPos rp{pre % S, (uint32_t)(pre / S) & 1u};
-      for (int b = pre; b < nb; ++b, rp.next(S)) {
+      for (int b = pre; b < (a.stall ? pre : nb); ++b, rp.next(S)) {
         const int s = rp.s;
         if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), rp.ph ^ 1u)) {
           record_error(a.err, LOWBIT_ERR_TIMEOUT);
@@ -805,7 +843,7 @@ nvfp4_stream_kernel(const __grid_constant__ StreamArgs a) {
     // converter c owns the stages s with s % 2 == c (each stage's phases met in order)
     if (hdr_ok) {
       RingPos rp{0, 0u};
-      for (int b = 0; b < nb; ++b, rp.next(S)) {
+      for (int b = 0; b < (a.stall ? min(nb, S) : nb); ++b, rp.next(S)) {
         const int s = rp.s;
         if (s % conv_warps<1>() != warp - kConvWarp) continue;
         const bool landed = ptx::mbar_wait(ptx::smem_addr(&full[s]), rp.ph);
@@ -835,7 +873,8 @@ nvfp4_stream_kernel(const __grid_constant__ StreamArgs a) {
     const int row = 32 * q + lane;
     float total = 0.f;
     RingPos rp{0, 0u};
-    for (int b = 0; b < nb; ++b, rp.next(S)) {
+    const int nbc = stalled_out(a, ptx::smem_addr(&never), a.err, gave_up, lane) ? 0 : nb;
+    for (int b = 0; b < nbc; ++b, rp.next(S)) {
       const int s = rp.s;
       const bool ready = ptx::mbar_wait(ptx::smem_addr(&xready[s]), rp.ph);
       if (!__all_sync(0xFFFFFFFFu, ready)) {
@@ -879,7 +918,7 @@ nvfp4_stream_kernel(const __grid_constant__ StreamArgs a) {
 
   // -------------------------------------------------------------------- reduction + output
   __syncthreads();
-  const bool out_ok = ok != 0;
+  const bool out_ok = ok != 0 && !gave_up;  // header verified, every wait completed
   if (!out_ok && live && threadIdx.x == 0 && rank == 0 && tile == 0)
     record_error(a.err, LOWBIT_ERR_INVALID_ARG);
   if (threadIdx.x < kRowTile) {
@@ -902,8 +941,12 @@ nvfp4_stream_kernel(const __grid_constant__ StreamArgs a) {
           ptx::mbar_arrive_remote(ptx::map_to_rank(ptx::smem_addr(&redbar), owner));
         }
       } else {
-        const bool got = ptx::mbar_wait_cluster(ptx::smem_addr(&redbar), 0);
-        if (!got) record_error(a.err, LOWBIT_ERR_TIMEOUT);
+        // under the stall setting no push can still be coming (see the INT4 kernel)
+        const bool got = ptx::mbar_wait_cluster(ptx::smem_addr(&redbar), 0, a.stall ? kStallLimit : kWaitLimit);
+        if (!got) {
+          record_error(a.err, LOWBIT_ERR_TIMEOUT);
+          tile_got = 0;
+        }
         y = part[threadIdx.x];
         for (int r = 1; r < ks; ++r) y += slots[(r - 1) * kRowTile + threadIdx.x];
         have = got && out_ok && n < pr.N;
@@ -930,7 +973,9 @@ nvfp4_stream_kernel(const __grid_constant__ StreamArgs a) {
         key = warp_max_u64(key);
         if (lane == 0 && key) atomicMax(&a.ws->keys[0], key);
       }
-      draft_finish(a.ws, 1, a.id_map, a.ids);
+      // a live tile whose sums are incomplete (a wait gave up here or in a peer) fails the call
+      __syncthreads();
+      draft_finish(a.ws, 1, a.id_map, a.ids, live && (gave_up || (ks > 1 && rank == 0 && !tile_got)));
     }
   }
 }
@@ -987,7 +1032,9 @@ struct MmaArgs {
   CUtensorMap xmap[kMaxGemvProblems];
   StreamArgs s;
 };
-constexpr int kEpiStore = 0, kEpiVerify = 1;
+// Epilogues: bf16 outputs; the LM-head argmax + acceptance; one shard of a row-sharded LM head
+// (the shard's best key per token).
+constexpr int kEpiStore = 0, kEpiVerify = 1, kEpiKeys = 2;
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -1023,6 +1070,7 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
   uint8_t* ring = smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u);
   __shared__ __align__(8) uint64_t full[kMaxStages];
   __shared__ __align__(8) uint64_t empty[kMaxStages];
+  __shared__ __align__(8) uint64_t never;  // nothing arrives on it (test-only stall setting)
   __shared__ int ok;
   __shared__ int gave_up;
   __shared__ int hdr_valid;  // the same in every CTA: they all read the one header
@@ -1065,6 +1113,7 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
       ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
       ptx::mbar_init(ptx::smem_addr(&empty[s]), kMmaWarps);
     }
+    ptx::mbar_init(ptx::smem_addr(&never), 1);
     ptx::fence_mbar_init();
   }
   __syncthreads();
@@ -1098,7 +1147,7 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
       for (int b = 0; b < pre; ++b) copy_x(b, b, ptx::smem_addr(&full[b]));
       int issued = pre;
       RingPos rp{pre % S, (uint32_t)(pre / S) & 1u};
-      for (int b = pre; b < nb; ++b, rp.next(S)) {
+      for (int b = pre; b < (a.stall ? pre : nb); ++b, rp.next(S)) {
         const int s = rp.s;
         if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), rp.ph ^ 1u)) {
           record_error(a.err, LOWBIT_ERR_TIMEOUT);
@@ -1131,7 +1180,8 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
 #pragma unroll
     for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     RingPos rp{0, 0u};
-    for (int b = 0; b < nb; ++b, rp.next(S)) {
+    const int nbc = stalled_out(a, ptx::smem_addr(&never), a.err, gave_up, lane) ? 0 : nb;
+    for (int b = 0; b < nbc; ++b, rp.next(S)) {
       const int s = rp.s;
       const bool landed = ptx::mbar_wait(ptx::smem_addr(&full[s]), rp.ph);
       if (!__all_sync(0xFFFFFFFFu, landed)) {
@@ -1290,8 +1340,17 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
     record_error(a.err, LOWBIT_ERR_INVALID_ARG);
   const bool owner_thread = threadIdx.x < kMmaWarps * 32;
   if (C > 1) ptx::cluster_sync();
-  const bool verify = EPI == kEpiVerify && hdr_valid;
-  if (live && out_ok && owner_thread) {
+  const bool verify = EPI != kEpiStore && hdr_valid;
+  // The tile's totals are complete only if no CTA sharing it gave up on a wait: lane q of
+  // each warp reads peer q's flag (one load per lane, all in flight together) and the warp
+  // votes.
+  bool tile_done = !gave_up;
+  if (ks > 1) {
+    const uint32_t flag = lane < ks ? ptx::ld_dsmem_u32(ptx::smem_addr(&gave_up),
+                                                       (uint32_t)(crank - rank + lane)) : 0u;
+    tile_done = !__any_sync(0xFFFFFFFFu, flag != 0u);
+  }
+  if (live && out_ok && tile_done && owner_thread) {
     grid_wait();  // outputs and the verify workspace belong to the previous kernel until now
     const int rows = kRowTile / ks, rbase = rank * rows;
     const uint32_t base = (uint32_t)(crank - rank);  // rank 0 of this tile
@@ -1312,7 +1371,7 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
       if constexpr (EPI == kEpiStore) {
         if (in) pr.Y[(size_t)m * pr.N + n] = float_to_bf16_bits(y);
       } else {
-        unsigned long long key = in ? argmax_key(y, n) : 0ull;
+        unsigned long long key = in ? argmax_key(y, n + a.row_offset) : 0ull;
         if (rows >= 32) {  // a warp's 32 values share one activation row
           key = warp_max_u64(key);
           if (lane == 0 && key) atomicMax(&kmax[min(m, MT - 1)], key);
@@ -1328,7 +1387,11 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
     __syncthreads();
     grid_wait();
     if (threadIdx.x < M && kmax[threadIdx.x]) atomicMax(&a.ws->keys[threadIdx.x], kmax[threadIdx.x]);
-    lmhead_finish(a.ws, M, a.draft, a.ids, a.n_accept, a.bonus);
+    // a live tile whose totals are incomplete fails the call: nothing is written
+    if constexpr (EPI == kEpiKeys)
+      keys_finish(a.ws, M, a.keys_out, live && !tile_done);
+    else
+      lmhead_finish(a.ws, M, a.draft, a.ids, a.n_accept, a.bonus, live && !tile_done);
   }
 }
 
@@ -1441,7 +1504,7 @@ constexpr int kMaxDevices = 64;
 struct OptIns {
   std::atomic<unsigned char> done[kMaxDevices];
 };
-OptIns g_int4_optins[3], g_bp_optins, g_sa_optins, g_nv_optins[2], g_mma_optins[8];  // one per kernel built
+OptIns g_int4_optins[3], g_bp_optins, g_sa_optins, g_nv_optins[2], g_mma_optins[10];  // one per kernel built
 
 template <typename Kernel>
 cudaError_t opt_in(Kernel kern, OptIns& o, size_t budget) {
@@ -1501,6 +1564,7 @@ cudaError_t launch_int4_stream_mt(const GemvProblem* probs, int count, int M, in
     return cudaErrorInvalidValue;
   a.err = err;
   a.m = M;
+  a.stall = debug_stall();
   // ring, then the partial-sum slots rank 0 of a split tile receives
   const size_t slots = (size_t)(sc.kmax - 1) * MT * kRowTile * sizeof(float);
   int S = slots < budget ? (int)((budget - slots) / stage) : 0;
@@ -1532,7 +1596,8 @@ PFN_cuTensorMapEncodeTiled_v12000 x_map_encoder() {
 template <int FMT, int MT, int EPI>
 cudaError_t launch_mma_mt(const GemvProblem* probs, int count, int M, LmheadWorkspace* ws,
                           const int32_t* draft, int32_t* argmax, int32_t* n_accept,
-                          int32_t* bonus, int* err, cudaStream_t s) {
+                          int32_t* bonus, int* err, cudaStream_t s,
+                          unsigned long long* keys_out = nullptr, int row_offset = 0) {
   const int P = FMT == kMmaInt4 ? 0 : probs[0].P, GS = FMT == kMmaSa ? probs[0].G : 0;
   for (int i = 1; i < count; ++i)  // one stage size per launch
     if (FMT != kMmaInt4 && (probs[i].P != P || probs[i].G != probs[0].G)) return cudaErrorInvalidValue;
@@ -1552,6 +1617,9 @@ cudaError_t launch_mma_mt(const GemvProblem* probs, int count, int M, LmheadWork
   a.ids = argmax;
   a.n_accept = n_accept;
   a.bonus = bonus;
+  a.keys_out = keys_out;
+  a.row_offset = row_offset;
+  a.stall = debug_stall();
   for (int i = 0; i < a.count; ++i) {
     // X [M][K] bf16 as matrix i's activations (in schedule order); rows >= M read as zero
     cuuint64_t dims[2] = {(cuuint64_t)a.p[i].K, (cuuint64_t)M};
@@ -1571,7 +1639,7 @@ cudaError_t launch_mma_mt(const GemvProblem* probs, int count, int M, LmheadWork
   const size_t smem = std::max((size_t)a.stages * stage, (size_t)MT * kRowTile * sizeof(float)) + 1024;
   if (smem > budget) return cudaErrorInvalidValue;
   if constexpr (FMT == kMmaInt4) {
-    constexpr int slot_i = (MT == 16 ? 0 : 1) + 2 * EPI;
+    constexpr int slot_i = (MT == 16 ? 0 : 1) + (EPI == kEpiKeys ? 8 : 2 * EPI);
     return launch_streaming(int4_mma_kernel<MT, EPI>, g_mma_optins[slot_i], budget, A, sc, smem,
                             kMmaThreads, s);
   } else if constexpr (FMT == kMmaPlanes) {
@@ -1624,6 +1692,16 @@ cudaError_t launch_lmhead_mma(const GemvProblem& prob, int M, LmheadWorkspace* w
                                                  err, s);
 }
 
+cudaError_t launch_lmhead_keys_mma(const GemvProblem& prob, int M, LmheadWorkspace* ws, int row_offset,
+                                   unsigned long long* keys_out, int* err, cudaStream_t s) {
+  if (M < 1 || M > 32) return cudaErrorInvalidValue;
+  if (M <= 16)
+    return launch_mma_mt<kMmaInt4, 16, kEpiKeys>(&prob, 1, M, ws, nullptr, nullptr, nullptr, nullptr,
+                                                 err, s, keys_out, row_offset);
+  return launch_mma_mt<kMmaInt4, 32, kEpiKeys>(&prob, 1, M, ws, nullptr, nullptr, nullptr, nullptr,
+                                               err, s, keys_out, row_offset);
+}
+
 cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int M, int* err, cudaStream_t s) {
   if (count < 1 || count > kMaxGemvProblems || M < 1 || M > kStreamMaxRows) return cudaErrorInvalidValue;
   if (M == 1) return launch_int4_stream_mt<1>(probs, count, M, err, s);
@@ -1645,6 +1723,7 @@ cudaError_t launch_bp_stream(const GemvProblem* probs, int count, int* err, cuda
   S = S < 2 ? 2 : (S > kMaxStages ? kMaxStages : S);
   S -= S % kLutWarps;  // the table warps share the stages evenly
   a.err = err;
+  a.stall = debug_stall();
   a.stages = sc.maxnb < S ? sc.maxnb : S;
   const size_t smem = (size_t)a.stages * stage + slots;
   return launch_streaming(bp_stream_kernel, g_bp_optins, kSmemBudget, a, sc, smem, kBpThreads, s);
@@ -1657,6 +1736,7 @@ cudaError_t launch_nvfp4_stream(const GemvProblem& prob, LmheadWorkspace* ws, co
   if (!make_schedule(&prob, 1, kGroup, kInt4TargetBlocks, kMaxSplit, a, sc)) return cudaErrorInvalidValue;
   a.err = err;
   a.m = 1;
+  a.stall = debug_stall();
   a.ws = ws;
   a.id_map = id_map;
   a.ids = ids;
@@ -1688,6 +1768,7 @@ cudaError_t launch_sa_stream(const GemvProblem* probs, int count, int* err, cuda
   S = S < 2 ? 2 : (S > kMaxStages ? kMaxStages : S);
   S -= S % kLutWarps;  // the table warps share the stages evenly
   a.err = err;
+  a.stall = debug_stall();
   a.stages = sc.maxnb < S ? sc.maxnb : S;
   const size_t smem = (size_t)a.stages * stage + slots;
   return launch_streaming(sa_stream_kernel, g_sa_optins, kSaSmemMax, a, sc, smem, kBpThreads, s);

@@ -255,6 +255,37 @@ lowbit_status lmhead_argmax_verify(const uint16_t* H, const void* packed_head, i
                                    size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Row-sharded LM head: verification with the vocabulary split across GPUs (small-vocabulary MTP
+ * study, section 3.3: drafts are verified against the full vocabulary; DFlash summary, section
+ * 4.1: greedy prefix acceptance).  Each GPU holds a contiguous slice of the head's rows, packed
+ * on its own with lowbit_pack_int4; the only exchange is W * M 64-bit keys.
+ *
+ *   1. On every GPU: lmhead_argmax_partial on its slice -> keys_out[M].
+ *   2. The caller all-gathers the keys of all W GPUs into keys[W][M] (shard order is free).
+ *   3. On every GPU: lmhead_accept_keys(keys, W, ...) -> the same argmax, n_accept and bonus
+ *      as lmhead_argmax_verify on the whole head (argmax over fp32 logits, lowest row on ties).
+ *
+ * Key of a token: (order-preserving bits of its best fp32 logit in the slice) << 32 |
+ * (0xFFFFFFFF - global row), so that a larger key is a larger logit and, between equal logits,
+ * the lower row; the maximum over slices is the full head's winner.
+ */
+
+/* Step 1.  packed_shard: lowbit_pack_int4 of rows row_offset .. row_offset + N - 1 of the head
+ * (N rows, K inputs); H: bf16 [M][K], 1 <= M <= 32; row_offset >= 0 and row_offset + N < 2^31.
+ *   keys_out : uint64 [M] out, 8-byte aligned (device).
+ *   workspace: as lmhead_argmax_verify (lmhead_workspace_bytes(2, N, K), zero once, left zero).
+ * Runs the default verify kernel (warp-level MMA); logits are never written. */
+lowbit_status lmhead_argmax_partial(const uint16_t* H, const void* packed_shard, int M, int N, int K,
+                                    int row_offset, uint64_t* keys_out, void* workspace,
+                                    size_t ws_bytes, void* stream);
+
+/* Step 3.  keys: uint64 [W][M] (device, 8-byte aligned), every shard's keys_out; draft: int32
+ * [M-1]; argmax: int32 [M] out; n_accept, bonus: int32 [1] out, as lmhead_argmax_verify.
+ * 2 <= M <= 32, W >= 1.  One small kernel. */
+lowbit_status lmhead_accept_keys(const uint64_t* keys, int W, int M, const int32_t* draft,
+                                 int32_t* argmax, int32_t* n_accept, int32_t* bonus, void* stream);
+
+/* ------------------------------------------------------------------------------------------
  * For callers that cannot allocate device memory.
  */
 
@@ -315,6 +346,16 @@ lowbit_status lowbit_draft_argmax_path(const uint16_t* H, const void* packed_hea
 /* ------------------------------------------------------------------------------------------
  * Device-side error word.
  */
+
+/* Testing only: with `on` nonzero, every later launch of the streaming and warp-MMA kernels
+ * (the library's default kernels, path 1 at M = 1 and path 3) has its compute warps wait for
+ * data on a barrier that nothing arrives on, so that its bounded waits give up: each data
+ * wait then ends after about a millisecond instead of about a second.  Such a call writes no
+ * output (Y, argmax, n_accept, bonus, ids keep their previous contents), leaves the LM-head
+ * workspace zeroed, and records LOWBIT_ERR_TIMEOUT in the device error word.  A CTA still
+ * waits for its own copies in flight before it exits.  The tcgen05 and CUDA-core kernels are
+ * not affected.  The setting is process-wide; pass 0 to restore normal operation. */
+lowbit_status lowbit_debug_inject_stall(int on);
 
 /* Synchronises `stream`, then returns (in *status_out) and clears the current device's
  * error word: LOWBIT_OK, LOWBIT_ERR_INVALID_ARG (a kernel found a packed header that did not

@@ -64,17 +64,6 @@ def gemm(x_bits: np.ndarray, codes: np.ndarray, scales_bits: np.ndarray,
     return Y
 
 
-def gemm_entries(x_bits: np.ndarray, codes: np.ndarray, scales_bits: np.ndarray,
-                 m_idx: np.ndarray, n_idx: np.ndarray, group: int = GROUP) -> np.ndarray:
-    """Selected outputs Y64[m_idx[i]][n_idx[i]], one dot product each (full-size spot checks)."""
-    X = bf16_to_f64(np.atleast_2d(x_bits))
-    out = np.empty(len(m_idx), dtype=np.float64)
-    for i, (m, n) in enumerate(zip(m_idx, n_idx)):
-        w = dequant(codes[n:n + 1], scales_bits[n:n + 1], group)[0]
-        out[i] = float(np.dot(X[m], w))
-    return out
-
-
 # ----------------------------------------------------------------------------- layout
 
 def packed_sizes(N: int, K: int):

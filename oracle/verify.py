@@ -37,3 +37,26 @@ def accept(target_ids, drafts):
     while n < len(d) and d[n] == a[n]:
         n += 1
     return n, a[n]
+
+
+def shard_winners(logits_shard: np.ndarray, row_offset: int):
+    """Best (logit, global row) per token within one slice of the vocabulary's rows (rows
+    row_offset .. row_offset + n - 1), lowest row on ties: (values [M], rows [M])."""
+    logits_shard = np.atleast_2d(logits_shard)
+    local = argmax_lowest(logits_shard)
+    return logits_shard[np.arange(logits_shard.shape[0]), local], local + row_offset
+
+
+def merge_winners(values: np.ndarray, rows: np.ndarray) -> np.ndarray:
+    """Full-vocabulary argmax from every slice's winners (values, rows: [W][M]): per token the
+    largest value, and among equal values the lowest global row."""
+    values, rows = np.atleast_2d(values), np.atleast_2d(rows)
+    out = np.empty(values.shape[1], dtype=np.int64)
+    for m in range(values.shape[1]):
+        best = None
+        for w in range(values.shape[0]):
+            cand = (values[w, m], -int(rows[w, m]))
+            if best is None or cand > best:
+                best = cand
+        out[m] = -best[1]
+    return out

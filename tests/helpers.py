@@ -1,6 +1,6 @@
 """Shared test helpers: device transfer and the parity criteria.
 
-Parity criteria (the spec bar, with the readings recorded in the design doc):
+Parity criteria (the bar every GPU result is held to):
   * packing and acceptance: bit-exact;
   * GEMM outputs: |gpu - RNE_bf16(Y64)| <= 1e-2 * rms(oracle row) + 1e-3, where an output
     whose exact value lies within a small band around the midpoint of two bf16 neighbours may
@@ -99,3 +99,30 @@ def check_argmax(a_gpu: np.ndarray, logits64: np.ndarray, what: str = ""):
             assert 0 <= a_gpu[m] < logits64.shape[1]
             assert logits64[m, a_gpu[m]] >= logits64[m, a_ref[m]] - MARGIN, what
     return ungraded
+
+
+class Guarded:
+    """A device tensor with canary bands on both sides: ``t`` is the view a call writes; the
+    bands (``band`` elements each side) hold a fixed byte pattern that ``check()`` asserts
+    is unchanged, so a write past either end of the output is caught."""
+
+    PATTERN = 0xA5
+
+    def __init__(self, shape, dtype, band=256, fill=None):
+        import torch
+        n = 1
+        for d in shape:
+            n *= d
+        self.band, self.n = band, n
+        self.buf = torch.empty(n + 2 * band, dtype=dtype, device="cuda")
+        self.buf.view(torch.uint8).fill_(self.PATTERN)
+        self.t = self.buf[band:band + n].view(*shape)
+        if fill is not None:
+            self.t.fill_(fill)
+
+    def check(self, what=""):
+        import torch
+        b = self.buf.view(torch.uint8).cpu().numpy()
+        es = self.buf.element_size()
+        lo, hi = b[:self.band * es], b[(self.band + self.n) * es:]
+        assert (lo == self.PATTERN).all() and (hi == self.PATTERN).all(), f"{what}: canary overwritten"

@@ -113,3 +113,4 @@ def test_kernel_family_selection_is_validated_on_the_host(lib):
     assert g(ctypes.cast(arr, vp), 2, 16, 4, None) == 1
     assert g(ctypes.cast(arr, vp), 2, 5, 1, None) == 2           # the streaming kernel takes M <= 4
     assert g(ctypes.cast(arr, vp), 9, 16, 0, None) == 1           # at most 8 problems
+

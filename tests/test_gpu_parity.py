@@ -398,3 +398,4 @@ def test_grouped_validation(lb):
     with pytest.raises(lb.LowbitError) as e:
         lb.lowbit_gemm_int4_grouped([], 1)
     assert e.value.status == 1
+

@@ -13,10 +13,13 @@ Modules
                dequantise, multiply, pack/unpack the layout.
   nvfp4     -- NVFP4 weights (E2M1 x E4M3 per 16 x fp32) and the trimmed draft head's
                argmax through an id map: dequantise, multiply, pack/unpack the layout.
-  verify    -- vocabulary argmax (lowest index on ties) and greedy prefix acceptance.
+  q8        -- Q8 weights for the draft head (int8 x one fp16 scale per 32 inputs):
+               dequantise, multiply, pack/unpack the layout.
+  verify    -- vocabulary argmax (lowest index on ties), greedy prefix acceptance, and the
+               merge of a row-sharded head's slice winners.
 
 Parity pins (tests/test_oracle_pins.py) tie every function to something other than
 itself: hand-worked 4x8 examples, brute force on tiny shapes, closed forms, invariants
 and library rounding routines.  No function here is "parity unpinned".
 """
-from . import numerics, int4, binplane, sa, nvfp4, verify  # noqa: F401
+from . import numerics, int4, binplane, sa, nvfp4, q8, verify  # noqa: F401

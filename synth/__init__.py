@@ -179,6 +179,24 @@ def nvfp4_problem(seed: int, M: int, N: int, K: int, *sub: int):
     return codes, scales, gs, ids, h
 
 
+def q8_weights(g: np.random.Generator, N: int, K: int):
+    """Q8 weights (the study's 8-bit head): codes int8 [N][K] uniform in [-127, 127] (the range
+    a symmetric 8-bit quantiser rounds onto), fp16 scales [N][K/32] ~ LogNormal(ln(0.02/64),
+    0.3), so weights are of order 0.02.  Draw order: codes, scales."""
+    codes = g.integers(-127, 128, size=(N, K), dtype=np.int64).astype(np.int8)
+    scales = to_f16_bits(g.lognormal(np.log(0.02 / 64), 0.3, size=(N, K // 32)))
+    return codes, scales
+
+
+def q8_problem(seed: int, M: int, N: int, K: int, *sub: int):
+    """One Q8 draft-head problem: (codes, scales, id_map, H)."""
+    gen = generator(seed, 0x08, M, N, K, *sub)
+    codes, scales = q8_weights(gen, N, K)
+    ids = id_map(gen, N)
+    h = activations(gen, M, K)
+    return codes, scales, ids, h
+
+
 ACTIVATION_KINDS = ("outlier", "mixed_scale", "tiny", "huge", "zero", "sparse")
 
 

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import synth
-from oracle import binplane, int4, numerics, nvfp4, sa, verify
+from oracle import q8, binplane, int4, numerics, nvfp4, sa, verify
 from oracle.numerics import bf16_to_f64, f16_to_f64
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -402,6 +402,10 @@ def test_sa_brute_force(G):
             ref[m, n] = acc
     Y = sa.gemm(x, bits, codes, d, G)
     assert np.allclose(Y, ref, rtol=1e-12, atol=1e-12)
+    # the sampled-rows form used on full-size matrices: the same brute-force values, per row
+    for rows in ([2], [0, 2], [2, 0, 1]):
+        assert np.allclose(sa.gemm_entries(x, bits, codes, d, G, np.array(rows)), ref[:, rows],
+                           rtol=1e-12, atol=1e-12)
 
 
 @pytest.mark.parametrize("G", sa.GROUPS)
@@ -564,3 +568,73 @@ def test_draft_ids_map_and_ties():
     assert len(set(m.tolist())) == 1000
     assert np.array_equal(nvfp4.draft_ids(L, m), m[np.argmax(L, axis=1)])
 
+
+
+# ------------------------------------------------------------------ Q8 (the 8-bit draft head)
+
+def test_q8_hand_example():
+    fx = _read_fixture("q8_hand_2x64.txt")
+    K = 64
+    codes = np.zeros((2, K), dtype=np.int8)
+    codes[0, :32], codes[0, 32:] = 1, -2
+    codes[0, 40] = -128
+    codes[1] = (np.arange(K) % 4) - 1
+    codes[1, 1] = 127
+    d = _f16([[float(v) for v in fx["d0"]], [float(v) for v in fx["d1"]]])
+    x = np.zeros((1, K))
+    x[0, :48] = 1.0
+    y = q8.gemm(_bf16(x), codes, d)
+    assert np.array_equal(y[0], np.array([float(v) for v in fx["y"]]))
+
+
+def test_q8_brute_force_and_closed_forms():
+    codes, scales, _, h = synth.q8_problem(60, 2, 5, 256)
+    H, dv = numerics.bf16_to_f64(h), numerics.f16_to_f64(scales)
+    ref = np.zeros((2, 5))
+    for m in range(2):
+        for n in range(5):
+            acc = 0.0
+            for blk in range(256 // 32):  # block-sum-first, pure Python
+                part = 0
+                for k in range(32 * blk, 32 * blk + 32):
+                    part += int(codes[n, k]) * float(H[m, k])
+                acc += float(dv[n, blk]) * part
+            ref[m, n] = acc
+    assert np.allclose(q8.gemm(h, codes, scales), ref, rtol=1e-12, atol=1e-12)
+    # one-hot activation picks d * q exactly; the extreme codes -128 and 127 decode as integers
+    codes[0, 7], codes[1, 200] = -128, 127
+    for n, k in ((0, 7), (1, 200), (4, 255)):
+        x = np.zeros((1, 256)); x[0, k] = 1.0
+        assert q8.gemm(_bf16(x), codes, scales)[0, n] == dv[n, k // 32] * int(codes[n, k])
+
+
+def test_q8_layout_positions_by_hand():
+    N, K = 200, 256
+    total, off, payload, block = q8.packed_sizes(N, K)
+    assert block == 17408 and payload == 2 * 2 * 17408
+    with open(os.path.join(GOLDEN, "q8_layout_positions.txt")) as f:
+        rows = [line.split() for line in f if line.strip() and not line.startswith("#")]
+    for kind, n, kj, byte in rows:
+        n, kj, byte = int(n), int(kj), int(byte)
+        codes = np.zeros((N, K), dtype=np.int8)
+        scales = np.zeros((N, K // 32), dtype=np.uint16)
+        expect = np.zeros(payload, dtype=np.uint8)
+        if kind == "code":
+            codes[n, kj] = -3
+            expect[byte] = 0xFD
+        else:
+            scales[n, kj] = 0x3C01
+            expect[byte], expect[byte + 1] = 0x01, 0x3C
+        assert np.array_equal(q8.pack(codes, scales)[off:off + payload], expect), (kind, n, kj)
+
+
+@pytest.mark.parametrize("N,K", [(1, 128), (130, 256), (256, 512)])
+def test_q8_pack_round_trip(N, K):
+    codes, scales, _, _ = synth.q8_problem(61, 1, N, K)
+    packed = q8.pack(codes, scales)
+    c2, s2 = q8.unpack(packed)
+    assert np.array_equal(c2, codes) and np.array_equal(s2, scales)
+    hd = int4.parse_header(packed)
+    assert hd["format"] == q8.FORMAT_Q8 and hd["block_bytes"] == 17408
+    if N % 128 == 0:
+        assert hd["payload_bytes"] == N * K + N * (K // 32) * 2

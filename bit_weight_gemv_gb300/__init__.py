@@ -20,6 +20,8 @@ __all__ = [
     "lowbit_draft_argmax", "lowbit_draft_argmax_path",
     "lowbit_debug_inject_stall",
     "lmhead_argmax_partial", "lmhead_accept_keys",
+    "lowbit_q8_packed_bytes", "lowbit_pack_q8", "lowbit_gemm_q8", "lowbit_gemm_q8_path",
+    "lowbit_draft_argmax_q8",
 ]
 
 

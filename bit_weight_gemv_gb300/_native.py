@@ -35,6 +35,11 @@ _SIGS = {
     "lowbit_device_error": (_i, [_vp, ctypes.POINTER(_i)]),
     "lowbit_debug_inject_stall": (_i, [_i]),
     "lmhead_argmax_partial": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
+    "lowbit_q8_packed_bytes": (_sz, [_i, _i]),
+    "lowbit_pack_q8": (_i, [_vp, _vp, _i, _i, _vp, _vp]),
+    "lowbit_gemm_q8": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp]),
+    "lowbit_gemm_q8_path": (_i, [_vp, _vp, _i, _i, _i, _vp, _i, _vp]),
+    "lowbit_draft_argmax_q8": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
     "lmhead_accept_keys": (_i, [_vp, _i, _i, _vp, _vp, _vp, _vp, _vp]),
     "lowbit_sa_packed_bytes": (_sz, [_i, _i, _i, _i]),
     "lowbit_pack_sa": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp]),
@@ -365,3 +370,40 @@ def lmhead_accept_keys(keys, W, M, draft, argmax, n_accept, bonus, stream=None):
         raise ValueError("keys, draft or argmax too small")
     _check(lib.lmhead_accept_keys(_ptr(keys), W, M, _ptr(draft), _ptr(argmax), _ptr(n_accept),
                                   _ptr(bonus), _stream(stream)), "lmhead_accept_keys")
+
+
+def lowbit_q8_packed_bytes(N: int, K: int) -> int:
+    return lib.lowbit_q8_packed_bytes(N, K)
+
+
+def lowbit_pack_q8(codes, scales, N, K, packed, stream=None):
+    """codes int8 [N][K], scales fp16 [N][K/32] -> packed uint8 [lowbit_q8_packed_bytes]."""
+    _need(codes, torch.int8, "codes")
+    _need(scales, torch.float16, "scales")
+    _need(packed, torch.uint8, "packed")
+    if packed.numel() < lowbit_q8_packed_bytes(N, K):
+        raise ValueError("packed buffer too small")
+    _check(lib.lowbit_pack_q8(_ptr(codes), _ptr(scales), N, K, _ptr(packed), _stream(stream)),
+           "lowbit_pack_q8")
+
+
+def lowbit_gemm_q8(X, packed, M, N, K, Y, stream=None):
+    """Y bf16 [M][N] = X bf16 [M][K] times the packed Q8 weights, transposed."""
+    _gemm_args(X, packed, M, N, K, Y)
+    _check(lib.lowbit_gemm_q8(_ptr(X), _ptr(packed), M, N, K, _ptr(Y), _stream(stream)),
+           "lowbit_gemm_q8")
+
+
+def lowbit_gemm_q8_path(X, packed, M, N, K, Y, path, stream=None):
+    """lowbit_gemm_q8 with the kernel forced (1 = streaming, M = 1; 3 = warp-level MMA)."""
+    _gemm_args(X, packed, M, N, K, Y)
+    _check(lib.lowbit_gemm_q8_path(_ptr(X), _ptr(packed), M, N, K, _ptr(Y), path, _stream(stream)),
+           "lowbit_gemm_q8_path")
+
+
+def lowbit_draft_argmax_q8(H, packed_head, M, N, K, id_map, ids, workspace, stream=None):
+    """ids int32 [M] = id_map[argmax over the N rows of a Q8 draft head] (id_map may be None)."""
+    _draft_args(H, packed_head, M, N, K, id_map, ids, workspace)
+    _check(lib.lowbit_draft_argmax_q8(_ptr(H), _ptr(packed_head), M, N, K, _ptr(id_map), _ptr(ids),
+                                      _ptr(workspace), workspace.numel(), _stream(stream)),
+           "lowbit_draft_argmax_q8")

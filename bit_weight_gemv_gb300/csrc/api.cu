@@ -126,6 +126,11 @@ size_t lowbit_nvfp4_packed_bytes(int N, int K) {
   return kHeaderBytes + nvfp4_payload_bytes(N, K);
 }
 
+size_t lowbit_q8_packed_bytes(int N, int K) {
+  if (check_shape(1, N, K, 1) != LOWBIT_OK) return 0;
+  return kHeaderBytes + q8_payload_bytes(N, K);
+}
+
 size_t lmhead_workspace_bytes(int M, int N, int K) {
   if (M < 2 || M > 32 || N < 1 || K <= 0 || K % kGroup != 0) return 0;
   return 512;
@@ -170,6 +175,58 @@ lowbit_status lowbit_pack_nvfp4(const uint8_t* codes, const uint8_t* scales, flo
   if (!aligned16(codes) || !aligned16(packed)) return LOWBIT_ERR_ALIGN;
   return from_cuda(launch_pack_nvfp4(codes, scales, g, N, K, static_cast<uint8_t*>(packed),
                                      static_cast<cudaStream_t>(stream)));
+}
+
+lowbit_status lowbit_pack_q8(const int8_t* codes, const uint16_t* scales, int N, int K, void* packed,
+                             void* stream) {
+  if (!codes || !scales || !packed) return LOWBIT_ERR_INVALID_ARG;
+  const lowbit_status st = check_shape(1, N, K, 1);
+  if (st != LOWBIT_OK) return st;
+  if (!aligned16(codes) || !aligned16(packed) || ((uintptr_t)scales & 1u)) return LOWBIT_ERR_ALIGN;
+  return from_cuda(launch_pack_q8(codes, scales, N, K, static_cast<uint8_t*>(packed),
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+lowbit_status lowbit_gemm_q8(const uint16_t* X, const void* packed, int M, int N, int K, uint16_t* Y,
+                             void* stream) {
+  return lowbit_gemm_q8_path(X, packed, M, N, K, Y, 0, stream);
+}
+
+lowbit_status lowbit_gemm_q8_path(const uint16_t* X, const void* packed, int M, int N, int K,
+                                  uint16_t* Y, int path, void* stream) {
+  if (!X || !packed || !Y || (path != 0 && path != 1 && path != 3)) return LOWBIT_ERR_INVALID_ARG;
+  const lowbit_status st = check_shape(M, N, K, 32);
+  if (st != LOWBIT_OK) return st;
+  if (path == 1 && M != 1) return LOWBIT_ERR_SHAPE;
+  if (!aligned16(X) || !aligned16(packed)) return LOWBIT_ERR_ALIGN;
+  int* err = device_error_word();
+  if (!err) return LOWBIT_ERR_CUDA;
+  const uint8_t* pk = static_cast<const uint8_t*>(packed);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  GemvProblem p = {X, pk, Y, N, K, 0, 1, 0, 0, 0};
+  p.early = allocation_covers(pk, kHeaderBytes + q8_payload_bytes(N, K)) ? 1 : 0;
+  if (path == 0) path = M == 1 ? 1 : 3;
+  if (path == 1) return from_cuda(launch_q8_stream(p, nullptr, nullptr, nullptr, err, s));
+  return from_cuda(launch_q8_mma(p, M, nullptr, nullptr, nullptr, err, s));
+}
+
+lowbit_status lowbit_draft_argmax_q8(const uint16_t* H, const void* packed_head, int M, int N, int K,
+                                     const int32_t* id_map, int32_t* ids, void* workspace,
+                                     size_t ws_bytes, void* stream) {
+  if (!H || !packed_head || !ids) return LOWBIT_ERR_INVALID_ARG;
+  const lowbit_status st = check_shape(M, N, K, 32);
+  if (st != LOWBIT_OK) return st;
+  if (!workspace || ws_bytes < lmhead_workspace_bytes(2, N, K)) return LOWBIT_ERR_WORKSPACE;
+  if (!aligned16(H) || !aligned16(packed_head) || !aligned16(workspace)) return LOWBIT_ERR_ALIGN;
+  int* err = device_error_word();
+  if (!err) return LOWBIT_ERR_CUDA;
+  const uint8_t* pk = static_cast<const uint8_t*>(packed_head);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  GemvProblem p = {H, pk, nullptr, N, K, 0, 1, 0, 0, 0};
+  p.early = allocation_covers(pk, kHeaderBytes + q8_payload_bytes(N, K)) ? 1 : 0;
+  LmheadWorkspace* ws = static_cast<LmheadWorkspace*>(workspace);
+  if (M == 1) return from_cuda(launch_q8_stream(p, ws, id_map, ids, err, s));
+  return from_cuda(launch_q8_mma(p, M, ws, id_map, ids, err, s));
 }
 
 lowbit_status lowbit_validate_packed(const void* packed, int format, int P, int N, int K,

@@ -16,6 +16,7 @@ constexpr uint32_t kFormatInt4 = 1;
 constexpr uint32_t kFormatBinplane = 2;
 constexpr uint32_t kFormatSa = 3;
 constexpr uint32_t kFormatNvfp4 = 4;
+constexpr uint32_t kFormatQ8 = 5;
 constexpr uint32_t kVersion = 2;
 constexpr int kHeaderBytes = 128;
 constexpr int kGroup = 128;    // inputs per quantisation group
@@ -51,6 +52,15 @@ constexpr uint32_t kNvfp4Block = 4 * kRowTile * 16 + 8 * kRowTile;
 constexpr uint32_t kNvfp4ScaleOff = 4 * kRowTile * 16;
 __host__ __device__ inline uint64_t nvfp4_payload_bytes(int N, int K) {
   return (uint64_t)row_tiles(N) * (uint64_t)(K / kGroup) * kNvfp4Block;
+}
+
+// Q8 (int8 codes, one fp16 scale per 32 inputs): one block per (128-row tile, group of 128
+// inputs): the codes [8 chunks of 16 inputs][128 rows][16 B], then the scales [4 runs of 32
+// inputs][128 rows] fp16.
+constexpr uint32_t kQ8Block = 8 * kRowTile * 16 + 4 * kRowTile * 2;
+constexpr uint32_t kQ8ScaleOff = 8 * kRowTile * 16;
+__host__ __device__ inline uint64_t q8_payload_bytes(int N, int K) {
+  return (uint64_t)row_tiles(N) * (uint64_t)(K / kGroup) * kQ8Block;
 }
 
 // The deployed ShiftAdd format: one block per (128-row tile, super-block of 256 inputs) holding
@@ -204,6 +214,16 @@ cudaError_t launch_nvfp4_stream(const GemvProblem& prob, LmheadWorkspace* ws, co
                                 int32_t* ids, int* err, cudaStream_t s);
 cudaError_t launch_pack_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, int N, int K,
                              uint8_t* packed, cudaStream_t s);
+cudaError_t launch_pack_q8(const int8_t* codes, const uint16_t* scales, int N, int K,
+                           uint8_t* packed, cudaStream_t s);
+// Q8 at M = 1 (one matrix): bf16 logits into prob.Y when ws is null, else the draft head's
+// id-mapped argmax (ids[0], workspace as lmhead_argmax_verify).
+cudaError_t launch_q8_stream(const GemvProblem& prob, LmheadWorkspace* ws, const int32_t* id_map,
+                             int32_t* ids, int* err, cudaStream_t s);
+// Q8 at 1 <= M <= 32 on the warp-level MMA: bf16 outputs into prob.Y when ws is null, else the
+// id-mapped argmax of every row (ids[0..M)).
+cudaError_t launch_q8_mma(const GemvProblem& prob, int M, LmheadWorkspace* ws, const int32_t* id_map,
+                          int32_t* ids, int* err, cudaStream_t s);
 cudaError_t launch_nvfp4_tc(const uint16_t* X, const uint8_t* packed, int M, int N, int K,
                             uint16_t* Y, int* err, cudaStream_t s);
 // Draft head: ids[m] = id_map[argmax_n logit[m][n]] (the row when id_map is null).

@@ -252,6 +252,45 @@ __global__ void pack_nvfp4_scales(const uint8_t* __restrict__ scales, int N, int
       (n < N) ? scales[n * (long long)(K / 16) + 8 * g + j] : (uint8_t)0;
 }
 
+// Q8: one thread per 16-byte code unit (tile t, group g, chunk c of 16 inputs, row r): the 16
+// code bytes of row n, k = 128g + 16c .. +15, at block(t, g) + c*2048 + r*16.
+__global__ void pack_q8_codes(const int8_t* __restrict__ codes, int N, int K,
+                              uint8_t* __restrict__ payload, long long units) {
+  const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= units) return;
+  const int G = K / kGroup;
+  const int r = (int)(u % kRowTile);
+  long long rest = u / kRowTile;
+  const int c = (int)(rest % 8);
+  rest /= 8;
+  const int g = (int)(rest % G);
+  const long long t = rest / G;
+  const long long n = t * kRowTile + r;
+  uint4 v = make_uint4(0, 0, 0, 0);  // padding rows: code 0
+  if (n < N) v = *reinterpret_cast<const uint4*>(codes + n * (long long)K + 128LL * g + 16 * c);
+  *reinterpret_cast<uint4*>(payload + (size_t)(t * G + g) * kQ8Block + (size_t)c * kRowTile * 16 +
+                            r * 16) = v;
+}
+
+// Q8: one thread per scale (tile t, group g, run j of 32 inputs, row r) at
+// block(t, g) + 16384 + j*256 + r*2.
+__global__ void pack_q8_scales(const uint16_t* __restrict__ scales, int N, int K,
+                               uint8_t* __restrict__ payload, long long units) {
+  const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= units) return;
+  const int G = K / kGroup;
+  const int r = (int)(u % kRowTile);
+  long long rest = u / kRowTile;
+  const int j = (int)(rest % 4);
+  rest /= 4;
+  const int g = (int)(rest % G);
+  const long long t = rest / G;
+  const long long n = t * kRowTile + r;
+  *reinterpret_cast<uint16_t*>(payload + (size_t)(t * G + g) * kQ8Block + kQ8ScaleOff +
+                               j * kRowTile * 2 + r * 2) =
+      (n < N) ? scales[n * (long long)(K / 32) + 4 * g + j] : (uint16_t)0;
+}
+
 // Launched last by every pack call: the multiplies read their weights before their
 // programmatic-dependency wait, so the kernel right before one must not be a weight writer.
 __global__ void pack_done() {}
@@ -294,6 +333,17 @@ cudaError_t launch_pack_sa(const uint8_t* bits, const uint8_t* codes, const uint
   pack_sa_signs<<<blocks_for(su, 256), 256, 0, s>>>(bits, P, G, N, K, packed + kHeaderBytes, su);
   pack_sa_codes<<<blocks_for(cu, 256), 256, 0, s>>>(codes, P, G, N, K, packed + kHeaderBytes, cu);
   pack_sa_d<<<blocks_for(du, 256), 256, 0, s>>>(d, P, G, N, K, packed + kHeaderBytes, du);
+  pack_done<<<1, 32, 0, s>>>();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_q8(const int8_t* codes, const uint16_t* scales, int N, int K,
+                           uint8_t* packed, cudaStream_t s) {
+  const long long blocks = (long long)row_tiles(N) * (K / kGroup);
+  const long long cu = blocks * 8 * kRowTile, su = blocks * 4 * kRowTile;
+  pack_header<<<1, 32, 0, s>>>(packed, kFormatQ8, 0, N, K, kGroup, q8_payload_bytes(N, K), kQ8Block);
+  pack_q8_codes<<<blocks_for(cu, 256), 256, 0, s>>>(codes, N, K, packed + kHeaderBytes, cu);
+  pack_q8_scales<<<blocks_for(su, 256), 256, 0, s>>>(scales, N, K, packed + kHeaderBytes, su);
   pack_done<<<1, 32, 0, s>>>();
   return cudaGetLastError();
 }

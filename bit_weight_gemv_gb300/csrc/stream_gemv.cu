@@ -253,8 +253,9 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
       grid_wait();  // the activations may be the previous kernel's output
       for (int b = 0; b < pre; ++b) copy_x(b, b, ptx::smem_addr(&full[b]));
       int issued = pre;
+      const int nbi = a.stall ? pre : nb;  // read once: the waits below clobber memory
       RingPos rp{pre % S, (uint32_t)(pre / S) & 1u};
-      for (int b = pre; b < (a.stall ? pre : nb); ++b, rp.next(S)) {
+      for (int b = pre; b < nbi; ++b, rp.next(S)) {
         const int s = rp.s;
         if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), rp.ph ^ 1u)) {
           record_error(a.err, LOWBIT_ERR_TIMEOUT);
@@ -281,7 +282,8 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
     // parity wait can never meet a phase two behind), whatever the stage count.
     if (hdr_ok) {
       RingPos rp{0, 0u};
-      for (int b = 0; b < (a.stall ? min(nb, S) : nb); ++b, rp.next(S)) {
+      const int nbs = a.stall ? min(nb, S) : nb;  // read once: the waits below clobber memory
+      for (int b = 0; b < nbs; ++b, rp.next(S)) {
         const int s = rp.s;
         if (s % conv_warps<MT>() != warp - kConvWarp) continue;
         const bool landed = ptx::mbar_wait(ptx::smem_addr(&full[s]), rp.ph);
@@ -538,8 +540,9 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
         ptx::bulk_g2s(ptx::smem_addr(stage(b) + BB), xsrc + (size_t)b * KIN, XB,
                       ptx::smem_addr(&full[b]));
       int issued = pre;
+      const int nbi = a.stall ? pre : nb;  // read once: the waits below clobber memory
       RingPos rp{pre % S, (uint32_t)(pre / S) & 1u};
-      for (int b = pre; b < (a.stall ? pre : nb); ++b, rp.next(S)) {
+      for (int b = pre; b < nbi; ++b, rp.next(S)) {
         const int s = rp.s;
         if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), rp.ph ^ 1u)) {
           record_error(a.err, LOWBIT_ERR_TIMEOUT);
@@ -563,7 +566,8 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
     // Lane l tabulates sets l, l + 32, ... (one per 128 inputs of the block).
     if (hdr_ok) {
       RingPos rp{0, 0u};
-      for (int b = 0; b < (a.stall ? min(nb, S) : nb); ++b, rp.next(S)) {
+      const int nbs = a.stall ? min(nb, S) : nb;  // read once: the waits below clobber memory
+      for (int b = 0; b < nbs; ++b, rp.next(S)) {
         const int s = rp.s;
         if (s % kLutWarps != warp - kLutWarp) continue;  // this warp's stages only
         const bool landed = ptx::mbar_wait(ptx::smem_addr(&full[s]), rp.ph);
@@ -818,8 +822,9 @@ nvfp4_stream_kernel(const __grid_constant__ StreamArgs a) {
         ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)b * kNvStage + kNvfp4Block), xsrc + (size_t)b * kGroup,
                       kXBytes, ptx::smem_addr(&full[b]));
       int issued = pre;
+      const int nbi = a.stall ? pre : nb;  // read once: the waits below clobber memory
       RingPos rp{pre % S, (uint32_t)(pre / S) & 1u};
-      for (int b = pre; b < (a.stall ? pre : nb); ++b, rp.next(S)) {
+      for (int b = pre; b < nbi; ++b, rp.next(S)) {
         const int s = rp.s;
         if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), rp.ph ^ 1u)) {
           record_error(a.err, LOWBIT_ERR_TIMEOUT);
@@ -843,7 +848,8 @@ nvfp4_stream_kernel(const __grid_constant__ StreamArgs a) {
     // converter c owns the stages s with s % 2 == c (each stage's phases met in order)
     if (hdr_ok) {
       RingPos rp{0, 0u};
-      for (int b = 0; b < (a.stall ? min(nb, S) : nb); ++b, rp.next(S)) {
+      const int nbs = a.stall ? min(nb, S) : nb;  // read once: the waits below clobber memory
+      for (int b = 0; b < nbs; ++b, rp.next(S)) {
         const int s = rp.s;
         if (s % conv_warps<1>() != warp - kConvWarp) continue;
         const bool landed = ptx::mbar_wait(ptx::smem_addr(&full[s]), rp.ph);
@@ -980,6 +986,252 @@ nvfp4_stream_kernel(const __grid_constant__ StreamArgs a) {
   }
 }
 
+// ------------------------------------------------------------------------------ Q8, M = 1
+// The trimmed draft head in 8 bits (small-vocabulary MTP study, section 3.3, the Q8 arm of its
+// table; w = d * q, int8 q, one fp16 d per 32 inputs) streamed as the INT4 kernel streams its
+// blocks, against the same int16 activations.  Each code word holds four signed bytes in input
+// order, so two integer dot products (16-bit x signed 8-bit, two products added into 32 bits)
+// take a word against the two activation pairs it meets; a run of 32 inputs (below 2^27 in
+// magnitude, so its fp32 value is within 2^-24 of exact) is scaled by its d in fp32.
+constexpr uint32_t kQ8Stage = kQ8Block + kXBytes;
+
+__device__ __forceinline__ int dp2a_lo_s8(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.lo.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp2a_hi_s8(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.hi.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(stream_threads<1>())
+q8_stream_kernel(const __grid_constant__ StreamArgs a) {
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ __align__(8) uint64_t full[kMaxStages];
+  __shared__ __align__(8) uint64_t xready[kMaxStages];
+  __shared__ __align__(8) uint64_t empty[kMaxStages];
+  __shared__ __align__(8) uint64_t redbar;
+  __shared__ __align__(8) uint64_t never;  // nothing arrives on it (test-only stall setting)
+  __shared__ __align__(16) uint32_t xq[kMaxStages][kGroup / 2];  // int16 pairs (X[2i], X[2i+1])
+  __shared__ float xdown[kMaxStages][2];                          // 2^-sh of inputs 0..63, 64..127
+  __shared__ float red[kCWarps][32];
+  __shared__ float part[kRowTile];
+  __shared__ int ok;
+  __shared__ int gave_up;
+  __shared__ int tile_got;   // rank 0 of a split tile: every peer's partial sums arrived
+  __shared__ int hdr_valid;  // the whole grid agrees on it: every CTA reads the same header
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int C = a.cluster;
+  const int cid = (int)blockIdx.x / C, crank = (int)blockIdx.x % C;
+  const GemvProblem& pr = a.p[0];  // one matrix per launch
+  const int ks = pr.ks, rank = crank % ks;
+  const int tile = (cid - pr.cluster_begin) * (C / ks) + crank / ks;
+  const int G = pr.K / kGroup;
+  const bool live = tile < row_tiles(pr.N);
+  const int g0 = (int)((long long)rank * G / ks), g1 = (int)((long long)(rank + 1) * G / ks);
+  const int nb = live ? g1 - g0 : 0;
+  const int S = a.stages;
+  const PackedHeader* hp = reinterpret_cast<const PackedHeader*>(pr.packed);
+
+  if (threadIdx.x == 0) {
+    ok = live && (pr.early || header_matches(hp, kFormatQ8, 0, pr.N, pr.K));
+    gave_up = 0;
+    tile_got = 1;
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&xready[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&empty[s]), kCWarps);
+    }
+    ptx::mbar_init(ptx::smem_addr(&redbar), (uint32_t)(kRowTile * (ks > 1 ? ks - 1 : 1)));
+    ptx::mbar_init(ptx::smem_addr(&never), 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp < kCWarps) red[warp][lane] = 0.f;
+  __syncthreads();
+  if (C > 1) ptx::cluster_arrive();
+  if (threadIdx.x == 0) grid_launch();
+  const bool hdr_ok = ok != 0;
+  if (threadIdx.x == 0) {
+    // every CTA, live or not, checks the header: the argmax epilogue's CTA count depends on it
+    hdr_valid = header_matches(hp, kFormatQ8, 0, pr.N, pr.K);
+    if (!hdr_valid) ok = 0;
+  }
+
+  if (warp == kCWarps) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0 && hdr_ok) {
+      const uint8_t* wsrc = pr.packed + kHeaderBytes + ((size_t)tile * G + g0) * kQ8Block;
+      const uint16_t* xsrc = pr.X + (size_t)g0 * kGroup;
+      const int pre = min(nb, S);
+      for (int b = 0; b < pre; ++b) {
+        const uint32_t bar = ptx::smem_addr(&full[b]);
+        ptx::mbar_arrive_expect_tx(bar, kQ8Stage);
+        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)b * kQ8Stage), wsrc + (size_t)b * kQ8Block,
+                      kQ8Block, bar);
+      }
+      grid_wait();  // the activations may be the previous kernel's output
+      for (int b = 0; b < pre; ++b)
+        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)b * kQ8Stage + kQ8Block), xsrc + (size_t)b * kGroup,
+                      kXBytes, ptx::smem_addr(&full[b]));
+      int issued = pre;
+      const int nbi = a.stall ? pre : nb;  // read once: the waits below clobber memory
+      RingPos rp{pre % S, (uint32_t)(pre / S) & 1u};
+      for (int b = pre; b < nbi; ++b, rp.next(S)) {
+        const int s = rp.s;
+        if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), rp.ph ^ 1u)) {
+          record_error(a.err, LOWBIT_ERR_TIMEOUT);
+          gave_up = 1;
+          break;
+        }
+        const uint32_t bar = ptx::smem_addr(&full[s]);
+        ptx::mbar_arrive_expect_tx(bar, kQ8Stage);
+        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)s * kQ8Stage), wsrc + (size_t)b * kQ8Block,
+                      kQ8Block, bar);
+        ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)s * kQ8Stage + kQ8Block),
+                      xsrc + (size_t)b * kGroup, kXBytes, bar);
+        issued = b + 1;
+      }
+      for (int b = max(0, issued - S); b < issued; ++b)
+        ptx::mbar_wait(ptx::smem_addr(&full[b % S]), (b / S) & 1);
+    }
+    __syncwarp();
+  } else if (warp >= kConvWarp) {
+    // ---------------------------------------------------------------- activation converters
+    // converter c owns the stages s with s % 2 == c (each stage's phases met in order)
+    if (hdr_ok) {
+      RingPos rp{0, 0u};
+      const int nbs = a.stall ? min(nb, S) : nb;  // read once: the waits below clobber memory
+      for (int b = 0; b < nbs; ++b, rp.next(S)) {
+        const int s = rp.s;
+        if (s % conv_warps<1>() != warp - kConvWarp) continue;
+        const bool landed = ptx::mbar_wait(ptx::smem_addr(&full[s]), rp.ph);
+        if (!__all_sync(0xFFFFFFFFu, landed)) {
+          if (lane == 0) {
+            record_error(a.err, LOWBIT_ERR_TIMEOUT);
+            gave_up = 1;
+          }
+          break;
+        }
+        const uint2 raw = reinterpret_cast<const uint2*>(ring + (size_t)s * kQ8Stage + kQ8Block)[lane];
+        const Converted cv = convert_run64(raw, lane);
+        reinterpret_cast<uint2*>(xq[s])[lane] = make_uint2(cv.i0 | (cv.i1 << 16), cv.i2 | (cv.i3 << 16));
+        if ((lane & 15) == 0) xdown[s][lane >> 4] = cv.down;
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&xready[s]));
+      }
+    }
+  } else if (warp < kCWarps && hdr_ok) {
+    // ---------------------------------------------------------------- compute
+    // Warp (q, h): rows 32q..32q+31, inputs 64h..64h+63 (chunks 4h..4h+3; scale runs 2h, 2h+1)
+    const int q = warp & 3, h = warp >> 2;
+    const int row = 32 * q + lane;
+    float total = 0.f;
+    RingPos rp{0, 0u};
+    const int nbc = stalled_out(a, ptx::smem_addr(&never), a.err, gave_up, lane) ? 0 : nb;
+    for (int b = 0; b < nbc; ++b, rp.next(S)) {
+      const int s = rp.s;
+      const bool ready = ptx::mbar_wait(ptx::smem_addr(&xready[s]), rp.ph);
+      if (!__all_sync(0xFFFFFFFFu, ready)) {
+        if (lane == 0) {
+          record_error(a.err, LOWBIT_ERR_TIMEOUT);
+          gave_up = 1;
+        }
+        break;
+      }
+      const uint8_t* st = ring + (size_t)s * kQ8Stage;
+      const uint2* xw = reinterpret_cast<const uint2*>(xq[s]) + 16 * h;  // pairs of 4 inputs
+      float sub = 0.f;  // sum over the two runs of 32: d * (integer dot product)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint4 c0 = *reinterpret_cast<const uint4*>(st + (4 * h + 2 * j) * (kRowTile * 16) + row * 16);
+        const uint4 c1 = *reinterpret_cast<const uint4*>(st + (4 * h + 2 * j + 1) * (kRowTile * 16) + row * 16);
+        const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        int acc0 = 0, acc1 = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {  // word i: inputs 64h + 32j + 4i .. +3
+          const uint2 x = xw[8 * j + i];
+          acc0 = dp2a_lo_s8(x.x, w[i], acc0);
+          acc1 = dp2a_hi_s8(x.y, w[i], acc1);
+        }
+        const float d = half_bits_to_float(
+            *reinterpret_cast<const uint16_t*>(st + kQ8ScaleOff + (2 * h + j) * (kRowTile * 2) + row * 2));
+        sub = fmaf(d, (float)(acc0 + acc1), sub);
+      }
+      const float down = xdown[s][h];
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&empty[s]));
+      total = fmaf(down, sub, total);
+    }
+    red[warp][lane] = total;
+  }
+
+  // -------------------------------------------------------------------- reduction + output
+  __syncthreads();
+  const bool out_ok = ok != 0 && !gave_up;  // header verified, every wait completed
+  if (!out_ok && live && threadIdx.x == 0 && rank == 0 && tile == 0)
+    record_error(a.err, LOWBIT_ERR_INVALID_ARG);
+  if (threadIdx.x < kRowTile) {
+    const int q = threadIdx.x >> 5, l = threadIdx.x & 31;
+    part[threadIdx.x] = red[q][l] + red[q + 4][l];
+  }
+  const int n = tile * kRowTile + (int)threadIdx.x;
+  if (C > 1) ptx::cluster_wait();
+  bool have = false;  // this thread holds row n's complete sum in y
+  float y = 0.f;
+  if (ks > 1) {
+    float* slots = reinterpret_cast<float*>(ring + (size_t)S * kQ8Stage);  // [ks-1][128]
+    const uint32_t owner = (uint32_t)(crank - rank);
+    if (live && threadIdx.x < kRowTile) {
+      if (rank != 0) {
+        // a CTA that gave up on a wait stays out of rank 0's shared memory
+        if (!gave_up) {
+          const uint32_t la = ptx::smem_addr(&slots[(rank - 1) * kRowTile + threadIdx.x]);
+          ptx::st_dsmem_f32(ptx::map_to_rank(la, owner), part[threadIdx.x]);
+          ptx::mbar_arrive_remote(ptx::map_to_rank(ptx::smem_addr(&redbar), owner));
+        }
+      } else {
+        // under the stall setting no push can still be coming (see the INT4 kernel)
+        const bool got = ptx::mbar_wait_cluster(ptx::smem_addr(&redbar), 0, a.stall ? kStallLimit : kWaitLimit);
+        if (!got) {
+          record_error(a.err, LOWBIT_ERR_TIMEOUT);
+          tile_got = 0;
+        }
+        y = part[threadIdx.x];
+        for (int r = 1; r < ks; ++r) y += slots[(r - 1) * kRowTile + threadIdx.x];
+        have = got && out_ok && n < pr.N;
+      }
+    }
+  } else {
+    __syncthreads();
+    if (threadIdx.x < kRowTile) {
+      y = part[threadIdx.x];
+      have = out_ok && n < pr.N;
+    }
+  }
+  if constexpr (EPI == 0) {
+    if (have) {
+      grid_wait();
+      pr.Y[n] = float_to_bf16_bits(y);
+    }
+  } else {
+    if (hdr_valid) {
+      grid_wait();  // the previous call on this workspace has reset it
+      if (warp < kRowTile / 32) {  // warps 0..3 hold the tile's rows
+        unsigned long long key = have ? argmax_key(y, n) : 0ull;
+        key = warp_max_u64(key);
+        if (lane == 0 && key) atomicMax(&a.ws->keys[0], key);
+      }
+      // a live tile whose sums are incomplete (a wait gave up here or in a peer) fails the call
+      __syncthreads();
+      draft_finish(a.ws, 1, a.id_map, a.ids, live && (gave_up || (ks > 1 && rank == 0 && !tile_got)));
+    }
+  }
+}
+
 // ------------------------------------------------------------------------------ warp MMA, M <= 32
 // The verify block (Efficient-Qwen report, section 2.2: the target checks a block of drafts
 // in one pass; block size 16) on the warp-level tensor-core MMA: mma.sync m16n8k16, bf16
@@ -996,13 +1248,14 @@ nvfp4_stream_kernel(const __grid_constant__ StreamArgs a) {
 // the A fragment of the MMA -- to exact bf16 q (the nibble ORed into bf16 128.0, minus 136),
 // loads the activations' B fragments with ldmatrix and issues one MMA per 8 activation rows.
 // After a group's 128 inputs it adds s * D to fp32 totals held in registers.
-constexpr int kMmaInt4 = 0, kMmaPlanes = 1, kMmaSa = 2;  // weight formats of the warp-MMA kernels
+constexpr int kMmaInt4 = 0, kMmaPlanes = 1, kMmaSa = 2, kMmaQ8 = 3;  // weight formats of the warp-MMA kernels
 // Inputs per block: a group of 128 (INT4, binary planes) or an sa super-block of 256.
 __host__ __device__ constexpr int mma_kin(int fmt) { return fmt == kMmaSa ? kSuper : kGroup; }
 // Stage layout: the block, then the activation tile (kin inputs x MT rows, 64-input swizzle
 // atoms) at the next 1024-byte boundary.
 __host__ __device__ constexpr uint32_t mma_block_bytes(int fmt, int P, int GS) {
   return fmt == kMmaInt4 ? kInt4Block
+       : fmt == kMmaQ8 ? kQ8Block
        : fmt == kMmaPlanes ? (uint32_t)P * (kRowTile * 16 + kRowTile * 2)
        : (uint32_t)P * 2 * kRowTile * 16 + (uint32_t)P * (kSuper / GS) * kRowTile + kRowTile * 2;
 }
@@ -1033,8 +1286,8 @@ struct MmaArgs {
   StreamArgs s;
 };
 // Epilogues: bf16 outputs; the LM-head argmax + acceptance; one shard of a row-sharded LM head
-// (the shard's best key per token).
-constexpr int kEpiStore = 0, kEpiVerify = 1, kEpiKeys = 2;
+// (the shard's best key per token); the draft head's id-mapped argmax.
+constexpr int kEpiStore = 0, kEpiVerify = 1, kEpiKeys = 2, kEpiDraft = 3;
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -1059,6 +1312,17 @@ __device__ __forceinline__ uint32_t bf16x2_sub_rn(uint32_t a, uint32_t b) {
 // (q[k], q[k+1]) exactly: 128 + u in bf16, minus 136.
 __device__ __forceinline__ uint32_t q_pair(uint32_t w) {
   return bf16x2_sub_rn((w & 0x000F000Fu) | 0x43004300u, 0x43084308u);
+}
+// Two int8 codes -> the exact bf16 pair: `w` holds u = q + 128 in each byte; sel picks the
+// first code's byte (sel + 1 the second's) under the fp32 exponent of 2^23, so the float is
+// 2^23 + u exactly, and subtracting 2^23 + 128 leaves q.
+__device__ __forceinline__ uint32_t q8_pair(uint32_t w, uint32_t sel) {
+  uint32_t lo, hi, d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(w), "r"(0x4B000000u), "r"(sel));
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(w), "r"(0x4B000000u), "r"(sel + 1u));
+  const float flo = __uint_as_float(lo) - 8388736.f, fhi = __uint_as_float(hi) - 8388736.f;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(fhi), "f"(flo));
+  return d;
 }
 
 template <int FMT, int MT, int EPI>
@@ -1101,8 +1365,9 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
   const uint32_t STG = mma_stage_bytes(FMT, P, GS, MT);  // block, then the activation atoms
   auto header_ok = [&]() {
     return FMT == kMmaSa ? header_matches_sa(hp, P, GS, pr.N, pr.K)
-                         : header_matches(hp, FMT == kMmaInt4 ? kFormatInt4 : kFormatBinplane, P,
-                                          pr.N, pr.K);
+                         : header_matches(hp, FMT == kMmaInt4 ? kFormatInt4
+                                                : FMT == kMmaQ8 ? kFormatQ8 : kFormatBinplane,
+                                          P, pr.N, pr.K);
   };
 
   if (threadIdx.x < MT) kmax[threadIdx.x] = 0ull;
@@ -1146,8 +1411,9 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
       grid_wait();  // the activations may be the previous kernel's output
       for (int b = 0; b < pre; ++b) copy_x(b, b, ptx::smem_addr(&full[b]));
       int issued = pre;
+      const int nbi = a.stall ? pre : nb;  // read once: the waits below clobber memory
       RingPos rp{pre % S, (uint32_t)(pre / S) & 1u};
-      for (int b = pre; b < (a.stall ? pre : nb); ++b, rp.next(S)) {
+      for (int b = pre; b < nbi; ++b, rp.next(S)) {
         const int s = rp.s;
         if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), rp.ph ^ 1u)) {
           record_error(a.err, LOWBIT_ERR_TIMEOUT);
@@ -1230,6 +1496,46 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
           acc[i][2] = fmaf(s1, d[i][2], acc[i][2]);
           acc[i][3] = fmaf(s1, d[i][3], acc[i][3]);
         }
+      } else if constexpr (FMT == kMmaQ8) {
+        // Q8 (int8 codes, fp16 d per run of 32 inputs): step ss is 16-input chunk ss; this
+        // lane's A share is bytes 2(t&1), 2(t&1)+1 of words t>>1 and 2 + (t>>1) of the chunk
+        // in rows r0 and r0 + 8.  The MMA sums of a run's two steps are scaled by its d.
+        const uint32_t sel = (uint32_t)(2 * (t & 1)) | 0x7540u;  // code byte, 0, 0, 0x4B
+        float d[NT][4];
+#pragma unroll
+        for (int i = 0; i < NT; ++i) d[i][0] = d[i][1] = d[i][2] = d[i][3] = 0.f;
+#pragma unroll
+        for (int ss = 0; ss < 8; ++ss) {
+          const uint8_t* cp = st + ss * (kRowTile * 16) + 4 * (t >> 1);
+          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(cp + r0 * 16) ^ 0x80808080u;
+          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(cp + (r0 + 8) * 16) ^ 0x80808080u;
+          const uint32_t w2 = *reinterpret_cast<const uint32_t*>(cp + r0 * 16 + 8) ^ 0x80808080u;
+          const uint32_t w3 = *reinterpret_cast<const uint32_t*>(cp + (r0 + 8) * 16 + 8) ^ 0x80808080u;
+          const uint32_t a0 = q8_pair(w0, sel), a1 = q8_pair(w1, sel);
+          const uint32_t a2 = q8_pair(w2, sel), a3 = q8_pair(w3, sel);
+#pragma unroll
+          for (int hh = 0; hh < MT / 16; ++hh) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(xs + xsw[ss & 3] + (ss >> 2) * (MT * 128) + hh * 16 * 128, b0, b1, b2, b3);
+            mma_16816(d[2 * hh], a0, a1, a2, a3, b0, b1);
+            mma_16816(d[2 * hh + 1], a0, a1, a2, a3, b2, b3);
+          }
+          if (ss & 1) {  // the run's second step: fold d * D into the totals
+            const uint8_t* sp = st + kQ8ScaleOff + (ss >> 1) * (kRowTile * 2);
+            const float s0 = half_bits_to_float(*reinterpret_cast<const uint16_t*>(sp + r0 * 2));
+            const float s1 = half_bits_to_float(*reinterpret_cast<const uint16_t*>(sp + (r0 + 8) * 2));
+#pragma unroll
+            for (int i = 0; i < NT; ++i) {
+              acc[i][0] = fmaf(s0, d[i][0], acc[i][0]);
+              acc[i][1] = fmaf(s0, d[i][1], acc[i][1]);
+              acc[i][2] = fmaf(s1, d[i][2], acc[i][2]);
+              acc[i][3] = fmaf(s1, d[i][3], acc[i][3]);
+              d[i][0] = d[i][1] = d[i][2] = d[i][3] = 0.f;
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&empty[s]));
       } else if constexpr (FMT == kMmaPlanes) {
         // Binary planes: word w of a plane row covers inputs 32w..32w+31, bit i the sign of
         // 32w + 2i and bit 16 + i that of 32w + 2i + 1.  Step s's A fragment takes pairs
@@ -1354,6 +1660,7 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
     grid_wait();  // outputs and the verify workspace belong to the previous kernel until now
     const int rows = kRowTile / ks, rbase = rank * rows;
     const uint32_t base = (uint32_t)(crank - rank);  // rank 0 of this tile
+    const int row0 = a.row_offset;  // read once: the loop's cluster loads clobber memory
     for (int i0 = 0; i0 < rows * MT; i0 += kMmaWarps * 32) {  // the same trip count in every lane
       const int idx = i0 + (int)threadIdx.x;
       const int m = idx / rows, row = rbase + idx % rows;
@@ -1371,7 +1678,7 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
       if constexpr (EPI == kEpiStore) {
         if (in) pr.Y[(size_t)m * pr.N + n] = float_to_bf16_bits(y);
       } else {
-        unsigned long long key = in ? argmax_key(y, n + a.row_offset) : 0ull;
+        unsigned long long key = in ? argmax_key(y, n + row0) : 0ull;
         if (rows >= 32) {  // a warp's 32 values share one activation row
           key = warp_max_u64(key);
           if (lane == 0 && key) atomicMax(&kmax[min(m, MT - 1)], key);
@@ -1390,6 +1697,8 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
     // a live tile whose totals are incomplete fails the call: nothing is written
     if constexpr (EPI == kEpiKeys)
       keys_finish(a.ws, M, a.keys_out, live && !tile_done);
+    else if constexpr (EPI == kEpiDraft)
+      draft_finish(a.ws, M, a.id_map, a.ids, live && !tile_done);
     else
       lmhead_finish(a.ws, M, a.draft, a.ids, a.n_accept, a.bonus, live && !tile_done);
   }
@@ -1407,6 +1716,13 @@ template <int MT>
 __global__ void __launch_bounds__(kMmaThreads, mma_resident<MT>())
 bp_mma_kernel(const __grid_constant__ MmaArgs A) {
   mma_body<kMmaPlanes, MT, kEpiStore>(A);
+}
+
+// And for Q8 weights (the 8-bit draft head): bf16 outputs or the id-mapped argmax.
+template <int MT, int EPI>
+__global__ void __launch_bounds__(kMmaThreads, mma_resident<MT>())
+q8_mma_kernel(const __grid_constant__ MmaArgs A) {
+  mma_body<kMmaQ8, MT, EPI>(A);
 }
 
 // And for the deployed sa format: super-blocks of 256 inputs, alpha = d * a per code group.
@@ -1504,7 +1820,8 @@ constexpr int kMaxDevices = 64;
 struct OptIns {
   std::atomic<unsigned char> done[kMaxDevices];
 };
-OptIns g_int4_optins[3], g_bp_optins, g_sa_optins, g_nv_optins[2], g_mma_optins[10];  // one per kernel built
+OptIns g_int4_optins[3], g_bp_optins, g_sa_optins, g_nv_optins[2], g_q8_optins[2],
+    g_mma_optins[14];  // one per kernel built
 
 template <typename Kernel>
 cudaError_t opt_in(Kernel kern, OptIns& o, size_t budget) {
@@ -1597,7 +1914,8 @@ template <int FMT, int MT, int EPI>
 cudaError_t launch_mma_mt(const GemvProblem* probs, int count, int M, LmheadWorkspace* ws,
                           const int32_t* draft, int32_t* argmax, int32_t* n_accept,
                           int32_t* bonus, int* err, cudaStream_t s,
-                          unsigned long long* keys_out = nullptr, int row_offset = 0) {
+                          unsigned long long* keys_out = nullptr, int row_offset = 0,
+                          const int32_t* id_map = nullptr) {
   const int P = FMT == kMmaInt4 ? 0 : probs[0].P, GS = FMT == kMmaSa ? probs[0].G : 0;
   for (int i = 1; i < count; ++i)  // one stage size per launch
     if (FMT != kMmaInt4 && (probs[i].P != P || probs[i].G != probs[0].G)) return cudaErrorInvalidValue;
@@ -1619,6 +1937,7 @@ cudaError_t launch_mma_mt(const GemvProblem* probs, int count, int M, LmheadWork
   a.bonus = bonus;
   a.keys_out = keys_out;
   a.row_offset = row_offset;
+  a.id_map = id_map;
   a.stall = debug_stall();
   for (int i = 0; i < a.count; ++i) {
     // X [M][K] bf16 as matrix i's activations (in schedule order); rows >= M read as zero
@@ -1641,6 +1960,10 @@ cudaError_t launch_mma_mt(const GemvProblem* probs, int count, int M, LmheadWork
   if constexpr (FMT == kMmaInt4) {
     constexpr int slot_i = (MT == 16 ? 0 : 1) + (EPI == kEpiKeys ? 8 : 2 * EPI);
     return launch_streaming(int4_mma_kernel<MT, EPI>, g_mma_optins[slot_i], budget, A, sc, smem,
+                            kMmaThreads, s);
+  } else if constexpr (FMT == kMmaQ8) {
+    constexpr int slot_q = 10 + (MT == 16 ? 0 : 1) + (EPI == kEpiDraft ? 2 : 0);
+    return launch_streaming(q8_mma_kernel<MT, EPI>, g_mma_optins[slot_q], budget, A, sc, smem,
                             kMmaThreads, s);
   } else if constexpr (FMT == kMmaPlanes) {
     return launch_streaming(bp_mma_kernel<MT>, g_mma_optins[MT == 16 ? 4 : 5], budget, A, sc,
@@ -1700,6 +2023,46 @@ cudaError_t launch_lmhead_keys_mma(const GemvProblem& prob, int M, LmheadWorkspa
                                                  err, s, keys_out, row_offset);
   return launch_mma_mt<kMmaInt4, 32, kEpiKeys>(&prob, 1, M, ws, nullptr, nullptr, nullptr, nullptr,
                                                err, s, keys_out, row_offset);
+}
+
+cudaError_t launch_q8_mma(const GemvProblem& prob, int M, LmheadWorkspace* ws, const int32_t* id_map,
+                          int32_t* ids, int* err, cudaStream_t s) {
+  if (M < 1 || M > 32) return cudaErrorInvalidValue;
+  if (!ws) {
+    if (M <= 16)
+      return launch_mma_mt<kMmaQ8, 16, kEpiStore>(&prob, 1, M, nullptr, nullptr, nullptr, nullptr,
+                                                  nullptr, err, s);
+    return launch_mma_mt<kMmaQ8, 32, kEpiStore>(&prob, 1, M, nullptr, nullptr, nullptr, nullptr,
+                                                nullptr, err, s);
+  }
+  if (M <= 16)
+    return launch_mma_mt<kMmaQ8, 16, kEpiDraft>(&prob, 1, M, ws, nullptr, ids, nullptr, nullptr, err,
+                                                s, nullptr, 0, id_map);
+  return launch_mma_mt<kMmaQ8, 32, kEpiDraft>(&prob, 1, M, ws, nullptr, ids, nullptr, nullptr, err, s,
+                                              nullptr, 0, id_map);
+}
+
+cudaError_t launch_q8_stream(const GemvProblem& prob, LmheadWorkspace* ws, const int32_t* id_map,
+                             int32_t* ids, int* err, cudaStream_t s) {
+  StreamArgs a = {};
+  Schedule sc;
+  if (!make_schedule(&prob, 1, kGroup, kInt4TargetBlocks, kMaxSplit, a, sc)) return cudaErrorInvalidValue;
+  a.err = err;
+  a.m = 1;
+  a.stall = debug_stall();
+  a.ws = ws;
+  a.id_map = id_map;
+  a.ids = ids;
+  const size_t slots = (size_t)(sc.kmax - 1) * kRowTile * sizeof(float);
+  int S = slots < kInt4SmemBudget ? (int)((kInt4SmemBudget - slots) / kQ8Stage) : 0;
+  S = S > kMaxStages ? kMaxStages : (S < 2 ? 2 : S);
+  S -= S % conv_warps<1>();
+  a.stages = sc.maxnb < S ? sc.maxnb : S;
+  const size_t smem = (size_t)a.stages * kQ8Stage + slots;
+  if (ws) return launch_streaming(q8_stream_kernel<1>, g_q8_optins[1], kSmemBudget, a, sc, smem,
+                                  stream_threads<1>(), s);
+  return launch_streaming(q8_stream_kernel<0>, g_q8_optins[0], kSmemBudget, a, sc, smem,
+                          stream_threads<1>(), s);
 }
 
 cudaError_t launch_int4_stream(const GemvProblem* probs, int count, int M, int* err, cudaStream_t s) {

@@ -78,6 +78,10 @@ size_t lowbit_sa_packed_bytes(int P, int G, int N, int K);
  * code bytes and K/16 scale bytes. */
 size_t lowbit_nvfp4_packed_bytes(int N, int K);
 
+/* Bytes of a packed Q8 buffer (lowbit_pack_q8): header + ceil(N/128)*128 rows of K code bytes
+ * and K/16 scale bytes (one fp16 per 32 inputs). */
+size_t lowbit_q8_packed_bytes(int N, int K);
+
 /* Bytes of the workspace lmhead_argmax_verify() needs (independent of N and K). */
 size_t lmhead_workspace_bytes(int M, int N, int K);
 
@@ -147,6 +151,19 @@ lowbit_status lowbit_pack_sa(const uint8_t* signbits, const uint8_t* codes, cons
  * inputs 128j + 16i .. +15 at 8192 + i*128 + r (i = 0..7). */
 lowbit_status lowbit_pack_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, int N, int K,
                                 void* packed, void* stream);
+
+/* Repack Q8 weights, the 8-bit arm of the small-vocabulary MTP study's trimmed draft head
+ * (section 3.3; read as the llama.cpp Q8_0 recipe the ShiftAddQwen README names):
+ *   w[n][k] = d[n][k/32] * q[n][k].
+ *   codes  : int8 [N][K] (two's complement, the full range -128..127), 16-byte aligned.
+ *   scales : fp16 [N][K/32], 2-byte aligned.
+ *   packed : lowbit_q8_packed_bytes(N, K) bytes, 16-byte aligned; fully overwritten.
+ * Layout: header (format 5), then per (tile t of 128 rows, group g of 128 inputs) one block of
+ * 17408 bytes at 128 + (t*(K/128) + g)*17408: for chunk c = 0..7 and row r the 16 code bytes of
+ * inputs 128g + 16c .. +15 at c*2048 + r*16, then d[n][4g + j] (fp16) at 16384 + j*256 + r*2
+ * (j = 0..3).  Padding rows hold code 0 and scale 0. */
+lowbit_status lowbit_pack_q8(const int8_t* codes, const uint16_t* scales, int N, int K, void* packed,
+                             void* stream);
 
 /* Synchronous check (copies the 128-byte header to the host after synchronising `stream`)
  * that `packed` holds format `format` (1 = INT4, 2 = binary planes) with these P, N, K.
@@ -223,6 +240,24 @@ lowbit_status lowbit_gemm_sa(const uint16_t* X, const void* packed, int P, int G
  * lowbit_draft_argmax, which chooses its kernel the same way.) */
 lowbit_status lowbit_gemm_nvfp4(const uint16_t* X, const void* packed, int M, int N, int K,
                                 uint16_t* Y, void* stream);
+
+/* Y = X * W^T for Q8 weights (lowbit_pack_q8), 1 <= M <= 32, fp32 accumulation, each output
+ * rounded once to bf16.  M = 1 streams the weights (activations held as int16 per run of 64 as
+ * in lowbit_gemm_int4; integer dot products against the signed codes, each run of 32 scaled
+ * by its d in fp32); M >= 2 runs the warp-level MMA (each code written exactly as bf16, the
+ * MMA sums of every 32 inputs scaled by d in fp32).  path: 0 the library's choice, 1 the
+ * streaming kernel (M = 1 only, else LOWBIT_ERR_SHAPE), 3 the warp-level MMA. */
+lowbit_status lowbit_gemm_q8(const uint16_t* X, const void* packed, int M, int N, int K, uint16_t* Y,
+                             void* stream);
+lowbit_status lowbit_gemm_q8_path(const uint16_t* X, const void* packed, int M, int N, int K,
+                                  uint16_t* Y, int path, void* stream);
+
+/* The draft step of a trimmed Q8 head: as lowbit_draft_argmax (ids[m] = id_map[argmax], fp32
+ * logits never rounded, lowest row on ties, the same workspace rules), for a head packed by
+ * lowbit_pack_q8.  M = 1 streams; M >= 2 runs the warp-level MMA. */
+lowbit_status lowbit_draft_argmax_q8(const uint16_t* H, const void* packed_head, int M, int N, int K,
+                                     const int32_t* id_map, int32_t* ids, void* workspace,
+                                     size_t ws_bytes, void* stream);
 
 /* Draft step of a trimmed NVFP4 head (small-vocabulary MTP study, section 3.3: the draft head
  * keeps the 32,768 most used rows of the vocabulary; its winners are mapped back to the full

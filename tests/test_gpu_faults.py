@@ -164,3 +164,29 @@ def test_draft_head_stall_writes_nothing_and_resets_workspace(lb):
     for gd in (ws, out):
         gd.check("draft")
     assert lb.lowbit_device_error() == 0
+
+
+@pytest.mark.parametrize("M", [1, 16])
+def test_q8_stall_times_out_and_recovers(lb, M):
+    from oracle import q8 as oq8
+    N, K = 700, 2048
+    codes, scales, ids, h = synth.q8_problem(46, M, N, K)
+    pk = torch.empty(lb.lowbit_q8_packed_bytes(N, K), dtype=torch.uint8, device="cuda")
+    lb.lowbit_pack_q8(dev(codes), f16_dev(scales), N, K, pk)
+    Y = Guarded((M, N), torch.bfloat16, fill=float("nan"))
+    assert _stalled(lb, lambda: lb.lowbit_gemm_q8(bf16_dev(h), pk, M, N, K, Y.t)) == TIMEOUT
+    assert torch.isnan(Y.t.float()).all()
+    ws = Guarded((lb.lmhead_workspace_bytes(2, N, K),), torch.uint8, fill=0)
+    out = Guarded((M,), torch.int32, fill=-7)
+    call = lambda: lb.lowbit_draft_argmax_q8(bf16_dev(h), pk, M, N, K, dev(ids), out.t, ws.t)
+    assert _stalled(lb, call) == TIMEOUT
+    assert (out.t == -7).all() and not ws.t.any()
+    lb.lowbit_gemm_q8(bf16_dev(h), pk, M, N, K, Y.t)
+    call()
+    torch.cuda.synchronize()
+    logits = oq8.gemm(h, codes, scales)
+    check_gemm(host_bits(Y.t), logits, f"q8 after stall M={M}")
+    check_argmax(np.searchsorted(ids, out.t.cpu().numpy()), logits, "q8 draft after stall")
+    for g in (Y, ws, out):
+        g.check("q8 stall")
+    assert lb.lowbit_device_error() == 0

@@ -61,6 +61,11 @@ def algorithmic_sa_bytes(P, G, N, K):
     return P * N * K // 8 + P * N * (K // G) + N * (K // 256) * 2
 
 
+def algorithmic_q8_bytes(N, K):
+    """int8 codes and one fp16 scale per 32 inputs."""
+    return N * K + N * (K // 32) * 2
+
+
 def algorithmic_nvfp4_bytes(N, K):
     """E2M1 codes and one E4M3 scale per 16 inputs."""
     return N * K // 2 + N * K // 16
@@ -343,6 +348,25 @@ def build_draft_head(lb, torch, l2, M, name, desc):
     return w
 
 
+def build_q8_head(lb, torch, l2, M, name, desc):
+    """The trimmed head in Q8: argmax over its rows, mapped to full-vocabulary ids."""
+    N, K = synth.DRAFT_ROWS, synth.HEAD_K
+    w = Workload(name, desc, "q8_stream_kernel" if M == 1 else "q8_mma_kernel")
+    codes, scales, ids, h = synth.q8_problem(4, M, N, K)
+    p = torch.empty(lb.lowbit_q8_packed_bytes(N, K), dtype=torch.uint8, device="cuda")
+    lb.lowbit_pack_q8(dev(codes), f16_dev(scales), N, K, p)
+    w.bytes = algorithmic_q8_bytes(N, K)
+    w.weights = N * K
+    packs = _copies(p, copies_for(w.bytes, l2), torch)
+    H, idm = bf16_dev(h), dev(ids)
+    out = torch.empty(M, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(lb.lmhead_workspace_bytes(2, N, K), dtype=torch.uint8, device="cuda")
+    for c in range(len(packs)):
+        w.calls.append([lambda c=c: lb.lowbit_draft_argmax_q8(H, packs[c], M, N, K, idm, out, ws)])
+    w.M, w.tokens, w.launches = M, M, 1
+    return w
+
+
 def build_lmhead(lb, torch, l2, N, path, name, desc):
     M, K = synth.VERIFY_BLOCK, synth.HEAD_K
     w = Workload(name, desc, {1: "int4_gemm_cc_kernel", 2: "tc_gemm_kernel"}.get(path, "int4_mma_kernel"))
@@ -434,6 +458,11 @@ def build_workload(lb, torch, l2, name, path):
         return build_draft_head(lb, torch, l2, M, name,
                                 f"trimmed NVFP4 draft head: {synth.DRAFT_ROWS} rows x K={synth.HEAD_K}, "
                                 f"M={M}, fused argmax mapped to full-vocabulary ids")
+    if name in ("draft_q8_m1", "draft_q8_m16"):
+        M = 1 if name == "draft_q8_m1" else 16
+        return build_q8_head(lb, torch, l2, M, name,
+                             f"trimmed Q8 draft head (int8, fp16 scale per 32): {synth.DRAFT_ROWS} rows x "
+                             f"K={synth.HEAD_K}, M={M}, fused argmax mapped to full-vocabulary ids")
     if name == "head_gemv":
         return build_head_gemv(lb, torch, l2, path, name,
                                f"INT4 GEMV at M=1 over the {synth.HEAD_ROWS[0]}-row vocabulary head, "
@@ -446,7 +475,7 @@ def build_workload(lb, torch, l2, name, path):
     raise ValueError(name)
 
 
-WORKLOADS = ("decode", "decode_deps", "decode_all", "verify", "verify_deps", "verify_all", "binplane_m1", "binplane_m16", "sa_m1", "sa_m16", "draft_m1", "draft_m16", "head_gemv", "lmhead_full", "lmhead_trim",
+WORKLOADS = ("decode", "decode_deps", "decode_all", "verify", "verify_deps", "verify_all", "binplane_m1", "binplane_m16", "sa_m1", "sa_m16", "draft_m1", "draft_m16", "draft_q8_m1", "draft_q8_m16", "head_gemv", "lmhead_full", "lmhead_trim",
              "tiny") + tuple(f"verify_m{m}" for m in synth.M_SWEEP if m not in (16,))
 
 
@@ -779,10 +808,10 @@ def run_ours(args):
 
 def arith_note(w):
     """What the timed kernels compute in: the JSON line's dtype names the data type in and out."""
-    if w.kernel in ("int4_stream_kernel", "nvfp4_stream_kernel"):
+    if w.kernel in ("int4_stream_kernel", "nvfp4_stream_kernel", "q8_stream_kernel"):
         return ("bf16 activations in, bf16 out; inside the kernel each run of 64 activations is "
                 "held as int16 under one power of two (exact within 2^7 of the run's largest), "
-                "integer dot products with the 4-bit codes, fp32 scaling and accumulation")
+                "integer dot products with the weight codes, fp32 scaling and accumulation")
     if w.kernel in ("bp_stream_kernel", "sa_stream_kernel"):
         return "bf16 in/out; fp32 tables of signed activation sums, fp32 accumulation"
     return "bf16 in/out; bf16 tensor-core operands, fp32 accumulation"

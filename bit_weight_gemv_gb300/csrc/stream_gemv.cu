@@ -1339,6 +1339,7 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
   __shared__ int gave_up;
   __shared__ int hdr_valid;  // the same in every CTA: they all read the one header
   __shared__ unsigned long long kmax[MT];  // verify: this CTA's best key per activation row
+  __shared__ uint32_t peer_gave_up[kMaxSplit];  // written by the split-K peers of this tile
   // Totals [MT][128], written once every stage has been consumed: they reuse the ring (the
   // launcher allocates at least MT * 512 bytes).  After a timed-out wait a late copy may still
   // land there; the outputs are wrong then anyway and the error word says so.
@@ -1390,7 +1391,36 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
     if (!hv) ok = 0;
   }
 
-  if (warp == kMmaWarps) {
+  if (a.stall) {
+    // ---------------------------------------------------------------- test-only stall setting
+    // The producer issues the first ring of copies and waits for them; the compute warps wait
+    // on a barrier nothing arrives on, give up and leave their totals unwritten.  Kept apart
+    // from the roles below so that normal operation runs exactly their code.
+    if (warp == kMmaWarps) {
+      if (hdr_ok && lane == 0) {
+        const uint8_t* wsrc = pr.packed + kHeaderBytes + ((size_t)tile * G + g0) * BB;
+        const uint32_t tx = BB + MT * 2 * KIN;
+        const int pre = min(nb, S);
+        for (int b = 0; b < pre; ++b) {
+          const uint32_t bar = ptx::smem_addr(&full[b]);
+          ptx::mbar_arrive_expect_tx(bar, tx);
+          ptx::bulk_g2s(ptx::smem_addr(ring + (size_t)b * STG), wsrc + (size_t)b * BB, BB, bar);
+        }
+        grid_wait();
+        for (int b = 0; b < pre; ++b) {
+          const uint32_t dst = ptx::smem_addr(ring + (size_t)b * STG + XOFF);
+#pragma unroll
+          for (int at = 0; at < NATOM; ++at)
+            ptx::tma_load_2d(dst + at * MT * 128, &A.xmap[pi], (g0 + b) * KIN + 64 * at, 0,
+                             ptx::smem_addr(&full[b]));
+        }
+        for (int b = 0; b < pre; ++b) ptx::mbar_wait(ptx::smem_addr(&full[b]), 0u);
+      }
+      __syncwarp();
+    } else if (hdr_ok) {
+      stalled_out(a, ptx::smem_addr(&never), a.err, gave_up, lane);
+    }
+  } else if (warp == kMmaWarps) {
     // ---------------------------------------------------------------- producer
     if (hdr_ok && lane == 0) {
       const uint8_t* wsrc = pr.packed + kHeaderBytes + ((size_t)tile * G + g0) * BB;
@@ -1411,9 +1441,8 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
       grid_wait();  // the activations may be the previous kernel's output
       for (int b = 0; b < pre; ++b) copy_x(b, b, ptx::smem_addr(&full[b]));
       int issued = pre;
-      const int nbi = a.stall ? pre : nb;  // read once: the waits below clobber memory
       RingPos rp{pre % S, (uint32_t)(pre / S) & 1u};
-      for (int b = pre; b < nbi; ++b, rp.next(S)) {
+      for (int b = pre; b < nb; ++b, rp.next(S)) {
         const int s = rp.s;
         if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), rp.ph ^ 1u)) {
           record_error(a.err, LOWBIT_ERR_TIMEOUT);
@@ -1446,8 +1475,7 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
 #pragma unroll
     for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     RingPos rp{0, 0u};
-    const int nbc = stalled_out(a, ptx::smem_addr(&never), a.err, gave_up, lane) ? 0 : nb;
-    for (int b = 0; b < nbc; ++b, rp.next(S)) {
+    for (int b = 0; b < nb; ++b, rp.next(S)) {
       const int s = rp.s;
       const bool landed = ptx::mbar_wait(ptx::smem_addr(&full[s]), rp.ph);
       if (!__all_sync(0xFFFFFFFFu, landed)) {
@@ -1645,17 +1673,17 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
   if (!out_ok && live && threadIdx.x == 0 && rank == 0 && tile == 0)
     record_error(a.err, LOWBIT_ERR_INVALID_ARG);
   const bool owner_thread = threadIdx.x < kMmaWarps * 32;
+  // The tile's totals are complete only if no CTA sharing it gave up on a wait: before the
+  // cluster barrier, thread q stores this CTA's flag into split-K peer q's shared memory (the
+  // barrier's release orders the stores); after it, each warp reads the ks flags it received.
+  if (ks > 1 && threadIdx.x < (unsigned)ks)
+    ptx::st_dsmem_u32(ptx::map_to_rank(ptx::smem_addr(&peer_gave_up[rank]),
+                                       (uint32_t)(crank - rank + (int)threadIdx.x)),
+                      (uint32_t)gave_up);
   if (C > 1) ptx::cluster_sync();
   const bool verify = EPI != kEpiStore && hdr_valid;
-  // The tile's totals are complete only if no CTA sharing it gave up on a wait: lane q of
-  // each warp reads peer q's flag (one load per lane, all in flight together) and the warp
-  // votes.
   bool tile_done = !gave_up;
-  if (ks > 1) {
-    const uint32_t flag = lane < ks ? ptx::ld_dsmem_u32(ptx::smem_addr(&gave_up),
-                                                       (uint32_t)(crank - rank + lane)) : 0u;
-    tile_done = !__any_sync(0xFFFFFFFFu, flag != 0u);
-  }
+  if (ks > 1) tile_done = !__any_sync(0xFFFFFFFFu, lane < ks && peer_gave_up[lane] != 0u);
   if (live && out_ok && tile_done && owner_thread) {
     grid_wait();  // outputs and the verify workspace belong to the previous kernel until now
     const int rows = kRowTile / ks, rbase = rank * rows;

@@ -185,17 +185,17 @@ int4_stream_kernel(const __grid_constant__ StreamArgs a) {
   __shared__ int gave_up;  // some wait of this CTA timed out
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int C = a.cluster;
-  const int cid = (int)blockIdx.x / C, crank = (int)blockIdx.x % C;  // cluster, rank in it
+  const int C = a.cluster, lc = __ffs(C) - 1;  // C and every ks are powers of two
+  const int cid = (int)blockIdx.x >> lc, crank = (int)blockIdx.x & (C - 1);  // cluster, rank in it
   int pi = 0;
   for (int i = 1; i < a.count; ++i)
     if (cid >= a.cl_begin[i]) pi = i;
   const GemvProblem& pr = a.p[pi];
-  const int ks = pr.ks, rank = crank % ks;  // this CTA's share of its tile's groups
-  const int tile = (cid - pr.cluster_begin) * (C / ks) + crank / ks;
+  const int ks = pr.ks, lk = __ffs(ks) - 1, rank = crank & (ks - 1);  // this CTA's share of its tile's groups
+  const int tile = ((cid - pr.cluster_begin) << (lc - lk)) + (crank >> lk);
   const int G = pr.K / kGroup;
   const bool live = tile < row_tiles(pr.N);  // the last cluster of a matrix may be partly idle
-  const int g0 = (int)((long long)rank * G / ks), g1 = (int)((long long)(rank + 1) * G / ks);
+  const int g0 = (rank * G) >> lk, g1 = ((rank + 1) * G) >> lk;
   const int nb = live ? g1 - g0 : 0;
   const int S = a.stages, M = MT == 1 ? 1 : a.m;
 
@@ -459,10 +459,33 @@ constexpr size_t kSaSmemMax = 96 * 1024;
 
 
 // acc += sum over the 8 nibbles of one sign word of the tabulated signed sums; `tab` points
-// at the word's 8 tables of 16 floats (nibble n: inputs of pair slots 4n..4n+3).
+// at the word's 8 tables of 16 floats (nibble n: inputs of pair slots 4n..4n+3).  The sa
+// kernel's form (the shared-address form below measured 3% slower there, 6% faster for the
+// binary planes).
 __device__ __forceinline__ void lut_word(uint32_t w, const float* tab, float (&acc)[2]) {
 #pragma unroll
   for (int n = 0; n < 8; ++n) acc[n & 1] += tab[16 * n + ((w >> (4 * n)) & 0xFu)];
+}
+// One table entry: the float at shared address a + OFF.
+template <int OFF>
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1+%2];" : "=f"(v) : "r"(a), "n"(OFF));
+  return v;
+}
+// acc += sum over the 8 nibbles of one sign word of the tabulated signed sums; `tab` is the
+// shared address of the word's 8 tables of 16 floats (nibble n: inputs of pair slots
+// 4n..4n+3), 64-byte aligned, so that a nibble's byte offset (4 x nibble, at most 60) can be
+// ORed into it: a shift, a masked OR, the load (table n at an immediate 64n) and the add.
+__device__ __forceinline__ void lut_word(uint32_t w, uint32_t tab, float (&acc)[2]) {
+  acc[0] += lds_f32<0>(ptx::and_or(w << 2, 0x3Cu, tab));
+  acc[1] += lds_f32<64>(ptx::and_or(w >> 2, 0x3Cu, tab));
+  acc[0] += lds_f32<128>(ptx::and_or(w >> 6, 0x3Cu, tab));
+  acc[1] += lds_f32<192>(ptx::and_or(w >> 10, 0x3Cu, tab));
+  acc[0] += lds_f32<256>(ptx::and_or(w >> 14, 0x3Cu, tab));
+  acc[1] += lds_f32<320>(ptx::and_or(w >> 18, 0x3Cu, tab));
+  acc[0] += lds_f32<384>(ptx::and_or(w >> 22, 0x3Cu, tab));
+  acc[1] += lds_f32<448>(ptx::and_or(w >> 26, 0x3Cu, tab));
 }
 
 // Body of both plane kernels.  SA = false: fp16-alpha planes, one block per (tile, group of
@@ -482,19 +505,19 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
   __shared__ int gave_up;  // some wait of this CTA timed out
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int C = a.cluster;
-  const int cid = (int)blockIdx.x / C, crank = (int)blockIdx.x % C;
+  const int C = a.cluster, lc = __ffs(C) - 1;  // C and every ks are powers of two
+  const int cid = (int)blockIdx.x >> lc, crank = (int)blockIdx.x & (C - 1);
   int pi = 0;
   for (int i = 1; i < a.count; ++i)
     if (cid >= a.cl_begin[i]) pi = i;
   const GemvProblem& pr = a.p[pi];
-  const int ks = pr.ks, rank = crank % ks;
-  const int tile = (cid - pr.cluster_begin) * (C / ks) + crank / ks;
+  const int ks = pr.ks, lk = __ffs(ks) - 1, rank = crank & (ks - 1);
+  const int tile = ((cid - pr.cluster_begin) << (lc - lk)) + (crank >> lk);
   constexpr int KIN = SA ? kSuper : kGroup;  // inputs per block
   constexpr uint32_t XB = KIN * 2, LUT = (KIN / 4) * 16 * sizeof(float);  // activations, tables
   const int G = pr.K / KIN, P = pr.P, GS = pr.G;
   const bool live = tile < row_tiles(pr.N);
-  const int g0 = (int)((long long)rank * G / ks), g1 = (int)((long long)(rank + 1) * G / ks);
+  const int g0 = (rank * G) >> lk, g1 = ((rank + 1) * G) >> lk;
   const int nb = live ? g1 - g0 : 0;
   const int S = a.stages;
   const uint32_t BB = SA ? sa_block(P, GS) : binplane_block(P), SB = BB + XB + LUT;
@@ -504,7 +527,8 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
   };
 
   if (threadIdx.x == 0) {
-    ok = live && (pr.early || header_ok());
+    // the table lookups OR byte offsets into 64-byte aligned table addresses
+    ok = live && (pr.early || header_ok()) && (ptx::smem_addr(smem) & 63u) == 0u;
     gave_up = 0;
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
@@ -625,14 +649,14 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
       const uint8_t* st = stage(s);
       if constexpr (!SA) {
         // inputs 64h..64h+63: sign words 2h, 2h+1 of each plane, nibble sets 16h..16h+15
-        const float* tab = reinterpret_cast<const float*>(st + BB + XB) + 16 * 16 * h;
+        const uint32_t tab = ptx::smem_addr(st + BB + XB) + 16 * 16 * 4 * h;
         for (int p = 0; p < P; ++p) {
           const uint2 sw = *reinterpret_cast<const uint2*>(st + p * (kRowTile * 16) + row * 16 + h * 8);
           const float al = half_bits_to_float(
               *reinterpret_cast<const uint16_t*>(st + binplane_alpha_off(P) + (p * kRowTile + row) * 2));
           float acc[2] = {0.f, 0.f};
           lut_word(sw.x, tab, acc);
-          lut_word(sw.y, tab + 8 * 16, acc);
+          lut_word(sw.y, tab + 8 * 64, acc);
           total = fmaf(al, acc[0] + acc[1], total);
         }
       } else {
@@ -768,14 +792,14 @@ nvfp4_stream_kernel(const __grid_constant__ StreamArgs a) {
   __shared__ float gscale;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int C = a.cluster;
-  const int cid = (int)blockIdx.x / C, crank = (int)blockIdx.x % C;
+  const int C = a.cluster, lc = __ffs(C) - 1;  // C and every ks are powers of two
+  const int cid = (int)blockIdx.x >> lc, crank = (int)blockIdx.x & (C - 1);
   const GemvProblem& pr = a.p[0];  // one matrix per launch
-  const int ks = pr.ks, rank = crank % ks;
-  const int tile = (cid - pr.cluster_begin) * (C / ks) + crank / ks;
+  const int ks = pr.ks, lk = __ffs(ks) - 1, rank = crank & (ks - 1);
+  const int tile = ((cid - pr.cluster_begin) << (lc - lk)) + (crank >> lk);
   const int G = pr.K / kGroup;
   const bool live = tile < row_tiles(pr.N);
-  const int g0 = (int)((long long)rank * G / ks), g1 = (int)((long long)(rank + 1) * G / ks);
+  const int g0 = (rank * G) >> lk, g1 = ((rank + 1) * G) >> lk;
   const int nb = live ? g1 - g0 : 0;
   const int S = a.stages;
   const PackedHeader* hp = reinterpret_cast<const PackedHeader*>(pr.packed);
@@ -1025,14 +1049,14 @@ q8_stream_kernel(const __grid_constant__ StreamArgs a) {
   __shared__ int hdr_valid;  // the whole grid agrees on it: every CTA reads the same header
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int C = a.cluster;
-  const int cid = (int)blockIdx.x / C, crank = (int)blockIdx.x % C;
+  const int C = a.cluster, lc = __ffs(C) - 1;  // C and every ks are powers of two
+  const int cid = (int)blockIdx.x >> lc, crank = (int)blockIdx.x & (C - 1);
   const GemvProblem& pr = a.p[0];  // one matrix per launch
-  const int ks = pr.ks, rank = crank % ks;
-  const int tile = (cid - pr.cluster_begin) * (C / ks) + crank / ks;
+  const int ks = pr.ks, lk = __ffs(ks) - 1, rank = crank & (ks - 1);
+  const int tile = ((cid - pr.cluster_begin) << (lc - lk)) + (crank >> lk);
   const int G = pr.K / kGroup;
   const bool live = tile < row_tiles(pr.N);
-  const int g0 = (int)((long long)rank * G / ks), g1 = (int)((long long)(rank + 1) * G / ks);
+  const int g0 = (rank * G) >> lk, g1 = ((rank + 1) * G) >> lk;
   const int nb = live ? g1 - g0 : 0;
   const int S = a.stages;
   const PackedHeader* hp = reinterpret_cast<const PackedHeader*>(pr.packed);
@@ -1346,18 +1370,18 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
   float (*part)[kRowTile] = reinterpret_cast<float (*)[kRowTile]>(ring);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int C = a.cluster;
-  const int cid = (int)blockIdx.x / C, crank = (int)blockIdx.x % C;
+  const int C = a.cluster, lc = __ffs(C) - 1;  // C and every ks are powers of two
+  const int cid = (int)blockIdx.x >> lc, crank = (int)blockIdx.x & (C - 1);
   int pi = 0;
   for (int i = 1; i < a.count; ++i)
     if (cid >= a.cl_begin[i]) pi = i;
   const GemvProblem& pr = a.p[pi];
-  const int ks = pr.ks, rank = crank % ks;
-  const int tile = (cid - pr.cluster_begin) * (C / ks) + crank / ks;
+  const int ks = pr.ks, lk = __ffs(ks) - 1, rank = crank & (ks - 1);
+  const int tile = ((cid - pr.cluster_begin) << (lc - lk)) + (crank >> lk);
   constexpr int KIN = mma_kin(FMT), NATOM = KIN / 64;
   const int G = pr.K / KIN;  // blocks along K
   const bool live = tile < row_tiles(pr.N);
-  const int g0 = (int)((long long)rank * G / ks), g1 = (int)((long long)(rank + 1) * G / ks);
+  const int g0 = (rank * G) >> lk, g1 = ((rank + 1) * G) >> lk;
   const int nb = live ? g1 - g0 : 0;
   const int S = a.stages, M = a.m;
   const PackedHeader* hp = reinterpret_cast<const PackedHeader*>(pr.packed);
@@ -1686,12 +1710,12 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
   if (ks > 1) tile_done = !__any_sync(0xFFFFFFFFu, lane < ks && peer_gave_up[lane] != 0u);
   if (live && out_ok && tile_done && owner_thread) {
     grid_wait();  // outputs and the verify workspace belong to the previous kernel until now
-    const int rows = kRowTile / ks, rbase = rank * rows;
+    const int lr = 7 - lk, rows = kRowTile >> lk, rbase = rank * rows;
     const uint32_t base = (uint32_t)(crank - rank);  // rank 0 of this tile
     const int row0 = a.row_offset;  // read once: the loop's cluster loads clobber memory
     for (int i0 = 0; i0 < rows * MT; i0 += kMmaWarps * 32) {  // the same trip count in every lane
       const int idx = i0 + (int)threadIdx.x;
-      const int m = idx / rows, row = rbase + idx % rows;
+      const int m = idx >> lr, row = rbase + (idx & (rows - 1));
       const int n = tile * kRowTile + row;
       const bool in = idx < rows * MT && m < M && n < pr.N;
       float y = 0.f;
@@ -1778,8 +1802,11 @@ struct Schedule {
   long long clusters;
 };
 
+// Every split ks, and so the cluster size C, is a power of two (doubled from 1): the kernels
+// place a CTA with shifts and masks.
 bool make_schedule(const GemvProblem* probs, int count, int kin, int target, int max_split,
                    StreamArgs& a, Schedule& out, int resident_per_sm = kResidentPerSm) {
+  static_assert((kMaxSplit & (kMaxSplit - 1)) == 0 && kRowTile == 128, "shift-based placement");
   const int nsm = sm_count();
   int ks[kMaxGemvProblems];
   long long ctas = 0;

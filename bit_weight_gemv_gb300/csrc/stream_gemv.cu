@@ -1290,9 +1290,17 @@ __host__ __device__ constexpr uint32_t mma_stage_bytes(int fmt, int P, int GS, i
   return mma_x_off(fmt, P, GS) + (uint32_t)MT * 2 * mma_kin(fmt);
 }
 // A pair of binary-plane signs -> the bf16 pair (+-1, +-1): bits 15 - sh and 31 - sh of w
-// (set = +1) shifted onto the sign bits and XORed into bf16 (-1.0, -1.0).
+// (set = +1) shifted onto the sign bits and XORed into bf16 (-1.0, -1.0).  Two forms that
+// compute the same: the compiler's lowering (binary planes, where the written-out logic op
+// spills registers at 16 rows and measured 15% slower) and one written-out logic op with
+// immediate constants (the sa kernel, 9% faster with it).
 __device__ __forceinline__ uint32_t pm1_pair(uint32_t w, int sh) {
   return ((w << sh) & 0x80008000u) ^ 0xBF80BF80u;
+}
+__device__ __forceinline__ uint32_t pm1_pair_lop(uint32_t w, int sh) {
+  uint32_t d;  // (x & mask) ^ bf16(-1.0, -1.0)
+  asm("lop3.b32 %0, %1, 0x80008000, 0xBF80BF80, 0x6A;" : "=r"(d) : "r"(w << sh));
+  return d;
 }
 constexpr int kMmaWarps = 8;
 constexpr int kMmaThreads = (kMmaWarps + 1) * 32;  // compute warps, producer
@@ -1335,7 +1343,11 @@ __device__ __forceinline__ uint32_t bf16x2_sub_rn(uint32_t a, uint32_t b) {
 // The nibbles at bits 0..3 and 16..19 of a code word (inputs k and k+1) -> the bf16 pair
 // (q[k], q[k+1]) exactly: 128 + u in bf16, minus 136.
 __device__ __forceinline__ uint32_t q_pair(uint32_t w) {
-  return bf16x2_sub_rn((w & 0x000F000Fu) | 0x43004300u, 0x43084308u);
+  uint32_t u;  // one logic op: (w & mask) | bf16(128.0, 128.0); written out, since the
+               // compiler's own lowering of this expression before the subtraction cost the
+               // 248,320-row LM head 15% of its time
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(u) : "r"(w), "r"(0x000F000Fu), "r"(0x43004300u));
+  return bf16x2_sub_rn(u, 0x43084308u);
 }
 // Two int8 codes -> the exact bf16 pair: `w` holds u = q + 128 in each byte; sel picks the
 // first code's byte (sel + 1 the second's) under the fp32 exponent of 2^23, so the float is
@@ -1646,8 +1658,8 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
             for (int ss = 0; ss < 8; ++ss) {
               const int kk = 8 * hb + ss;  // step within the super-block
               const int sh = 15 - 8 * (ss & 1) - t;
-              const uint32_t a0 = pm1_pair(W0[ss >> 1], sh), a1 = pm1_pair(W1[ss >> 1], sh);
-              const uint32_t a2 = pm1_pair(W0[ss >> 1], sh - 4), a3 = pm1_pair(W1[ss >> 1], sh - 4);
+              const uint32_t a0 = pm1_pair_lop(W0[ss >> 1], sh), a1 = pm1_pair_lop(W1[ss >> 1], sh);
+              const uint32_t a2 = pm1_pair_lop(W0[ss >> 1], sh - 4), a3 = pm1_pair_lop(W1[ss >> 1], sh - 4);
 #pragma unroll
               for (int hh = 0; hh < MT / 16; ++hh) {
                 uint32_t b0, b1, b2, b3;

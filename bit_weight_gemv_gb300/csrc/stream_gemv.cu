@@ -1290,13 +1290,9 @@ __host__ __device__ constexpr uint32_t mma_stage_bytes(int fmt, int P, int GS, i
   return mma_x_off(fmt, P, GS) + (uint32_t)MT * 2 * mma_kin(fmt);
 }
 // A pair of binary-plane signs -> the bf16 pair (+-1, +-1): bits 15 - sh and 31 - sh of w
-// (set = +1) shifted onto the sign bits and XORed into bf16 (-1.0, -1.0).  Two forms that
-// compute the same: the compiler's lowering (binary planes, where the written-out logic op
-// spills registers at 16 rows and measured 15% slower) and one written-out logic op with
-// immediate constants (the sa kernel, 9% faster with it).
-__device__ __forceinline__ uint32_t pm1_pair(uint32_t w, int sh) {
-  return ((w << sh) & 0x80008000u) ^ 0xBF80BF80u;
-}
+// (set = +1) shifted onto the sign bits and XORed into bf16 (-1.0, -1.0), as one written-out
+// logic op with immediate constants: the compiler's lowering of the expression took about
+// twice the logic ops (binary planes at M=16 11% and the sa format 9% faster without it).
 __device__ __forceinline__ uint32_t pm1_pair_lop(uint32_t w, int sh) {
   uint32_t d;  // (x & mask) ^ bf16(-1.0, -1.0)
   asm("lop3.b32 %0, %1, 0x80008000, 0xBF80BF80, 0x6A;" : "=r"(d) : "r"(w << sh));
@@ -1605,23 +1601,27 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
         // 32w + 2i and bit 16 + i that of 32w + 2i + 1.  Step s's A fragment takes pairs
         // i = 8 (s % 2) + t and i + 4 of word s / 2.
         for (int p = 0; p < P; ++p) {
-          const uint4 w0 = *reinterpret_cast<const uint4*>(st + p * (kRowTile * 16) + r0 * 16);
-          const uint4 w1 = *reinterpret_cast<const uint4*>(st + p * (kRowTile * 16) + (r0 + 8) * 16);
-          const uint32_t W0[4] = {w0.x, w0.y, w0.z, w0.w}, W1[4] = {w1.x, w1.y, w1.z, w1.w};
           float d[NT][4];
 #pragma unroll
           for (int i = 0; i < NT; ++i) d[i][0] = d[i][1] = d[i][2] = d[i][3] = 0.f;
 #pragma unroll
-          for (int ss = 0; ss < 8; ++ss) {
-            const int sh = 15 - 8 * (ss & 1) - t;  // bit i to bit 15
-            const uint32_t a0 = pm1_pair(W0[ss >> 1], sh), a1 = pm1_pair(W1[ss >> 1], sh);
-            const uint32_t a2 = pm1_pair(W0[ss >> 1], sh - 4), a3 = pm1_pair(W1[ss >> 1], sh - 4);
+          for (int hw = 0; hw < 2; ++hw) {  // words 2hw, 2hw + 1 (fewer live registers)
+            const uint2 w0 = *reinterpret_cast<const uint2*>(st + p * (kRowTile * 16) + r0 * 16 + 8 * hw);
+            const uint2 w1 = *reinterpret_cast<const uint2*>(st + p * (kRowTile * 16) + (r0 + 8) * 16 + 8 * hw);
+            const uint32_t W0[2] = {w0.x, w0.y}, W1[2] = {w1.x, w1.y};
 #pragma unroll
-            for (int hh = 0; hh < MT / 16; ++hh) {
-              uint32_t b0, b1, b2, b3;
-              ldsm_x4(xs + xsw[ss & 3] + (ss >> 2) * (MT * 128) + hh * 16 * 128, b0, b1, b2, b3);
-              mma_16816(d[2 * hh], a0, a1, a2, a3, b0, b1);
-              mma_16816(d[2 * hh + 1], a0, a1, a2, a3, b2, b3);
+            for (int sq = 0; sq < 4; ++sq) {
+              const int ss = 4 * hw + sq;
+              const int sh = 15 - 8 * (ss & 1) - t;  // bit i to bit 15
+              const uint32_t a0 = pm1_pair_lop(W0[sq >> 1], sh), a1 = pm1_pair_lop(W1[sq >> 1], sh);
+              const uint32_t a2 = pm1_pair_lop(W0[sq >> 1], sh - 4), a3 = pm1_pair_lop(W1[sq >> 1], sh - 4);
+#pragma unroll
+              for (int hh = 0; hh < MT / 16; ++hh) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(xs + xsw[ss & 3] + (ss >> 2) * (MT * 128) + hh * 16 * 128, b0, b1, b2, b3);
+                mma_16816(d[2 * hh], a0, a1, a2, a3, b0, b1);
+                mma_16816(d[2 * hh + 1], a0, a1, a2, a3, b2, b3);
+              }
             }
           }
           const uint8_t* al = st + binplane_alpha_off(P) + p * (kRowTile * 2);

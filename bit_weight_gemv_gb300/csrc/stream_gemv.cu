@@ -664,7 +664,7 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
         // nibble sets 32h..32h+31; code group of word w is (128h + 32w) / G.
         const float* tab = reinterpret_cast<const float*>(st + BB + XB) + 32 * 16 * h;
         const uint8_t* codes = st + sa_code_off(P) + row;
-        const int GJ = kSuper / GS;
+        const int GJ = kSuper >> (31 - __clz(GS));  // code groups per block (G a power of two)
         float sb = 0.f;  // sum_p sum_g a[p][g] * (sum of the selected activations of group g)
         for (int p = 0; p < P; ++p) {
           const uint4 sw = *reinterpret_cast<const uint4*>(st + (p * 2 + h) * (kRowTile * 16) + row * 16);
@@ -681,8 +681,8 @@ __device__ __forceinline__ void plane_stream_body(const StreamArgs& a) {
           const int gl = GS == 64 ? 2 * h + 1 : (GS == 128 ? h : 0);
           sb = fmaf((float)ap[gl * kRowTile], acc[0] + acc[1], sb);
         }
-        total = fmaf(half_bits_to_float(*reinterpret_cast<const uint16_t*>(st + sa_d_off(P, GS) + row * 2)),
-                     sb, total);
+        const uint32_t doff = sa_code_off(P) + (uint32_t)(P * GJ) * kRowTile;  // d of the rows
+        total = fmaf(half_bits_to_float(*reinterpret_cast<const uint16_t*>(st + doff + row * 2)), sb, total);
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&empty[s]));
@@ -1642,9 +1642,13 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
         // halves of 128 laid out as a binary plane; alpha = d * a with one u8 code a per plane
         // and group of GS inputs, so the MMA sums of every GS / 16 steps are folded with
         // d * a (exact in fp32: 8 x 11 significant bits).
-        const int fk = GS / 16;  // steps per code group: 4, 8 or 16
-        const float d0 = half_bits_to_float(*reinterpret_cast<const uint16_t*>(st + sa_d_off(P, GS) + r0 * 2));
-        const float d1 = half_bits_to_float(*reinterpret_cast<const uint16_t*>(st + sa_d_off(P, GS) + (r0 + 8) * 2));
+        // G is 64, 128 or 256: code-group arithmetic by shifts (a runtime division per fold
+        // cost as much as the fold itself)
+        const int lg = 31 - __clz(GS), lfk = lg - 4, fk = 1 << lfk;  // steps per code group
+        const int gj = kSuper >> lg;                                  // code groups per block
+        const uint32_t doff = sa_code_off(P) + (uint32_t)(P * gj) * kRowTile;
+        const float d0 = half_bits_to_float(*reinterpret_cast<const uint16_t*>(st + doff + r0 * 2));
+        const float d1 = half_bits_to_float(*reinterpret_cast<const uint16_t*>(st + doff + (r0 + 8) * 2));
         for (int p = 0; p < P; ++p) {
           float d[NT][4];
 #pragma unroll
@@ -1668,7 +1672,7 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
                 mma_16816(d[2 * hh + 1], a0, a1, a2, a3, b2, b3);
               }
               if ((kk & (fk - 1)) == fk - 1) {  // the code group's last step
-                const uint8_t* cd = st + sa_code_off(P) + (p * (kSuper / GS) + kk / fk) * kRowTile;
+                const uint8_t* cd = st + sa_code_off(P) + (p * gj + (kk >> lfk)) * kRowTile;
                 const float s0 = d0 * (float)cd[r0], s1 = d1 * (float)cd[r0 + 8];
 #pragma unroll
                 for (int i = 0; i < NT; ++i) {

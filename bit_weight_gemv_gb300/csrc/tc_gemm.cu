@@ -188,6 +188,33 @@ __device__ __forceinline__ void dequant_nvfp4_chunk(const uint4 c, uint32_t sa, 
     v[j] = bf16x2_mul(lut[(w[j >> 2] >> (8 * (j & 3))) & 0xFFu], j < 8 ? sa : sb);
 }
 
+// Where unit u of a CTA's walk stands: unit ub of its block (plane p, sa half hb), the block's
+// stage s and that stage's phase parity, the TMEM buffer a and that buffer's phase parity.
+// Advanced one unit at a time: recomputing these with runtime divisions (by the units per
+// block, the groups, the ring depth) cost the MMA-issuing thread about a hundred
+// instructions per unit of eight MMAs.
+struct UnitPos {
+  int ub = 0, p = 0, hb = 0, s = 0, a = 0;
+  uint32_t sph = 0u, aph = 0u;
+  __device__ __forceinline__ void next(int UB, int P, int S, int NB) {
+    if (++a == NB) {
+      a = 0;
+      aph ^= 1u;
+    }
+    if (++p == P) {
+      p = 0;
+      ++hb;
+    }
+    if (++ub == UB) {
+      ub = p = hb = 0;
+      if (++s == S) {
+        s = 0;
+        sph ^= 1u;
+      }
+    }
+  }
+};
+
 template <int FMT, int NMMA, int EPI>
 __global__ void __launch_bounds__(kThreads, 2)
 tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
@@ -197,7 +224,8 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int C = batch.cluster;
-  const int cid = (int)blockIdx.x / C, crank = (int)blockIdx.x % C;  // cluster, rank in it
+  const int lc = __ffs(C) - 1;  // C and every ks are powers of two
+  const int cid = (int)blockIdx.x >> lc, crank = (int)blockIdx.x & (C - 1);  // cluster, rank in it
   int pi = 0;
   for (int i = 1; i < batch.count; ++i)
     if (cid >= batch.p[i].cl_begin) pi = i;
@@ -220,10 +248,10 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
   uint32_t* lut = reinterpret_cast<uint32_t*>(ctrl + L::kCtrl);  // NVFP4: code byte -> bf16 pair
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ks = args.ks, rank = crank % ks;
+  const int ks = args.ks, lk = __ffs(ks) - 1, rank = crank & (ks - 1);
   const int N = args.N, K = args.K, G = K / L::KIN, RB = row_tiles(N);
-  const int tile0 = (cid - args.cl_begin) * (C / ks) + crank / ks;  // first row block
-  const int tstride = args.ncl * (C / ks);                            // row-block stride
+  const int tile0 = ((cid - args.cl_begin) << (lc - lk)) + (crank >> lk);  // first row block
+  const int tstride = args.ncl << (lc - lk);                               // row-block stride
   const int g0 = min(G, rank * args.groups_per_rank);
   const int g1 = min(G, g0 + args.groups_per_rank);
   const int ngroups = g1 - g0;
@@ -289,37 +317,53 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
 
   if (hdr_ok && warp == kProducerWarp) {
     if (lane == 0) {
-      auto issue_block = [&](int gi) {
-        const int s = gi % S, it = gi / ngroups, g = g0 + gi % ngroups;
+      // block gi = it * ngroups + (g - g0) in stage s, walked in order
+      auto issue_block = [&](int s, int it, int g) {
         bulk_g2s(smem_addr(stage_blk(s)), payload + ((size_t)item_rb(it) * G + g) * BB, BB,
                  smem_addr(&full[s]));
       };
-      auto issue_x = [&](int gi) {
-        const int s = gi % S, g = g0 + gi % ngroups;
+      auto issue_x = [&](int s, int g) {
 #pragma unroll
         for (int at = 0; at < L::KIN / 64; ++at)
           tma_load_2d(smem_addr(stage_x(s)) + at * L::kAtom, xmap, g * L::KIN + 64 * at, 0,
                       smem_addr(&full[s]));
       };
       const int pre = min(S, total_groups);
+      int it = 0, g = g0;  // item and group of the next block
       for (int gi = 0; gi < pre; ++gi) {
-        mbar_arrive_expect_tx(smem_addr(&full[gi % S]), L::kX + BB);
-        issue_block(gi);
+        mbar_arrive_expect_tx(smem_addr(&full[gi]), L::kX + BB);
+        issue_block(gi, it, g);
+        if (++g == g1) {
+          g = g0;
+          ++it;
+        }
       }
       grid_dependency_wait();  // activations come from the previous kernel in the stream
-      for (int gi = 0; gi < pre; ++gi) issue_x(gi);
+      for (int gi = 0, gx = g0; gi < pre; ++gi) {
+        issue_x(gi, gx);
+        if (++gx == g1) gx = g0;
+      }
       int issued = pre;
+      int s = pre % S;
+      uint32_t ph = (uint32_t)(pre / S) & 1u;  // phase parity of block gi in stage s
       for (int gi = pre; gi < total_groups; ++gi) {
-        const int s = gi % S;
-        if (!mbar_wait(smem_addr(&empty[s]), ((gi / S) - 1) & 1)) {
+        if (!mbar_wait(smem_addr(&empty[s]), ph ^ 1u)) {
           fail();
           break;
         }
         if (flags[1]) break;
         mbar_arrive_expect_tx(smem_addr(&full[s]), L::kX + BB);
-        issue_block(gi);
-        issue_x(gi);
+        issue_block(s, it, g);
+        issue_x(s, g);
         issued = gi + 1;
+        if (++g == g1) {
+          g = g0;
+          ++it;
+        }
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       // No copy may still be in flight when the CTA exits.
       for (int gi = max(0, issued - S); gi < issued; ++gi)
@@ -328,14 +372,14 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
   } else if (hdr_ok && warp == kMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t idesc = umma_idesc_bf16(kBlockRows, NMMA);
-      for (int u = 0; u < total_units; ++u) {
-        const int lu = u % upi, i = lu / UB, ub = lu % UB, p = ub % P, a = u % NB;
-        const int gi = (u / upi) * ngroups + i, s = gi % S;
-        if (!mbar_wait(smem_addr(&aready[a]), (u / NB) & 1)) {
+      UnitPos up;
+      for (int u = 0; u < total_units; ++u, up.next(UB, P, S, NB)) {
+        const int ub = up.ub, p = up.p, a = up.a, s = up.s;
+        if (!mbar_wait(smem_addr(&aready[a]), up.aph)) {
           fail();
           break;
         }
-        if (FMT == kFmtBinplane && p == 0 && !mbar_wait(smem_addr(&xready[s]), (gi / S) & 1)) {
+        if (FMT == kFmtBinplane && p == 0 && !mbar_wait(smem_addr(&xready[s]), up.sph)) {
           fail();
           break;
         }
@@ -343,7 +387,7 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
         tc_fence_after();
         const uint32_t d_tmem = tmem + L::kColD + a * NMMA;
         const uint32_t a_tmem = tmem + L::kColA + a * 64;
-        const uint32_t xs = smem_addr(stage_x(s)) + (FMT == kFmtSa ? (ub / P) * 2 * L::kAtom : 0);
+        const uint32_t xs = smem_addr(stage_x(s)) + (FMT == kFmtSa ? up.hb * 2 * L::kAtom : 0);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t bdesc = smem_desc_sw128(xs + (kk >> 2) * L::kAtom + (kk & 3) * 32);
@@ -359,9 +403,10 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
     if constexpr (FMT == kFmtBinplane) {
       // Pre-scale each staged activation tile in place: input k of pair i = (k % 32) / 2 is
       // multiplied by 2^(8 - j(i)) (exact for normal bf16 values).
-      for (int gi = 0; gi < total_groups; ++gi) {
-        const int s = gi % S;
-        if (flags[1] || !mbar_wait(smem_addr(&full[s]), (gi / S) & 1)) {
+      int s = 0;
+      uint32_t ph = 0u;
+      for (int gi = 0; gi < total_groups; ++gi, s = (s + 1 == S) ? 0 : s + 1, ph ^= (s == 0) ? 1u : 0u) {
+        if (flags[1] || !mbar_wait(smem_addr(&full[s]), ph)) {
           fail();
           break;
         }
@@ -414,9 +459,9 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
         }
       }
     };
-    auto epilogue = [&](int v, float sc) {
-      const int a = v % NB, lv = v % upi;
-      wait_or_fail(smem_addr(&mmadone[a]), (v / NB) & 1);
+    // unit v's results: TMEM buffer a with phase parity aph; `last` = the item's last unit
+    auto epilogue = [&](int a, uint32_t aph, bool last, int vit, float sc) {
+      wait_or_fail(smem_addr(&mmadone[a]), aph);
       tc_fence_after();
       if (epi_active) {
         uint32_t d[TOK];
@@ -426,9 +471,9 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
 #pragma unroll
         for (int j = 0; j < TOK; ++j) acc[j] = fmaf(sc, __uint_as_float(d[j]), acc[j]);
       }
-      if (lv == upi - 1) {  // last unit of an item: its outputs are complete
+      if (last) {  // last unit of an item: its outputs are complete
         if (ks == 1) {
-          output_item(v / upi);
+          output_item(vit);
 #pragma unroll
           for (int j = 0; j < TOK; ++j) acc[j] = 0.f;
         }
@@ -439,17 +484,25 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
     float scq[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) scq[b] = 0.f;
-    for (int u = 0; u < total_units; ++u) {
-      const int lu = u % upi, i = lu / UB, ub = lu % UB, p = ub % P, a = u % NB;
-      const int gi = (u / upi) * ngroups + i, s = gi % S;
-      if (u >= NB) {
+    UnitPos up;
+    int vlu = 0, vit = 0;  // unit-in-item and item of the next epilogue's unit
+    auto next_v = [&]() {
+      if (++vlu == upi) {
+        vlu = 0;
+        ++vit;
+      }
+    };
+    for (int u = 0; u < total_units; ++u, up.next(UB, P, S, NB)) {
+      const int ub = up.ub, p = up.p, a = up.a, s = up.s;
+      if (u >= NB) {  // unit u - NB used buffer a one phase earlier
         float scv = 0.f;
 #pragma unroll
         for (int b = 0; b < NB; ++b)
           if (b == a) scv = scq[b];
-        epilogue(u - NB, scv);
+        epilogue(a, up.aph ^ 1u, vlu == upi - 1, vit, scv);
+        next_v();
       }
-      if (ub == 0) wait_or_fail(smem_addr(&full[s]), (gi / S) & 1);
+      if (ub == 0) wait_or_fail(smem_addr(&full[s]), up.sph);
       // Dequantise this thread's 64 inputs of unit u into TMEM columns of A[a].
       float sc;
       uint32_t v[16];
@@ -481,12 +534,12 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
         tmem_st16(acol + 16, v);
       } else if constexpr (FMT == kFmtSa) {
         // unit (half hb, plane p); this thread's inputs 128hb + 64h .. +63 share code group
-        // (128hb + 64h) / GS of the super-block
-        const int hb = ub / P;
+        // (128hb + 64h) / GS of the super-block (G a power of two: shifts)
+        const int hb = up.hb, lg = 31 - __clz(GS), gj = kSuper >> lg;
         const uint2 wv = *reinterpret_cast<const uint2*>(blk + (p * 2 + hb) * 2048 + r * 16 + h * 8);
-        const int gl = (128 * hb + 64 * h) / GS;
-        const uint32_t ab = __float_as_uint((float)blk[sa_code_off(P) + (p * (kSuper / GS) + gl) * kBlockRows + r]) >> 16;
-        sc = half_bits_to_float(*reinterpret_cast<const uint16_t*>(blk + sa_d_off(P, GS) + r * 2));
+        const int gl = (128 * hb + 64 * h) >> lg;
+        const uint32_t ab = __float_as_uint((float)blk[sa_code_off(P) + (p * gj + gl) * kBlockRows + r]) >> 16;
+        sc = half_bits_to_float(*reinterpret_cast<const uint16_t*>(blk + sa_code_off(P) + P * gj * kBlockRows + r * 2));
         if (ub == UB - 1) {
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
@@ -515,12 +568,14 @@ tc_gemm_kernel(const __grid_constant__ TcBatch batch) {
       for (int b = 0; b < NB; ++b)
         if (b == a) scq[b] = sc;
     }
-    for (int v = max(0, total_units - NB); v < total_units; ++v) {
+    for (int v = max(0, total_units - NB); v < total_units; ++v) {  // the last NB units
+      const int a = v % NB;
       float scv = 0.f;
 #pragma unroll
       for (int b = 0; b < NB; ++b)
-        if (b == v % NB) scv = scq[b];
-      epilogue(v, scv);
+        if (b == a) scv = scq[b];
+      epilogue(a, (uint32_t)(v / NB) & 1u, vlu == upi - 1, vit, scv);
+      next_v();
     }
   }
 

@@ -1292,7 +1292,8 @@ __host__ __device__ constexpr uint32_t mma_stage_bytes(int fmt, int P, int GS, i
 // A pair of binary-plane signs -> the bf16 pair (+-1, +-1): bits 15 - sh and 31 - sh of w
 // (set = +1) shifted onto the sign bits and XORed into bf16 (-1.0, -1.0), as one written-out
 // logic op with immediate constants: the compiler's lowering of the expression took about
-// twice the logic ops (binary planes at M=16 11% and the sa format 9% faster without it).
+// twice the logic ops (with the written-out op binary planes at M=16 ran 11% faster and the
+// sa format 9%).
 __device__ __forceinline__ uint32_t pm1_pair_lop(uint32_t w, int sh) {
   uint32_t d;  // (x & mask) ^ bf16(-1.0, -1.0)
   asm("lop3.b32 %0, %1, 0x80008000, 0xBF80BF80, 0x6A;" : "=r"(d) : "r"(w << sh));

@@ -1346,16 +1346,17 @@ __device__ __forceinline__ uint32_t q_pair(uint32_t w) {
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(u) : "r"(w), "r"(0x000F000Fu), "r"(0x43004300u));
   return bf16x2_sub_rn(u, 0x43084308u);
 }
-// Two int8 codes -> the exact bf16 pair: `w` holds u = q + 128 in each byte; sel picks the
-// first code's byte (sel + 1 the second's) under the fp32 exponent of 2^23, so the float is
-// 2^23 + u exactly, and subtracting 2^23 + 128 leaves q.
+// Two int8 codes (two's complement bytes of `w`) -> the exact bf16 pair (q, q').  One
+// permute puts the two code bytes under the bf16 exponent byte 0x43; with bit 7 masked off a
+// half is 128 + (q mod 128), and the byte's bit 7 (the code's sign) turns the subtrahend
+// bf16 128.0 into 256.0, so one bf16 subtraction leaves q exactly: four ops per pair.
+// sel: byte b of w to half 0, byte b + 1 to half 1, 0x43 above each.
 __device__ __forceinline__ uint32_t q8_pair(uint32_t w, uint32_t sel) {
-  uint32_t lo, hi, d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(w), "r"(0x4B000000u), "r"(sel));
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(w), "r"(0x4B000000u), "r"(sel + 1u));
-  const float flo = __uint_as_float(lo) - 8388736.f, fhi = __uint_as_float(hi) - 8388736.f;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(fhi), "f"(flo));
-  return d;
+  uint32_t r, v, s;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(w), "r"(0x43434343u), "r"(sel));
+  asm("lop3.b32 %0, %1, 0xFF7FFF7F, 0, 0xC0;" : "=r"(v) : "r"(r));      // r & mask
+  asm("lop3.b32 %0, %1, 0x00800080, 0x43004300, 0xEA;" : "=r"(s) : "r"(r));  // (r & m) | c
+  return bf16x2_sub_rn(v, s);
 }
 
 template <int FMT, int MT, int EPI>
@@ -1561,17 +1562,18 @@ __device__ __forceinline__ void mma_body(const MmaArgs& A) {
         // Q8 (int8 codes, fp16 d per run of 32 inputs): step ss is 16-input chunk ss; this
         // lane's A share is bytes 2(t&1), 2(t&1)+1 of words t>>1 and 2 + (t>>1) of the chunk
         // in rows r0 and r0 + 8.  The MMA sums of a run's two steps are scaled by its d.
-        const uint32_t sel = (uint32_t)(2 * (t & 1)) | 0x7540u;  // code byte, 0, 0, 0x4B
+        const uint32_t b0 = (uint32_t)(2 * (t & 1));
+        const uint32_t sel = b0 | 0x4040u | ((b0 + 1u) << 8);  // code, 0x43, next code, 0x43
         float d[NT][4];
 #pragma unroll
         for (int i = 0; i < NT; ++i) d[i][0] = d[i][1] = d[i][2] = d[i][3] = 0.f;
 #pragma unroll
         for (int ss = 0; ss < 8; ++ss) {
           const uint8_t* cp = st + ss * (kRowTile * 16) + 4 * (t >> 1);
-          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(cp + r0 * 16) ^ 0x80808080u;
-          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(cp + (r0 + 8) * 16) ^ 0x80808080u;
-          const uint32_t w2 = *reinterpret_cast<const uint32_t*>(cp + r0 * 16 + 8) ^ 0x80808080u;
-          const uint32_t w3 = *reinterpret_cast<const uint32_t*>(cp + (r0 + 8) * 16 + 8) ^ 0x80808080u;
+          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(cp + r0 * 16);
+          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(cp + (r0 + 8) * 16);
+          const uint32_t w2 = *reinterpret_cast<const uint32_t*>(cp + r0 * 16 + 8);
+          const uint32_t w3 = *reinterpret_cast<const uint32_t*>(cp + (r0 + 8) * 16 + 8);
           const uint32_t a0 = q8_pair(w0, sel), a1 = q8_pair(w1, sel);
           const uint32_t a2 = q8_pair(w2, sel), a3 = q8_pair(w3, sel);
 #pragma unroll

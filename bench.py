@@ -652,7 +652,7 @@ def cpu_baseline_child(threads, budget_s):
 
 
 def cpu_baseline_two_modes(budget_s):
-    """SURVEY-style CPU baseline: the oracle with one thread and with every host core."""
+    """CPU baseline: the oracle with one thread and with every host core."""
     cores = os.cpu_count() or 1
     one = cpu_baseline_child(1, budget_s / 2)
     allc = cpu_baseline_child(cores, budget_s / 2)

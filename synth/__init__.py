@@ -46,16 +46,16 @@ HEAD_ROWS = (248_320, 32_768)
 VERIFY_BLOCK = 16  # tokens in one draft block (one anchor/bonus row + 15 drafts)
 M_SWEEP = (1, 2, 4, 8, 16, 32)
 
-CONFIGS = {
-    0: dict(name="tiny INT4 GEMV", kind="int4", M=1, shapes=((512, 256),), seed=0),
-    1: dict(name="decode W4A16 GEMV, 4B-class layer", kind="int4", M=1,
-            shapes=tuple((k, n) for _, k, n in LAYER_4B), seed=1),
-    2: dict(name="speculative-verify skinny GEMM, 4B-class layer", kind="int4", M=16,
-            shapes=tuple((k, n) for _, k, n in LAYER_4B), seed=2, m_sweep=M_SWEEP),
-    3: dict(name="binary-plane GEMV/GEMM", kind="binplane", M=(1, 16),
-            shapes=BINPLANE_SHAPES, planes=BINPLANE_PLANES, seed=3),
-    4: dict(name="LM-head verify", kind="lmhead", M=VERIFY_BLOCK, K=HEAD_K,
-            rows=HEAD_ROWS, seed=4),
+WORKLOADS = {
+    "tiny": dict(name="tiny INT4 GEMV", kind="int4", M=1, shapes=((512, 256),), seed=0),
+    "decode": dict(name="decode W4A16 GEMV, 4B-class layer", kind="int4", M=1,
+                   shapes=tuple((k, n) for _, k, n in LAYER_4B), seed=1),
+    "verify": dict(name="speculative-verify skinny GEMM, 4B-class layer", kind="int4", M=16,
+                   shapes=tuple((k, n) for _, k, n in LAYER_4B), seed=2, m_sweep=M_SWEEP),
+    "binplane": dict(name="binary-plane GEMV/GEMM", kind="binplane", M=(1, 16),
+                     shapes=BINPLANE_SHAPES, planes=BINPLANE_PLANES, seed=3),
+    "lmhead": dict(name="LM-head verify", kind="lmhead", M=VERIFY_BLOCK, K=HEAD_K,
+                   rows=HEAD_ROWS, seed=4),
 }
 
 

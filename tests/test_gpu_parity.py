@@ -159,7 +159,7 @@ def test_binplane_m1_ring_at_default_smem_limit(lb, P, N, K):
 
 
 def test_int4_config0_tiny_gemv(lb):
-    cfg = synth.CONFIGS[0]
+    cfg = synth.WORKLOADS["tiny"]
     (K, N), = cfg["shapes"]
     codes, scales, x = synth.int4_problem(cfg["seed"], 1, N, K)
     y = gemm_int4_gpu(lb, x, pack_int4_gpu(lb, codes, scales), 1, N, K)
@@ -169,7 +169,7 @@ def test_int4_config0_tiny_gemv(lb):
 @pytest.mark.parametrize("path", INT4_PATHS)
 @pytest.mark.parametrize("proj", range(7))
 def test_int4_config1_decode_layer(lb, proj, path):
-    cfg = synth.CONFIGS[1]
+    cfg = synth.WORKLOADS["decode"]
     K, N = cfg["shapes"][proj]
     codes, scales, x = synth.int4_problem(cfg["seed"], 1, N, K, proj)
     y = gemm_int4_gpu(lb, x, pack_int4_gpu(lb, codes, scales), 1, N, K, path)
@@ -180,7 +180,7 @@ def test_int4_config1_decode_layer(lb, proj, path):
 @pytest.mark.parametrize("M", synth.M_SWEEP)
 @pytest.mark.parametrize("proj", [0, 1, 6])
 def test_int4_config2_verify_sweep(lb, proj, M, path):
-    cfg = synth.CONFIGS[2]
+    cfg = synth.WORKLOADS["verify"]
     K, N = cfg["shapes"][proj]
     codes, scales, x = synth.int4_problem(cfg["seed"], M, N, K, proj)
     y = gemm_int4_gpu(lb, x, pack_int4_gpu(lb, codes, scales), M, N, K, path)
@@ -189,7 +189,7 @@ def test_int4_config2_verify_sweep(lb, proj, M, path):
 
 @pytest.mark.parametrize("proj", [2, 3, 4, 5])
 def test_int4_config2_remaining_projections(lb, proj):
-    cfg = synth.CONFIGS[2]
+    cfg = synth.WORKLOADS["verify"]
     K, N = cfg["shapes"][proj]
     codes, scales, x = synth.int4_problem(cfg["seed"], 16, N, K, proj)
     y = gemm_int4_gpu(lb, x, pack_int4_gpu(lb, codes, scales), 16, N, K)
@@ -213,7 +213,7 @@ def test_binplane_small_and_ragged(lb, P, M, N, K, path):
 @pytest.mark.parametrize("P", synth.BINPLANE_PLANES)
 @pytest.mark.parametrize("M", (1, 16))
 def test_binplane_config3(lb, shape, P, M, path):
-    cfg = synth.CONFIGS[3]
+    cfg = synth.WORKLOADS["binplane"]
     K, N = cfg["shapes"][shape]
     bits, alpha, x = synth.binplane_problem(cfg["seed"], P, M, N, K, shape)
     packed = pack_bp_gpu(lb, bits, alpha)
@@ -248,7 +248,7 @@ def check_lmhead(a, n, b, logits, drafts, j, what):
 @pytest.mark.parametrize("path", INT4_PATHS)
 @pytest.mark.parametrize("rows", synth.HEAD_ROWS)
 def test_lmhead_config4(lb, rows, path):
-    cfg = synth.CONFIGS[4]
+    cfg = synth.WORKLOADS["lmhead"]
     M, K = cfg["M"], cfg["K"]
     codes, scales, h = synth.int4_problem(cfg["seed"], M, rows, K)
     packed = pack_int4_gpu(lb, codes, scales)
@@ -354,8 +354,8 @@ def _grouped(lb, M, shapes, seed, path=0):
 @pytest.mark.parametrize("M", [1, 16])
 def test_grouped_config1_layer_in_one_call(lb, M):
     """The seven projections of the 4B-class layer as one grouped call (one launch at M=1)."""
-    shapes = synth.CONFIGS[1]["shapes"]
-    ys, refs = _grouped(lb, M, shapes, synth.CONFIGS[1]["seed"] if M == 1 else synth.CONFIGS[2]["seed"])
+    shapes = synth.WORKLOADS["decode"]["shapes"]
+    ys, refs = _grouped(lb, M, shapes, synth.WORKLOADS["decode"]["seed"] if M == 1 else synth.WORKLOADS["verify"]["seed"])
     for j, (y, r) in enumerate(zip(ys, refs)):
         check_gemm(y, r, f"grouped M={M} proj {j}")
 

@@ -12,8 +12,8 @@ replayed from CUDA graphs (one per rotation of the weight copies) and timed with
 Also reported under "rows": the same layer as seven single-matrix calls ("decode") and as one
 grouped call ("decode_all"), the M=16 verify GEMM over the same layer and its batch sweep,
 binary-plane GEMV/GEMM, the deployed ShiftAdd format (u8 scale codes, "sa_m1"/"sa_m16"), the
-248,320-row vocabulary head as one M=1 GEMV ("head_gemv"), the trimmed NVFP4 draft head with its
-id-mapped argmax ("draft_m1"/"draft_m16"), and the
+248,320-row vocabulary head as one M=1 GEMV ("head_gemv"), the trimmed NVFP4 and Q8 draft heads
+with their id-mapped argmax ("draft_m1"/"draft_m16", "draft_q8_m1"/"draft_q8_m16"), and the
 LM-head argmax+verify over 248,320 and 32,768 rows.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-rows]
@@ -512,7 +512,7 @@ class Replay:
         if steps <= self.short:
             return [self._graph(start, steps)]
         out, i = [], start
-        head = (-i) % self.n
+        head = min((-i) % self.n, steps)  # up to the next rotation boundary, or the whole run
         if head:
             out.append(self._graph(i, head))
             i += head

@@ -128,7 +128,7 @@ SA_TYPES = ((3, 64), (4, 128))   # (planes, group) of the benchmark rows: sa3 an
 def sa_weights(g: np.random.Generator, P: int, N: int, K: int, G: int):
     """sa-format weights: d fp16 bits [N][K/256] ~ |N(0, 0.02)| / 255; codes uint8
     [P][N][K/G] with a_1 ~ U{128..255} and a_{p+1} = max(1, round(a_p * U(0.3, 0.6))) (the
-    plane-scale decay of the binary-plane configuration on the u8 grid); sign bits uint8
+    plane-scale decay of the binary-plane workload on the u8 grid); sign bits uint8
     [P][N][K/8] uniform.  Draw order: d, codes, bits."""
     d = to_f16_bits(np.abs(g.normal(0.0, 0.02, size=(N, K // 256))) / 255.0)
     a = np.empty((P, N, K // G), dtype=np.float64)

@@ -158,42 +158,42 @@ def test_binplane_m1_ring_at_default_smem_limit(lb, P, N, K):
     check_gemm(y, obp.gemm(x, bits, alpha), f"binplane M=1 P={P} N={N} K={K}")
 
 
-def test_int4_config0_tiny_gemv(lb):
+def test_int4_tiny_gemv(lb):
     cfg = synth.WORKLOADS["tiny"]
     (K, N), = cfg["shapes"]
     codes, scales, x = synth.int4_problem(cfg["seed"], 1, N, K)
     y = gemm_int4_gpu(lb, x, pack_int4_gpu(lb, codes, scales), 1, N, K)
-    check_gemm(y, oint4.gemm(x, codes, scales), "config 0")
+    check_gemm(y, oint4.gemm(x, codes, scales), "tiny GEMV")
 
 
 @pytest.mark.parametrize("path", INT4_PATHS)
 @pytest.mark.parametrize("proj", range(7))
-def test_int4_config1_decode_layer(lb, proj, path):
+def test_int4_decode_layer(lb, proj, path):
     cfg = synth.WORKLOADS["decode"]
     K, N = cfg["shapes"][proj]
     codes, scales, x = synth.int4_problem(cfg["seed"], 1, N, K, proj)
     y = gemm_int4_gpu(lb, x, pack_int4_gpu(lb, codes, scales), 1, N, K, path)
-    check_gemm(y, oint4.gemm(x, codes, scales), f"config 1 proj {proj} path={path}")
+    check_gemm(y, oint4.gemm(x, codes, scales), f"decode layer proj {proj} path={path}")
 
 
 @pytest.mark.parametrize("path", INT4_PATHS)
 @pytest.mark.parametrize("M", synth.M_SWEEP)
 @pytest.mark.parametrize("proj", [0, 1, 6])
-def test_int4_config2_verify_sweep(lb, proj, M, path):
+def test_int4_verify_layer_m_sweep(lb, proj, M, path):
     cfg = synth.WORKLOADS["verify"]
     K, N = cfg["shapes"][proj]
     codes, scales, x = synth.int4_problem(cfg["seed"], M, N, K, proj)
     y = gemm_int4_gpu(lb, x, pack_int4_gpu(lb, codes, scales), M, N, K, path)
-    check_gemm(y, oint4.gemm(x, codes, scales), f"config 2 proj {proj} M={M} path={path}")
+    check_gemm(y, oint4.gemm(x, codes, scales), f"verify layer proj {proj} M={M} path={path}")
 
 
 @pytest.mark.parametrize("proj", [2, 3, 4, 5])
-def test_int4_config2_remaining_projections(lb, proj):
+def test_int4_verify_layer_remaining_projections(lb, proj):
     cfg = synth.WORKLOADS["verify"]
     K, N = cfg["shapes"][proj]
     codes, scales, x = synth.int4_problem(cfg["seed"], 16, N, K, proj)
     y = gemm_int4_gpu(lb, x, pack_int4_gpu(lb, codes, scales), 16, N, K)
-    check_gemm(y, oint4.gemm(x, codes, scales), f"config 2 proj {proj}")
+    check_gemm(y, oint4.gemm(x, codes, scales), f"verify layer proj {proj}")
 
 
 # ------------------------------------------------------------------------- binary planes
@@ -212,13 +212,13 @@ def test_binplane_small_and_ragged(lb, P, M, N, K, path):
 @pytest.mark.parametrize("shape", [0, 1])
 @pytest.mark.parametrize("P", synth.BINPLANE_PLANES)
 @pytest.mark.parametrize("M", (1, 16))
-def test_binplane_config3(lb, shape, P, M, path):
+def test_binplane_matrices(lb, shape, P, M, path):
     cfg = synth.WORKLOADS["binplane"]
     K, N = cfg["shapes"][shape]
     bits, alpha, x = synth.binplane_problem(cfg["seed"], P, M, N, K, shape)
     packed = pack_bp_gpu(lb, bits, alpha)
     y = gemm_bp_gpu(lb, x, packed, P, M, N, K, path)
-    check_gemm(y, obp.gemm(x, bits, alpha), f"config 3 K={K} N={N} P={P} M={M} path={path}")
+    check_gemm(y, obp.gemm(x, bits, alpha), f"binary planes K={K} N={N} P={P} M={M} path={path}")
 
 
 # ------------------------------------------------------------------------- LM head verify
@@ -247,7 +247,7 @@ def check_lmhead(a, n, b, logits, drafts, j, what):
 
 @pytest.mark.parametrize("path", INT4_PATHS)
 @pytest.mark.parametrize("rows", synth.HEAD_ROWS)
-def test_lmhead_config4(lb, rows, path):
+def test_lmhead_full_and_trimmed_heads(lb, rows, path):
     cfg = synth.WORKLOADS["lmhead"]
     M, K = cfg["M"], cfg["K"]
     codes, scales, h = synth.int4_problem(cfg["seed"], M, rows, K)
@@ -258,7 +258,7 @@ def test_lmhead_config4(lb, rows, path):
     for trial, j in enumerate((None, 0, 15)):
         drafts, jj = synth.plant_drafts(cfg["seed"] + trial, a_ref, rows, j)
         a, n, b, ws = run_lmhead(lb, h, packed, M, rows, K, drafts, ws, path)
-        check_lmhead(a, n, b, logits, drafts, jj, f"config 4 N={rows} j={jj}")
+        check_lmhead(a, n, b, logits, drafts, jj, f"LM head N={rows} j={jj}")
     # the workspace is left zeroed for the next call
     assert int(ws.sum().item()) == 0
 
@@ -352,7 +352,7 @@ def _grouped(lb, M, shapes, seed, path=0):
 
 
 @pytest.mark.parametrize("M", [1, 16])
-def test_grouped_config1_layer_in_one_call(lb, M):
+def test_grouped_decode_layer_in_one_call(lb, M):
     """The seven projections of the 4B-class layer as one grouped call (one launch at M=1)."""
     shapes = synth.WORKLOADS["decode"]["shapes"]
     ys, refs = _grouped(lb, M, shapes, synth.WORKLOADS["decode"]["seed"] if M == 1 else synth.WORKLOADS["verify"]["seed"])

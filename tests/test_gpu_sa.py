@@ -63,18 +63,18 @@ def test_sa_small_and_ragged(lb, P, G, N, K, M, path):
 @pytest.mark.parametrize("M,path", [(1, 0), (16, 0), (16, 1), (16, 2)])
 @pytest.mark.parametrize("P,G", synth.SA_TYPES)
 @pytest.mark.parametrize("shape", range(len(synth.SA_SHAPES)))
-def test_sa_config3_shapes(lb, shape, P, G, M, path):
-    """The binary-plane configuration's matrices (K, N) in {(4096, 12288), (12288, 4096)} in
+def test_sa_binary_plane_matrices(lb, shape, P, G, M, path):
+    """The binary-plane workload's matrices (K, N) in {(4096, 12288), (12288, 4096)} in
     the deployed format; every output at M = 1, every output of 1024 sampled rows at M = 16."""
     K, N = synth.SA_SHAPES[shape]
     bits, codes, d, x = synth.sa_problem(3, P, G, M, N, K, shape)
     y = gemm_sa_gpu(lb, x, pack_sa_gpu(lb, bits, codes, d, G), P, G, M, N, K, path)
     if M == 1:
-        check_gemm(y, osa.gemm(x, bits, codes, d, G), f"sa config 3 shape {shape} M=1")
+        check_gemm(y, osa.gemm(x, bits, codes, d, G), f"sa binary-plane shape {shape} M=1")
     else:
         rows = np.sort(synth.generator(22, shape).choice(N, size=1024, replace=False))
         check_gemm(y[:, rows], osa.gemm_entries(x, bits, codes, d, G, rows),
-                   f"sa config 3 shape {shape} M=16 sampled")
+                   f"sa binary-plane shape {shape} M=16 sampled")
 
 
 @pytest.mark.parametrize("M,path", [(1, 0), (16, 2), (16, 3)])

@@ -24,12 +24,29 @@ def gather_keys(keys_local, keys_all, group=None) -> None:
     dist.all_gather_into_tensor(keys_all.view(-1), keys_local.view(-1), group=group)
 
 
+def _on_stream(stream):
+    """Context that makes `stream` (a torch stream or a raw CUDA stream handle; None keeps the
+    current one) torch's current stream, so a collective is ordered with the library's launches
+    on it: NCCL collectives wait for the current stream's earlier work and hold back its later
+    work until they complete."""
+    import contextlib
+    if stream is None:
+        return contextlib.nullcontext()
+    import torch
+    if not isinstance(stream, torch.cuda.Stream):
+        stream = torch.cuda.ExternalStream(int(stream))
+    return torch.cuda.stream(stream)
+
+
 def lmhead_verify_sharded(H, packed_shard, M, N_shard, K, row_offset, draft, argmax, n_accept,
                           bonus, workspace, keys_local, keys_all, group=None, stream=None):
     """Steps 1-3 of the sharded verify on this rank (see include/lowbit.h): score the slice,
-    all-gather the keys, merge them and apply the prefix rule."""
+    all-gather the keys, merge them and apply the prefix rule, all three in order on `stream`
+    (torch's current stream when None)."""
     import bit_weight_gemv_gb300 as lb
-    lb.lmhead_argmax_partial(H, packed_shard, M, N_shard, K, row_offset, keys_local, workspace,
-                             stream)
-    gather_keys(keys_local, keys_all, group)
-    lb.lmhead_accept_keys(keys_all, keys_all.shape[0], M, draft, argmax, n_accept, bonus, stream)
+    with _on_stream(stream):
+        lb.lmhead_argmax_partial(H, packed_shard, M, N_shard, K, row_offset, keys_local,
+                                 workspace, stream)
+        gather_keys(keys_local, keys_all, group)
+        lb.lmhead_accept_keys(keys_all, keys_all.shape[0], M, draft, argmax, n_accept, bonus,
+                              stream)

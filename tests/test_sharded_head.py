@@ -4,7 +4,9 @@ vocabulary) split over ranks.
 CPU, no GPU: the oracle's slice winners and their merge against the whole-head argmax (pins),
 the slice plan, and two gloo ranks running the protocol end to end -- each rank scores its
 slice with the oracle, the ranks all-gather their winners with the library's gather step, and
-both ranks must reach the whole-head oracle's argmax and acceptance.
+both ranks must reach the whole-head oracle's argmax and acceptance; and two gloo ranks running
+lmhead_verify_sharded itself with host stand-ins for its two kernels (score, gather, merge in
+that order, each rank's keys at its own row of the gathered array).
 GPU: slices scored by lmhead_argmax_partial on one GPU, merged by lmhead_accept_keys, against
 the oracle (the all-gather is then a concatenation on one device; the kernels never wait on one
 another)."""
@@ -107,6 +109,97 @@ def test_two_gloo_ranks_reach_the_whole_head_result():
         assert a == full
         assert n == j and b == full[n]
     assert got[0][1] == got[1][1]
+
+
+def _key(value, row):
+    """The slice key of the library (reading 17): order-preserving fp32 bits of the logit above
+    0xFFFFFFFF - global row, so the largest key is the largest logit, then the lowest row."""
+    b = int(np.float32(value).view(np.uint32))
+    ordered = (b ^ 0xFFFFFFFF) if b & 0x80000000 else (b | 0x80000000)
+    return (ordered << 32) | (0xFFFFFFFF - int(row))  # unsigned 64-bit
+
+
+def _rank_flow(rank, world, port, q):
+    """One rank of lmhead_verify_sharded with the two kernels replaced by host stand-ins (the
+    oracle's slice scores packed into keys; the merge of the gathered keys), so the host
+    sequence -- score, all-gather, merge -- runs over gloo without a GPU."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    sys.path.insert(0, ROOT)
+    import torch
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import synth as sy
+        from oracle import int4 as oi
+        from oracle import verify as ov
+        import bit_weight_gemv_gb300 as lb
+        from bit_weight_gemv_gb300.sharded import lmhead_verify_sharded, shard_rows
+        M, N, K = 16, 1001, 256
+        codes, scales, h = sy.int4_problem(53, M, N, K)
+        full = ov.argmax_lowest(oi.gemm(h, codes, scales))
+        drafts, j = sy.plant_drafts(54, full, N, 9)
+        off, n = shard_rows(N, world, rank)
+        calls = []
+
+        def partial(H, packed, M_, N_, K_, row_offset, keys_out, ws, stream):
+            calls.append("partial")
+            v, r = ov.shard_winners(oi.gemm(h, codes[row_offset:row_offset + N_],
+                                            scales[row_offset:row_offset + N_]), row_offset)
+            u = np.array([_key(v[m], r[m]) for m in range(M_)], dtype=np.uint64)
+            keys_out.copy_(torch.from_numpy(u.view(np.int64)))
+
+        def accept(keys, W, M_, draft, argmax, n_accept, bonus, stream):
+            calls.append("accept")
+            k = keys.view(W, M_).numpy().view(np.uint64).max(axis=0)
+            a = (0xFFFFFFFF - (k & np.uint64(0xFFFFFFFF))).astype(np.int32)
+            argmax.copy_(torch.from_numpy(a))
+            nn, b = ov.accept(a, draft.numpy())
+            n_accept.fill_(nn)
+            bonus.fill_(b)
+
+        lb.lmhead_argmax_partial, lb.lmhead_accept_keys = partial, accept
+        keys_local = torch.zeros(M, dtype=torch.int64)
+        keys_all = torch.zeros((world, M), dtype=torch.int64)
+        argmax = torch.full((M,), -1, dtype=torch.int32)
+        n_acc = torch.full((1,), -1, dtype=torch.int32)
+        bonus = torch.full((1,), -1, dtype=torch.int32)
+        lmhead_verify_sharded(None, None, M, n, K, off, torch.from_numpy(drafts.astype(np.int32)),
+                              argmax, n_acc, bonus, None, keys_local, keys_all)
+        q.put((rank, calls, argmax.tolist(), full.tolist(), int(n_acc.item()), int(bonus.item()),
+               j, bool(torch.equal(keys_all[rank], keys_local))))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_run_the_sharded_verify_sequence():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_flow, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=180)
+    codes = [p.exitcode for p in procs]
+    for p in procs:
+        if p.is_alive():
+            p.kill()
+    assert codes == [0, 0], codes
+    got = sorted(q.get(timeout=5) for _ in range(2))
+    for rank, calls, a, full, n, b, j, own_row in got:
+        assert calls == ["partial", "accept"]
+        assert own_row, "the gathered keys hold each rank's own keys at its rank"
+        assert a == full
+        assert n == j and b == full[n]
+
+
+def test_slice_key_orders_by_logit_then_lowest_row():
+    vals = [-3.5, -0.0, 0.0, 1e-30, 0.25, 7.0, 7.0]
+    rows = [5, 9, 8, 1, 4, 12, 3]
+    keys = [_key(v, r) for v, r in zip(vals, rows)]
+    best = int(np.argmax(np.array(keys, dtype=np.uint64)))
+    assert (vals[best], rows[best]) == (7.0, 3)
+    assert keys[0] < keys[1] < keys[2] < keys[3] < keys[4] < keys[5] < keys[6]
 
 
 # ------------------------------------------------------------------------------------ GPU

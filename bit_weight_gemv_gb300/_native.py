@@ -94,6 +94,12 @@ def _need(t, dtype, name):
         raise TypeError(f"{name} must be a contiguous CUDA tensor of dtype {dtype}")
 
 
+def _need_scalar_outs(n_accept, bonus):
+    """The accepted count and the bonus token are written as one int32 each."""
+    if n_accept.numel() < 1 or bonus.numel() < 1:
+        raise ValueError("n_accept and bonus must hold one element each")
+
+
 def lowbit_status_string(status: int) -> str:
     return lib.lowbit_status_string(int(status)).decode()
 
@@ -299,6 +305,7 @@ def _lmhead_args(H, packed_head, M, K, draft, argmax, n_accept, bonus, workspace
     _need(workspace, torch.uint8, "workspace")
     if H.numel() < M * K or draft.numel() < M - 1 or argmax.numel() < M:
         raise ValueError("H, draft or argmax too small")
+    _need_scalar_outs(n_accept, bonus)
 
 
 def lmhead_argmax_verify(H, packed_head, M, N, K, draft, argmax, n_accept, bonus, workspace,
@@ -330,6 +337,7 @@ def lmhead_argmax_verify_noalloc(H, packed_head, M, N, K, draft, argmax, n_accep
         _need(t, torch.int32, nm)
     if H.numel() < M * K or draft.numel() < M - 1 or argmax.numel() < M:
         raise ValueError("H, draft or argmax too small")
+    _need_scalar_outs(n_accept, bonus)
     _check(lib.lmhead_argmax_verify_noalloc(_ptr(H), _ptr(packed_head), M, N, K, _ptr(draft),
                                             _ptr(argmax), _ptr(n_accept), _ptr(bonus),
                                             _stream(stream)), "lmhead_argmax_verify_noalloc")
@@ -368,6 +376,7 @@ def lmhead_accept_keys(keys, W, M, draft, argmax, n_accept, bonus, stream=None):
         _need(t, torch.int32, nm)
     if keys.numel() < W * M or draft.numel() < M - 1 or argmax.numel() < M:
         raise ValueError("keys, draft or argmax too small")
+    _need_scalar_outs(n_accept, bonus)
     _check(lib.lmhead_accept_keys(_ptr(keys), W, M, _ptr(draft), _ptr(argmax), _ptr(n_accept),
                                   _ptr(bonus), _stream(stream)), "lmhead_accept_keys")
 

@@ -114,3 +114,27 @@ def test_kernel_family_selection_is_validated_on_the_host(lib):
     assert g(ctypes.cast(arr, vp), 2, 5, 1, None) == 2           # the streaming kernel takes M <= 4
     assert g(ctypes.cast(arr, vp), 9, 16, 0, None) == 1           # at most 8 problems
 
+
+
+def test_binding_refuses_host_tensors_and_empty_scalar_outputs(lib):
+    """The Python binding passes raw pointers only for contiguous CUDA tensors of the declared
+    dtype: host tensors are refused before anything reaches the library (there is no CPU
+    path), and the one-element outputs of the verify calls must exist."""
+    torch = pytest.importorskip("torch")
+    import bit_weight_gemv_gb300 as lb
+    from bit_weight_gemv_gb300 import _native
+    X = torch.zeros((1, 128), dtype=torch.bfloat16)
+    packed = torch.zeros(lb.lowbit_int4_packed_bytes(128, 128), dtype=torch.uint8)
+    Y = torch.zeros((1, 128), dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        lb.lowbit_gemm_int4(X, packed, 1, 128, 128, Y)
+    with pytest.raises(TypeError):
+        lb.lmhead_argmax_verify(X, packed, 1, 128, 128, torch.zeros(1, dtype=torch.int32),
+                                torch.zeros(1, dtype=torch.int32),
+                                torch.zeros(1, dtype=torch.int32),
+                                torch.zeros(1, dtype=torch.int32), torch.zeros(512, dtype=torch.uint8))
+    one, none = torch.zeros(1, dtype=torch.int32), torch.zeros(0, dtype=torch.int32)
+    _native._need_scalar_outs(one, one)
+    for a, b in ((none, one), (one, none)):
+        with pytest.raises(ValueError):
+            _native._need_scalar_outs(a, b)

@@ -16,7 +16,9 @@ constexpr int kMaxK = 65536;
 // One error word per device (see lowbit_device_error).
 __device__ int g_device_error;
 std::atomic<int> g_debug_stall{0};
-int* g_err_ptr[kMaxDevices] = {nullptr};
+// Device address of the error word per device; concurrent first calls on one device both
+// store the same value.
+std::atomic<int*> g_err_ptr[kMaxDevices];
 
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -44,26 +46,28 @@ int debug_stall() { return g_debug_stall.load(std::memory_order_relaxed); }
 int* device_error_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (!g_err_ptr[dev]) {
+  int* w = g_err_ptr[dev].load(std::memory_order_relaxed);
+  if (!w) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-    g_err_ptr[dev] = static_cast<int*>(p);
+    w = static_cast<int*>(p);
+    g_err_ptr[dev].store(w, std::memory_order_relaxed);
   }
-  return g_err_ptr[dev];
+  return w;
 }
 
 bool allocation_covers(const void* p, size_t bytes) {
-  static PFN_cuPointerGetAttribute_v4000 get_attr = nullptr;
-  static bool looked_up = false;
-  if (!looked_up) {
+  // looked up once, on the first call (a function-local static initialises exactly once even
+  // when several host threads make that call together)
+  static const PFN_cuPointerGetAttribute_v4000 get_attr = [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult qr;
     if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &fn, 4000, cudaEnableDefault,
-                                         &qr) == cudaSuccess &&
-        qr == cudaDriverEntryPointSuccess)
-      get_attr = reinterpret_cast<PFN_cuPointerGetAttribute_v4000>(fn);
-    looked_up = true;
-  }
+                                         &qr) != cudaSuccess ||
+        qr != cudaDriverEntryPointSuccess)
+      return static_cast<PFN_cuPointerGetAttribute_v4000>(nullptr);
+    return reinterpret_cast<PFN_cuPointerGetAttribute_v4000>(fn);
+  }();
   if (!get_attr || !p) return false;
   CUdeviceptr start = 0;
   size_t size = 0;

@@ -239,10 +239,16 @@ lowbit_status lowbit_validate_packed(const void* packed, int format, int P, int 
   PackedHeader h;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LOWBIT_ERR_CUDA;
   if (cudaMemcpy(&h, packed, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return LOWBIT_ERR_CUDA;
-  const uint32_t want_p = (format == (int)kFormatInt4) ? 0u : (uint32_t)P;
+  // INT4, NVFP4 and Q8 headers record no plane count; the sa header records its code group G,
+  // which this call does not take, so any supported G is accepted there.
+  const bool planes = format == (int)kFormatBinplane || format == (int)kFormatSa;
+  const uint32_t want_p = planes ? (uint32_t)P : 0u;
+  const bool group_ok = format == (int)kFormatSa
+                            ? (h.group == 64u || h.group == 128u || h.group == 256u)
+                            : h.group == (uint32_t)kGroup;
   const bool ok = h.magic == kMagic && h.format == (uint32_t)format && h.version == kVersion &&
-                  h.N == (uint32_t)N && h.K == (uint32_t)K && h.P == want_p &&
-                  h.group == (uint32_t)kGroup && h.row_tile == (uint32_t)kRowTile;
+                  h.N == (uint32_t)N && h.K == (uint32_t)K && h.P == want_p && group_ok &&
+                  h.row_tile == (uint32_t)kRowTile;
   return ok ? LOWBIT_OK : LOWBIT_ERR_INVALID_ARG;
 }
 

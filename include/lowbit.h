@@ -166,7 +166,9 @@ lowbit_status lowbit_pack_q8(const int8_t* codes, const uint16_t* scales, int N,
                              void* stream);
 
 /* Synchronous check (copies the 128-byte header to the host after synchronising `stream`)
- * that `packed` holds format `format` (1 = INT4, 2 = binary planes) with these P, N, K.
+ * that `packed` holds format `format` (1 = INT4, 2 = binary planes, 3 = sa, 4 = NVFP4, 5 = Q8)
+ * with these N, K and, for formats 2 and 3, P (pass 0 for the others).  For the sa format the
+ * header's code group G is only checked to be 64, 128 or 256.
  * Returns LOWBIT_OK or LOWBIT_ERR_INVALID_ARG. */
 lowbit_status lowbit_validate_packed(const void* packed, int format, int P, int N, int K,
                                      void* stream);
